@@ -1,0 +1,607 @@
+// Fused split-K decode attention over the mixed-precision paged cache (INT2 format).
+//
+// OSCAR technical summary (gist.science), §2.2-B (kernel integration): one kernel
+// unpacks and dequantises the INT2 history, works in the rotated basis and applies the
+// inverse rotation, over paged KV with prefix sharing, without extra memory traffic.
+//
+// Launches per layer:
+//   1. qrot_kernel     q~ = R_K^T q per query head (fp32) and per-group sums of q~.
+//   2. split_kernel    one CTA per work item (plan): either INT2 pages [p0, p1) of one
+//                      (request, kv-head), or BF16 sink/ring tokens.  Writes a partial
+//                      (m, l, o~) in the rotated basis; the last CTA of each (request,
+//                      kv-head) merges the partials (log-sum-exp), applies o = R_V o~ and
+//                      stores bf16 (and optional fp32) output.
+//
+// INT2 page pipeline (per warp, no block barriers): lane 0 issues cp.async.bulk copies of
+// the page's code block (K 2 KB + V 2 KB) and scale/zero block into a private ring of
+// kStages shared-memory stages, completion on an mbarrier; waits are bounded.
+//
+// Tensor-core formulation (mma.sync m16n8k16, fp16 in, fp32 accumulate), per 16 tokens:
+//   scores  S[t, n] = sum_c code_K[t, c] * B[c, n],  B = q~ (hi and lo fp16 halves as two
+//           columns per head, so q~ keeps ~22 bits).  Scale and zero factor out per
+//           (token, group): q~.k^ = s * (q~ . code) + z * sum(q~).
+//   values  O[c, n] += sum_t code_V[c, t] * P'[t, n],  P' = p * s_V (fp16), and
+//           sum_t p * z_V is added per group at the end.
+// A 2-bit field masked in place (w & 0x00030003 << 2k) is an fp16 subnormal equal to
+// code * 4^k * 2^-24; the power of two is folded into B (keys) or into the output scale
+// (values), so one AND turns two codes into an MMA operand.
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "common.cuh"
+#include "oscar_internal.h"
+
+namespace oscar {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 4;
+
+// ---------------------------------------------------------------- MMA helpers
+__device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t movtrans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+  __half2 h = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+// 2-bit field f (0..7) of each 16-bit half of w, as fp16 code * 4^(f&3) * 2^-24.
+__device__ __forceinline__ uint32_t field(uint32_t w, uint32_t w_shr8, int f) {
+  const uint32_t m = 0x00030003u << (2 * (f & 3));
+  return (f < 4 ? w : w_shr8) & m;
+}
+
+// Token order inside a 16-token block used by both MMAs: row m of the score tile (and
+// k-index m of the value MMA) is token tau(m); this makes every shared-memory read below
+// bank-conflict free.
+__device__ __forceinline__ int tau8(int m) { return (m >> 1) + 4 * (m & 1); }
+
+// ---------------------------------------------------------------- q rotation
+template <int G>
+__global__ void __launch_bounds__(128) qrot_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
+                                                   float* __restrict__ qt, float* __restrict__ qsum) {
+  __shared__ float qs[G][kHeadDim];
+  __shared__ float red[G][4];
+  pdl_wait();
+  pdl_trigger();
+  const int req = blockIdx.x / kp.n_kv_heads, kvh = blockIdx.x % kp.n_kv_heads, c = threadIdx.x;
+  const size_t head0 = size_t(req) * kp.n_q_heads + size_t(kvh) * G;
+  for (int h = 0; h < G; ++h) qs[h][c] = __uint_as_float(uint32_t(q[(head0 + h) * kHeadDim + c]) << 16);
+  __syncthreads();
+  const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) +
+                   (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
+  float acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = 0.f;
+#pragma unroll 8
+  for (int i = 0; i < kHeadDim; ++i) {
+    const float r = __ldg(R + size_t(i) * kHeadDim + c);
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = fmaf(r, qs[h][i], acc[h]);
+  }
+  const int warp = c >> 5, lane = c & 31;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    qt[(head0 + h) * kHeadDim + c] = acc[h];
+    float s = acc[h];
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) red[h][warp] = s;
+  }
+  __syncthreads();
+  if (c < G * 4) {
+    const int h = c >> 2, grp = c & 3;
+    float v;
+    if (kp.group == 32)
+      v = red[h][grp];
+    else
+      v = grp == 0 ? (red[h][0] + red[h][1]) + (red[h][2] + red[h][3]) : 0.f;
+    qsum[(head0 + h) * 4 + grp] = v;
+  }
+}
+
+// ---------------------------------------------------------------- split kernel
+template <int G, int GROUP>
+struct Cfg {
+  static constexpr int NG = kHeadDim / GROUP;           // groups per token
+  static constexpr int NT = G / 4;                      // score n-tiles (4 heads x hi/lo each)
+  static constexpr int kCodeBytes = 2 * kPage * kRowBytes;  // K then V codes
+  static constexpr int kSzBytes = 2 * kPage * NG * 4;       // K then V (scale, zero)
+  static constexpr int kStageBytes = kCodeBytes + kSzBytes;
+  static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers and flags
+};
+
+// Merge all partials of (request, kv-head), rotate back and store.  128 threads.
+template <int G>
+__device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
+                                const float* partials, uint16_t* out, float* out_f32, float* sm_o /*[G][d]*/) {
+  const int c = threadIdx.x;
+  float mstar[G], lstar[G], o[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    mstar[h] = -INFINITY;
+    lstar[h] = 0.f;
+    o[h] = 0.f;
+  }
+  for (int i = 0; i < it.head_count; ++i) {
+    const float* pp = partials + size_t(it.head_first + i) * G * (kHeadDim + 2);
+#pragma unroll
+    for (int h = 0; h < G; ++h) mstar[h] = fmaxf(mstar[h], __ldcg(pp + h * (kHeadDim + 2)));
+  }
+  for (int i = 0; i < it.head_count; ++i) {
+    const float* pp = partials + size_t(it.head_first + i) * G * (kHeadDim + 2);
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      const float m = __ldcg(pp + h * (kHeadDim + 2));
+      if (m == -INFINITY) continue;
+      const float w = ex2(m - mstar[h]);
+      lstar[h] = fmaf(w, __ldcg(pp + h * (kHeadDim + 2) + 1), lstar[h]);
+      o[h] = fmaf(w, __ldcg(pp + h * (kHeadDim + 2) + 2 + c), o[h]);
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) sm_o[h * kHeadDim + c] = lstar[h] > 0.f ? o[h] / lstar[h] : 0.f;
+  __syncthreads();
+  // o = R_V o~ : thread c' reads column c' of R_V^T (coalesced)
+  const float* RVt = reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
+                     (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim;
+  float acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) acc[h] = 0.f;
+#pragma unroll 8
+  for (int j = 0; j < kHeadDim; ++j) {
+    const float r = __ldg(RVt + size_t(j) * kHeadDim + c);
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = fmaf(r, sm_o[h * kHeadDim + j], acc[h]);
+  }
+  const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    out[(head0 + h) * kHeadDim + c] = bf16_rne(acc[h]);
+    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = acc[h];
+  }
+  (void)dr;
+}
+
+// BF16 tokens of the sink + ring list: list index u < min(L, S) is sink u, otherwise
+// position H + u - min(L, S) in ring slot p % W.
+template <int G>
+__device__ void bf16_tokens_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
+                                 const float* qt_head0, float* part, uint8_t* smem) {
+  const int S = kp.n_sink;
+  const int n_s = min(dr.L, S);
+  const uint16_t* sinkK = reinterpret_cast<const uint16_t*>(
+      kp.base + kp.lay.sink + size_t(dr.slot) * kp.lay.sink_slot_stride + size_t(layer) * kp.lay.sink_layer_stride +
+      size_t(it.kvh) * kp.lay.sink_head_stride);
+  const uint16_t* sinkV = sinkK + size_t(S) * kHeadDim;
+  const uint16_t* ringK = reinterpret_cast<const uint16_t*>(
+      kp.base + kp.lay.ring + size_t(dr.slot) * kp.lay.ring_slot_stride + size_t(layer) * kp.lay.ring_layer_stride +
+      size_t(it.kvh) * kp.lay.ring_head_stride);
+  const uint16_t* ringV = ringK + size_t(kp.window) * kHeadDim;
+  const int W = kp.window, H = dr.H;
+  auto rowK = [=](int u) {
+    return u < n_s ? sinkK + size_t(u) * kHeadDim : ringK + size_t((H + u - n_s) % W) * kHeadDim;
+  };
+  auto rowV = [=](int u) {
+    return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t((H + u - n_s) % W) * kHeadDim;
+  };
+  float* qs = reinterpret_cast<float*>(smem);
+  for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[e] = qt_head0[e];
+  __syncthreads();
+  rows_attention<G>(rowK, rowV, it.begin, it.end, qs, part, smem + G * kHeadDim * 4);
+}
+
+// INT2 history pages [it.begin, it.end) of one (request, kv-head).  Positions outside
+// [S, H) inside those pages are masked.  Warp w takes pages begin + w, + kWarps, ...
+template <int G, int GROUP>
+__device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
+                                const float* qt_head0, const float* qsum_head0, float* part, uint8_t* smem) {
+  using C = Cfg<G, GROUP>;
+  constexpr int NG = C::NG, NT = C::NT;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int gid = lane >> 2, tig = lane & 3;
+  uint8_t* pipe = smem + size_t(warp) * kStages * C::kStageBytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes) + warp * kStages;
+  const int S = kp.n_sink, H = dr.H;
+  const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
+  const uint8_t* code_base = kp.base + kp.lay.codes + size_t(layer) * kp.lay.codes_layer_stride +
+                             size_t(it.kvh) * kp.lay.codes_head_stride;
+  const uint8_t* sz_base =
+      kp.base + kp.lay.sz + size_t(layer) * kp.lay.sz_layer_stride + size_t(it.kvh) * kp.lay.sz_head_stride;
+
+  // my pages: it.begin + warp + kWarps * k
+  const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
+  // issue the copy of my k-th page into stage k % kStages; returns false if the page id is bad
+  auto issue = [&](int k) -> bool {
+    const int lp = it.begin + warp + kWarps * k;
+    int phys = -1;
+    if (lp < kp.max_pages_per_request) phys = ptab[lp];
+    if (phys < 0 || phys >= kp.max_pages) return false;
+    if (lane == 0) {
+      const int st = k % kStages;
+      const uint32_t bar = smem_u32(&bars[st]);
+      uint8_t* dst = pipe + size_t(st) * C::kStageBytes;
+      fence_proxy_async();
+      mbar_expect_tx(bar, C::kStageBytes);
+      bulk_g2s(smem_u32(dst), code_base + size_t(phys) * kp.lay.codes_page_stride, C::kCodeBytes, bar);
+      bulk_g2s(smem_u32(dst + C::kCodeBytes), sz_base + size_t(phys) * kp.lay.sz_page_stride, C::kSzBytes, bar);
+    }
+    return true;
+  };
+  uint32_t ok_mask = 0;     // bit st: stage st has a copy in flight
+  uint32_t phase_bits = 0;  // bit st: parity of the next completion of stage st's barrier
+  for (int k = 0; k < min(kStages, n_my); ++k)
+    if (issue(k)) ok_mask |= 1u << k;
+
+  // ---- B fragments of q~ (hi/lo fp16 columns), scaled by 4^-(kc & 3) for field kc
+  uint32_t bq[8][NT][2];
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc) {
+    const float fs = 1.0f / float(1 << (2 * (kc & 3)));
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int head = 4 * j + (gid >> 1), part_lo = gid & 1;
+      const float4 v4 = *reinterpret_cast<const float4*>(qt_head0 + head * kHeadDim + 16 * kc + 4 * tig);
+      const float v[4] = {v4.x * fs, v4.y * fs, v4.z * fs, v4.w * fs};
+      float o4[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float hi = __half2float(__float2half_rn(v[e]));
+        o4[e] = part_lo ? v[e] - hi : hi;
+      }
+      bq[kc][j][0] = pack_h2(o4[0], o4[1]);
+      bq[kc][j][1] = pack_h2(o4[2], o4[3]);
+    }
+  }
+  // per-thread heads: n-tile j gives head 4j + tig
+  const float scale = kLog2e * rsqrtf(float(kHeadDim));
+  float qs_scaled[NT][NG];  // sum(q~) over the group, times scale
+#pragma unroll
+  for (int j = 0; j < NT; ++j)
+#pragma unroll
+    for (int g = 0; g < NG; ++g) qs_scaled[j][g] = qsum_head0[(4 * j + tig) * 4 + g] * scale;
+
+  float m_run[NT], l_part[NT], zv[NT][NG];
+  float oacc[8][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    m_run[j] = -INFINITY;
+    l_part[j] = 0.f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) zv[j][g] = 0.f;
+  }
+#pragma unroll
+  for (int f = 0; f < 8; ++f)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) oacc[f][e] = 0.f;
+
+  const float two24 = 16777216.0f;
+  const int tok_a = tau8(gid);  // rows gid and gid + 8 of the score tile: tokens tok_a, tok_a + 8
+  bool broken = false;
+  for (int k = 0; k < n_my; ++k) {
+    const int st = k % kStages;
+    const int lp = it.begin + warp + kWarps * k;
+    const bool have = (ok_mask >> st) & 1u;
+    if (have) {
+      if (!mbar_wait(smem_u32(&bars[st]), (phase_bits >> st) & 1u)) {
+        if (lane == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+        broken = true;
+        break;
+      }
+      phase_bits ^= 1u << st;
+      ok_mask &= ~(1u << st);
+    } else if (lane == 0) {
+      flag(kp, OSCAR_FLAG_BAD_PAGE);
+    }
+    const uint8_t* stage = pipe + size_t(st) * C::kStageBytes;
+    const uint8_t* kcodes = stage;
+    const uint8_t* vcodes = stage + kPage * kRowBytes;
+    const uint32_t* ksz = reinterpret_cast<const uint32_t*>(stage + C::kCodeBytes);
+    const uint32_t* vsz = ksz + kPage * NG;
+
+    // ---- scores for the 64 tokens of the page (4 blocks of 16)
+    float lg[4][NT][2];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int t0 = 16 * b + tok_a, t1 = t0 + 8;
+      const uint2 wa = *reinterpret_cast<const uint2*>(kcodes + t0 * kRowBytes + 8 * tig);
+      const uint2 wb = *reinterpret_cast<const uint2*>(kcodes + t1 * kRowBytes + 8 * tig);
+      const uint32_t wa0s = wa.x >> 8, wa1s = wa.y >> 8, wb0s = wb.x >> 8, wb1s = wb.y >> 8;
+      float acc[4][NT][4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+#pragma unroll
+        for (int j = 0; j < NT; ++j)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[p][j][e] = 0.f;
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        const uint32_t a0 = field(wa.x, wa0s, kc), a1 = field(wb.x, wb0s, kc);
+        const uint32_t a2 = field(wa.y, wa1s, kc), a3 = field(wb.y, wb1s, kc);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma16816(acc[kc >> 1][j], a0, a1, a2, a3, bq[kc][j][0], bq[kc][j][1]);
+      }
+      const int pos0 = lp * kPage + t0, pos1 = lp * kPage + t1;
+      const bool v0 = have && pos0 >= S && pos0 < H, v1 = have && pos1 >= S && pos1 < H;
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) {
+          float T0, T1;
+          if (NG == 1) {
+            T0 = ((acc[0][j][0] + acc[0][j][1]) + (acc[1][j][0] + acc[1][j][1])) +
+                 ((acc[2][j][0] + acc[2][j][1]) + (acc[3][j][0] + acc[3][j][1]));
+            T1 = ((acc[0][j][2] + acc[0][j][3]) + (acc[1][j][2] + acc[1][j][3])) +
+                 ((acc[2][j][2] + acc[2][j][3]) + (acc[3][j][2] + acc[3][j][3]));
+          } else {
+            T0 = acc[g][j][0] + acc[g][j][1];
+            T1 = acc[g][j][2] + acc[g][j][3];
+          }
+          const uint32_t sz0 = ksz[t0 * NG + g], sz1 = ksz[t1 * NG + g];
+          s0 += fmaf(T0 * two24, bf16_lo(sz0) * scale, bf16_hi(sz0) * qs_scaled[j][g]);
+          s1 += fmaf(T1 * two24, bf16_lo(sz1) * scale, bf16_hi(sz1) * qs_scaled[j][g]);
+        }
+        lg[b][j][0] = v0 ? s0 : -INFINITY;
+        lg[b][j][1] = v1 ? s1 : -INFINITY;
+      }
+    }
+    // ---- online softmax over the page (per head: 8 scores per thread, 8 lanes per head)
+    float muse[NT];
+    bool rescale = false;
+    float alpha[NT];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      float mx = -INFINITY;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) mx = fmaxf(mx, fmaxf(lg[b][j][0], lg[b][j][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mnew = fmaxf(m_run[j], mx);
+      muse[j] = mnew == -INFINITY ? 0.f : mnew;
+      alpha[j] = ex2(m_run[j] - muse[j]);
+      rescale |= mnew > m_run[j];
+      m_run[j] = mnew;
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        l_part[j] *= alpha[j];
+#pragma unroll
+        for (int g = 0; g < NG; ++g) zv[j][g] *= alpha[j];
+      }
+      // value accumulator columns: G = 4 -> (hi, lo) of head tig; G = 8 -> heads tig, 4 + tig
+#pragma unroll
+      for (int f = 0; f < 8; ++f) {
+        const float a0 = alpha[0], a1 = NT == 2 ? alpha[NT - 1] : alpha[0];
+        oacc[f][0] *= a0;
+        oacc[f][1] *= a1;
+        oacc[f][2] *= a0;
+        oacc[f][3] *= a1;
+      }
+    }
+    // ---- values
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const int t0 = 16 * b + tok_a, t1 = t0 + 8;
+      float p[NT][2];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        p[j][0] = lg[b][j][0] == -INFINITY ? 0.f : ex2(lg[b][j][0] - muse[j]);
+        p[j][1] = lg[b][j][1] == -INFINITY ? 0.f : ex2(lg[b][j][1] - muse[j]);
+        l_part[j] += p[j][0] + p[j][1];
+      }
+      // B fragments of P' = p * s_V per group (movmatrix turns score rows into value k-rows)
+      uint32_t bp[NG][2];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const uint32_t vz0 = vsz[t0 * NG + g], vz1 = vsz[t1 * NG + g];
+        const float sv0 = bf16_lo(vz0), sv1 = bf16_lo(vz1);
+        const float zv0 = bf16_hi(vz0), zv1 = bf16_hi(vz1);
+        uint32_t x0, x1;
+        if (NT == 1) {
+          const float q0 = p[0][0] == 0.f ? 0.f : p[0][0] * sv0;
+          const float q1 = p[0][1] == 0.f ? 0.f : p[0][1] * sv1;
+          const float h0 = __half2float(__float2half_rn(q0)), h1 = __half2float(__float2half_rn(q1));
+          x0 = pack_h2(h0, q0 - h0);
+          x1 = pack_h2(h1, q1 - h1);
+        } else {
+          x0 = pack_h2(p[0][0] == 0.f ? 0.f : p[0][0] * sv0, p[NT - 1][0] == 0.f ? 0.f : p[NT - 1][0] * sv0);
+          x1 = pack_h2(p[0][1] == 0.f ? 0.f : p[0][1] * sv1, p[NT - 1][1] == 0.f ? 0.f : p[NT - 1][1] * sv1);
+        }
+        bp[g][0] = movtrans(x0);
+        bp[g][1] = movtrans(x1);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          if (p[j][0] != 0.f) zv[j][g] = fmaf(p[j][0], zv0, zv[j][g]);
+          if (p[j][1] != 0.f) zv[j][g] = fmaf(p[j][1], zv1, zv[j][g]);
+        }
+      }
+      // A fragments: word gid of tokens tig, tig+4, tig+8, tig+12 (k = 2tig, 2tig+1, 2tig+8, 2tig+9)
+      const uint32_t* vw = reinterpret_cast<const uint32_t*>(vcodes + (16 * b) * kRowBytes) + gid;
+      const uint32_t wA = vw[(tig)*8], wB = vw[(tig + 4) * 8], wC = vw[(tig + 8) * 8], wD = vw[(tig + 12) * 8];
+      const uint32_t X = prmt(wA, wB, 0x5410), Y = prmt(wA, wB, 0x7632);
+      const uint32_t X2 = prmt(wC, wD, 0x5410), Y2 = prmt(wC, wD, 0x7632);
+      const uint32_t Xs = X >> 8, Ys = Y >> 8, X2s = X2 >> 8, Y2s = Y2 >> 8;
+#pragma unroll
+      for (int f = 0; f < 8; ++f) {
+        const int g = NG == 1 ? 0 : (f >> 1);
+        mma16816(oacc[f], field(X, Xs, f), field(Y, Ys, f), field(X2, X2s, f), field(Y2, Y2s, f), bp[g][0], bp[g][1]);
+      }
+    }
+    // ---- refill this stage with my page k + kStages
+    __syncwarp();
+    if (k + kStages < n_my && issue(k + kStages)) ok_mask |= 1u << st;
+  }
+  if (broken) {
+    // drain copies still in flight (bounded) before the stages are reused or the CTA exits
+    for (int st = 0; st < kStages; ++st)
+      if ((ok_mask >> st) & 1u) mbar_wait(smem_u32(&bars[st]), (phase_bits >> st) & 1u);
+  }
+
+  // ---- per-warp results -> shared memory, then merge the 4 warps into the partial
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 4);
+    l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 8);
+    l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 16);
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      zv[j][g] += __shfl_xor_sync(0xffffffffu, zv[j][g], 4);
+      zv[j][g] += __shfl_xor_sync(0xffffffffu, zv[j][g], 8);
+      zv[j][g] += __shfl_xor_sync(0xffffffffu, zv[j][g], 16);
+    }
+  }
+  __syncthreads();  // every warp is done with its stages: reuse the pipeline memory
+  float* wres = reinterpret_cast<float*>(smem);  // [kWarps][G][2 + d]
+  float* mine = wres + size_t(warp) * G * (kHeadDim + 2);
+  if (gid == 0) {
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int head = 4 * j + tig;
+      mine[head * (kHeadDim + 2)] = broken ? -INFINITY : m_run[j];
+      mine[head * (kHeadDim + 2) + 1] = broken ? 0.f : l_part[j];
+    }
+  }
+#pragma unroll
+  for (int f = 0; f < 8; ++f) {
+    const float us = two24 / float(1 << (2 * (f & 3)));
+    const int ch0 = 16 * f + 2 * gid, ch1 = ch0 + 1;
+    const int g = NG == 1 ? 0 : (f >> 1);
+    if (NT == 1) {
+      const int head = tig;
+      mine[head * (kHeadDim + 2) + 2 + ch0] = (oacc[f][0] + oacc[f][1]) * us + zv[0][g];
+      mine[head * (kHeadDim + 2) + 2 + ch1] = (oacc[f][2] + oacc[f][3]) * us + zv[0][g];
+    } else {
+      mine[tig * (kHeadDim + 2) + 2 + ch0] = oacc[f][0] * us + zv[0][g];
+      mine[(4 + tig) * (kHeadDim + 2) + 2 + ch0] = oacc[f][1] * us + zv[NT - 1][g];
+      mine[tig * (kHeadDim + 2) + 2 + ch1] = oacc[f][2] * us + zv[0][g];
+      mine[(4 + tig) * (kHeadDim + 2) + 2 + ch1] = oacc[f][3] * us + zv[NT - 1][g];
+    }
+  }
+  __syncthreads();
+  const int t = threadIdx.x;
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float mw[kWarps], ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      mw[w] = wres[(w * G + h) * (kHeadDim + 2)];
+      ms = fmaxf(ms, mw[w]);
+    }
+    float l = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      if (mw[w] == -INFINITY) continue;
+      const float a = ex2(mw[w] - ms);
+      l = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 1], l);
+      o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + t], o);
+    }
+    float* ph = part + size_t(h) * (kHeadDim + 2);
+    if (t == 0) {
+      ph[0] = ms;
+      ph[1] = l;
+    }
+    ph[2 + t] = o;
+  }
+}
+
+template <int G, int GROUP>
+__global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, const float* __restrict__ qt,
+                                                    const float* __restrict__ qsum, float* __restrict__ partials,
+                                                    uint16_t* __restrict__ out, float* __restrict__ out_f32) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  using C = Cfg<G, GROUP>;
+  __shared__ int s_last;
+  const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[blockIdx.x];
+  const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
+  if (threadIdx.x == 0) {
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
+    for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  pdl_wait();
+  pdl_trigger();
+  float* part = partials + size_t(blockIdx.x) * G * (kHeadDim + 2);
+  const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
+  if (dr.slot < 0 || dr.slot >= kp.max_requests) {
+    if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+    for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += 128) part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
+  } else if (it.kind == 0) {
+    int2_pages_item<G, GROUP>(kp, layer, it, dr, qt + head0 * kHeadDim, qsum + head0 * 4, part, smem);
+  } else {
+    bf16_tokens_item<G>(kp, layer, it, dr, qt + head0 * kHeadDim, part, smem);
+  }
+  // ---- the last CTA of this (request, kv-head) merges and stores
+  __threadfence();  // this thread's partial stores are visible device-wide before the count
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned* ctr = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
+    const unsigned prev = atomicAdd(ctr, 1u);
+    s_last = prev == unsigned(it.head_count - 1);
+    if (s_last) *ctr = 0u;  // every partial has arrived; ready for the next layer
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  merge_and_store<G>(kp, layer, it, dr, partials, out, out_f32, reinterpret_cast<float*>(smem));
+}
+
+template <int G, int GROUP>
+int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
+                    const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches) {
+  using C = Cfg<G, GROUP>;
+  float* qt = reinterpret_cast<float*>(ws + wl.qt);
+  float* qsum = reinterpret_cast<float*>(ws + wl.qsum);
+  float* partials = reinterpret_cast<float*>(ws + wl.partials);
+  int e = launch_ex(qrot_kernel<G>, dim3(n_req * kp.n_kv_heads), dim3(128), 0, stream, kp, layer,
+                    static_cast<const uint16_t*>(q), qt, qsum);
+  if (e) return e;
+  *launches += 1;
+  static bool attr_set = false;
+  if (!attr_set) {
+    e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    if (e) return e;
+    attr_set = true;
+  }
+  e = launch_ex(split_kernel<G, GROUP>, dim3(n_items), dim3(128), size_t(C::kSmemBytes), stream, kp, layer,
+                static_cast<const float*>(qt), static_cast<const float*>(qsum), partials, static_cast<uint16_t*>(out),
+                out_f32);
+  if (!e) *launches += 1;
+  return e;
+}
+
+}  // namespace
+
+int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
+                  const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches) {
+  if (kp.gqa == 4 && kp.group == 128)
+    return launch_decode_t<4, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+  if (kp.gqa == 4 && kp.group == 32)
+    return launch_decode_t<4, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+  if (kp.gqa == 8 && kp.group == 128)
+    return launch_decode_t<8, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+  if (kp.gqa == 8 && kp.group == 32)
+    return launch_decode_t<8, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+  return int(cudaErrorInvalidValue);
+}
+
+}  // namespace oscar

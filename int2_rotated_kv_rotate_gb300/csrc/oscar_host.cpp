@@ -1,0 +1,698 @@
+// Host side of the C ABI (include/oscar.h): configuration checks, the device-block layout,
+// the page allocator with reference-counted prefix sharing, request state, append and
+// split-K decode planning, uploads of plans and page-table rows, status readback.
+//
+// Paged KV with prefix caching, BF16 sinks / recent tokens and INT2 history follow the
+// online-serving part of the OSCAR technical summary (gist.science), section 2.2-B.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+#include <string>
+#include <vector>
+
+#include "oscar_internal.h"
+
+using namespace oscar;
+
+namespace {
+
+thread_local std::string g_error;
+thread_local int g_launches = 0;
+
+oscar_status fail(oscar_status st, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+oscar_status fail(oscar_status st, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  g_error = buf;
+  return st;
+}
+
+#define CUDA_TRY(expr)                                                                        \
+  do {                                                                                        \
+    cudaError_t e_ = (expr);                                                                  \
+    if (e_ != cudaSuccess) return fail(OSCAR_ERR_CUDA, "%s: %s", #expr, cudaGetErrorString(e_)); \
+  } while (0)
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+constexpr int kAppendChunk = 16;     // tokens (or ring slots) per append work item
+constexpr int kMaxAppendTokenItems = 65536;
+constexpr int kBf16ItemTokens = 128;  // sink+ring tokens per decode work item
+
+bool config_ok(const oscar_config* c, std::string* why) {
+  auto bad = [&](const char* m) {
+    *why = m;
+    return false;
+  };
+  if (!c) return bad("config is NULL");
+  if (c->format != OSCAR_FORMAT_INT2 && c->format != OSCAR_FORMAT_BF16) return bad("format must be INT2 or BF16");
+  if (c->head_dim != kHeadDim) return bad("head_dim must be 128");
+  if (c->page != kPage) return bad("page must be 64");
+  if (c->n_kv_heads <= 0 || c->n_q_heads <= 0 || c->n_q_heads % c->n_kv_heads) return bad("bad head counts");
+  int g = c->n_q_heads / c->n_kv_heads;
+  if (g != 4 && g != 8) return bad("H_q / H_kv must be 4 or 8");
+  if (c->n_layers <= 0 || c->max_requests <= 0 || c->max_pages <= 0 || c->max_pages_per_request <= 0)
+    return bad("layers, requests and pages must be positive");
+  if (c->max_pages_per_request > (1 << 20)) return bad("max_pages_per_request too large");
+  if (c->format == OSCAR_FORMAT_INT2) {
+    if (c->group != 32 && c->group != 128) return bad("group must be 32 or 128");
+    if (c->n_sink < 0 || c->n_sink > kPage) return bad("n_sink must be in [0, 64]");
+    if (c->window < 0 || c->window > kMaxWindow || c->window % 16) return bad("window must be a multiple of 16 in [0, 1024]");
+  }
+  return true;
+}
+
+DeviceLayout compute_layout(const oscar_config& c) {
+  DeviceLayout L;
+  std::memset(&L, 0, sizeof L);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    size_t at = off;
+    off = align256(off + bytes);
+    return at;
+  };
+  const size_t d = kHeadDim, Hkv = c.n_kv_heads, layers = c.n_layers, pages = c.max_pages;
+  const size_t reqs = c.max_requests;
+  if (c.format == OSCAR_FORMAT_INT2) {
+    const size_t ng = d / c.group;
+    L.codes_head_stride = 2 * kPage * kRowBytes;
+    L.codes_page_stride = Hkv * L.codes_head_stride;
+    L.codes_layer_stride = pages * L.codes_page_stride;
+    L.codes = take(layers * L.codes_layer_stride);
+    L.sz_head_stride = 2 * kPage * ng * 4;
+    L.sz_page_stride = Hkv * L.sz_head_stride;
+    L.sz_layer_stride = pages * L.sz_page_stride;
+    L.sz = take(layers * L.sz_layer_stride);
+    L.sink_head_stride = 2 * size_t(c.n_sink) * d * 2;
+    L.sink_layer_stride = Hkv * L.sink_head_stride;
+    L.sink_slot_stride = layers * L.sink_layer_stride;
+    L.sink = take(reqs * L.sink_slot_stride);
+    L.ring_head_stride = 2 * size_t(c.window) * d * 2;
+    L.ring_layer_stride = Hkv * L.ring_head_stride;
+    L.ring_slot_stride = layers * L.ring_layer_stride;
+    L.ring = take(reqs * L.ring_slot_stride);
+    L.R_K = take(layers * Hkv * d * d * 4);
+    L.R_V = take(layers * Hkv * d * d * 4);
+    L.R_Vt = take(layers * Hkv * d * d * 4);
+    L.clip_K = take(layers * Hkv * 4);
+    L.clip_V = take(layers * Hkv * 4);
+  } else {
+    L.bf16_head_stride = 2 * kPage * d * 2;
+    L.bf16_page_stride = Hkv * L.bf16_head_stride;
+    L.bf16_layer_stride = pages * L.bf16_page_stride;
+    L.bf16_pages = take(layers * L.bf16_layer_stride);
+  }
+  L.page_table = take(reqs * size_t(c.max_pages_per_request) * 4);
+  L.status = take(256);
+  L.counters = take(reqs * Hkv * 4);
+  L.max_append_items = kMaxAppendTokenItems + reqs * (kMaxWindow / kAppendChunk);
+  L.max_decode_items = reqs * Hkv * (2 + kMaxWindow / kBf16ItemTokens) + 16384;
+  L.append_reqs = take(reqs * sizeof(AppendReq));
+  L.append_items = take(L.max_append_items * sizeof(AppendItem));
+  L.decode_reqs = take(reqs * sizeof(DecodeReq));
+  L.decode_items = take(L.max_decode_items * sizeof(DecodeItem));
+  L.total = off;
+  return L;
+}
+
+struct Request {
+  bool in_use = false;
+  int L = 0, H = 0;
+  std::vector<int> pages;
+};
+
+}  // namespace
+
+struct oscar_cache {
+  oscar_config cfg;
+  DeviceLayout lay;
+  uint8_t* base = nullptr;
+  int n_sm = 148;
+  std::vector<Request> reqs;
+  std::vector<int> refcount;
+  std::vector<int> free_pages;
+  // pinned host mirrors / staging
+  int32_t* h_page_table = nullptr;
+  uint8_t* h_staging = nullptr;
+  size_t staging_bytes = 0;
+  uint32_t* h_status = nullptr;
+  cudaEvent_t upload_done = nullptr;
+  bool upload_pending = false;
+  // pending append
+  bool reserved = false;
+  std::vector<AppendReq> app_reqs;
+  int app_items = 0, app_rows = 0;
+  // decode plan
+  bool planned = false;
+  int dec_n_req = 0, dec_items = 0, dec_bf16_items = 0, dec_max_pages = 0;
+  DecodeWorkspace ws{};
+};
+
+namespace {
+
+KernelParams kernel_params(const oscar_cache* c) {
+  KernelParams kp;
+  kp.base = c->base;
+  kp.n_q_heads = c->cfg.n_q_heads;
+  kp.n_kv_heads = c->cfg.n_kv_heads;
+  kp.gqa = c->cfg.n_q_heads / c->cfg.n_kv_heads;
+  kp.group = c->cfg.group;
+  kp.n_sink = c->cfg.n_sink;
+  kp.window = c->cfg.window;
+  kp.n_layers = c->cfg.n_layers;
+  kp.max_requests = c->cfg.max_requests;
+  kp.max_pages = c->cfg.max_pages;
+  kp.max_pages_per_request = c->cfg.max_pages_per_request;
+  kp.lay = c->lay;
+  return kp;
+}
+
+// The pinned staging buffers are rewritten only after the previous uploads finished.
+oscar_status wait_uploads(oscar_cache* c) {
+  if (c->upload_pending) {
+    CUDA_TRY(cudaEventSynchronize(c->upload_done));
+    c->upload_pending = false;
+  }
+  return OSCAR_OK;
+}
+
+oscar_status upload_rows(oscar_cache* c, const std::vector<int>& slots, cudaStream_t s) {
+  const size_t row = size_t(c->cfg.max_pages_per_request) * 4;
+  for (int slot : slots) {
+    CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.page_table + slot * row, c->h_page_table + size_t(slot) * c->cfg.max_pages_per_request,
+                             row, cudaMemcpyHostToDevice, s));
+  }
+  return OSCAR_OK;
+}
+
+bool is_int2(const oscar_cache* c) { return c->cfg.format == OSCAR_FORMAT_INT2; }
+
+// Pages a request needs to hold its stored tokens: the INT2 format pages positions < H
+// (sinks and recent tokens live elsewhere), the BF16 format pages all L positions.
+int pages_needed(const oscar_cache* c, int L, int H) {
+  if (is_int2(c)) return H > c->cfg.n_sink ? ceil_div(H, kPage) : 0;
+  return ceil_div(L, kPage);
+}
+
+oscar_status check_slot(const oscar_cache* c, int slot) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (slot < 0 || slot >= c->cfg.max_requests) return fail(OSCAR_ERR_INVALID_ARG, "slot %d out of range", slot);
+  if (!c->reqs[slot].in_use) return fail(OSCAR_ERR_INVALID_ARG, "slot %d is not allocated", slot);
+  return OSCAR_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* oscar_last_error(void) { return g_error.c_str(); }
+int oscar_last_launch_count(void) { return g_launches; }
+
+size_t oscar_cache_device_bytes(const oscar_config* cfg) {
+  std::string why;
+  if (!config_ok(cfg, &why)) {
+    g_error = why;
+    return 0;
+  }
+  return compute_layout(*cfg).total;
+}
+
+oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_t bytes, oscar_cache** out) {
+  std::string why;
+  if (!out) return fail(OSCAR_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!config_ok(cfg, &why)) return fail(OSCAR_ERR_INVALID_ARG, "%s", why.c_str());
+  if (!device_mem) return fail(OSCAR_ERR_INVALID_ARG, "device_mem is NULL");
+  if (reinterpret_cast<uintptr_t>(device_mem) % 256) return fail(OSCAR_ERR_INVALID_ARG, "device_mem must be 256-byte aligned");
+  DeviceLayout lay = compute_layout(*cfg);
+  if (bytes < lay.total) return fail(OSCAR_ERR_INVALID_ARG, "device block of %zu bytes < %zu needed", bytes, lay.total);
+  oscar_cache* c = new (std::nothrow) oscar_cache();
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "host allocation failed");
+  c->cfg = *cfg;
+  c->lay = lay;
+  c->base = static_cast<uint8_t*>(device_mem);
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, dev);
+  c->reqs.resize(cfg->max_requests);
+  c->refcount.assign(cfg->max_pages, 0);
+  c->free_pages.reserve(cfg->max_pages);
+  for (int p = cfg->max_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
+  const size_t pt_bytes = size_t(cfg->max_requests) * cfg->max_pages_per_request * 4;
+  c->staging_bytes = align256(size_t(cfg->max_requests) * std::max(sizeof(AppendReq), sizeof(DecodeReq))) +
+                     std::max(lay.max_append_items * sizeof(AppendItem), lay.max_decode_items * sizeof(DecodeItem));
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_page_table), pt_bytes);
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_staging), c->staging_bytes);
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_status), 256);
+  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->upload_done, cudaEventDisableTiming);
+  if (e == cudaSuccess) {
+    std::memset(c->h_page_table, 0xff, pt_bytes);  // -1 = unmapped
+    e = cudaMemcpy(c->base + lay.page_table, c->h_page_table, pt_bytes, cudaMemcpyHostToDevice);
+  }
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.status, 0, 256);
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.counters, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 4);
+  if (e == cudaSuccess && is_int2(c)) {
+    // layer params start as zeros until oscar_set_layer_params
+    e = cudaMemset(c->base + lay.R_K, 0, lay.clip_K - lay.R_K);
+  }
+  if (e != cudaSuccess) {
+    fail(OSCAR_ERR_CUDA, "cache_create: %s", cudaGetErrorString(e));
+    oscar_cache_destroy(c);
+    return OSCAR_ERR_CUDA;
+  }
+  *out = c;
+  return OSCAR_OK;
+}
+
+void oscar_cache_destroy(oscar_cache* c) {
+  if (!c) return;
+  if (c->upload_done) {
+    cudaEventSynchronize(c->upload_done);
+    cudaEventDestroy(c->upload_done);
+  }
+  if (c->h_page_table) cudaFreeHost(c->h_page_table);
+  if (c->h_staging) cudaFreeHost(c->h_staging);
+  if (c->h_status) cudaFreeHost(c->h_status);
+  delete c;
+}
+
+oscar_status oscar_cache_layout(const oscar_cache* c, oscar_layout* out) {
+  if (!c || !out) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  const DeviceLayout& L = c->lay;
+  out->codes = L.codes;
+  out->sz = L.sz;
+  out->sink = L.sink;
+  out->ring = L.ring;
+  out->bf16_pages = L.bf16_pages;
+  out->codes_page_bytes = L.codes_head_stride;
+  out->sz_page_bytes = L.sz_head_stride;
+  out->bf16_page_bytes = L.bf16_head_stride;
+  out->sink_bytes_per_head = L.sink_head_stride;
+  out->ring_bytes_per_head = L.ring_head_stride;
+  out->page_table = L.page_table;
+  out->total = L.total;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_set_layer_params(oscar_cache* c, int layer, const float* R_K, const float* R_V, const float* clip_K,
+                                    const float* clip_V, void* stream) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (!is_int2(c)) return fail(OSCAR_ERR_STATE, "layer params apply to the INT2 format only");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (!R_K || !R_V || !clip_K || !clip_V) return fail(OSCAR_ERR_INVALID_ARG, "NULL parameter array");
+  const int H = c->cfg.n_kv_heads, d = kHeadDim;
+  for (int h = 0; h < H; ++h) {
+    if (!(clip_K[h] > 0.f) || !(clip_V[h] > 0.f)) return fail(OSCAR_ERR_INVALID_ARG, "clip thresholds must be > 0");
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t mat = size_t(d) * d;
+  std::vector<float> Vt(size_t(H) * mat);
+  for (int h = 0; h < H; ++h)
+    for (int i = 0; i < d; ++i)
+      for (int j = 0; j < d; ++j) Vt[h * mat + size_t(j) * d + i] = R_V[h * mat + size_t(i) * d + j];
+  const size_t lmat = size_t(layer) * H * mat * 4;
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.R_K + lmat, R_K, H * mat * 4, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.R_V + lmat, R_V, H * mat * 4, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.R_Vt + lmat, Vt.data(), H * mat * 4, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.clip_K + size_t(layer) * H * 4, clip_K, H * 4, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.clip_V + size_t(layer) * H * 4, clip_V, H * 4, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaStreamSynchronize(s));  // Vt is a temporary
+  return OSCAR_OK;
+}
+
+oscar_status oscar_request_alloc(oscar_cache* c, int* slot) {
+  if (!c || !slot) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+  for (int i = 0; i < c->cfg.max_requests; ++i) {
+    if (!c->reqs[i].in_use) {
+      c->reqs[i] = Request();
+      c->reqs[i].in_use = true;
+      c->reqs[i].H = is_int2(c) ? c->cfg.n_sink : 0;
+      *slot = i;
+      return OSCAR_OK;
+    }
+  }
+  return fail(OSCAR_ERR_OUT_OF_PAGES, "no free request slot");
+}
+
+oscar_status oscar_request_free(oscar_cache* c, int slot) {
+  oscar_status st = check_slot(c, slot);
+  if (st) return st;
+  if (c->reserved)
+    for (const AppendReq& r : c->app_reqs)
+      if (r.slot == slot) return fail(OSCAR_ERR_STATE, "slot %d has a pending reservation", slot);
+  Request& r = c->reqs[slot];
+  for (int p : r.pages)
+    if (--c->refcount[p] == 0) c->free_pages.push_back(p);
+  // the device row keeps stale ids; it is rewritten before the slot is used again
+  st = wait_uploads(c);
+  if (st) return st;
+  std::fill(c->h_page_table + size_t(slot) * c->cfg.max_pages_per_request,
+            c->h_page_table + size_t(slot + 1) * c->cfg.max_pages_per_request, -1);
+  r = Request();
+  c->planned = false;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_request_info(const oscar_cache* c, int slot, int* length, int* history_end, int* n_pages) {
+  oscar_status st = check_slot(c, slot);
+  if (st) return st;
+  const Request& r = c->reqs[slot];
+  if (length) *length = r.L;
+  if (history_end) *history_end = r.H;
+  if (n_pages) *n_pages = int(r.pages.size());
+  return OSCAR_OK;
+}
+
+oscar_status oscar_request_pages(const oscar_cache* c, int slot, int* pages, int n) {
+  oscar_status st = check_slot(c, slot);
+  if (st) return st;
+  const Request& r = c->reqs[slot];
+  if (!pages || n < 0 || n > int(r.pages.size())) return fail(OSCAR_ERR_INVALID_ARG, "bad page buffer");
+  std::copy(r.pages.begin(), r.pages.begin() + n, pages);
+  return OSCAR_OK;
+}
+
+oscar_status oscar_request_share_prefix(oscar_cache* c, int dst, int src, int n_tokens, void* stream) {
+  oscar_status st = check_slot(c, dst);
+  if (st) return st;
+  st = check_slot(c, src);
+  if (st) return st;
+  if (dst == src) return fail(OSCAR_ERR_INVALID_ARG, "dst == src");
+  if (c->reserved) return fail(OSCAR_ERR_STATE, "a reservation is pending");
+  Request& d = c->reqs[dst];
+  const Request& s = c->reqs[src];
+  if (d.L != 0 || !d.pages.empty()) return fail(OSCAR_ERR_INVALID_ARG, "dst must be empty");
+  if (n_tokens <= 0 || n_tokens % kPage) return fail(OSCAR_ERR_INVALID_ARG, "n_tokens must be a positive multiple of 64");
+  const int limit = is_int2(c) ? s.H : s.L / kPage * kPage;
+  if (n_tokens > limit)
+    return fail(OSCAR_ERR_INVALID_ARG, "n_tokens %d exceeds the shareable prefix %d of src", n_tokens, limit);
+  if (n_tokens / kPage > c->cfg.max_pages_per_request) return fail(OSCAR_ERR_INVALID_ARG, "prefix too long");
+  st = wait_uploads(c);
+  if (st) return st;
+  cudaStream_t strm = static_cast<cudaStream_t>(stream);
+  const int n = n_tokens / kPage;
+  d.pages.assign(s.pages.begin(), s.pages.begin() + n);
+  for (int p : d.pages) ++c->refcount[p];
+  int32_t* row = c->h_page_table + size_t(dst) * c->cfg.max_pages_per_request;
+  std::fill(row, row + c->cfg.max_pages_per_request, -1);
+  std::copy(d.pages.begin(), d.pages.end(), row);
+  d.L = n_tokens;
+  d.H = is_int2(c) ? n_tokens : n_tokens;
+  st = upload_rows(c, {dst}, strm);
+  if (st) return st;
+  if (is_int2(c) && c->lay.sink_slot_stride > 0) {
+    CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.sink + size_t(dst) * c->lay.sink_slot_stride,
+                             c->base + c->lay.sink + size_t(src) * c->lay.sink_slot_stride, c->lay.sink_slot_stride,
+                             cudaMemcpyDeviceToDevice, strm));
+  }
+  CUDA_TRY(cudaEventRecord(c->upload_done, strm));
+  c->upload_pending = true;
+  c->planned = false;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_reserve(oscar_cache* c, const int* slots, const int* n_new, int n_req, void* stream) {
+  if (!c || !slots || !n_new || n_req <= 0 || n_req > c->cfg.max_requests)
+    return fail(OSCAR_ERR_INVALID_ARG, "bad reserve arguments");
+  if (c->reserved) return fail(OSCAR_ERR_STATE, "previous reservation not committed");
+  std::vector<char> seen(c->cfg.max_requests, 0);
+  long long rows = 0;
+  int new_pages = 0;
+  const int S = is_int2(c) ? c->cfg.n_sink : 0, W = c->cfg.window;
+  std::vector<AppendReq> reqs(n_req);
+  for (int i = 0; i < n_req; ++i) {
+    oscar_status st = check_slot(c, slots[i]);
+    if (st) return st;
+    if (seen[slots[i]]) return fail(OSCAR_ERR_INVALID_ARG, "slot %d listed twice", slots[i]);
+    seen[slots[i]] = 1;
+    if (n_new[i] < 0) return fail(OSCAR_ERR_INVALID_ARG, "negative n_new");
+    const Request& r = c->reqs[slots[i]];
+    AppendReq& a = reqs[i];
+    a.slot = slots[i];
+    a.L0 = r.L;
+    a.H0 = r.H;
+    long long L1 = (long long)r.L + n_new[i];
+    if (L1 > (long long)kPage * c->cfg.max_pages_per_request)
+      return fail(OSCAR_ERR_INVALID_ARG, "request %d would exceed its page-table row", slots[i]);
+    a.L1 = int(L1);
+    a.H1 = is_int2(c) ? std::max(r.H, a.L1 - W) : a.L1;
+    a.x_offset = int(rows);
+    rows += n_new[i];
+    new_pages += std::max(0, pages_needed(c, a.L1, a.H1) - int(r.pages.size()));
+  }
+  if (rows > (1 << 30)) return fail(OSCAR_ERR_INVALID_ARG, "too many rows");
+  if (new_pages > int(c->free_pages.size()))
+    return fail(OSCAR_ERR_OUT_OF_PAGES, "need %d pages, %zu free", new_pages, c->free_pages.size());
+  // work items
+  std::vector<AppendItem> items;
+  for (int i = 0; i < n_req; ++i) {
+    const AppendReq& a = reqs[i];
+    if (is_int2(c) && W > 0) {
+      std::vector<char> touched(W, 0);
+      for (int p = a.H0; p < std::min(a.L0, a.H1); ++p) touched[p % W] = 1;   // evicted
+      for (int p = std::max(a.L0, a.H1); p < a.L1; ++p) touched[p % W] = 1;  // new ring tokens
+      for (int s0 = 0; s0 < W; s0 += kAppendChunk) {
+        bool any = false;
+        for (int s = s0; s < s0 + kAppendChunk; ++s) any |= touched[s] != 0;
+        if (any) items.push_back({i, 0, s0, kAppendChunk});
+      }
+    }
+    const int d0 = a.L0, d1 = is_int2(c) ? std::min(a.L1, a.H1) : a.L1;
+    for (int p = d0; p < d1; p += kAppendChunk) items.push_back({i, 1, p, std::min(kAppendChunk, d1 - p)});
+  }
+  if (items.size() > c->lay.max_append_items)
+    return fail(OSCAR_ERR_INVALID_ARG, "append of %lld tokens is too large for one reservation; split it", rows);
+  oscar_status st = wait_uploads(c);
+  if (st) return st;
+  // allocate pages and update the host mirror
+  std::vector<int> changed;
+  for (const AppendReq& a : reqs) {
+    Request& r = c->reqs[a.slot];
+    int need = pages_needed(c, a.L1, a.H1);
+    if (need > int(r.pages.size())) {
+      int32_t* row = c->h_page_table + size_t(a.slot) * c->cfg.max_pages_per_request;
+      while (int(r.pages.size()) < need) {
+        int p = c->free_pages.back();
+        c->free_pages.pop_back();
+        c->refcount[p] = 1;
+        row[r.pages.size()] = p;
+        r.pages.push_back(p);
+      }
+      changed.push_back(a.slot);
+    }
+  }
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = upload_rows(c, changed, s);
+  if (st) return st;
+  std::memcpy(c->h_staging, reqs.data(), reqs.size() * sizeof(AppendReq));
+  std::memcpy(c->h_staging + align256(reqs.size() * sizeof(AppendReq)), items.data(), items.size() * sizeof(AppendItem));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.append_reqs, c->h_staging, reqs.size() * sizeof(AppendReq),
+                           cudaMemcpyHostToDevice, s));
+  if (!items.empty())
+    CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.append_items, c->h_staging + align256(reqs.size() * sizeof(AppendReq)),
+                             items.size() * sizeof(AppendItem), cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaEventRecord(c->upload_done, s));
+  c->upload_pending = true;
+  c->app_reqs = reqs;
+  c->app_items = int(items.size());
+  c->app_rows = int(rows);
+  c->reserved = true;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_commit_append(oscar_cache* c) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->reserved) return fail(OSCAR_ERR_STATE, "no reservation to commit");
+  for (const AppendReq& a : c->app_reqs) {
+    c->reqs[a.slot].L = a.L1;
+    c->reqs[a.slot].H = a.H1;
+  }
+  c->reserved = false;
+  c->planned = false;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_quantize_append(oscar_cache* c, int layer, const void* k_new, const void* v_new, void* stream) {
+  g_launches = 0;
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (!is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_quantize_append needs the INT2 format");
+  if (!c->reserved) return fail(OSCAR_ERR_STATE, "no reservation");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
+  if (c->app_items == 0) return OSCAR_OK;
+  int e = launch_append(kernel_params(c), layer, k_new, v_new, c->app_items, c->app_rows, stream, &g_launches);
+  if (e) return fail(OSCAR_ERR_CUDA, "append launch: %s", cudaGetErrorString(cudaError_t(e)));
+  return OSCAR_OK;
+}
+
+oscar_status oscar_bf16_append(oscar_cache* c, int layer, const void* k_new, const void* v_new, void* stream) {
+  g_launches = 0;
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_bf16_append needs the BF16 format");
+  if (!c->reserved) return fail(OSCAR_ERR_STATE, "no reservation");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
+  if (c->app_items == 0) return OSCAR_OK;
+  int e = launch_bf16_append(kernel_params(c), layer, k_new, v_new, c->app_items, c->app_rows, stream, &g_launches);
+  if (e) return fail(OSCAR_ERR_CUDA, "bf16 append launch: %s", cudaGetErrorString(cudaError_t(e)));
+  return OSCAR_OK;
+}
+
+oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int max_split_pages, void* stream) {
+  if (!c || !slots || n_req <= 0 || n_req > c->cfg.max_requests)
+    return fail(OSCAR_ERR_INVALID_ARG, "bad plan arguments");
+  if (c->reserved) return fail(OSCAR_ERR_STATE, "commit the pending append before planning a decode");
+  if (max_split_pages < 0) return fail(OSCAR_ERR_INVALID_ARG, "max_split_pages < 0");
+  std::vector<char> seen(c->cfg.max_requests, 0);
+  const int Hkv = c->cfg.n_kv_heads, S = is_int2(c) ? c->cfg.n_sink : 0;
+  long long total_pages = 0;
+  for (int i = 0; i < n_req; ++i) {
+    oscar_status st = check_slot(c, slots[i]);
+    if (st) return st;
+    if (seen[slots[i]]) return fail(OSCAR_ERR_INVALID_ARG, "slot %d listed twice", slots[i]);
+    seen[slots[i]] = 1;
+    const Request& r = c->reqs[slots[i]];
+    total_pages += (long long)Hkv * pages_needed(c, r.L, r.H);
+  }
+  int chunk = max_split_pages;
+  if (chunk == 0) {
+    const long long target = 2LL * c->n_sm;
+    chunk = int(std::max<long long>(4, (total_pages + target - 1) / target));
+  }
+  std::vector<DecodeReq> reqs(n_req);
+  std::vector<DecodeItem> items;
+  int n_bf16 = 0, max_pages = 0;
+  for (int i = 0; i < n_req; ++i) {
+    const Request& r = c->reqs[slots[i]];
+    DecodeReq& q = reqs[i];
+    q.slot = slots[i];
+    q.L = r.L;
+    q.H = is_int2(c) ? r.H : r.L;
+    const int np = pages_needed(c, r.L, q.H);
+    const int n_bf = is_int2(c) ? std::min(r.L, S) + std::max(0, r.L - r.H) : 0;
+    const int n_bf_items = n_bf > 0 ? ceil_div(n_bf, kBf16ItemTokens) : 0;
+    const int n_pg_items = np > 0 ? ceil_div(np, chunk) : 0;
+    int per_head = n_bf_items + n_pg_items;
+    if (per_head == 0) per_head = 1;  // empty request: one empty item writes zeros
+    q.first_item = int(items.size());
+    q.items_per_head = per_head;
+    for (int h = 0; h < Hkv; ++h) {
+      const int first = int(items.size());
+      if (n_bf_items + n_pg_items == 0) {
+        items.push_back({i, h, 1, 0, 0, first, per_head, 0});
+        continue;
+      }
+      for (int t = 0; t < n_bf; t += kBf16ItemTokens) {
+        items.push_back({i, h, 1, t, std::min(n_bf, t + kBf16ItemTokens), first, per_head, 0});
+        ++n_bf16;
+      }
+      for (int p = 0; p < np; p += chunk) {
+        items.push_back({i, h, 0, p, std::min(np, p + chunk), first, per_head, 0});
+        max_pages = std::max(max_pages, std::min(np, p + chunk) - p);
+      }
+    }
+  }
+  if (items.size() > c->lay.max_decode_items)
+    return fail(OSCAR_ERR_INVALID_ARG, "plan of %zu items exceeds %zu; raise max_split_pages", items.size(),
+                c->lay.max_decode_items);
+  oscar_status st = wait_uploads(c);
+  if (st) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t rb = reqs.size() * sizeof(DecodeReq);
+  std::memcpy(c->h_staging, reqs.data(), rb);
+  std::memcpy(c->h_staging + align256(rb), items.data(), items.size() * sizeof(DecodeItem));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_reqs, c->h_staging, rb, cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_items, c->h_staging + align256(rb), items.size() * sizeof(DecodeItem),
+                           cudaMemcpyHostToDevice, s));
+  CUDA_TRY(cudaEventRecord(c->upload_done, s));
+  c->upload_pending = true;
+  const int G = c->cfg.n_q_heads / Hkv;
+  DecodeWorkspace w;
+  size_t off = 0;
+  w.qt = off;
+  off = align256(off + size_t(n_req) * c->cfg.n_q_heads * kHeadDim * 4);
+  w.qsum = off;
+  off = align256(off + size_t(n_req) * c->cfg.n_q_heads * 4 * 4);
+  w.partials = off;
+  off = align256(off + items.size() * size_t(G) * (kHeadDim + 2) * 4);
+  w.total = off;
+  c->ws = w;
+  c->dec_n_req = n_req;
+  c->dec_items = int(items.size());
+  c->dec_bf16_items = n_bf16;
+  c->dec_max_pages = max_pages;
+  c->planned = true;
+  return OSCAR_OK;
+}
+
+size_t oscar_decode_workspace_bytes(const oscar_cache* c) { return (c && c->planned) ? c->ws.total : 0; }
+
+oscar_status oscar_plan_info(const oscar_cache* c, int* n_items, int* n_bf16_items, int* max_item_pages) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->planned) return fail(OSCAR_ERR_STATE, "no decode plan");
+  if (n_items) *n_items = c->dec_items;
+  if (n_bf16_items) *n_bf16_items = c->dec_bf16_items;
+  if (max_item_pages) *max_item_pages = c->dec_max_pages;
+  return OSCAR_OK;
+}
+
+static oscar_status check_decode(oscar_cache* c, int layer, const void* q, void* out, void* ws, size_t ws_bytes) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (!c->planned) return fail(OSCAR_ERR_STATE, "no decode plan (plan after every append commit)");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (!q || !out || !ws) return fail(OSCAR_ERR_INVALID_ARG, "NULL q, out or workspace");
+  if (reinterpret_cast<uintptr_t>(ws) % 256) return fail(OSCAR_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  if (ws_bytes < c->ws.total) return fail(OSCAR_ERR_INVALID_ARG, "workspace %zu < %zu bytes", ws_bytes, c->ws.total);
+  return OSCAR_OK;
+}
+
+oscar_status oscar_decode_attention(oscar_cache* c, int layer, const void* q, void* out, void* workspace, size_t ws_bytes,
+                                    float* out_f32, void* stream) {
+  g_launches = 0;
+  oscar_status st = check_decode(c, layer, q, out, workspace, ws_bytes);
+  if (st) return st;
+  if (!is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_decode_attention needs the INT2 format");
+  int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_n_req,
+                        c->dec_items, stream, &g_launches);
+  if (e) return fail(OSCAR_ERR_CUDA, "decode launch: %s", cudaGetErrorString(cudaError_t(e)));
+  return OSCAR_OK;
+}
+
+oscar_status oscar_bf16_decode_attention(oscar_cache* c, int layer, const void* q, void* out, void* workspace,
+                                         size_t ws_bytes, float* out_f32, void* stream) {
+  g_launches = 0;
+  oscar_status st = check_decode(c, layer, q, out, workspace, ws_bytes);
+  if (st) return st;
+  if (is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_bf16_decode_attention needs the BF16 format");
+  int e = launch_bf16_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws,
+                             c->dec_n_req, c->dec_items, stream, &g_launches);
+  if (e) return fail(OSCAR_ERR_CUDA, "bf16 decode launch: %s", cudaGetErrorString(cudaError_t(e)));
+  return OSCAR_OK;
+}
+
+oscar_status oscar_get_status(oscar_cache* c, void* stream, uint32_t* flags) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  CUDA_TRY(cudaMemcpyAsync(c->h_status, c->base + c->lay.status, 4, cudaMemcpyDeviceToHost, s));
+  CUDA_TRY(cudaStreamSynchronize(s));
+  uint32_t f = c->h_status[0];
+  if (flags) *flags = f;
+  if (f) {
+    CUDA_TRY(cudaMemsetAsync(c->base + c->lay.status, 0, 4, s));
+    CUDA_TRY(cudaStreamSynchronize(s));
+    if (f & OSCAR_FLAG_TIMEOUT) return fail(OSCAR_ERR_TIMEOUT, "device flags 0x%x: a bounded wait gave up", f);
+    return fail(OSCAR_ERR_BAD_PAGE, "device flags 0x%x: an out-of-range page or slot was skipped", f);
+  }
+  return OSCAR_OK;
+}
+
+}  // extern "C"

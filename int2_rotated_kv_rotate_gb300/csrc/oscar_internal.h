@@ -1,0 +1,102 @@
+// Internal layout shared by the host side (oscar_host.cpp) and the kernels (*.cu).
+// Plain structs only; the C ABI is include/oscar.h.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "oscar.h"
+
+namespace oscar {
+
+constexpr int kHeadDim = 128;
+constexpr int kPage = 64;
+constexpr int kRowBytes = kHeadDim / 4;  // 32 B of 2-bit codes per token
+constexpr int kMaxWindow = 1024;
+
+// One request of an append plan (same for every layer).
+struct AppendReq {
+  int slot;        // request slot
+  int L0, H0;      // length and history end before the append
+  int L1, H1;      // after
+  int x_offset;    // first row of this request in k_new / v_new
+};
+
+// One work item of the append kernel.  kind 0: ring slots [begin, begin+count) of the
+// request (evict old occupant to INT2, then write new occupant); kind 1: new positions
+// [begin, begin+count) that go to sinks or directly to INT2.
+struct AppendItem {
+  int req;    // index into AppendReq array
+  int kind;
+  int begin;
+  int count;
+};
+
+// One request of a decode plan.
+struct DecodeReq {
+  int slot;
+  int L, H;          // length, history end (INT2 format); H = L for BF16 format
+  int first_item;    // items of this request, kv-head-major: first_item + kvh*items_per_head ..
+  int items_per_head;
+};
+
+// One split-K work item: pages [p0, p1) of the INT2 history (kind 0) or BF16 tokens
+// [t0, t1) of the sink+ring list (kind 1; index < S is sink j, else ring position H + j - S)
+// of request `req` (plan index), kv-head `kvh`.  Partial results go to slot `item`.
+struct DecodeItem {
+  int req;
+  int kvh;
+  int kind;
+  int begin;
+  int end;
+  int head_first;  // first partial slot of this (req, kvh)
+  int head_count;  // number of partial slots of this (req, kvh)
+  int pad;
+};
+
+struct DeviceLayout {
+  // pools (byte offsets in the device block)
+  size_t codes, sz, sink, ring, bf16_pages;
+  size_t codes_layer_stride, codes_page_stride, codes_head_stride;  // K at +0, V at +half
+  size_t sz_layer_stride, sz_page_stride, sz_head_stride;
+  size_t sink_slot_stride, sink_layer_stride, sink_head_stride;
+  size_t ring_slot_stride, ring_layer_stride, ring_head_stride;
+  size_t bf16_layer_stride, bf16_page_stride, bf16_head_stride;
+  // params
+  size_t R_K, R_V, R_Vt, clip_K, clip_V;  // fp32 [layer][H_kv][d][d] (R_Vt = R_V transposed), [layer][H_kv]
+  // control
+  size_t page_table;  // int32 [max_requests][max_pages_per_request]
+  size_t status;      // uint32 flags
+  size_t counters;    // uint32 [max_requests][H_kv] merge counters
+  size_t append_reqs, append_items, decode_reqs, decode_items;
+  size_t max_append_items, max_decode_items;
+  size_t total;
+};
+
+// Everything a kernel needs, passed by value.
+struct KernelParams {
+  uint8_t* base;
+  int n_q_heads, n_kv_heads, gqa, group, n_sink, window, n_layers;
+  int max_requests, max_pages, max_pages_per_request;
+  DeviceLayout lay;
+};
+
+// Decode workspace layout (per plan).
+struct DecodeWorkspace {
+  size_t qt;        // fp32 [n_req][H_q][d] rotated queries
+  size_t qsum;      // fp32 [n_req][H_q][4] per-group sums of q~
+  size_t partials;  // fp32 [n_items][G][d + 2] (m, l, o~)
+  size_t total;
+};
+
+// Launchers (defined in the .cu files); return a cudaError_t as int.
+int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_items,
+                  int rows_total, void* stream, int* launches);
+int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_reqs,
+                       int rows_total, void* stream, int* launches);
+int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
+                  const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches);
+int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
+                       const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches);
+
+}  // namespace oscar

@@ -1,0 +1,247 @@
+"""Parity of the CUDA path (through the C ABI) against the CPU oracle, on a GPU.
+
+INT2 code rows, scale/zero words, BF16 sinks and ring slots must match bit for bit;
+decode outputs must match the oracle's fp64 attention on the same stored values within
+max-abs 2e-2 and relative L2 5e-3 (fp32 output), and the bf16 output must be the
+round-to-nearest-even of the fp32 output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from int2_rotated_kv_rotate_gb300 import workloads as wl
+from int2_rotated_kv_rotate_gb300 import _native as N
+from oracle.model import bf16_reference
+
+from helpers import bits, check_pages, compare_decode, make_pair
+
+pytestmark = pytest.mark.gpu
+
+SEED = 1234
+
+
+def decode_and_compare(cache, oc, w, layer, slots, reqs, step, label, max_split_pages=0):
+    cache.plan(slots, max_split_pages=max_split_pages)
+    q = wl.gen_q(w, SEED, layer, step, len(slots), device="cuda")
+    out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    out = cache.decode(layer, q, out_f32=out32)
+    torch.cuda.synchronize()
+    st, flags = cache.status()
+    assert st == 0 and flags == 0, f"device flags {flags:#x}"
+    qb = bits(q)
+    for i, r in enumerate(reqs):
+        ref = oc.decode(layer, r, qb[i])
+        compare_decode(out32[i], out[i], ref, f"{label} req {r}")
+    return out32
+
+
+def append_both(cache, oc, w, layer, slots, reqs, starts, counts, stream_req=None):
+    ks, vs = [], []
+    for r, s0, n in zip(stream_req or reqs, starts, counts):
+        k, v = wl.gen_kv(w, SEED, layer, r, s0, n, device="cuda")
+        ks.append(k)
+        vs.append(v)
+    K = torch.cat(ks).contiguous()
+    V = torch.cat(vs).contiguous()
+    cache.quantize_append(layer, K, V)
+    kb, vb = bits(K), bits(V)
+    off = 0
+    for r, n in zip(reqs, counts):
+        oc.append(layer, r, kb[off:off + n], vb[off:off + n])
+        off += n
+
+
+def test_tiny_workload_full_context():
+    """Tiny workload: B1, 8q/2kv, 4096 tokens (4 sink + 128 recent + 3964 INT2), g128."""
+    w = wl.WORKLOADS["tiny"]
+    cache, oc, _ = make_pair(w, SEED, 1, 1, w.context)
+    slot = cache.alloc()
+    cache.reserve([slot], [w.context])
+    append_both(cache, oc, w, 0, [slot], [0], [0], [w.context])
+    cache.commit()
+    torch.cuda.synchronize()
+    check_pages(cache, oc, 0, slot, 0)
+    decode_and_compare(cache, oc, w, 0, [slot], [0], 0, "tiny")
+    # several split plans give the same answer within tolerance
+    for msp in (1, 3, 64):
+        decode_and_compare(cache, oc, w, 0, [slot], [0], 1, f"tiny split {msp}", max_split_pages=msp)
+
+
+@pytest.mark.parametrize("name,gqa,group,window,sink", [
+    ("g128_w128", 4, 128, 128, 4),
+    ("g32_w256", 4, 32, 256, 4),
+    ("gqa8_g128", 8, 128, 128, 4),
+    ("gqa8_g32", 8, 32, 64, 4),
+    ("no_window", 4, 128, 0, 4),
+    ("no_sink", 4, 128, 32, 0),
+])
+def test_chunked_appends_with_eviction(name, gqa, group, window, sink):
+    """Appends of many sizes (1 token to several pages) across the window: eviction,
+    direct-to-INT2 and sink routing, page boundaries; pages and decode after each step."""
+    base = wl.WORKLOADS["tiny"]
+    w = wl.scaled(base, name=f"chunks_{name}", n_q_heads=2 * gqa, group=group, window=window, n_sink=sink,
+                  lognormal_sigma=0.5)
+    sizes = [1, 2, 1, 60, 3, 64, 17, 128, 1, 200, 5, 64, 300, 1, 16]
+    total = sum(sizes)
+    cache, oc, _ = make_pair(w, SEED, 1, 1, total)
+    slot = cache.alloc()
+    pos = 0
+    for step, n in enumerate(sizes):
+        cache.reserve([slot], [n])
+        append_both(cache, oc, w, 0, [slot], [0], [pos], [n])
+        cache.commit()
+        pos += n
+        torch.cuda.synchronize()
+        check_pages(cache, oc, 0, slot, 0)
+        if step % 3 == 2 or step == len(sizes) - 1:
+            decode_and_compare(cache, oc, w, 0, [slot], [0], step, f"{name} step {step}")
+
+
+def test_short_contexts_and_empty_request():
+    """L < S (sinks only), L <= S + W (no INT2), L = 0 (zero output)."""
+    w = wl.scaled(wl.WORKLOADS["tiny"], name="short", lognormal_sigma=0.5)
+    cache, oc, _ = make_pair(w, SEED, 1, 4, 512)
+    slots = [cache.alloc() for _ in range(4)]
+    lens = [2, 4, 132, 0]
+    cache.reserve(slots[:3], lens[:3])
+    append_both(cache, oc, w, 0, slots[:3], [0, 1, 2], [0, 0, 0], lens[:3])
+    cache.commit()
+    cache.plan(slots)
+    q = wl.gen_q(w, SEED, 0, 0, 4, device="cuda")
+    out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    out = cache.decode(0, q, out_f32=out32)
+    torch.cuda.synchronize()
+    qb = bits(q)
+    for i in range(3):
+        check_pages(cache, oc, 0, slots[i], i)
+        compare_decode(out32[i], out[i], oc.decode(0, i, qb[i]), f"short L={lens[i]}")
+    assert not out32[3].any() and not out[3].float().any()
+
+
+def test_ragged_batch_with_prefix_sharing():
+    """Ragged batch, several requests in one append and one decode plan; a request that
+    maps another's prefix pages decodes exactly like a private copy of the same tokens."""
+    w = wl.scaled(wl.WORKLOADS["ragged_prefix"], batch=6, context=3000, ragged_min=300, prefix_tokens=1024,
+                  prefix_group=3, n_layers=2)
+    lens = [3000, 1700, 1100, 2500, 400, 1400]
+    n_layers = 2
+    cache, oc, params = make_pair(w, SEED, n_layers, 6, 3000 + 600)
+    slots = [cache.alloc() for _ in range(6)]
+    # requests 0 and 3 own their prefixes; 1, 2 share 0's, 4 and 5 share 3's when long enough
+    owners = [0, 3]
+    cache.reserve([slots[o] for o in owners], [lens[o] for o in owners])
+    for layer in range(n_layers):
+        append_both(cache, oc, w, layer, [slots[o] for o in owners], owners, [0, 0], [lens[o] for o in owners])
+    cache.commit()
+    shared = {}
+    for r in (1, 2, 4, 5):
+        src = 0 if r < 3 else 3
+        n_sh = wl.shared_prefix_tokens(w, lens[r])
+        if n_sh > 0:
+            cache.share_prefix(slots[r], slots[src], n_sh)
+            oc.share_prefix(r, src, n_sh)
+            shared[r] = n_sh
+            assert cache.pages(slots[r]) == cache.pages(slots[src])[: n_sh // 64]
+        else:
+            shared[r] = 0
+    rest = [r for r in (1, 2, 4, 5)]
+    cache.reserve([slots[r] for r in rest], [lens[r] - shared[r] for r in rest])
+    for layer in range(n_layers):
+        append_both(cache, oc, w, layer, [slots[r] for r in rest], rest, [shared[r] for r in rest],
+                    [lens[r] - shared[r] for r in rest])
+    cache.commit()
+    torch.cuda.synchronize()
+    for layer in range(n_layers):
+        for r in range(6):
+            check_pages(cache, oc, layer, slots[r], r)
+        decode_and_compare(cache, oc, w, layer, slots, list(range(6)), 0, f"ragged layer {layer}")
+    # one decode step with appends of 1 token for all and a 512-token chunk for two
+    n_new = [1, 512, 1, 1, 512, 1]
+    cache.reserve(slots, n_new)
+    for layer in range(n_layers):
+        append_both(cache, oc, w, layer, slots, list(range(6)), lens, n_new)
+    cache.commit()
+    torch.cuda.synchronize()
+    for layer in range(n_layers):
+        for r in range(6):
+            check_pages(cache, oc, layer, slots[r], r)
+        decode_and_compare(cache, oc, w, layer, slots, list(range(6)), 1, f"ragged step layer {layer}")
+
+
+def test_shared_prefix_bit_identical_to_private_copy():
+    """Same tokens, same lengths, same plan shape: a shared-prefix request's output equals
+    a private copy's bit for bit."""
+    w = wl.scaled(wl.WORKLOADS["tiny"], name="share_ident", lognormal_sigma=0.5)
+    cache, oc, _ = make_pair(w, SEED, 1, 3, 2048)
+    a, b, c = cache.alloc(), cache.alloc(), cache.alloc()
+    K, V = wl.gen_kv(w, SEED, 0, 0, 0, 2048, device="cuda")
+    cache.reserve([a, c], [1500, 1500])
+    cache.quantize_append(0, torch.cat([K[:1500], K[:1500]]), torch.cat([V[:1500], V[:1500]]))
+    cache.commit()
+    cache.share_prefix(b, a, 1024)
+    cache.reserve([b], [476])
+    cache.quantize_append(0, K[1024:1500].contiguous(), V[1024:1500].contiguous())
+    cache.commit()
+    q = wl.gen_q(w, SEED, 0, 0, 1, device="cuda")
+    outs = []
+    for s in (b, c):
+        cache.plan([s], max_split_pages=5)
+        o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        cache.decode(0, q, out_f32=o)
+        outs.append(o)
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0], outs[1])
+    # freeing the prefix owner keeps the sharer's pages alive (reference counts)
+    cache.free(a)
+    cache.plan([b], max_split_pages=5)
+    o = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    cache.decode(0, q, out_f32=o)
+    torch.cuda.synchronize()
+    assert torch.equal(o, outs[0])
+
+
+@pytest.mark.parametrize("gqa", [4, 8])
+def test_bf16_comparison_path(gqa):
+    """Uncompressed BF16 pages: decode equals plain softmax attention on the bf16 tokens."""
+    w = wl.scaled(wl.WORKLOADS["tiny"], name=f"bf16_{gqa}", n_q_heads=2 * gqa, lognormal_sigma=0.5)
+    lens = [1000, 77, 1]
+    cache, _, _ = make_pair(w, SEED, 1, 3, 1000, fmt=N.OSCAR_FORMAT_BF16)
+    slots = [cache.alloc() for _ in lens]
+    Ks, Vs = [], []
+    for r, n in enumerate(lens):
+        k, v = wl.gen_kv(w, SEED, 0, r, 0, n, device="cuda")
+        Ks.append(k)
+        Vs.append(v)
+    cache.reserve(slots, lens)
+    cache.bf16_append(0, torch.cat(Ks).contiguous(), torch.cat(Vs).contiguous())
+    cache.commit()
+    cache.plan(slots, max_split_pages=4)
+    q = wl.gen_q(w, SEED, 0, 0, 3, device="cuda")
+    out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    out = cache.decode(0, q, out_f32=out32)
+    torch.cuda.synchronize()
+    qb = bits(q)
+    for r in range(3):
+        ref = bf16_reference(qb[r], bits(Ks[r]), bits(Vs[r]))
+        compare_decode(out32[r], out[r], ref, f"bf16 req {r}")
+
+
+def test_bad_page_entry_is_flagged_not_faulting():
+    """A page-table entry out of range (written on the host) is skipped and flagged."""
+    w = wl.WORKLOADS["tiny"]
+    cache, oc, _ = make_pair(w, SEED, 1, 1, 1024)
+    slot = cache.alloc()
+    cache.reserve([slot], [1024])
+    append_both(cache, oc, w, 0, [slot], [0], [0], [1024])
+    cache.commit()
+    torch.cuda.synchronize()
+    # corrupt logical page 3 of the request in the device page table (host-side write)
+    row = cache.layout.page_table + slot * cache.cfg.max_pages_per_request * 4
+    bad = torch.tensor([cache.cfg.max_pages + 5], dtype=torch.int32).view(torch.uint8).cuda()
+    cache.mem[row + 3 * 4: row + 4 * 4] = bad
+    cache.plan([slot], max_split_pages=2)
+    q = wl.gen_q(w, SEED, 0, 0, 1, device="cuda")
+    out = cache.decode(0, q)
+    st, flags = cache.status()
+    assert flags & N.OSCAR_FLAG_BAD_PAGE and st == 4
+    assert torch.isfinite(out.float()).all()
