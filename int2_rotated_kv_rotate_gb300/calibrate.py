@@ -124,3 +124,38 @@ def calibrate_layer(q, k, v, percentile: float = 99.9):
     for h in range(Hkv):
         RK[h], RV[h], cK[h], cV[h] = calibrate_kv_head(q[:, h * G:(h + 1) * G], k[:, h], v[:, h], percentile)
     return RK, RV, cK, cV
+
+
+def calibrate_layer_device(q, k, v, percentile: float = 99.9):
+    """Same calibration with the heavy products on the tensors' device (torch): the causal
+    attention in fp32, covariances and rotated activations in fp64, eigendecomposition
+    on the host in fp64.  q [N, H_q, d], k and v [N, H_kv, d] torch tensors.
+    Returns fp32 numpy R_K, R_V [H_kv, d, d] and clip_K, clip_V [H_kv]."""
+    import torch
+
+    n, Hq, d = q.shape
+    Hkv = k.shape[1]
+    G = Hq // Hkv
+    qf, kf, vf = q.float(), k.float(), v.float()
+    future = torch.ones(n, n, dtype=torch.bool, device=q.device).triu(1)
+    RK = np.empty((Hkv, d, d), np.float32)
+    RV = np.empty((Hkv, d, d), np.float32)
+    cK = np.empty(Hkv, np.float32)
+    cV = np.empty(Hkv, np.float32)
+    num, den = _decimal_ratio(percentile)
+    for h in range(Hkv):
+        Qh = qf[:, h * G:(h + 1) * G, :]
+        flat = Qh.reshape(-1, d).double()
+        C_Q = (flat.T @ flat) / (n * G)
+        logits = torch.einsum("ngd,md->gnm", Qh, kf[:, h]) / math.sqrt(d)
+        logits.masked_fill_(future, float("-inf"))
+        O = torch.softmax(logits, dim=-1) @ vf[:, h]
+        Of = O.reshape(-1, d).double()
+        C_S = (Of.T @ Of) / (n * G)
+        RK[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_Q.cpu().numpy())).astype(np.float32)
+        RV[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_S.cpu().numpy())).astype(np.float32)
+        for R, X, out in ((RK[h], kf[:, h], cK), (RV[h], vf[:, h], cV)):
+            rot = (X.double() @ torch.from_numpy(R).to(X.device).double()).abs().flatten()
+            rank = max(1, -(-(num * rot.numel()) // (den * 100)))
+            out[h] = np.float32(torch.kthvalue(rot, rank).values.item())
+    return RK, RV, cK, cV

@@ -138,12 +138,8 @@ __device__ void quantize_tokens(Smem& sm, const float (&x)[kTok], const KernelPa
 }
 
 template <int GROUP>
-__global__ void __launch_bounds__(128) append_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ k_new,
-                                                     const uint16_t* __restrict__ v_new) {
-  __shared__ Smem sm;
-  pdl_wait();
-  pdl_trigger();
-  const AppendItem it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[blockIdx.x];
+__device__ void append_item(Smem& sm, const KernelParams& kp, int layer, const AppendItem& it,
+                            const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new) {
   const AppendReq a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];
   const int kvh = blockIdx.y, kv = blockIdx.z, j = threadIdx.x;
   if (a.slot < 0 || a.slot >= kp.max_requests) {
@@ -250,17 +246,33 @@ __global__ void __launch_bounds__(128) append_kernel(KernelParams kp, int layer,
   if (n_q > 0) quantize_tokens<GROUP>(sm, xq, kp, a.slot, layer, kvh, kv);
 }
 
+template <int GROUP>
+__global__ void __launch_bounds__(128) append_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ k_new,
+                                                     const uint16_t* __restrict__ v_new) {
+  __shared__ Smem sm;
+  pdl_wait();
+  pdl_trigger();
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[0];
+  for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
+    const AppendItem it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
+    append_item<GROUP>(sm, kp, layer, it, k_new, v_new);
+    __syncthreads();  // shared memory is reused by the next item
+  }
+}
+
 // Plain BF16 pages: copy K and V rows of new positions into [page][kvh][K|V][64][d].
 __global__ void __launch_bounds__(128) bf16_append_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ k_new,
                                                           const uint16_t* __restrict__ v_new) {
   pdl_wait();
   pdl_trigger();
-  const AppendItem it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[blockIdx.x];
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[0];
+  for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
+  const AppendItem it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
   const AppendReq a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];
   const int kvh = blockIdx.y, kv = blockIdx.z;
   if (a.slot < 0 || a.slot >= kp.max_requests) {
     if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
-    return;
+    continue;
   }
   const uint16_t* X = kv ? v_new : k_new;
   for (int e = threadIdx.x; e < it.count * 16; e += blockDim.x) {
@@ -284,14 +296,14 @@ __global__ void __launch_bounds__(128) bf16_append_kernel(KernelParams kp, int l
                    size_t(kv) * (kPage * kHeadDim * 2) + size_t(p % kPage) * (kHeadDim * 2);
     reinterpret_cast<uint4*>(dst)[c16] = v;
   }
+  }
 }
 
 }  // namespace
 
-int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_items, int rows_total,
-                  void* stream, int* launches) {
-  (void)rows_total;
-  dim3 grid(n_items, kp.n_kv_heads, 2);
+int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid_x, void* stream,
+                  int* launches) {
+  dim3 grid(grid_x, kp.n_kv_heads, 2);
   const uint16_t* k = static_cast<const uint16_t*>(k_new);
   const uint16_t* v = static_cast<const uint16_t*>(v_new);
   int e = kp.group == 32 ? launch_ex(append_kernel<32>, grid, dim3(128), 0, stream, kp, layer, k, v)
@@ -300,10 +312,9 @@ int launch_append(const KernelParams& kp, int layer, const void* k_new, const vo
   return e;
 }
 
-int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_items,
-                       int rows_total, void* stream, int* launches) {
-  (void)rows_total;
-  dim3 grid(n_items, kp.n_kv_heads, 2);
+int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid_x,
+                       void* stream, int* launches) {
+  dim3 grid(grid_x, kp.n_kv_heads, 2);
   int e = launch_ex(bf16_append_kernel, grid, dim3(128), 0, stream, kp, layer, static_cast<const uint16_t*>(k_new),
                     static_cast<const uint16_t*>(v_new));
   if (!e) *launches += 1;

@@ -20,76 +20,91 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
                                                          float* __restrict__ partials, uint16_t* __restrict__ out,
                                                          float* __restrict__ out_f32) {
   __shared__ float qs[G * kHeadDim];
-  __shared__ __align__(16) uint8_t scratch[G * 32 * 4 + G * kHeadDim * 4];
+  __shared__ __align__(16) uint8_t scratch[G * 32 * 4];
   __shared__ int s_last;
-  const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[blockIdx.x];
-  const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
   pdl_wait();
   pdl_trigger();
-  const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-  float* part = partials + size_t(blockIdx.x) * G * (kHeadDim + 2);
-  for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[e] = bf16_f32(q[head0 * kHeadDim + e]);
-  __syncthreads();
-  const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
-  if (!slot_ok && threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
-  int t0 = 0, t1 = 0;
-  if (slot_ok && it.kind == 0) {
-    t0 = it.begin * kPage;
-    t1 = min(it.end * kPage, dr.L);
-  }
-  const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(max(dr.slot, 0)) * kp.max_pages_per_request;
-  const uint8_t* head_base = kp.base + kp.lay.bf16_pages + size_t(layer) * kp.lay.bf16_layer_stride +
-                             size_t(it.kvh) * kp.lay.bf16_head_stride;
-  // a bad page id reads page 0 of the pool instead and raises the flag
-  auto page_of = [=](int u) -> const uint16_t* {
-    int phys = ptab[u / kPage];
-    if (phys < 0 || phys >= kp.max_pages) {
-      flag(kp, OSCAR_FLAG_BAD_PAGE);
-      phys = 0;
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
+  for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
+    const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
+    const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
+    const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
+    float* part = partials + size_t(ix) * G * (kHeadDim + 2);
+    for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[e] = bf16_f32(q[head0 * kHeadDim + e]);
+    __syncthreads();
+    const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
+    if (!slot_ok && threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+    int t0 = 0, t1 = 0;
+    if (slot_ok && it.kind == 0) {
+      t0 = it.begin * kPage;
+      t1 = min(it.end * kPage, dr.L);
     }
-    return reinterpret_cast<const uint16_t*>(head_base + size_t(phys) * kp.lay.bf16_page_stride);
-  };
-  auto rowK = [=](int u) { return page_of(u) + size_t(u % kPage) * kHeadDim; };
-  auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
-  rows_attention<G>(rowK, rowV, t0, t1, qs, part, scratch);
+    const int* ptab =
+        reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(slot_ok ? dr.slot : 0) * kp.max_pages_per_request;
+    const uint8_t* head_base = kp.base + kp.lay.bf16_pages + size_t(layer) * kp.lay.bf16_layer_stride +
+                               size_t(it.kvh) * kp.lay.bf16_head_stride;
+    // a bad page id reads page 0 of the pool instead and raises the flag
+    auto page_of = [=](int u) -> const uint16_t* {
+      int phys = ptab[u / kPage];
+      if (phys < 0 || phys >= kp.max_pages) {
+        flag(kp, OSCAR_FLAG_BAD_PAGE);
+        phys = 0;
+      }
+      return reinterpret_cast<const uint16_t*>(head_base + size_t(phys) * kp.lay.bf16_page_stride);
+    };
+    auto rowK = [=](int u) { return page_of(u) + size_t(u % kPage) * kHeadDim; };
+    auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
+    rows_attention<G>(rowK, rowV, t0, t1, qs, part, scratch);
 
-  __threadfence();
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned* ctr = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
-    const unsigned prev = atomicAdd(ctr, 1u);
-    s_last = prev == unsigned(it.head_count - 1);
-    if (s_last) *ctr = 0u;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  const int c = threadIdx.x;
-  for (int h = 0; h < G; ++h) {
-    float ms = -INFINITY;
-    for (int i = 0; i < it.head_count; ++i)
-      ms = fmaxf(ms, __ldcg(partials + size_t(it.head_first + i) * G * (kHeadDim + 2) + h * (kHeadDim + 2)));
-    float l = 0.f, o = 0.f;
-    for (int i = 0; i < it.head_count; ++i) {
-      const float* ph = partials + size_t(it.head_first + i) * G * (kHeadDim + 2) + h * (kHeadDim + 2);
-      const float m = __ldcg(ph);
-      if (m == -INFINITY) continue;
-      const float w = ex2(m - ms);
-      l = fmaf(w, __ldcg(ph + 1), l);
-      o = fmaf(w, __ldcg(ph + 2 + c), o);
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned* ctr = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
+      const unsigned prev = atomicAdd(ctr, 1u);
+      s_last = prev == unsigned(it.head_count - 1);
+      if (s_last) *ctr = 0u;
     }
-    const float r = l > 0.f ? o / l : 0.f;
-    out[(head0 + h) * kHeadDim + c] = bf16_rne(r);
-    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = r;
+    __syncthreads();
+    if (s_last) {
+      __threadfence();
+      const int c = threadIdx.x;
+      for (int h = 0; h < G; ++h) {
+        float ms = -INFINITY;
+        for (int i = 0; i < it.head_count; ++i)
+          ms = fmaxf(ms, __ldcg(partials + size_t(it.head_first + i) * G * (kHeadDim + 2) + h * (kHeadDim + 2)));
+        float l = 0.f, o = 0.f;
+        for (int i = 0; i < it.head_count; ++i) {
+          const float* ph = partials + size_t(it.head_first + i) * G * (kHeadDim + 2) + h * (kHeadDim + 2);
+          const float m = __ldcg(ph);
+          if (m == -INFINITY) continue;
+          const float w = ex2(m - ms);
+          l = fmaf(w, __ldcg(ph + 1), l);
+          o = fmaf(w, __ldcg(ph + 2 + c), o);
+        }
+        const float r = l > 0.f ? o / l : 0.f;
+        out[(head0 + h) * kHeadDim + c] = bf16_rne(r);
+        if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = r;
+      }
+    }
+    __syncthreads();
   }
 }
 
 template <int G>
 int launch_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-             const DecodeWorkspace& wl, int n_items, void* stream, int* launches) {
+             const DecodeWorkspace& wl, int n_items, int n_sm, void* stream, int* launches) {
   float* partials = reinterpret_cast<float*>(ws + wl.partials);
-  int e = launch_ex(bf16_split_kernel<G>, dim3(n_items), dim3(128), 0, stream, kp, layer,
-                    static_cast<const uint16_t*>(q), partials, static_cast<uint16_t*>(out), out_f32);
+  static int resident = 0;
+  if (resident == 0) {
+    int per_sm = 0;
+    int e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf16_split_kernel<G>, 128, 0));
+    if (e) return e;
+    resident = (per_sm > 0 ? per_sm : 1) * n_sm;
+  }
+  (void)n_items;
+  const int grid = resident;  // persistent-style: CTAs loop over the plan's items
+  int e = launch_ex(bf16_split_kernel<G>, dim3(grid), dim3(128), 0, stream, kp, layer, static_cast<const uint16_t*>(q),
+                    partials, static_cast<uint16_t*>(out), out_f32);
   if (!e) *launches += 1;
   return e;
 }
@@ -97,10 +112,10 @@ int launch_t(const KernelParams& kp, int layer, const void* q, void* out, float*
 }  // namespace
 
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                       const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches) {
+                       const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
   (void)n_req;
-  if (kp.gqa == 4) return launch_t<4>(kp, layer, q, out, out_f32, ws, wl, n_items, stream, launches);
-  if (kp.gqa == 8) return launch_t<8>(kp, layer, q, out, out_f32, ws, wl, n_items, stream, launches);
+  if (kp.gqa == 4) return launch_t<4>(kp, layer, q, out, out_f32, ws, wl, n_items, n_sm, stream, launches);
+  if (kp.gqa == 8) return launch_t<8>(kp, layer, q, out, out_f32, ws, wl, n_items, n_sm, stream, launches);
   return int(cudaErrorInvalidValue);
 }
 

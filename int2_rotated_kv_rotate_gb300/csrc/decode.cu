@@ -124,7 +124,7 @@ struct Cfg {
   static constexpr int kSzBytes = 2 * kPage * NG * 4;       // K then V (scale, zero)
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
-  static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers and flags
+  static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers (128 B) and the merge flag
 };
 
 // Merge all partials of (request, kv-head), rotate back and store.  128 threads.
@@ -211,7 +211,8 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
 // [S, H) inside those pages are masked.  Warp w takes pages begin + w, + kWarps, ...
 template <int G, int GROUP>
 __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
-                                const float* qt_head0, const float* qsum_head0, float* part, uint8_t* smem) {
+                                const float* qt_head0, const float* qsum_head0, float* part, uint8_t* smem,
+                                uint32_t& phase_bits) {
   using C = Cfg<G, GROUP>;
   constexpr int NG = C::NG, NT = C::NT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -244,8 +245,8 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     }
     return true;
   };
-  uint32_t ok_mask = 0;     // bit st: stage st has a copy in flight
-  uint32_t phase_bits = 0;  // bit st: parity of the next completion of stage st's barrier
+  uint32_t ok_mask = 0;  // bit st: stage st has a copy in flight
+  // phase_bits (kept across items): bit st = parity of the next completion of stage st
   for (int k = 0; k < min(kStages, n_my); ++k)
     if (issue(k)) ok_mask |= 1u << k;
 
@@ -453,7 +454,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   if (broken) {
     // drain copies still in flight (bounded) before the stages are reused or the CTA exits
     for (int st = 0; st < kStages; ++st)
-      if ((ok_mask >> st) & 1u) mbar_wait(smem_u32(&bars[st]), (phase_bits >> st) & 1u);
+      if (((ok_mask >> st) & 1u) && mbar_wait(smem_u32(&bars[st]), (phase_bits >> st) & 1u)) phase_bits ^= 1u << st;
   }
 
   // ---- per-warp results -> shared memory, then merge the 4 warps into the partial
@@ -529,9 +530,7 @@ __global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, 
                                                     uint16_t* __restrict__ out, float* __restrict__ out_f32) {
   extern __shared__ __align__(128) uint8_t smem[];
   using C = Cfg<G, GROUP>;
-  __shared__ int s_last;
-  const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[blockIdx.x];
-  const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
+  int* s_last = reinterpret_cast<int*>(smem + C::kPipeBytes + kWarps * kStages * 8);
   if (threadIdx.x == 0) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
     for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -540,34 +539,45 @@ __global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, 
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  float* part = partials + size_t(blockIdx.x) * G * (kHeadDim + 2);
-  const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-  if (dr.slot < 0 || dr.slot >= kp.max_requests) {
-    if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
-    for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += 128) part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
-  } else if (it.kind == 0) {
-    int2_pages_item<G, GROUP>(kp, layer, it, dr, qt + head0 * kHeadDim, qsum + head0 * 4, part, smem);
-  } else {
-    bf16_tokens_item<G>(kp, layer, it, dr, qt + head0 * kHeadDim, part, smem);
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
+  uint32_t phase_bits = 0;
+  for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
+    const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
+    const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
+    float* part = partials + size_t(ix) * G * (kHeadDim + 2);
+    const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
+    if (dr.slot < 0 || dr.slot >= kp.max_requests) {
+      if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+      for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += 128)
+        part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
+    } else if (it.kind == 0) {
+      int2_pages_item<G, GROUP>(kp, layer, it, dr, qt + head0 * kHeadDim, qsum + head0 * 4, part, smem, phase_bits);
+    } else {
+      bf16_tokens_item<G>(kp, layer, it, dr, qt + head0 * kHeadDim, part, smem);
+    }
+    // ---- the last CTA of this (request, kv-head) merges and stores
+    __threadfence();  // this thread's partial stores are visible device-wide before the count
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned* ctr = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
+      const unsigned prev = atomicAdd(ctr, 1u);
+      *s_last = prev == unsigned(it.head_count - 1);
+      if (*s_last) *ctr = 0u;  // every partial has arrived; ready for the next launch
+    }
+    __syncthreads();
+    if (*s_last) {
+      __threadfence();
+      merge_and_store<G>(kp, layer, it, dr, partials, out, out_f32, reinterpret_cast<float*>(smem));
+    }
+    // generic-proxy use of the stage memory is over before the next item's bulk copies
+    fence_proxy_async();
+    __syncthreads();
   }
-  // ---- the last CTA of this (request, kv-head) merges and stores
-  __threadfence();  // this thread's partial stores are visible device-wide before the count
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned* ctr = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
-    const unsigned prev = atomicAdd(ctr, 1u);
-    s_last = prev == unsigned(it.head_count - 1);
-    if (s_last) *ctr = 0u;  // every partial has arrived; ready for the next layer
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  merge_and_store<G>(kp, layer, it, dr, partials, out, out_f32, reinterpret_cast<float*>(smem));
 }
 
 template <int G, int GROUP>
 int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                    const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches) {
+                    const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
   using C = Cfg<G, GROUP>;
   float* qt = reinterpret_cast<float*>(ws + wl.qt);
   float* qsum = reinterpret_cast<float*>(ws + wl.qsum);
@@ -576,13 +586,20 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
                     static_cast<const uint16_t*>(q), qt, qsum);
   if (e) return e;
   *launches += 1;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
+  if (resident == 0) {
     e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     if (e) return e;
-    attr_set = true;
+    int per_sm = 0;
+    e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP>, 128, C::kSmemBytes));
+    if (e) return e;
+    resident = (per_sm > 0 ? per_sm : 1) * n_sm;
   }
-  e = launch_ex(split_kernel<G, GROUP>, dim3(n_items), dim3(128), size_t(C::kSmemBytes), stream, kp, layer,
+  // persistent-style grid: every resident CTA slot, each looping over work items, so a
+  // captured launch serves later plans with other item counts
+  (void)n_items;
+  const int grid = resident;
+  e = launch_ex(split_kernel<G, GROUP>, dim3(grid), dim3(128), size_t(C::kSmemBytes), stream, kp, layer,
                 static_cast<const float*>(qt), static_cast<const float*>(qsum), partials, static_cast<uint16_t*>(out),
                 out_f32);
   if (!e) *launches += 1;
@@ -592,15 +609,15 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
 }  // namespace
 
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                  const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches) {
+                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
   if (kp.gqa == 4 && kp.group == 128)
-    return launch_decode_t<4, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+    return launch_decode_t<4, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
   if (kp.gqa == 4 && kp.group == 32)
-    return launch_decode_t<4, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+    return launch_decode_t<4, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
   if (kp.gqa == 8 && kp.group == 128)
-    return launch_decode_t<8, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+    return launch_decode_t<8, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
   if (kp.gqa == 8 && kp.group == 32)
-    return launch_decode_t<8, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, stream, launches);
+    return launch_decode_t<8, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
   return int(cudaErrorInvalidValue);
 }
 

@@ -114,6 +114,7 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.page_table = take(reqs * size_t(c.max_pages_per_request) * 4);
   L.status = take(256);
   L.counters = take(reqs * Hkv * 4);
+  L.plan_counts = take(16);
   L.max_append_items = kMaxAppendTokenItems + reqs * (kMaxWindow / kAppendChunk);
   L.max_decode_items = reqs * Hkv * (2 + kMaxWindow / kBf16ItemTokens) + 16384;
   L.append_reqs = take(reqs * sizeof(AppendReq));
@@ -145,6 +146,7 @@ struct oscar_cache {
   uint8_t* h_staging = nullptr;
   size_t staging_bytes = 0;
   uint32_t* h_status = nullptr;
+  int32_t* h_counts = nullptr;  // pinned: [append items, decode items, decode requests, 0]
   cudaEvent_t upload_done = nullptr;
   bool upload_pending = false;
   // pending append
@@ -153,6 +155,7 @@ struct oscar_cache {
   int app_items = 0, app_rows = 0;
   // decode plan
   bool planned = false;
+  bool planned_with_reservation = false;  // the plan already counts the reserved tokens
   int dec_n_req = 0, dec_items = 0, dec_bf16_items = 0, dec_max_pages = 0;
   DecodeWorkspace ws{};
 };
@@ -253,6 +256,9 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_page_table), pt_bytes);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_staging), c->staging_bytes);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_status), 256);
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_counts), 64);
+  if (e == cudaSuccess) std::memset(c->h_counts, 0, 64);
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.plan_counts, 0, 16);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->upload_done, cudaEventDisableTiming);
   if (e == cudaSuccess) {
     std::memset(c->h_page_table, 0xff, pt_bytes);  // -1 = unmapped
@@ -282,6 +288,7 @@ void oscar_cache_destroy(oscar_cache* c) {
   if (c->h_page_table) cudaFreeHost(c->h_page_table);
   if (c->h_staging) cudaFreeHost(c->h_staging);
   if (c->h_status) cudaFreeHost(c->h_status);
+  if (c->h_counts) cudaFreeHost(c->h_counts);
   delete c;
 }
 
@@ -495,6 +502,8 @@ oscar_status oscar_reserve(oscar_cache* c, const int* slots, const int* n_new, i
   if (st) return st;
   std::memcpy(c->h_staging, reqs.data(), reqs.size() * sizeof(AppendReq));
   std::memcpy(c->h_staging + align256(reqs.size() * sizeof(AppendReq)), items.data(), items.size() * sizeof(AppendItem));
+  c->h_counts[0] = int(items.size());
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.plan_counts, c->h_counts, 4, cudaMemcpyHostToDevice, s));
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.append_reqs, c->h_staging, reqs.size() * sizeof(AppendReq),
                            cudaMemcpyHostToDevice, s));
   if (!items.empty())
@@ -506,6 +515,8 @@ oscar_status oscar_reserve(oscar_cache* c, const int* slots, const int* n_new, i
   c->app_items = int(items.size());
   c->app_rows = int(rows);
   c->reserved = true;
+  c->planned = false;  // lengths change: plan again (a plan made now counts the new tokens)
+  c->planned_with_reservation = false;
   return OSCAR_OK;
 }
 
@@ -517,7 +528,8 @@ oscar_status oscar_commit_append(oscar_cache* c) {
     c->reqs[a.slot].H = a.H1;
   }
   c->reserved = false;
-  c->planned = false;
+  if (!c->planned_with_reservation) c->planned = false;
+  c->planned_with_reservation = false;
   return OSCAR_OK;
 }
 
@@ -529,7 +541,7 @@ oscar_status oscar_quantize_append(oscar_cache* c, int layer, const void* k_new,
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
   if (c->app_items == 0) return OSCAR_OK;
-  int e = launch_append(kernel_params(c), layer, k_new, v_new, c->app_items, c->app_rows, stream, &g_launches);
+  int e = launch_append(kernel_params(c), layer, k_new, v_new, std::min(c->app_items, 4 * c->n_sm), stream, &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "append launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }
@@ -542,7 +554,8 @@ oscar_status oscar_bf16_append(oscar_cache* c, int layer, const void* k_new, con
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
   if (c->app_items == 0) return OSCAR_OK;
-  int e = launch_bf16_append(kernel_params(c), layer, k_new, v_new, c->app_items, c->app_rows, stream, &g_launches);
+  int e = launch_bf16_append(kernel_params(c), layer, k_new, v_new, std::min(c->app_items, 4 * c->n_sm), stream,
+                             &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "bf16 append launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }
@@ -550,10 +563,11 @@ oscar_status oscar_bf16_append(oscar_cache* c, int layer, const void* k_new, con
 oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int max_split_pages, void* stream) {
   if (!c || !slots || n_req <= 0 || n_req > c->cfg.max_requests)
     return fail(OSCAR_ERR_INVALID_ARG, "bad plan arguments");
-  if (c->reserved) return fail(OSCAR_ERR_STATE, "commit the pending append before planning a decode");
   if (max_split_pages < 0) return fail(OSCAR_ERR_INVALID_ARG, "max_split_pages < 0");
   std::vector<char> seen(c->cfg.max_requests, 0);
   const int Hkv = c->cfg.n_kv_heads, S = is_int2(c) ? c->cfg.n_sink : 0;
+  // lengths the decode will see: a pending reservation's tokens count (append before decode)
+  std::vector<int> Ls(n_req), Hs(n_req);
   long long total_pages = 0;
   for (int i = 0; i < n_req; ++i) {
     oscar_status st = check_slot(c, slots[i]);
@@ -561,7 +575,15 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     if (seen[slots[i]]) return fail(OSCAR_ERR_INVALID_ARG, "slot %d listed twice", slots[i]);
     seen[slots[i]] = 1;
     const Request& r = c->reqs[slots[i]];
-    total_pages += (long long)Hkv * pages_needed(c, r.L, r.H);
+    Ls[i] = r.L;
+    Hs[i] = r.H;
+    if (c->reserved)
+      for (const AppendReq& a : c->app_reqs)
+        if (a.slot == slots[i]) {
+          Ls[i] = a.L1;
+          Hs[i] = a.H1;
+        }
+    total_pages += (long long)Hkv * pages_needed(c, Ls[i], Hs[i]);
   }
   int chunk = max_split_pages;
   if (chunk == 0) {
@@ -572,13 +594,12 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   std::vector<DecodeItem> items;
   int n_bf16 = 0, max_pages = 0;
   for (int i = 0; i < n_req; ++i) {
-    const Request& r = c->reqs[slots[i]];
     DecodeReq& q = reqs[i];
     q.slot = slots[i];
-    q.L = r.L;
-    q.H = is_int2(c) ? r.H : r.L;
-    const int np = pages_needed(c, r.L, q.H);
-    const int n_bf = is_int2(c) ? std::min(r.L, S) + std::max(0, r.L - r.H) : 0;
+    q.L = Ls[i];
+    q.H = is_int2(c) ? Hs[i] : Ls[i];
+    const int np = pages_needed(c, q.L, q.H);
+    const int n_bf = is_int2(c) ? std::min(q.L, S) + std::max(0, q.L - q.H) : 0;
     const int n_bf_items = n_bf > 0 ? ceil_div(n_bf, kBf16ItemTokens) : 0;
     const int n_pg_items = np > 0 ? ceil_div(np, chunk) : 0;
     int per_head = n_bf_items + n_pg_items;
@@ -610,6 +631,9 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   const size_t rb = reqs.size() * sizeof(DecodeReq);
   std::memcpy(c->h_staging, reqs.data(), rb);
   std::memcpy(c->h_staging + align256(rb), items.data(), items.size() * sizeof(DecodeItem));
+  c->h_counts[1] = int(items.size());
+  c->h_counts[2] = n_req;
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.plan_counts + 4, c->h_counts + 1, 8, cudaMemcpyHostToDevice, s));
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_reqs, c->h_staging, rb, cudaMemcpyHostToDevice, s));
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_items, c->h_staging + align256(rb), items.size() * sizeof(DecodeItem),
                            cudaMemcpyHostToDevice, s));
@@ -631,6 +655,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   c->dec_bf16_items = n_bf16;
   c->dec_max_pages = max_pages;
   c->planned = true;
+  c->planned_with_reservation = c->reserved;
   return OSCAR_OK;
 }
 
@@ -662,7 +687,7 @@ oscar_status oscar_decode_attention(oscar_cache* c, int layer, const void* q, vo
   if (st) return st;
   if (!is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_decode_attention needs the INT2 format");
   int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_n_req,
-                        c->dec_items, stream, &g_launches);
+                        c->dec_items, c->n_sm, stream, &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "decode launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }
@@ -674,7 +699,7 @@ oscar_status oscar_bf16_decode_attention(oscar_cache* c, int layer, const void* 
   if (st) return st;
   if (is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_bf16_decode_attention needs the BF16 format");
   int e = launch_bf16_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws,
-                             c->dec_n_req, c->dec_items, stream, &g_launches);
+                             c->dec_n_req, c->dec_items, c->n_sm, stream, &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "bf16 decode launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }

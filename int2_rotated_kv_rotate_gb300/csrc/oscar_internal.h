@@ -68,6 +68,7 @@ struct DeviceLayout {
   size_t page_table;  // int32 [max_requests][max_pages_per_request]
   size_t status;      // uint32 flags
   size_t counters;    // uint32 [max_requests][H_kv] merge counters
+  size_t plan_counts; // int32 [4]: append items, decode items, decode requests, unused
   size_t append_reqs, append_items, decode_reqs, decode_items;
   size_t max_append_items, max_decode_items;
   size_t total;
@@ -90,13 +91,16 @@ struct DecodeWorkspace {
 };
 
 // Launchers (defined in the .cu files); return a cudaError_t as int.
-int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_items,
-                  int rows_total, void* stream, int* launches);
-int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_reqs,
-                       int rows_total, void* stream, int* launches);
+// Work-item counts live in device memory (plan_counts); `grid` is the number of CTAs the
+// host launches, each CTA loops over items blockIdx.x, + gridDim.x, ... so a captured
+// launch stays valid when a later plan has a different item count.
+int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid, void* stream,
+                  int* launches);
+int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid, void* stream,
+                       int* launches);
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                  const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches);
+                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                       const DecodeWorkspace& wl, int n_req, int n_items, void* stream, int* launches);
+                       const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
 
 }  // namespace oscar
