@@ -185,6 +185,24 @@ oscar_status oscar_bf16_append(oscar_cache* cache, int layer, const void* k_new,
 oscar_status oscar_bf16_decode_attention(oscar_cache* cache, int layer, const void* q, void* out, void* workspace,
                                          size_t ws_bytes, float* out_f32, void* stream);
 
+/* oscar_decode_attention without a caller workspace.  The paper has no counterpart:
+ * this exists for callers that cannot allocate device memory themselves, for example a
+ * plugin whose host framework owns every device allocation and gives it none, or a
+ * serving loop that must not allocate once it is running, and so cannot supply the
+ * decode workspace.  The scratch is instead a fixed 8 MiB array inside the library
+ * (static device memory, held on every GPU that loads the library until exit).
+ *   - Same semantics, inputs and outputs as oscar_decode_attention (q, out, out_f32).
+ *   - Returns OSCAR_ERR_INVALID_ARG, launching nothing, when the current plan needs more
+ *     than 8 MiB (oscar_decode_workspace_bytes tells the need).
+ *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
+ *   - The first call on a device looks up the array's device address (with that device
+ *     current); make that first call before any stream capture.
+ *   - Every call, on every cache and stream, shares the one array and leaves its
+ *     contents behind; nothing in it needs to start at zero.  Calls that overlap on the
+ *     GPU race on it: order them on one stream or serialise them. */
+oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int layer, const void* q, void* out, float* out_f32,
+                                            void* stream);
+
 /* Synchronises `stream`, returns the device status word in *flags (OSCAR_FLAG_*) and
  * clears it.  Returns OSCAR_ERR_BAD_PAGE / OSCAR_ERR_TIMEOUT if a flag was set. */
 oscar_status oscar_get_status(oscar_cache* cache, void* stream, uint32_t* flags);

@@ -29,6 +29,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "common.cuh"
 #include "oscar_internal.h"
@@ -619,6 +620,54 @@ int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, f
   if (kp.gqa == 8 && kp.group == 32)
     return launch_decode_t<8, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
   return int(cudaErrorInvalidValue);
+}
+
+
+// ---------------------------------------------------------------- no-allocation variant
+// Decode scratch (rotated queries, per-group query sums, split partials) owned by the
+// library itself, for callers that cannot allocate device memory.  Every GPU that loads
+// the library holds this array until the process exits; all calls share it.
+constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
+
+size_t static_scratch_bytes() { return kStaticScratchBytes; }
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mutex;
+uint8_t* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_decode_scratch on the current device.  The host-side name of the
+// array is only a stand-in, so the address is looked up once per device, with that
+// device current, and cached.
+int scratch_address(uint8_t** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return int(e);
+  if (dev < 0 || dev >= kMaxDevices) return int(cudaErrorInvalidDevice);
+  std::lock_guard<std::mutex> lock(g_scratch_mutex);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_decode_scratch);
+    if (e != cudaSuccess) return int(e);
+    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_scratch_ptr[dev];
+  return 0;
+}
+}  // namespace
+
+int launch_decode_static_scratch(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32,
+                                 const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream,
+                                 int* launches, bool* too_big) {
+  *too_big = wl.total > kStaticScratchBytes;
+  if (*too_big) return int(cudaErrorInvalidValue);
+  uint8_t* ws = nullptr;
+  int e = scratch_address(&ws);
+  if (e) return e;
+  // Nothing in the scratch has to start at zero: the q rotation writes the rotated
+  // queries and sums, and every work item writes its partial before the merge reads it.
+  return launch_decode(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
 }
 
 }  // namespace oscar

@@ -704,6 +704,26 @@ oscar_status oscar_bf16_decode_attention(oscar_cache* c, int layer, const void* 
   return OSCAR_OK;
 }
 
+oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int layer, const void* q, void* out, float* out_f32,
+                                            void* stream) {
+  g_launches = 0;
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (!is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_decode_attention_noalloc needs the INT2 format");
+  if (!c->planned) return fail(OSCAR_ERR_STATE, "no decode plan (plan after every append commit)");
+  if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
+  if (!q || !out) return fail(OSCAR_ERR_INVALID_ARG, "NULL q or out");
+  bool too_big = false;
+  int e = launch_decode_static_scratch(kernel_params(c), layer, q, out, out_f32, c->ws, c->dec_n_req, c->dec_items,
+                                       c->n_sm, stream, &g_launches, &too_big);
+  if (too_big)
+    return fail(OSCAR_ERR_INVALID_ARG,
+                "decode plan needs %zu bytes of scratch, more than the library's fixed %zu; use "
+                "oscar_decode_attention with a caller workspace or plan fewer requests / larger splits",
+                c->ws.total, static_scratch_bytes());
+  if (e) return fail(OSCAR_ERR_CUDA, "decode launch (library scratch): %s", cudaGetErrorString(cudaError_t(e)));
+  return OSCAR_OK;
+}
+
 oscar_status oscar_get_status(oscar_cache* c, void* stream, uint32_t* flags) {
   if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -103,4 +103,12 @@ int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, f
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                        const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
 
+// Decode with the library's own fixed device scratch instead of a caller workspace
+// (decode.cu).  Returns a cudaError_t as int; `too_big` is set when the plan's workspace
+// exceeds static_scratch_bytes().
+size_t static_scratch_bytes();
+int launch_decode_static_scratch(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32,
+                                 const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream,
+                                 int* launches, bool* too_big);
+
 }  // namespace oscar
