@@ -3,8 +3,10 @@
 // summary §4; the OScaR abstract compares against BF16 FlashDecoding-v2); this kernel is
 // that comparison, on the same page tables and plans.
 //
-// One CTA per work item (pages [p0, p1) of one (request, kv-head)); the last CTA of each
-// (request, kv-head) merges the partials and stores bf16 (and optional fp32) output.
+// Persistent-style grid: each CTA loops over work items (pages [p0, p1) of one (request,
+// kv-head)); 64-token pages are staged by cp.async and attended with bf16 tensor-core
+// MMAs (bf16_rows_mma); the last CTA of each (request, kv-head) merges the partials and
+// stores bf16 (and optional fp32) output.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -19,9 +21,10 @@ template <int G>
 __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
                                                          float* __restrict__ partials, uint16_t* __restrict__ out,
                                                          float* __restrict__ out_f32) {
-  __shared__ float qs[G * kHeadDim];
-  __shared__ __align__(16) uint8_t scratch[G * 32 * 4];
-  __shared__ int s_last;
+  extern __shared__ __align__(128) uint8_t smem[];
+  float* qs = reinterpret_cast<float*>(smem + kBf16SmemBytes);
+  int* s_last_p = reinterpret_cast<int*>(smem + kBf16SmemBytes + G * kHeadDim * 4);
+  int& s_last = *s_last_p;
   pdl_wait();
   pdl_trigger();
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
@@ -54,7 +57,7 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     };
     auto rowK = [=](int u) { return page_of(u) + size_t(u % kPage) * kHeadDim; };
     auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
-    rows_attention<G>(rowK, rowV, t0, t1, qs, part, scratch);
+    bf16_rows_mma<G>(rowK, rowV, t0, t1, qs, part, smem);
 
     __threadfence();
     __syncthreads();
@@ -94,17 +97,20 @@ template <int G>
 int launch_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
              const DecodeWorkspace& wl, int n_items, int n_sm, void* stream, int* launches) {
   float* partials = reinterpret_cast<float*>(ws + wl.partials);
+  constexpr int kSmem = kBf16SmemBytes + G * kHeadDim * 4 + 16;
   static int resident = 0;
   if (resident == 0) {
+    int e = int(cudaFuncSetAttribute(bf16_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
+    if (e) return e;
     int per_sm = 0;
-    int e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf16_split_kernel<G>, 128, 0));
+    e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf16_split_kernel<G>, 128, kSmem));
     if (e) return e;
     resident = (per_sm > 0 ? per_sm : 1) * n_sm;
   }
   (void)n_items;
   const int grid = resident;  // persistent-style: CTAs loop over the plan's items
-  int e = launch_ex(bf16_split_kernel<G>, dim3(grid), dim3(128), 0, stream, kp, layer, static_cast<const uint16_t*>(q),
-                    partials, static_cast<uint16_t*>(out), out_f32);
+  int e = launch_ex(bf16_split_kernel<G>, dim3(grid), dim3(128), size_t(kSmem), stream, kp, layer,
+                    static_cast<const uint16_t*>(q), partials, static_cast<uint16_t*>(out), out_f32);
   if (!e) *launches += 1;
   return e;
 }

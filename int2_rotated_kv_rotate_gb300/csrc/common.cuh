@@ -71,6 +71,243 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
 __device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 
+// Ampere-style 16-byte asynchronous copy global -> shared; src_bytes = 0 zero-fills.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// bf16 x bf16 -> fp32 tensor-core MMA, m16n8k16, A row-major, B column-major.
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldmatrix_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldmatrix_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                                  uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+// Two floats as bf16 (round to nearest even), first in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+  return uint32_t(bf16_rne(lo)) | (uint32_t(bf16_rne(hi)) << 16);
+}
+
+// ---------------------------------------------------------------- BF16 rows on tensor cores
+// Shared-memory footprint of bf16_rows_mma: two buffers of 64 K rows + 64 V rows, each row
+// padded to 272 bytes so that ldmatrix reads of 8 rows hit 8 distinct bank groups.
+constexpr int kRowPad = 272;
+constexpr int kChunkTok = 64;
+constexpr int kBf16BufBytes = 2 * kChunkTok * kRowPad;     // K and V rows of one chunk
+constexpr int kBf16SmemBytes = 2 * kBf16BufBytes;          // double buffered (69632 B)
+
+// Softmax attention of G query heads over bf16 token rows u in [begin, end) (row pointers
+// from rowK(u), rowV(u): 128 bf16 channels each), CTA of 4 warps.  qg is fp32 [G][128]
+// (global or shared).  Chunks of 64 tokens are staged by cp.async (zero-filled past
+// `end`), double buffered; warp w takes tokens 16w..16w+15 of each chunk.  Scores and
+// values use mma.sync bf16 with q split into bf16 hi + lo columns (4 heads per n-tile)
+// and p split the same way, so both products keep ~16 significant bits.  Writes the
+// partial m (log2 units), l, o~ (unnormalised) per head to part[G][2 + d].
+// smem must hold kBf16SmemBytes + 4 * G * (d + 2) * 4 bytes (the second part may alias).
+template <int G, typename RowK, typename RowV>
+__device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const float* qg, float* part, uint8_t* smem) {
+  constexpr int NT = G / 4;
+  const int t = threadIdx.x, lane = t & 31, warp = t >> 5, gid = lane >> 2, tig = lane & 3;
+  const float scale = kLog2e * rsqrtf(float(kHeadDim));
+  // B fragments of q (k = channels 16kc + 2tig.., n = gid -> head 4j + gid/2, hi or lo)
+  uint32_t bq[8][NT][2];
+#pragma unroll
+  for (int kc = 0; kc < 8; ++kc)
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const int head = 4 * j + (gid >> 1);
+      const bool lo = gid & 1;
+      const float* qh = qg + head * kHeadDim + 16 * kc + 2 * tig;
+      float v[4] = {qh[0], qh[1], qh[8], qh[9]};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float hi = bf16_f32(bf16_rne(v[e]));
+        v[e] = lo ? v[e] - hi : hi;
+      }
+      bq[kc][j][0] = pack_bf16(v[0], v[1]);
+      bq[kc][j][1] = pack_bf16(v[2], v[3]);
+    }
+  float m_run[NT], l_part[NT], oacc[8][NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    m_run[j] = -INFINITY;
+    l_part[j] = 0.f;
+#pragma unroll
+    for (int f = 0; f < 8; ++f)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) oacc[f][j][e] = 0.f;
+  }
+  const uint32_t sbase = smem_u32(smem);
+  const int n_chunks = end > begin ? (end - begin + kChunkTok - 1) / kChunkTok : 0;
+  // stage chunk c into buffer c & 1: thread t copies 16-byte segment (t & 15) of rows t/16 + 8k
+  auto stage = [&](int c) {
+    const uint32_t buf = sbase + (c & 1) * kBf16BufBytes;
+    const int seg = t & 15;
+#pragma unroll 4
+    for (int k = 0; k < 16; ++k) {
+      const int row = (t >> 4) + 8 * k;  // 0..127: K rows then V rows
+      const int tok = row & (kChunkTok - 1);
+      const int u = begin + c * kChunkTok + tok;
+      const bool ok = u < end;
+      const uint16_t* src = ok ? (row < kChunkTok ? rowK(u) : rowV(u)) : rowK(begin);
+      cp_async16(buf + row * kRowPad + seg * 16, src + seg * 8, ok ? 16u : 0u);
+    }
+    cp_async_commit();
+  };
+  if (n_chunks > 0) stage(0);
+  for (int c = 0; c < n_chunks; ++c) {
+    if (c + 1 < n_chunks) {
+      stage(c + 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const uint32_t kb = sbase + (c & 1) * kBf16BufBytes;
+    const uint32_t vb = kb + kChunkTok * kRowPad;
+    // ---- scores of my 16 tokens
+    float acc[NT][4];
+#pragma unroll
+    for (int j = 0; j < NT; ++j)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[j][e] = 0.f;
+    {
+      const int i = lane >> 3, r = lane & 7;
+      const uint32_t a_row = kb + (16 * warp + (i & 1) * 8 + r) * kRowPad + (i >> 1) * 16;
+#pragma unroll
+      for (int kc = 0; kc < 8; ++kc) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4(a_row + kc * 32, a0, a1, a2, a3);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_bf16_16816(acc[j], a0, a1, a2, a3, bq[kc][j][0], bq[kc][j][1]);
+      }
+    }
+    const int u0 = begin + c * kChunkTok + 16 * warp + gid, u1 = u0 + 8;
+    float lg[NT][2], alpha[NT], muse[NT];
+    bool rescale = false;
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      lg[j][0] = u0 < end ? (acc[j][0] + acc[j][1]) * scale : -INFINITY;
+      lg[j][1] = u1 < end ? (acc[j][2] + acc[j][3]) * scale : -INFINITY;
+      float mx = fmaxf(lg[j][0], lg[j][1]);
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mnew = fmaxf(m_run[j], mx);
+      muse[j] = mnew == -INFINITY ? 0.f : mnew;
+      alpha[j] = ex2(m_run[j] - muse[j]);
+      rescale |= mnew > m_run[j];
+      m_run[j] = mnew;
+    }
+    if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        l_part[j] *= alpha[j];
+#pragma unroll
+        for (int f = 0; f < 8; ++f)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) oacc[f][j][e] *= alpha[j];
+      }
+    }
+    // ---- P (bf16 hi, lo columns per head) as value-MMA B fragments
+    uint32_t bp[NT][2];
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const float p0 = lg[j][0] == -INFINITY ? 0.f : ex2(lg[j][0] - muse[j]);
+      const float p1 = lg[j][1] == -INFINITY ? 0.f : ex2(lg[j][1] - muse[j]);
+      l_part[j] += p0 + p1;
+      const float h0 = bf16_f32(bf16_rne(p0)), h1 = bf16_f32(bf16_rne(p1));
+      bp[j][0] = movmatrix_trans(pack_bf16(h0, p0 - h0));
+      bp[j][1] = movmatrix_trans(pack_bf16(h1, p1 - h1));
+    }
+    // ---- values: A = V^T (16 channels x my 16 tokens) by ldmatrix.trans
+    {
+      const int i = lane >> 3, r = lane & 7;
+      const uint32_t v_row = vb + (16 * warp + (i >> 1) * 8 + r) * kRowPad + (i & 1) * 16;
+#pragma unroll
+      for (int f = 0; f < 8; ++f) {
+        uint32_t a0, a1, a2, a3;
+        ldmatrix_x4_trans(v_row + f * 32, a0, a1, a2, a3);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) mma_bf16_16816(oacc[f][j], a0, a1, a2, a3, bp[j][0], bp[j][1]);
+      }
+    }
+    __syncthreads();  // buffer (c & 1) is refilled by stage(c + 2)
+  }
+  // ---- per-warp results -> shared memory, then merge the 4 warps into the partial
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 4);
+    l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 8);
+    l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 16);
+  }
+  float* wres = reinterpret_cast<float*>(smem);  // [4][G][2 + d], aliases the buffers
+  float* mine = wres + size_t(warp) * G * (kHeadDim + 2);
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int head = 4 * j + tig;
+    if (gid == 0) {
+      mine[head * (kHeadDim + 2)] = m_run[j];
+      mine[head * (kHeadDim + 2) + 1] = l_part[j];
+    }
+#pragma unroll
+    for (int f = 0; f < 8; ++f) {
+      mine[head * (kHeadDim + 2) + 2 + 16 * f + gid] = oacc[f][j][0] + oacc[f][j][1];
+      mine[head * (kHeadDim + 2) + 2 + 16 * f + gid + 8] = oacc[f][j][2] + oacc[f][j][3];
+    }
+  }
+  __syncthreads();
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float mw[4], ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      mw[w] = wres[(w * G + h) * (kHeadDim + 2)];
+      ms = fmaxf(ms, mw[w]);
+    }
+    float l = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      if (mw[w] == -INFINITY) continue;
+      const float a = ex2(mw[w] - ms);
+      l = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 1], l);
+      o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + t], o);
+    }
+    float* ph = part + size_t(h) * (kHeadDim + 2);
+    if (t == 0) {
+      ph[0] = ms;
+      ph[1] = l;
+    }
+    ph[2 + t] = o;
+  }
+  __syncthreads();
+}
+
 // Launch with programmatic stream serialization (PDL) allowed.
 template <typename Kern, typename... Args>
 int launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, void* stream, Args... args) {
@@ -85,84 +322,6 @@ int launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, void* stream, Arg
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return int(cudaLaunchKernelEx(&cfg, kernel, args...));
-}
-
-// Softmax attention of G query heads (fp32 q in shared memory, qs[G][d], already in the
-// keys' basis) over bf16 token rows u in [begin, end), CUDA cores, 128 threads, 32
-// tokens per round: warp w scores heads {w, w + 4} with lane = token; every thread then
-// rebuilds the same running statistics from the stored logits and accumulates channel
-// t of the values.  Writes the partial m (log2 units), l, o~[d] (unnormalised) per head.
-template <int G, typename RowK, typename RowV>
-__device__ void rows_attention(RowK rowK, RowV rowV, int begin, int end, const float* qs, float* part, uint8_t* smem) {
-  float* lgs = reinterpret_cast<float*>(smem);  // [G][32]
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31;
-  const float scale = kLog2e * rsqrtf(float(kHeadDim));
-  float m_run[G], l_run[G], o[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    m_run[h] = -INFINITY;
-    l_run[h] = 0.f;
-    o[h] = 0.f;
-  }
-  for (int u0 = begin; u0 < end; u0 += 32) {
-    const int u = u0 + lane;
-    const bool valid = u < end;
-#pragma unroll
-    for (int hh = 0; hh < G / 4; ++hh) {
-      const int h = warp + 4 * hh;
-      float s = 0.f;
-      if (valid) {
-        const uint4* kr = reinterpret_cast<const uint4*>(rowK(u));
-#pragma unroll 4
-        for (int v = 0; v < kHeadDim / 8; ++v) {
-          const uint4 x = kr[v];
-          const float* qh = qs + h * kHeadDim + 8 * v;
-          s = fmaf(qh[0], bf16_lo(x.x), s);
-          s = fmaf(qh[1], bf16_hi(x.x), s);
-          s = fmaf(qh[2], bf16_lo(x.y), s);
-          s = fmaf(qh[3], bf16_hi(x.y), s);
-          s = fmaf(qh[4], bf16_lo(x.z), s);
-          s = fmaf(qh[5], bf16_hi(x.z), s);
-          s = fmaf(qh[6], bf16_lo(x.w), s);
-          s = fmaf(qh[7], bf16_hi(x.w), s);
-        }
-      }
-      lgs[h * 32 + lane] = valid ? s * scale : -INFINITY;
-    }
-    __syncthreads();
-    const int n = min(32, end - u0);
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      float cm = -INFINITY;
-      for (int k = 0; k < n; ++k) cm = fmaxf(cm, lgs[h * 32 + k]);
-      const float mnew = fmaxf(m_run[h], cm);
-      const float muse = mnew == -INFINITY ? 0.f : mnew;
-      const float alpha = ex2(m_run[h] - muse);
-      l_run[h] *= alpha;
-      o[h] *= alpha;
-      m_run[h] = mnew;
-    }
-    for (int k = 0; k < n; ++k) {
-      const float v = bf16_f32(rowV(u0 + k)[t]);
-#pragma unroll
-      for (int h = 0; h < G; ++h) {
-        const float lg = lgs[h * 32 + k];
-        const float p = lg == -INFINITY ? 0.f : ex2(lg - m_run[h]);
-        l_run[h] += p;
-        o[h] = fmaf(p, v, o[h]);
-      }
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float* ph = part + size_t(h) * (kHeadDim + 2);
-    if (t == 0) {
-      ph[0] = m_run[h];
-      ph[1] = l_run[h];
-    }
-    ph[2 + t] = o[h];
-  }
 }
 
 }  // namespace oscar

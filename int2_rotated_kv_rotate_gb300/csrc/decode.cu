@@ -74,44 +74,74 @@ __device__ __forceinline__ uint32_t field(uint32_t w, uint32_t w_shr8, int f) {
 __device__ __forceinline__ int tau8(int m) { return (m >> 1) + 4 * (m & 1); }
 
 // ---------------------------------------------------------------- q rotation
+// One CTA per (request, kv-head): R_K (64 KB) arrives in shared memory by one bulk copy,
+// issued before the wait on the preceding kernel (R_K is written long before by
+// oscar_set_layer_params); R_V^T is prefetched into L2 for the merge of this layer.
+template <int G>
+struct QrotSmem {
+  static constexpr int kR = kHeadDim * kHeadDim * 4;  // R_K, fp32
+  static constexpr int kQ = G * kHeadDim * 4;
+  static constexpr int kBytes = kR + kQ + G * 4 * 4 + 16;
+};
+
 template <int G>
 __global__ void __launch_bounds__(128) qrot_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
                                                    float* __restrict__ qt, float* __restrict__ qsum) {
-  __shared__ float qs[G][kHeadDim];
-  __shared__ float red[G][4];
+  extern __shared__ __align__(128) uint8_t smem[];
+  using SM = QrotSmem<G>;
+  float* Rs = reinterpret_cast<float*>(smem);
+  float* qs = reinterpret_cast<float*>(smem + SM::kR);
+  float* red = qs + G * kHeadDim;  // [G][4]
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::kR + SM::kQ + G * 4 * 4);
+  const int req = blockIdx.x / kp.n_kv_heads, kvh = blockIdx.x % kp.n_kv_heads, c = threadIdx.x;
+  const size_t mat = size_t(kHeadDim) * kHeadDim;
+  const size_t lh = size_t(layer) * kp.n_kv_heads + kvh;
+  const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) + lh * mat;
+  if (c == 0) {
+    mbar_init(smem_u32(bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_expect_tx(smem_u32(bar), SM::kR);
+    bulk_g2s(smem_u32(Rs), R, SM::kR, smem_u32(bar));
+    bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) + lh * mat, SM::kR);
+  }
   pdl_wait();
   pdl_trigger();
-  const int req = blockIdx.x / kp.n_kv_heads, kvh = blockIdx.x % kp.n_kv_heads, c = threadIdx.x;
   const size_t head0 = size_t(req) * kp.n_q_heads + size_t(kvh) * G;
-  for (int h = 0; h < G; ++h) qs[h][c] = __uint_as_float(uint32_t(q[(head0 + h) * kHeadDim + c]) << 16);
+  for (int h = 0; h < G; ++h) qs[h * kHeadDim + c] = bf16_f32(q[(head0 + h) * kHeadDim + c]);
   __syncthreads();
-  const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) +
-                   (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
+  if (!mbar_wait(smem_u32(bar), 0)) {
+    if (c == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+    mbar_wait(smem_u32(bar), 0);
+  }
   float acc[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) acc[h] = 0.f;
 #pragma unroll 8
-  for (int i = 0; i < kHeadDim; ++i) {
-    const float r = __ldg(R + size_t(i) * kHeadDim + c);
+  for (int i = 0; i < kHeadDim; i += 4) {
+    const float r0 = Rs[(i + 0) * kHeadDim + c], r1 = Rs[(i + 1) * kHeadDim + c];
+    const float r2 = Rs[(i + 2) * kHeadDim + c], r3 = Rs[(i + 3) * kHeadDim + c];
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = fmaf(r, qs[h][i], acc[h]);
+    for (int h = 0; h < G; ++h) {
+      const float4 x = *reinterpret_cast<const float4*>(qs + h * kHeadDim + i);
+      acc[h] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[h]))));
+    }
   }
   const int warp = c >> 5, lane = c & 31;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
     qt[(head0 + h) * kHeadDim + c] = acc[h];
-    float s = acc[h];
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) red[h][warp] = s;
+    float sum = acc[h];
+    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (lane == 0) red[h * 4 + warp] = sum;
   }
   __syncthreads();
   if (c < G * 4) {
     const int h = c >> 2, grp = c & 3;
     float v;
     if (kp.group == 32)
-      v = red[h][grp];
+      v = red[h * 4 + grp];
     else
-      v = grp == 0 ? (red[h][0] + red[h][1]) + (red[h][2] + red[h][3]) : 0.f;
+      v = grp == 0 ? (red[h * 4 + 0] + red[h * 4 + 1]) + (red[h * 4 + 2] + red[h * 4 + 3]) : 0.f;
     qsum[(head0 + h) * 4 + grp] = v;
   }
 }
@@ -125,59 +155,110 @@ struct Cfg {
   static constexpr int kSzBytes = 2 * kPage * NG * 4;       // K then V (scale, zero)
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
-  static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers (128 B) and the merge flag
+  static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers (128 B), merge flag and merge barrier
+  static_assert(kPipeBytes >= kBf16SmemBytes, "BF16 items reuse the page pipeline memory");
+  static_assert(kPipeBytes >= (kHeadDim * kHeadDim + G * kHeadDim + 64 * G + 4 * G + 2 * G) * 4,
+                "the merge reuses the page pipeline memory");
 };
 
 // Merge all partials of (request, kv-head), rotate back and store.  128 threads.
+// R_V^T (64 KB) comes into shared memory by one bulk copy while the partials merge:
+// pass 1 finds the max and the sum of exponentials per head (thread t owns head t % G,
+// loads spread over all threads), pass 2 forms the weights of up to kMergeChunk partials
+// at a time in shared memory and accumulates channel t of every head.
+constexpr int kMergeChunk = 64;
+
 template <int G>
-__device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
-                                const float* partials, uint16_t* out, float* out_f32, float* sm_o /*[G][d]*/) {
-  const int c = threadIdx.x;
-  float mstar[G], lstar[G], o[G];
-#pragma unroll
-  for (int h = 0; h < G; ++h) {
-    mstar[h] = -INFINITY;
-    lstar[h] = 0.f;
-    o[h] = 0.f;
-  }
-  for (int i = 0; i < it.head_count; ++i) {
-    const float* pp = partials + size_t(it.head_first + i) * G * (kHeadDim + 2);
-#pragma unroll
-    for (int h = 0; h < G; ++h) mstar[h] = fmaxf(mstar[h], __ldcg(pp + h * (kHeadDim + 2)));
-  }
-  for (int i = 0; i < it.head_count; ++i) {
-    const float* pp = partials + size_t(it.head_first + i) * G * (kHeadDim + 2);
-#pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float m = __ldcg(pp + h * (kHeadDim + 2));
-      if (m == -INFINITY) continue;
-      const float w = ex2(m - mstar[h]);
-      lstar[h] = fmaf(w, __ldcg(pp + h * (kHeadDim + 2) + 1), lstar[h]);
-      o[h] = fmaf(w, __ldcg(pp + h * (kHeadDim + 2) + 2 + c), o[h]);
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < G; ++h) sm_o[h * kHeadDim + c] = lstar[h] > 0.f ? o[h] / lstar[h] : 0.f;
-  __syncthreads();
-  // o = R_V o~ : thread c' reads column c' of R_V^T (coalesced)
+__device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeItem& it, const float* partials,
+                                uint16_t* out, float* out_f32, uint8_t* smem, uint32_t mbar, uint32_t& mphase) {
+  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, hh = t % G;
+  constexpr int P = kHeadDim + 2;
+  float* Rs = reinterpret_cast<float*>(smem);      // R_V^T [128][128]
+  float* os = Rs + kHeadDim * kHeadDim;            // o~ [G][128]
+  float* ws = os + G * kHeadDim;                   // weights [kMergeChunk][G]
+  float* red = ws + kMergeChunk * G;               // [4 warps][G]
+  float* stat = red + 4 * G;                       // m*[G], l*[G]
   const float* RVt = reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                      (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim;
+  if (t == 0) {
+    fence_proxy_async();
+    mbar_expect_tx(mbar, kHeadDim * kHeadDim * 4);
+    bulk_g2s(smem_u32(Rs), RVt, kHeadDim * kHeadDim * 4, mbar);
+  }
+  const int n = it.head_count;
+  const float* base = partials + size_t(it.head_first) * G * P;
+  // ---- pass 1: max and sum of exponentials per head
+  float mloc = -INFINITY;
+  for (int e = t; e < n * G; e += 128) mloc = fmaxf(mloc, __ldcg(base + size_t(e / G) * G * P + hh * P));
+  for (int off = G; off < 32; off <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
+  if (lane < G) red[warp * G + lane] = mloc;
+  __syncthreads();
+  const float mstar = fmaxf(fmaxf(red[hh], red[G + hh]), fmaxf(red[2 * G + hh], red[3 * G + hh]));
+  __syncthreads();
+  float lloc = 0.f;
+  for (int e = t; e < n * G; e += 128) {
+    const float* ph = base + size_t(e / G) * G * P + hh * P;
+    const float m = __ldcg(ph);
+    if (m != -INFINITY) lloc = fmaf(ex2(m - mstar), __ldcg(ph + 1), lloc);
+  }
+  for (int off = G; off < 32; off <<= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
+  if (lane < G) red[warp * G + lane] = lloc;
+  __syncthreads();
+  if (t < G) {
+    stat[t] = mstar;
+    stat[G + t] = (red[t] + red[G + t]) + (red[2 * G + t] + red[3 * G + t]);
+  }
+  __syncthreads();
+  // ---- pass 2: weights in chunks, channel t of every head
+  float o[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) o[h] = 0.f;
+  for (int i0 = 0; i0 < n; i0 += kMergeChunk) {
+    const int cnt = min(kMergeChunk, n - i0);
+    for (int e = t; e < cnt * G; e += 128) {
+      const int h = e % G;
+      const float m = __ldcg(base + size_t(i0 + e / G) * G * P + h * P);
+      const float l = stat[G + h];
+      ws[e] = (m == -INFINITY || !(l > 0.f)) ? 0.f : ex2(m - stat[h]) / l;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int i = 0; i < cnt; ++i) {
+      const float* pi = base + size_t(i0 + i) * G * P + 2 + t;
+#pragma unroll
+      for (int h = 0; h < G; ++h) o[h] = fmaf(ws[i * G + h], __ldcg(pi + h * P), o[h]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int h = 0; h < G; ++h) os[h * kHeadDim + t] = o[h];
+  __syncthreads();
+  const bool ok = mbar_wait(mbar, mphase);
+  if (!ok) {
+    if (t == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+    mbar_wait(mbar, mphase);  // drain (bounded) before the memory is reused
+  }
+  mphase ^= 1u;
+  // ---- o = R_V o~: thread t reads column t of R_V^T (conflict-free), o~ broadcast
   float acc[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) acc[h] = 0.f;
-#pragma unroll 8
-  for (int j = 0; j < kHeadDim; ++j) {
-    const float r = __ldg(RVt + size_t(j) * kHeadDim + c);
+#pragma unroll 4
+  for (int j = 0; j < kHeadDim; j += 4) {
+    const float r0 = Rs[(j + 0) * kHeadDim + t], r1 = Rs[(j + 1) * kHeadDim + t];
+    const float r2 = Rs[(j + 2) * kHeadDim + t], r3 = Rs[(j + 3) * kHeadDim + t];
 #pragma unroll
-    for (int h = 0; h < G; ++h) acc[h] = fmaf(r, sm_o[h * kHeadDim + j], acc[h]);
+    for (int h = 0; h < G; ++h) {
+      const float4 x = *reinterpret_cast<const float4*>(os + h * kHeadDim + j);
+      acc[h] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[h]))));
+    }
   }
   const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
 #pragma unroll
   for (int h = 0; h < G; ++h) {
-    out[(head0 + h) * kHeadDim + c] = bf16_rne(acc[h]);
-    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = acc[h];
+    out[(head0 + h) * kHeadDim + t] = bf16_rne(ok ? acc[h] : 0.f);
+    if (out_f32) out_f32[(head0 + h) * kHeadDim + t] = ok ? acc[h] : 0.f;
   }
-  (void)dr;
 }
 
 // BF16 tokens of the sink + ring list: list index u < min(L, S) is sink u, otherwise
@@ -202,10 +283,36 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
   auto rowV = [=](int u) {
     return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t((H + u - n_s) % W) * kHeadDim;
   };
-  float* qs = reinterpret_cast<float*>(smem);
-  for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[e] = qt_head0[e];
-  __syncthreads();
-  rows_attention<G>(rowK, rowV, it.begin, it.end, qs, part, smem + G * kHeadDim * 4);
+  bf16_rows_mma<G>(rowK, rowV, it.begin, it.end, qt_head0, part, smem);
+}
+
+// Issue (lane 0 of the calling warp) the bulk copies of the warp's k-th page of an INT2
+// item into stage k % kStages; false (no copy) if the page id is out of range.
+template <int G, int GROUP>
+__device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr, int k,
+                                uint8_t* smem) {
+  using C = Cfg<G, GROUP>;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lp = it.begin + warp + kWarps * k;
+  const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
+  int phys = -1;
+  if (lp < kp.max_pages_per_request) phys = ptab[lp];
+  if (phys < 0 || phys >= kp.max_pages) return false;
+  if (lane == 0) {
+    const int st = k % kStages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes) + warp * kStages;
+    const uint32_t bar = smem_u32(&bars[st]);
+    uint8_t* dst = smem + size_t(warp) * kStages * C::kStageBytes + size_t(st) * C::kStageBytes;
+    const uint8_t* code = kp.base + kp.lay.codes + size_t(layer) * kp.lay.codes_layer_stride +
+                          size_t(phys) * kp.lay.codes_page_stride + size_t(it.kvh) * kp.lay.codes_head_stride;
+    const uint8_t* sz = kp.base + kp.lay.sz + size_t(layer) * kp.lay.sz_layer_stride +
+                        size_t(phys) * kp.lay.sz_page_stride + size_t(it.kvh) * kp.lay.sz_head_stride;
+    fence_proxy_async();
+    mbar_expect_tx(bar, C::kStageBytes);
+    bulk_g2s(smem_u32(dst), code, C::kCodeBytes, bar);
+    bulk_g2s(smem_u32(dst + C::kCodeBytes), sz, C::kSzBytes, bar);
+  }
+  return true;
 }
 
 // INT2 history pages [it.begin, it.end) of one (request, kv-head).  Positions outside
@@ -213,7 +320,7 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
 template <int G, int GROUP>
 __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
                                 const float* qt_head0, const float* qsum_head0, float* part, uint8_t* smem,
-                                uint32_t& phase_bits) {
+                                uint32_t& phase_bits, bool pre_issued, uint32_t pre_mask) {
   using C = Cfg<G, GROUP>;
   constexpr int NG = C::NG, NT = C::NT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -221,35 +328,20 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   uint8_t* pipe = smem + size_t(warp) * kStages * C::kStageBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes) + warp * kStages;
   const int S = kp.n_sink, H = dr.H;
-  const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
-  const uint8_t* code_base = kp.base + kp.lay.codes + size_t(layer) * kp.lay.codes_layer_stride +
-                             size_t(it.kvh) * kp.lay.codes_head_stride;
-  const uint8_t* sz_base =
-      kp.base + kp.lay.sz + size_t(layer) * kp.lay.sz_layer_stride + size_t(it.kvh) * kp.lay.sz_head_stride;
 
   // my pages: it.begin + warp + kWarps * k
   const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
-  // issue the copy of my k-th page into stage k % kStages; returns false if the page id is bad
-  auto issue = [&](int k) -> bool {
-    const int lp = it.begin + warp + kWarps * k;
-    int phys = -1;
-    if (lp < kp.max_pages_per_request) phys = ptab[lp];
-    if (phys < 0 || phys >= kp.max_pages) return false;
-    if (lane == 0) {
-      const int st = k % kStages;
-      const uint32_t bar = smem_u32(&bars[st]);
-      uint8_t* dst = pipe + size_t(st) * C::kStageBytes;
-      fence_proxy_async();
-      mbar_expect_tx(bar, C::kStageBytes);
-      bulk_g2s(smem_u32(dst), code_base + size_t(phys) * kp.lay.codes_page_stride, C::kCodeBytes, bar);
-      bulk_g2s(smem_u32(dst + C::kCodeBytes), sz_base + size_t(phys) * kp.lay.sz_page_stride, C::kSzBytes, bar);
-    }
-    return true;
-  };
-  uint32_t ok_mask = 0;  // bit st: stage st has a copy in flight
-  // phase_bits (kept across items): bit st = parity of the next completion of stage st
-  for (int k = 0; k < min(kStages, n_my); ++k)
-    if (issue(k)) ok_mask |= 1u << k;
+  auto issue = [&](int k) -> bool { return int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem); };
+  // ok_mask bit st: stage st has a copy in flight; phase_bits (kept across items):
+  // bit st = parity of the next completion of stage st.  The first item of a CTA may
+  // have been issued before the wait on the preceding kernel (pre_mask).
+  uint32_t ok_mask = 0;
+  if (pre_issued) {
+    ok_mask = pre_mask;
+  } else {
+    for (int k = 0; k < min(kStages, n_my); ++k)
+      if (issue(k)) ok_mask |= 1u << k;
+  }
 
   // ---- B fragments of q~ (hi/lo fp16 columns), scaled by 4^-(kc & 3) for field kc
   uint32_t bq[8][NT][2];
@@ -532,16 +624,34 @@ __global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, 
   extern __shared__ __align__(128) uint8_t smem[];
   using C = Cfg<G, GROUP>;
   int* s_last = reinterpret_cast<int*>(smem + C::kPipeBytes + kWarps * kStages * 8);
+  uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes + kWarps * kStages * 8 + 8);
   if (threadIdx.x == 0) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
     for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
+    mbar_init(smem_u32(merge_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
+  // The plan was uploaded before the preceding kernels, and the q rotation (the kernel
+  // right before this one) only lets this grid start after its own wait on the append:
+  // the first INT2 item's page copies can be issued before waiting for the rotated q.
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
+  bool pre_issued = false;
+  uint32_t pre_mask = 0;
+  if (int(blockIdx.x) < n_items) {
+    const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[blockIdx.x];
+    const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
+    if (it.kind == 0 && dr.slot >= 0 && dr.slot < kp.max_requests) {
+      const int warp = threadIdx.x >> 5;
+      const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
+      for (int k = 0; k < min(kStages, n_my); ++k)
+        if (int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem)) pre_mask |= 1u << k;
+      pre_issued = true;
+    }
+  }
   pdl_wait();
   pdl_trigger();
-  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
-  uint32_t phase_bits = 0;
+  uint32_t phase_bits = 0, merge_phase = 0;
   for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
@@ -552,7 +662,9 @@ __global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, 
       for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += 128)
         part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
     } else if (it.kind == 0) {
-      int2_pages_item<G, GROUP>(kp, layer, it, dr, qt + head0 * kHeadDim, qsum + head0 * 4, part, smem, phase_bits);
+      const bool pre = pre_issued && ix == int(blockIdx.x);
+      int2_pages_item<G, GROUP>(kp, layer, it, dr, qt + head0 * kHeadDim, qsum + head0 * 4, part, smem, phase_bits,
+                                pre, pre_mask);
     } else {
       bf16_tokens_item<G>(kp, layer, it, dr, qt + head0 * kHeadDim, part, smem);
     }
@@ -568,7 +680,7 @@ __global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, 
     __syncthreads();
     if (*s_last) {
       __threadfence();
-      merge_and_store<G>(kp, layer, it, dr, partials, out, out_f32, reinterpret_cast<float*>(smem));
+      merge_and_store<G>(kp, layer, it, partials, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
     }
     // generic-proxy use of the stage memory is over before the next item's bulk copies
     fence_proxy_async();
@@ -583,11 +695,15 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
   float* qt = reinterpret_cast<float*>(ws + wl.qt);
   float* qsum = reinterpret_cast<float*>(ws + wl.qsum);
   float* partials = reinterpret_cast<float*>(ws + wl.partials);
-  int e = launch_ex(qrot_kernel<G>, dim3(n_req * kp.n_kv_heads), dim3(128), 0, stream, kp, layer,
-                    static_cast<const uint16_t*>(q), qt, qsum);
+  static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
+  if (resident == 0) {
+    int eq = int(cudaFuncSetAttribute(qrot_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, QrotSmem<G>::kBytes));
+    if (eq) return eq;
+  }
+  int e = launch_ex(qrot_kernel<G>, dim3(n_req * kp.n_kv_heads), dim3(128), size_t(QrotSmem<G>::kBytes), stream, kp,
+                    layer, static_cast<const uint16_t*>(q), qt, qsum);
   if (e) return e;
   *launches += 1;
-  static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
   if (resident == 0) {
     e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     if (e) return e;
