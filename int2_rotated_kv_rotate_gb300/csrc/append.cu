@@ -4,8 +4,9 @@
 // BF16; history is stored INT2 after the fixed rotation and clipping (§2.2-A.3, A.4).
 // Tokens leaving the BF16 recent window are evicted into INT2 here.
 //
-// One CTA = one work item x one kv-head x {K, V}; 128 threads, thread j owns rotated
-// channel j.  An item is either
+// One CTA = one work item x one kv-head x {K, V}; 512 threads: thread (g, j) owns rotated
+// channel j of the item's tokens 4g..4g+3 (four token groups keep four warps per
+// scheduler busy; one warp each left the kernel latency-bound).  An item is either
 //   kind 0: ring slots [s0, s0+16) of one request: first the old occupants that leave the
 //           window are quantised from their stored bf16 value into INT2, then (after a
 //           barrier) the new tokens that land in those slots are rotated and stored.  The
@@ -23,15 +24,19 @@
 namespace oscar {
 namespace {
 
-constexpr int kTok = 16;
+constexpr int kTok = 16;   // tokens (or ring slots) per item
+constexpr int kTokPer = 4;  // tokens per thread
+constexpr int kThreads = 128 * (kTok / kTokPer);
 
 struct Smem {
   float xs[kHeadDim][kTok];  // fp32 inputs, transposed: xs[i][t]
   uint32_t words[kTok][8];   // packed code rows being assembled
   float red_mn[kTok][4];
   float red_mx[kTok][4];
-  int q_pos[kTok];  // positions to quantise into INT2 (this phase)
-  int n_q;
+  // INT2 destinations of the item's tokens: [0] evicted ring tokens, [1] new tokens
+  // (nullptr = token not quantised here or page id out of range)
+  uint8_t* code_row[2][kTok];
+  uint8_t* sz_row[2][kTok];
 };
 
 // Byte address of the INT2 row / sz entry of position p, or nullptr (flagged) if the page
@@ -76,186 +81,193 @@ __device__ __forceinline__ uint16_t* sink_ptr(const KernelParams& kp, int slot, 
          size_t(p) * kHeadDim;
 }
 
-// Quantise sm.n_q tokens whose clipped value for channel j is x[t] (thread j), store
-// codes and scale/zero.  Format: per group s = bf16((max-min)/3), z = bf16(min),
-// code = s == 0 ? 0 : clamp(rint((x - z) / s), 0, 3); channel c = 16f + 2w + h at bit
-// 16h + 2f of word w.
+// Quantise the item's tokens t with a destination row in sm.code_row[which][t], whose
+// clipped value for channel j is x[t] (thread j), and store codes and scale/zero.
+// Format: per group s = bf16((max-min)/3), z = bf16(min), code = s == 0 ? 0 :
+// clamp(rint((x - z) / s), 0, 3); channel c = 16f + 2w + h at bit 16h + 2f of word w.
 template <int GROUP>
-__device__ void quantize_tokens(Smem& sm, const float (&x)[kTok], const KernelParams& kp, int slot, int layer, int kvh,
-                                int kv) {
-  const int j = threadIdx.x, warp = j >> 5, lane = j & 31;
-  const int n = sm.n_q;
-  if (j < kTok * 8) (&sm.words[0][0])[j] = 0u;
-  float mn[kTok], mx[kTok];
+__device__ void quantize_tokens(Smem& sm, const float (&x)[kTokPer], int which) {
+  const int tid = threadIdx.x, j = tid & 127, tg = tid >> 7, warp = tid >> 5, lane = tid & 31;
+  if (tid < kTok * 8) (&sm.words[0][0])[tid] = 0u;
+  float mn[kTokPer], mx[kTokPer];
 #pragma unroll
-  for (int t = 0; t < kTok; ++t) {
-    mn[t] = x[t];
-    mx[t] = x[t];
+  for (int u = 0; u < kTokPer; ++u) {
+    mn[u] = x[u];
+    mx[u] = x[u];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      mn[t] = fminf(mn[t], __shfl_xor_sync(0xffffffffu, mn[t], off));
-      mx[t] = fmaxf(mx[t], __shfl_xor_sync(0xffffffffu, mx[t], off));
+      mn[u] = fminf(mn[u], __shfl_xor_sync(0xffffffffu, mn[u], off));
+      mx[u] = fmaxf(mx[u], __shfl_xor_sync(0xffffffffu, mx[u], off));
     }
     if (GROUP == 128 && lane == 0) {
-      sm.red_mn[t][warp] = mn[t];
-      sm.red_mx[t][warp] = mx[t];
+      sm.red_mn[kTokPer * tg + u][warp & 3] = mn[u];
+      sm.red_mx[kTokPer * tg + u][warp & 3] = mx[u];
     }
   }
   __syncthreads();
   const int f = j >> 4, w = (j & 15) >> 1, h = j & 1;
   const int shift = 16 * h + 2 * f;
 #pragma unroll
-  for (int t = 0; t < kTok; ++t) {
-    if (t >= n) break;
-    float gmn = mn[t], gmx = mx[t];
+  for (int u = 0; u < kTokPer; ++u) {
+    const int t = kTokPer * tg + u;
+    uint8_t* szr = sm.sz_row[which][t];
+    if (!szr) continue;
+    float gmn = mn[u], gmx = mx[u];
     if (GROUP == 128) {
       gmn = fminf(fminf(sm.red_mn[t][0], sm.red_mn[t][1]), fminf(sm.red_mn[t][2], sm.red_mn[t][3]));
       gmx = fmaxf(fmaxf(sm.red_mx[t][0], sm.red_mx[t][1]), fmaxf(sm.red_mx[t][2], sm.red_mx[t][3]));
     }
     const uint16_t sb = bf16_rne(__fdiv_rn(__fsub_rn(gmx, gmn), 3.0f));
     const uint16_t zb = bf16_rne(gmn);
-    const float s = bf16_f32(sb), z = bf16_f32(zb);
+    const float sc = bf16_f32(sb), z = bf16_f32(zb);
     uint32_t code = 0;
-    if (s != 0.0f) {
-      const float u = __fdiv_rn(__fsub_rn(x[t], z), s);
-      code = static_cast<uint32_t>(fminf(fmaxf(rintf(u), 0.0f), 3.0f));
+    if (sc != 0.0f) {
+      const float q = __fdiv_rn(__fsub_rn(x[u], z), sc);
+      code = static_cast<uint32_t>(fminf(fmaxf(rintf(q), 0.0f), 3.0f));
     }
     atomicOr(&sm.words[t][w], code << shift);
-    if ((j % GROUP) == 0) {
-      RowPtr rp = int2_row(kp, slot, layer, kvh, kv, sm.q_pos[t]);
-      if (rp.sz) reinterpret_cast<uint32_t*>(rp.sz)[j / GROUP] = uint32_t(sb) | (uint32_t(zb) << 16);
-    }
+    if ((j % GROUP) == 0) reinterpret_cast<uint32_t*>(szr)[j / GROUP] = uint32_t(sb) | (uint32_t(zb) << 16);
   }
   __syncthreads();
-  if (j < kTok * 8) {
-    const int t = j >> 3, wd = j & 7;
-    if (t < n) {
-      RowPtr rp = int2_row(kp, slot, layer, kvh, kv, sm.q_pos[t]);
-      if (rp.code) reinterpret_cast<uint32_t*>(rp.code)[wd] = sm.words[t][wd];
-    }
+  if (tid < kTok * 8) {
+    const int t = tid >> 3, wd = tid & 7;
+    uint8_t* cr = sm.code_row[which][t];
+    if (cr) reinterpret_cast<uint32_t*>(cr)[wd] = sm.words[t][wd];
   }
   __syncthreads();
 }
 
+// One work item.  Every memory access of a token is independent of the other tokens'
+// (positions are plain arithmetic on the item), so all loads of the 16 tokens are issued
+// together; thread j only ever touches channel j of a ring slot, so reading an evicted
+// token's value before writing the slot's new token needs no barrier.
 template <int GROUP>
-__device__ void append_item(Smem& sm, const KernelParams& kp, int layer, const AppendItem& it,
+__device__ void append_item(Smem& sm, const float* Rs, const KernelParams& kp, int layer, const AppendItem& it,
                             const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new) {
   const AppendReq a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];
-  const int kvh = blockIdx.y, kv = blockIdx.z, j = threadIdx.x;
+  const int kvh = blockIdx.y, kv = blockIdx.z, tid = threadIdx.x, j = tid & 127, tg = tid >> 7;
   if (a.slot < 0 || a.slot >= kp.max_requests) {
-    if (j == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+    if (tid == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
     return;
   }
   const uint16_t* X = kv ? v_new : k_new;
-  const size_t mat = size_t(kHeadDim) * kHeadDim;
-  const float* R = reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.R_V : kp.lay.R_K)) +
-                   (size_t(layer) * kp.n_kv_heads + kvh) * mat;
   const float clip =
       reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.clip_V : kp.lay.clip_K))[layer * kp.n_kv_heads + kvh];
   const int W = kp.window, S = kp.n_sink;
-
-  // ---- phase 1 (ring items): old occupants of this item's slots leave the window -> INT2
-  int rot_pos[kTok];  // new positions this CTA rotates; -1 = none
-  int n_rot = 0;
-  if (it.kind == 0) {
-    const int e0 = a.H0, e1 = min(a.L0, a.H1);
-    const int n0 = max(a.L0, a.H1), n1 = a.L1;
-    int n_ev = 0;
-    float x[kTok];
-#pragma unroll
-    for (int t = 0; t < kTok; ++t) x[t] = 0.f;
-    for (int k = 0; k < it.count; ++k) {
-      const int s = it.begin + k;
-      if (e1 > e0) {
-        const int p = e0 + ((s - e0 % W) % W + W) % W;
-        if (p < e1) {
-          if (j == 0) sm.q_pos[n_ev] = p;
-          const float r = bf16_f32(ring_ptr(kp, a.slot, layer, kvh, kv, p)[j]);
-#pragma unroll
-          for (int t = 0; t < kTok; ++t)
-            if (t == n_ev) x[t] = fmaxf(fminf(r, clip), -clip);
-          ++n_ev;
-        }
-      }
-      if (n1 > n0) {
-        const int p = n0 + ((s - n0 % W) % W + W) % W;
-        if (p < n1) rot_pos[n_rot++] = p;
-      }
+  const int e0 = a.H0, e1 = min(a.L0, a.H1);  // evicted ring positions
+  const int n0 = max(a.L0, a.H1), n1 = a.L1;  // new ring positions
+  // positions of item token t (-1 = none): evicted occupant and new token of slot / position t
+  auto position = [&](int t, int which) -> int {
+    if (t >= it.count) return -1;
+    if (it.kind == 1) return which == 0 ? -1 : it.begin + t;
+    const int s = it.begin + t;
+    if (which == 0) {
+      if (e1 <= e0) return -1;
+      const int p = e0 + ((s - e0 % W) % W + W) % W;
+      return p < e1 ? p : -1;
     }
-    if (j == 0) sm.n_q = n_ev;
-    __syncthreads();
-    if (n_ev > 0) quantize_tokens<GROUP>(sm, x, kp, a.slot, layer, kvh, kv);
-  } else {
-    for (int k = 0; k < it.count; ++k) rot_pos[n_rot++] = it.begin + k;
+    if (n1 <= n0) return -1;
+    const int p = n0 + ((s - n0 % W) % W + W) % W;
+    return p < n1 ? p : -1;
+  };
+  // ---- INT2 row pointers, one thread per (token, evicted|new)
+  if (tid < 2 * kTok) {
+    const int t = tid & (kTok - 1), which = tid >> 4;
+    const int p = position(t, which);
+    const bool q = which == 0 ? p >= 0 : (p >= S && p < a.H1);
+    RowPtr rp{nullptr, nullptr};
+    if (q) rp = int2_row(kp, a.slot, layer, kvh, kv, p);
+    sm.code_row[which][t] = rp.code;
+    sm.sz_row[which][t] = rp.sz;
   }
-  for (int t = n_rot; t < kTok; ++t) rot_pos[t] = -1;
-  if (n_rot == 0) return;
-
-  // ---- phase 2: rotate the new tokens (fixed-order fp32 fma chain per output channel)
-  for (int t = 0; t < kTok; ++t) {
-    float v = 0.f;
-    if (rot_pos[t] >= 0) {
-      const size_t row = size_t(a.x_offset + rot_pos[t] - a.L0) * kp.n_kv_heads + kvh;
-      v = bf16_f32(X[row * kHeadDim + j]);
-    }
-    sm.xs[j][t] = v;
+  // ---- my 4 tokens: all loads at once (evicted ring values, new input rows), channel j
+  int ev[kTokPer], nw[kTokPer];
+  float xe[kTokPer], xn[kTokPer];
+#pragma unroll
+  for (int u = 0; u < kTokPer; ++u) {
+    ev[u] = position(kTokPer * tg + u, 0);
+    nw[u] = position(kTokPer * tg + u, 1);
+    xe[u] = ev[u] >= 0 ? bf16_f32(ring_ptr(kp, a.slot, layer, kvh, kv, ev[u])[j]) : 0.f;
+    xn[u] = nw[u] >= 0 ? bf16_f32(X[(size_t(a.x_offset + nw[u] - a.L0) * kp.n_kv_heads + kvh) * kHeadDim + j]) : 0.f;
+  }
+#pragma unroll
+  for (int u = 0; u < kTokPer; ++u) {
+    sm.xs[j][kTokPer * tg + u] = xn[u];
+    xe[u] = fmaxf(fminf(xe[u], clip), -clip);
   }
   __syncthreads();
-  float acc[kTok];
+  // ---- evicted ring tokens -> INT2 (their stored bf16 value, clipped)
+  if (it.kind == 0 && e1 > e0) quantize_tokens<GROUP>(sm, xe, 0);
+  // ---- rotate my new tokens: one fixed-order fp32 fma chain per output channel
+  float acc[kTokPer];
 #pragma unroll
-  for (int t = 0; t < kTok; ++t) acc[t] = 0.0f;
-  const float* Rc = R + j;
-#pragma unroll 4
+  for (int u = 0; u < kTokPer; ++u) acc[u] = 0.0f;
+  const float* Rc = Rs + j;  // column j of R, in shared memory
+#pragma unroll 8
   for (int i = 0; i < kHeadDim; ++i) {
-    const float rij = __ldg(Rc + size_t(i) * kHeadDim);
-    const float4* xv = reinterpret_cast<const float4*>(&sm.xs[i][0]);
-#pragma unroll
-    for (int q = 0; q < kTok / 4; ++q) {
-      const float4 x4 = xv[q];
-      acc[4 * q + 0] = __fmaf_rn(rij, x4.x, acc[4 * q + 0]);
-      acc[4 * q + 1] = __fmaf_rn(rij, x4.y, acc[4 * q + 1]);
-      acc[4 * q + 2] = __fmaf_rn(rij, x4.z, acc[4 * q + 2]);
-      acc[4 * q + 3] = __fmaf_rn(rij, x4.w, acc[4 * q + 3]);
-    }
+    const float rij = Rc[i * kHeadDim];
+    const float4 x4 = *reinterpret_cast<const float4*>(&sm.xs[i][kTokPer * tg]);
+    acc[0] = __fmaf_rn(rij, x4.x, acc[0]);
+    acc[1] = __fmaf_rn(rij, x4.y, acc[1]);
+    acc[2] = __fmaf_rn(rij, x4.z, acc[2]);
+    acc[3] = __fmaf_rn(rij, x4.w, acc[3]);
   }
   // ---- route: sink / ring (bf16 r) or INT2 (clip + quantise)
-  float xq[kTok];
-  int n_q = 0;
+  float xq[kTokPer];
+  bool any_q = false;
 #pragma unroll
-  for (int t = 0; t < kTok; ++t) xq[t] = 0.f;
-#pragma unroll
-  for (int t = 0; t < kTok; ++t) {
-    const int p = rot_pos[t];
+  for (int u = 0; u < kTokPer; ++u) {
+    const int p = nw[u];
+    const uint16_t rb = bf16_rne(acc[u]);
+    xq[u] = fmaxf(fminf(bf16_f32(rb), clip), -clip);
     if (p < 0) continue;
-    const uint16_t rb = bf16_rne(acc[t]);
-    if (p < S && p < a.H1) {
+    if (p < S) {
       sink_ptr(kp, a.slot, layer, kvh, kv, p)[j] = rb;
     } else if (p >= a.H1) {
       ring_ptr(kp, a.slot, layer, kvh, kv, p)[j] = rb;
     } else {
-      const float r = bf16_f32(rb);
-#pragma unroll
-      for (int u = 0; u < kTok; ++u)
-        if (u == n_q) xq[u] = fmaxf(fminf(r, clip), -clip);
-      if (j == 0) sm.q_pos[n_q] = p;
-      ++n_q;
+      any_q = true;
     }
   }
-  if (j == 0) sm.n_q = n_q;
-  __syncthreads();
-  if (n_q > 0) quantize_tokens<GROUP>(sm, xq, kp, a.slot, layer, kvh, kv);
+  if (__syncthreads_or(any_q)) quantize_tokens<GROUP>(sm, xq, 1);
 }
 
+// R of this CTA's (layer, kv-head, K|V) arrives in shared memory by one bulk copy, issued
+// before the wait on the preceding kernel (R is written long before, by
+// oscar_set_layer_params).
+constexpr int kRBytes = kHeadDim * kHeadDim * 4;
+constexpr int kAppendSmem = kRBytes + 16;
+
 template <int GROUP>
-__global__ void __launch_bounds__(128) append_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ k_new,
+__global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ k_new,
                                                      const uint16_t* __restrict__ v_new) {
   __shared__ Smem sm;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  float* Rs = reinterpret_cast<float*>(dsm);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + kRBytes);
+  const int kvh = blockIdx.y, kv = blockIdx.z;
+  const float* R = reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.R_V : kp.lay.R_K)) +
+                   (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[0];
+  const bool work = int(blockIdx.x) < n_items;
+  if (threadIdx.x == 0 && work) {
+    mbar_init(smem_u32(bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    mbar_expect_tx(smem_u32(bar), kRBytes);
+    bulk_g2s(smem_u32(Rs), R, kRBytes, smem_u32(bar));
+  }
   pdl_wait();
   pdl_trigger();
-  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[0];
+  if (!work) return;
+  __syncthreads();  // barrier initialised
+  if (!mbar_wait(smem_u32(bar), 0)) {
+    if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+    mbar_wait(smem_u32(bar), 0);  // drain (bounded) before exit
+    return;
+  }
   for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
     const AppendItem it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
-    append_item<GROUP>(sm, kp, layer, it, k_new, v_new);
+    append_item<GROUP>(sm, Rs, kp, layer, it, k_new, v_new);
     __syncthreads();  // shared memory is reused by the next item
   }
 }
@@ -306,8 +318,16 @@ int launch_append(const KernelParams& kp, int layer, const void* k_new, const vo
   dim3 grid(grid_x, kp.n_kv_heads, 2);
   const uint16_t* k = static_cast<const uint16_t*>(k_new);
   const uint16_t* v = static_cast<const uint16_t*>(v_new);
-  int e = kp.group == 32 ? launch_ex(append_kernel<32>, grid, dim3(128), 0, stream, kp, layer, k, v)
-                         : launch_ex(append_kernel<128>, grid, dim3(128), 0, stream, kp, layer, k, v);
+  static bool attr = false;
+  if (!attr) {
+    int e = int(cudaFuncSetAttribute(append_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem));
+    if (!e) e = int(cudaFuncSetAttribute(append_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem));
+    if (e) return e;
+    attr = true;
+  }
+  int e = kp.group == 32
+              ? launch_ex(append_kernel<32>, grid, dim3(kThreads), size_t(kAppendSmem), stream, kp, layer, k, v)
+              : launch_ex(append_kernel<128>, grid, dim3(kThreads), size_t(kAppendSmem), stream, kp, layer, k, v);
   if (!e) *launches += 1;
   return e;
 }

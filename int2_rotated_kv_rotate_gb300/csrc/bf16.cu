@@ -22,8 +22,8 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
                                                          float* __restrict__ partials, uint16_t* __restrict__ out,
                                                          float* __restrict__ out_f32) {
   extern __shared__ __align__(128) uint8_t smem[];
-  float* qs = reinterpret_cast<float*>(smem + kBf16SmemBytes);
-  int* s_last_p = reinterpret_cast<int*>(smem + kBf16SmemBytes + G * kHeadDim * 4);
+  float* qs = reinterpret_cast<float*>(smem + Bf16Rows<4, 2>::kSmemBytes);
+  int* s_last_p = reinterpret_cast<int*>(smem + Bf16Rows<4, 2>::kSmemBytes + G * kHeadDim * 4);
   int& s_last = *s_last_p;
   pdl_wait();
   pdl_trigger();
@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     };
     auto rowK = [=](int u) { return page_of(u) + size_t(u % kPage) * kHeadDim; };
     auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
-    bf16_rows_mma<G>(rowK, rowV, t0, t1, qs, part, smem);
+    bf16_rows_mma<G, 4, 2>(rowK, rowV, t0, t1, qs, part, smem);
 
     __threadfence();
     __syncthreads();
@@ -93,29 +93,43 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
   }
 }
 
+constexpr int kBf16KernelSmem(int G) { return Bf16Rows<4, 2>::kSmemBytes + G * kHeadDim * 4 + 16; }
+
+template <int G>
+int resident_ctas(int n_sm) {
+  static int resident = 0;
+  if (resident == 0) {
+    int e = int(cudaFuncSetAttribute(bf16_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kBf16KernelSmem(G)));
+    int per_sm = 0;
+    if (!e) e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf16_split_kernel<G>, 128, kBf16KernelSmem(G)));
+    if (e) return -e;
+    resident = (per_sm > 0 ? per_sm : 1) * n_sm;
+  }
+  return resident;
+}
+
 template <int G>
 int launch_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
              const DecodeWorkspace& wl, int n_items, int n_sm, void* stream, int* launches) {
   float* partials = reinterpret_cast<float*>(ws + wl.partials);
-  constexpr int kSmem = kBf16SmemBytes + G * kHeadDim * 4 + 16;
-  static int resident = 0;
-  if (resident == 0) {
-    int e = int(cudaFuncSetAttribute(bf16_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem));
-    if (e) return e;
-    int per_sm = 0;
-    e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf16_split_kernel<G>, 128, kSmem));
-    if (e) return e;
-    resident = (per_sm > 0 ? per_sm : 1) * n_sm;
-  }
+  const int resident = resident_ctas<G>(n_sm);
+  if (resident < 0) return -resident;
   (void)n_items;
   const int grid = resident;  // persistent-style: CTAs loop over the plan's items
-  int e = launch_ex(bf16_split_kernel<G>, dim3(grid), dim3(128), size_t(kSmem), stream, kp, layer,
+  int e = launch_ex(bf16_split_kernel<G>, dim3(grid), dim3(128), size_t(kBf16KernelSmem(G)), stream, kp, layer,
                     static_cast<const uint16_t*>(q), partials, static_cast<uint16_t*>(out), out_f32);
   if (!e) *launches += 1;
   return e;
 }
 
 }  // namespace
+
+int bf16_decode_resident_ctas(int gqa, int n_sm) {
+  if (gqa == 4) return resident_ctas<4>(n_sm);
+  if (gqa == 8) return resident_ctas<8>(n_sm);
+  return n_sm;
+}
 
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                        const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {

@@ -114,24 +114,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 // ---------------------------------------------------------------- BF16 rows on tensor cores
-// Shared-memory footprint of bf16_rows_mma: two buffers of 64 K rows + 64 V rows, each row
+// A chunk is 16 tokens per warp; its K and V rows are staged in shared memory, each row
 // padded to 272 bytes so that ldmatrix reads of 8 rows hit 8 distinct bank groups.
 constexpr int kRowPad = 272;
-constexpr int kChunkTok = 64;
-constexpr int kBf16BufBytes = 2 * kChunkTok * kRowPad;     // K and V rows of one chunk
-constexpr int kBf16SmemBytes = 2 * kBf16BufBytes;          // double buffered (69632 B)
+template <int NW, int NBUF>
+struct Bf16Rows {
+  static constexpr int kChunk = 16 * NW;                   // tokens per chunk
+  static constexpr int kBufBytes = 2 * kChunk * kRowPad;   // K and V rows of one chunk
+  static constexpr int kSmemBytes = NBUF * kBufBytes;
+};
 
 // Softmax attention of G query heads over bf16 token rows u in [begin, end) (row pointers
-// from rowK(u), rowV(u): 128 bf16 channels each), CTA of 4 warps.  qg is fp32 [G][128]
-// (global or shared).  Chunks of 64 tokens are staged by cp.async (zero-filled past
-// `end`), double buffered; warp w takes tokens 16w..16w+15 of each chunk.  Scores and
-// values use mma.sync bf16 with q split into bf16 hi + lo columns (4 heads per n-tile)
-// and p split the same way, so both products keep ~16 significant bits.  Writes the
-// partial m (log2 units), l, o~ (unnormalised) per head to part[G][2 + d].
-// smem must hold kBf16SmemBytes + 4 * G * (d + 2) * 4 bytes (the second part may alias).
-template <int G, typename RowK, typename RowV>
+// from rowK(u), rowV(u): 128 bf16 channels each), CTA of NW warps.  qg is fp32 [G][128]
+// (global or shared).  Chunks of 16 NW tokens are staged by cp.async (zero-filled past
+// `end`) into NBUF buffers (2 = double buffered); warp w takes tokens 16w..16w+15 of each
+// chunk.  Scores and values use mma.sync bf16 with q split into bf16 hi + lo columns
+// (4 heads per n-tile) and p split the same way, so both products keep ~16 significant
+// bits.  Writes the partial m (log2 units), l, o~ (unnormalised) per head to
+// part[G][2 + d].  smem must hold Bf16Rows<NW, NBUF>::kSmemBytes and NW * G * (d + 2)
+// floats (the two may alias).
+template <int G, int NW, int NBUF, typename RowK, typename RowV>
 __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const float* qg, float* part, uint8_t* smem) {
   constexpr int NT = G / 4;
+  using B = Bf16Rows<NW, NBUF>;
+  constexpr int kChunkTok = B::kChunk;
+  constexpr int kBf16BufBytes = B::kBufBytes;
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5, gid = lane >> 2, tig = lane & 3;
   const float scale = kLog2e * rsqrtf(float(kHeadDim));
   // B fragments of q (k = channels 16kc + 2tig.., n = gid -> head 4j + gid/2, hi or lo)
@@ -166,11 +173,11 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
   const int n_chunks = end > begin ? (end - begin + kChunkTok - 1) / kChunkTok : 0;
   // stage chunk c into buffer c & 1: thread t copies 16-byte segment (t & 15) of rows t/16 + 8k
   auto stage = [&](int c) {
-    const uint32_t buf = sbase + (c & 1) * kBf16BufBytes;
+    const uint32_t buf = sbase + (c % NBUF) * kBf16BufBytes;
     const int seg = t & 15;
 #pragma unroll 4
     for (int k = 0; k < 16; ++k) {
-      const int row = (t >> 4) + 8 * k;  // 0..127: K rows then V rows
+      const int row = (t >> 4) + 2 * NW * k;  // K rows then V rows
       const int tok = row & (kChunkTok - 1);
       const int u = begin + c * kChunkTok + tok;
       const bool ok = u < end;
@@ -181,14 +188,14 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
   };
   if (n_chunks > 0) stage(0);
   for (int c = 0; c < n_chunks; ++c) {
-    if (c + 1 < n_chunks) {
+    if (NBUF > 1 && c + 1 < n_chunks) {
       stage(c + 1);
       cp_async_wait<1>();
     } else {
       cp_async_wait<0>();
     }
     __syncthreads();
-    const uint32_t kb = sbase + (c & 1) * kBf16BufBytes;
+    const uint32_t kb = sbase + (c % NBUF) * kBf16BufBytes;
     const uint32_t vb = kb + kChunkTok * kRowPad;
     // ---- scores of my 16 tokens
     float acc[NT][4];
@@ -257,7 +264,8 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
         for (int j = 0; j < NT; ++j) mma_bf16_16816(oacc[f][j], a0, a1, a2, a3, bp[j][0], bp[j][1]);
       }
     }
-    __syncthreads();  // buffer (c & 1) is refilled by stage(c + 2)
+    __syncthreads();  // the buffer is refilled by the next stage()
+    if (NBUF == 1 && c + 1 < n_chunks) stage(c + 1);
   }
   // ---- per-warp results -> shared memory, then merge the 4 warps into the partial
 #pragma unroll
@@ -266,7 +274,7 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
     l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 8);
     l_part[j] += __shfl_xor_sync(0xffffffffu, l_part[j], 16);
   }
-  float* wres = reinterpret_cast<float*>(smem);  // [4][G][2 + d], aliases the buffers
+  float* wres = reinterpret_cast<float*>(smem);  // [NW][G][2 + d], aliases the buffers
   float* mine = wres + size_t(warp) * G * (kHeadDim + 2);
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
@@ -282,28 +290,26 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
     }
   }
   __syncthreads();
+  for (int e = t; e < G * kHeadDim; e += 32 * NW) {
+    const int h = e / kHeadDim, c = e % kHeadDim;
+    float ms = -INFINITY;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float mw[4], ms = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      mw[w] = wres[(w * G + h) * (kHeadDim + 2)];
-      ms = fmaxf(ms, mw[w]);
-    }
+    for (int w = 0; w < NW; ++w) ms = fmaxf(ms, wres[(w * G + h) * (kHeadDim + 2)]);
     float l = 0.f, o = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      if (mw[w] == -INFINITY) continue;
-      const float a = ex2(mw[w] - ms);
+    for (int w = 0; w < NW; ++w) {
+      const float mw = wres[(w * G + h) * (kHeadDim + 2)];
+      if (mw == -INFINITY) continue;
+      const float a = ex2(mw - ms);
       l = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 1], l);
-      o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + t], o);
+      o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + c], o);
     }
     float* ph = part + size_t(h) * (kHeadDim + 2);
-    if (t == 0) {
+    if (c == 0) {
       ph[0] = ms;
       ph[1] = l;
     }
-    ph[2 + t] = o;
+    ph[2 + c] = o;
   }
   __syncthreads();
 }

@@ -37,8 +37,9 @@
 namespace oscar {
 namespace {
 
-constexpr int kWarps = 4;
-constexpr int kStages = 4;
+constexpr int kWarps = 8;   // warps per split-kernel CTA
+constexpr int kStages = 2;  // page stages per warp
+constexpr int kThreads = 32 * kWarps;
 
 // ---------------------------------------------------------------- MMA helpers
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -85,19 +86,21 @@ struct QrotSmem {
 };
 
 template <int G>
-__global__ void __launch_bounds__(128) qrot_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
+__global__ void __launch_bounds__(512) qrot_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
                                                    float* __restrict__ qt, float* __restrict__ qsum) {
   extern __shared__ __align__(128) uint8_t smem[];
   using SM = QrotSmem<G>;
+  constexpr int HPT = G / 4;  // heads per thread: thread (c, hg) takes heads hg, hg + 4
   float* Rs = reinterpret_cast<float*>(smem);
   float* qs = reinterpret_cast<float*>(smem + SM::kR);
   float* red = qs + G * kHeadDim;  // [G][4]
   uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::kR + SM::kQ + G * 4 * 4);
-  const int req = blockIdx.x / kp.n_kv_heads, kvh = blockIdx.x % kp.n_kv_heads, c = threadIdx.x;
+  const int req = blockIdx.x / kp.n_kv_heads, kvh = blockIdx.x % kp.n_kv_heads;
+  const int tid = threadIdx.x, c = tid & 127, hg = tid >> 7;
   const size_t mat = size_t(kHeadDim) * kHeadDim;
   const size_t lh = size_t(layer) * kp.n_kv_heads + kvh;
   const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) + lh * mat;
-  if (c == 0) {
+  if (tid == 0) {
     mbar_init(smem_u32(bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     mbar_expect_tx(smem_u32(bar), SM::kR);
@@ -107,36 +110,37 @@ __global__ void __launch_bounds__(128) qrot_kernel(KernelParams kp, int layer, c
   pdl_wait();
   pdl_trigger();
   const size_t head0 = size_t(req) * kp.n_q_heads + size_t(kvh) * G;
-  for (int h = 0; h < G; ++h) qs[h * kHeadDim + c] = bf16_f32(q[(head0 + h) * kHeadDim + c]);
+  for (int e = tid; e < G * kHeadDim; e += 512) qs[e] = bf16_f32(q[head0 * kHeadDim + e]);
   __syncthreads();
   if (!mbar_wait(smem_u32(bar), 0)) {
-    if (c == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+    if (tid == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
     mbar_wait(smem_u32(bar), 0);
   }
-  float acc[G];
+  float acc[HPT];
 #pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = 0.f;
+  for (int k = 0; k < HPT; ++k) acc[k] = 0.f;
 #pragma unroll 8
   for (int i = 0; i < kHeadDim; i += 4) {
     const float r0 = Rs[(i + 0) * kHeadDim + c], r1 = Rs[(i + 1) * kHeadDim + c];
     const float r2 = Rs[(i + 2) * kHeadDim + c], r3 = Rs[(i + 3) * kHeadDim + c];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float4 x = *reinterpret_cast<const float4*>(qs + h * kHeadDim + i);
-      acc[h] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[h]))));
+    for (int k = 0; k < HPT; ++k) {
+      const float4 x = *reinterpret_cast<const float4*>(qs + (hg + 4 * k) * kHeadDim + i);
+      acc[k] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[k]))));
     }
   }
-  const int warp = c >> 5, lane = c & 31;
+  const int lane = tid & 31, wq = (tid >> 5) & 3;  // warp wq of this head group covers channels 32wq..
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    qt[(head0 + h) * kHeadDim + c] = acc[h];
-    float sum = acc[h];
+  for (int k = 0; k < HPT; ++k) {
+    const int h = hg + 4 * k;
+    qt[(head0 + h) * kHeadDim + c] = acc[k];
+    float sum = acc[k];
     for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane == 0) red[h * 4 + warp] = sum;
+    if (lane == 0) red[h * 4 + wq] = sum;
   }
   __syncthreads();
-  if (c < G * 4) {
-    const int h = c >> 2, grp = c & 3;
+  if (tid < G * 4) {
+    const int h = tid >> 2, grp = tid & 3;
     float v;
     if (kp.group == 32)
       v = red[h * 4 + grp];
@@ -156,8 +160,8 @@ struct Cfg {
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
   static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers (128 B), merge flag and merge barrier
-  static_assert(kPipeBytes >= kBf16SmemBytes, "BF16 items reuse the page pipeline memory");
-  static_assert(kPipeBytes >= (kHeadDim * kHeadDim + G * kHeadDim + 64 * G + 4 * G + 2 * G) * 4,
+  static_assert(kPipeBytes >= Bf16Rows<kWarps, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
+  static_assert(kPipeBytes >= (kHeadDim * kHeadDim + G * kHeadDim + 64 * G + kWarps * G + (2 + kWarps) * G) * 4,
                 "the merge reuses the page pipeline memory");
 };
 
@@ -172,12 +176,14 @@ template <int G>
 __device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeItem& it, const float* partials,
                                 uint16_t* out, float* out_f32, uint8_t* smem, uint32_t mbar, uint32_t& mphase) {
   const int t = threadIdx.x, warp = t >> 5, lane = t & 31, hh = t % G;
+  const int c = t & (kHeadDim - 1), hb = t >> 7;  // pass 2 and the rotation: channel c, heads hb, hb + 2, ..
+  constexpr int HPT = G / (kThreads / kHeadDim);
   constexpr int P = kHeadDim + 2;
   float* Rs = reinterpret_cast<float*>(smem);      // R_V^T [128][128]
   float* os = Rs + kHeadDim * kHeadDim;            // o~ [G][128]
   float* ws = os + G * kHeadDim;                   // weights [kMergeChunk][G]
   float* red = ws + kMergeChunk * G;               // [4 warps][G]
-  float* stat = red + 4 * G;                       // m*[G], l*[G]
+  float* stat = red + kWarps * G;                  // m*[G], l*[G], per-warp sums [kWarps][G]
   const float* RVt = reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                      (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim;
   if (t == 0) {
@@ -187,51 +193,68 @@ __device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeI
   }
   const int n = it.head_count;
   const float* base = partials + size_t(it.head_first) * G * P;
-  // ---- pass 1: max and sum of exponentials per head
-  float mloc = -INFINITY;
-  for (int e = t; e < n * G; e += 128) mloc = fmaxf(mloc, __ldcg(base + size_t(e / G) * G * P + hh * P));
-  for (int off = G; off < 32; off <<= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, off));
-  if (lane < G) red[warp * G + lane] = mloc;
-  __syncthreads();
-  const float mstar = fmaxf(fmaxf(red[hh], red[G + hh]), fmaxf(red[2 * G + hh], red[3 * G + hh]));
-  __syncthreads();
-  float lloc = 0.f;
-  for (int e = t; e < n * G; e += 128) {
+  // ---- pass 1: running (max, sum of exponentials) per head, one load round for m and l
+  float mloc = -INFINITY, lloc = 0.f;
+  for (int e = t; e < n * G; e += kThreads) {
     const float* ph = base + size_t(e / G) * G * P + hh * P;
-    const float m = __ldcg(ph);
-    if (m != -INFINITY) lloc = fmaf(ex2(m - mstar), __ldcg(ph + 1), lloc);
+    const float m = __ldcg(ph), l = __ldcg(ph + 1);
+    if (m == -INFINITY) continue;
+    const float mn = fmaxf(mloc, m);
+    lloc = lloc * ex2(mloc - mn) + l * ex2(m - mn);
+    mloc = mn;
   }
-  for (int off = G; off < 32; off <<= 1) lloc += __shfl_xor_sync(0xffffffffu, lloc, off);
-  if (lane < G) red[warp * G + lane] = lloc;
+  for (int off = G; off < 32; off <<= 1) {
+    const float mo = __shfl_xor_sync(0xffffffffu, mloc, off), lo = __shfl_xor_sync(0xffffffffu, lloc, off);
+    const float mn = fmaxf(mloc, mo);
+    lloc = (mloc == -INFINITY ? 0.f : lloc * ex2(mloc - mn)) + (mo == -INFINITY ? 0.f : lo * ex2(mo - mn));
+    mloc = mn;
+  }
+  if (lane < G) {
+    red[warp * G + lane] = mloc;
+    stat[2 * G + warp * G + lane] = lloc;  // scratch for the per-warp sums
+  }
   __syncthreads();
   if (t < G) {
-    stat[t] = mstar;
-    stat[G + t] = (red[t] + red[G + t]) + (red[2 * G + t] + red[3 * G + t]);
+    float ms = -INFINITY, ls = 0.f;
+    for (int w = 0; w < kWarps; ++w) ms = fmaxf(ms, red[w * G + t]);
+    for (int w = 0; w < kWarps; ++w) {
+      const float mw = red[w * G + t];
+      if (mw != -INFINITY) ls += stat[2 * G + w * G + t] * ex2(mw - ms);
+    }
+    stat[t] = ms;
+    stat[G + t] = ls;
   }
   __syncthreads();
-  // ---- pass 2: weights in chunks, channel t of every head
-  float o[G];
+  // ---- pass 2: weights in chunks; channel c of heads hb, hb + 2, .., 8 partials' loads per round
+  float o[HPT];
 #pragma unroll
-  for (int h = 0; h < G; ++h) o[h] = 0.f;
+  for (int k = 0; k < HPT; ++k) o[k] = 0.f;
   for (int i0 = 0; i0 < n; i0 += kMergeChunk) {
     const int cnt = min(kMergeChunk, n - i0);
-    for (int e = t; e < cnt * G; e += 128) {
+    for (int e = t; e < cnt * G; e += kThreads) {
       const int h = e % G;
       const float m = __ldcg(base + size_t(i0 + e / G) * G * P + h * P);
       const float l = stat[G + h];
       ws[e] = (m == -INFINITY || !(l > 0.f)) ? 0.f : ex2(m - stat[h]) / l;
     }
     __syncthreads();
-#pragma unroll 4
-    for (int i = 0; i < cnt; ++i) {
-      const float* pi = base + size_t(i0 + i) * G * P + 2 + t;
+    for (int i = 0; i < cnt; i += 8) {
+      float v[8][HPT];
 #pragma unroll
-      for (int h = 0; h < G; ++h) o[h] = fmaf(ws[i * G + h], __ldcg(pi + h * P), o[h]);
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int q = 0; q < HPT; ++q)
+          v[k][q] = i + k < cnt ? __ldcg(base + size_t(i0 + i + k) * G * P + (hb + 2 * q) * P + 2 + c) : 0.f;
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+#pragma unroll
+        for (int q = 0; q < HPT; ++q)
+          if (i + k < cnt) o[q] = fmaf(ws[(i + k) * G + hb + 2 * q], v[k][q], o[q]);
     }
     __syncthreads();
   }
 #pragma unroll
-  for (int h = 0; h < G; ++h) os[h * kHeadDim + t] = o[h];
+  for (int q = 0; q < HPT; ++q) os[(hb + 2 * q) * kHeadDim + c] = o[q];
   __syncthreads();
   const bool ok = mbar_wait(mbar, mphase);
   if (!ok) {
@@ -239,27 +262,29 @@ __device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeI
     mbar_wait(mbar, mphase);  // drain (bounded) before the memory is reused
   }
   mphase ^= 1u;
-  // ---- o = R_V o~: thread t reads column t of R_V^T (conflict-free), o~ broadcast
-  float acc[G];
+  // ---- o = R_V o~: thread reads column c of R_V^T (conflict-free), o~ broadcast
+  float acc[HPT];
 #pragma unroll
-  for (int h = 0; h < G; ++h) acc[h] = 0.f;
+  for (int q = 0; q < HPT; ++q) acc[q] = 0.f;
 #pragma unroll 4
   for (int j = 0; j < kHeadDim; j += 4) {
-    const float r0 = Rs[(j + 0) * kHeadDim + t], r1 = Rs[(j + 1) * kHeadDim + t];
-    const float r2 = Rs[(j + 2) * kHeadDim + t], r3 = Rs[(j + 3) * kHeadDim + t];
+    const float r0 = Rs[(j + 0) * kHeadDim + c], r1 = Rs[(j + 1) * kHeadDim + c];
+    const float r2 = Rs[(j + 2) * kHeadDim + c], r3 = Rs[(j + 3) * kHeadDim + c];
 #pragma unroll
-    for (int h = 0; h < G; ++h) {
-      const float4 x = *reinterpret_cast<const float4*>(os + h * kHeadDim + j);
-      acc[h] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[h]))));
+    for (int q = 0; q < HPT; ++q) {
+      const float4 x = *reinterpret_cast<const float4*>(os + (hb + 2 * q) * kHeadDim + j);
+      acc[q] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[q]))));
     }
   }
   const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    out[(head0 + h) * kHeadDim + t] = bf16_rne(ok ? acc[h] : 0.f);
-    if (out_f32) out_f32[(head0 + h) * kHeadDim + t] = ok ? acc[h] : 0.f;
+  for (int q = 0; q < HPT; ++q) {
+    const int h = hb + 2 * q;
+    out[(head0 + h) * kHeadDim + c] = bf16_rne(ok ? acc[q] : 0.f);
+    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = ok ? acc[q] : 0.f;
   }
 }
+
 
 // BF16 tokens of the sink + ring list: list index u < min(L, S) is sink u, otherwise
 // position H + u - min(L, S) in ring slot p % W.
@@ -283,7 +308,7 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
   auto rowV = [=](int u) {
     return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t((H + u - n_s) % W) * kHeadDim;
   };
-  bf16_rows_mma<G>(rowK, rowV, it.begin, it.end, qt_head0, part, smem);
+  bf16_rows_mma<G, kWarps, 1>(rowK, rowV, it.begin, it.end, qt_head0, part, smem);
 }
 
 // Issue (lane 0 of the calling warp) the bulk copies of the warp's k-th page of an INT2
@@ -498,35 +523,35 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       float p[NT][2];
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        p[j][0] = lg[b][j][0] == -INFINITY ? 0.f : ex2(lg[b][j][0] - muse[j]);
-        p[j][1] = lg[b][j][1] == -INFINITY ? 0.f : ex2(lg[b][j][1] - muse[j]);
+        // masked tokens carry lg = -inf and muse is finite: ex2 gives exactly 0
+        p[j][0] = ex2(lg[b][j][0] - muse[j]);
+        p[j][1] = ex2(lg[b][j][1] - muse[j]);
         l_part[j] += p[j][0] + p[j][1];
       }
-      // B fragments of P' = p * s_V per group (movmatrix turns score rows into value k-rows)
+      const int pos0 = lp * kPage + t0, pos1 = lp * kPage + t1;
+      const bool v0 = have && pos0 >= S && pos0 < H, v1 = have && pos1 >= S && pos1 < H;
+      // B fragments of P' = p * s_V per group (movmatrix turns score rows into value k-rows);
+      // scale/zero of masked rows may hold anything, so they are selected away, not multiplied
       uint32_t bp[NG][2];
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         const uint32_t vz0 = vsz[t0 * NG + g], vz1 = vsz[t1 * NG + g];
-        const float sv0 = bf16_lo(vz0), sv1 = bf16_lo(vz1);
-        const float zv0 = bf16_hi(vz0), zv1 = bf16_hi(vz1);
+        const float sv0 = v0 ? bf16_lo(vz0) : 0.f, sv1 = v1 ? bf16_lo(vz1) : 0.f;
+        const float zv0 = v0 ? bf16_hi(vz0) : 0.f, zv1 = v1 ? bf16_hi(vz1) : 0.f;
         uint32_t x0, x1;
         if (NT == 1) {
-          const float q0 = p[0][0] == 0.f ? 0.f : p[0][0] * sv0;
-          const float q1 = p[0][1] == 0.f ? 0.f : p[0][1] * sv1;
+          const float q0 = p[0][0] * sv0, q1 = p[0][1] * sv1;
           const float h0 = __half2float(__float2half_rn(q0)), h1 = __half2float(__float2half_rn(q1));
           x0 = pack_h2(h0, q0 - h0);
           x1 = pack_h2(h1, q1 - h1);
         } else {
-          x0 = pack_h2(p[0][0] == 0.f ? 0.f : p[0][0] * sv0, p[NT - 1][0] == 0.f ? 0.f : p[NT - 1][0] * sv0);
-          x1 = pack_h2(p[0][1] == 0.f ? 0.f : p[0][1] * sv1, p[NT - 1][1] == 0.f ? 0.f : p[NT - 1][1] * sv1);
+          x0 = pack_h2(p[0][0] * sv0, p[NT - 1][0] * sv0);
+          x1 = pack_h2(p[0][1] * sv1, p[NT - 1][1] * sv1);
         }
         bp[g][0] = movtrans(x0);
         bp[g][1] = movtrans(x1);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) {
-          if (p[j][0] != 0.f) zv[j][g] = fmaf(p[j][0], zv0, zv[j][g]);
-          if (p[j][1] != 0.f) zv[j][g] = fmaf(p[j][1], zv1, zv[j][g]);
-        }
+        for (int j = 0; j < NT; ++j) zv[j][g] = fmaf(p[j][1], zv1, fmaf(p[j][0], zv0, zv[j][g]));
       }
       // A fragments: word gid of tokens tig, tig+4, tig+8, tig+12 (k = 2tig, 2tig+1, 2tig+8, 2tig+9)
       const uint32_t* vw = reinterpret_cast<const uint32_t*>(vcodes + (16 * b) * kRowBytes) + gid;
@@ -591,34 +616,31 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     }
   }
   __syncthreads();
-  const int t = threadIdx.x;
+  for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) {
+    const int h = e / kHeadDim, c = e % kHeadDim;
+    float ms = -INFINITY;
 #pragma unroll
-  for (int h = 0; h < G; ++h) {
-    float mw[kWarps], ms = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
-      mw[w] = wres[(w * G + h) * (kHeadDim + 2)];
-      ms = fmaxf(ms, mw[w]);
-    }
+    for (int w = 0; w < kWarps; ++w) ms = fmaxf(ms, wres[(w * G + h) * (kHeadDim + 2)]);
     float l = 0.f, o = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      if (mw[w] == -INFINITY) continue;
-      const float a = ex2(mw[w] - ms);
+      const float mw = wres[(w * G + h) * (kHeadDim + 2)];
+      if (mw == -INFINITY) continue;
+      const float a = ex2(mw - ms);
       l = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 1], l);
-      o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + t], o);
+      o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + c], o);
     }
     float* ph = part + size_t(h) * (kHeadDim + 2);
-    if (t == 0) {
+    if (c == 0) {
       ph[0] = ms;
       ph[1] = l;
     }
-    ph[2 + t] = o;
+    ph[2 + c] = o;
   }
 }
 
 template <int G, int GROUP>
-__global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, const float* __restrict__ qt,
+__global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int layer, const float* __restrict__ qt,
                                                     const float* __restrict__ qsum, float* __restrict__ partials,
                                                     uint16_t* __restrict__ out, float* __restrict__ out_f32) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -659,7 +681,7 @@ __global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, 
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
     if (dr.slot < 0 || dr.slot >= kp.max_requests) {
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
-      for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += 128)
+      for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += kThreads)
         part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
     } else if (it.kind == 0) {
       const bool pre = pre_issued && ix == int(blockIdx.x);
@@ -689,34 +711,39 @@ __global__ void __launch_bounds__(128) split_kernel(KernelParams kp, int layer, 
 }
 
 template <int G, int GROUP>
+int resident_ctas(int n_sm) {
+  using C = Cfg<G, GROUP>;
+  static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
+  if (resident == 0) {
+    int e = int(cudaFuncSetAttribute(qrot_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, QrotSmem<G>::kBytes));
+    if (!e)
+      e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    int per_sm = 0;
+    if (!e)
+      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP>, kThreads, C::kSmemBytes));
+    if (e) return -e;
+    resident = (per_sm > 0 ? per_sm : 1) * n_sm;
+  }
+  return resident;
+}
+
+template <int G, int GROUP>
 int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                     const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
   using C = Cfg<G, GROUP>;
   float* qt = reinterpret_cast<float*>(ws + wl.qt);
   float* qsum = reinterpret_cast<float*>(ws + wl.qsum);
   float* partials = reinterpret_cast<float*>(ws + wl.partials);
-  static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
-  if (resident == 0) {
-    int eq = int(cudaFuncSetAttribute(qrot_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, QrotSmem<G>::kBytes));
-    if (eq) return eq;
-  }
-  int e = launch_ex(qrot_kernel<G>, dim3(n_req * kp.n_kv_heads), dim3(128), size_t(QrotSmem<G>::kBytes), stream, kp,
+  const int resident = resident_ctas<G, GROUP>(n_sm);
+  if (resident < 0) return -resident;
+  int e = launch_ex(qrot_kernel<G>, dim3(n_req * kp.n_kv_heads), dim3(512), size_t(QrotSmem<G>::kBytes), stream, kp,
                     layer, static_cast<const uint16_t*>(q), qt, qsum);
   if (e) return e;
   *launches += 1;
-  if (resident == 0) {
-    e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
-    if (e) return e;
-    int per_sm = 0;
-    e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP>, 128, C::kSmemBytes));
-    if (e) return e;
-    resident = (per_sm > 0 ? per_sm : 1) * n_sm;
-  }
   // persistent-style grid: every resident CTA slot, each looping over work items, so a
   // captured launch serves later plans with other item counts
   (void)n_items;
-  const int grid = resident;
-  e = launch_ex(split_kernel<G, GROUP>, dim3(grid), dim3(128), size_t(C::kSmemBytes), stream, kp, layer,
+  e = launch_ex(split_kernel<G, GROUP>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes), stream, kp, layer,
                 static_cast<const float*>(qt), static_cast<const float*>(qsum), partials, static_cast<uint16_t*>(out),
                 out_f32);
   if (!e) *launches += 1;
@@ -724,6 +751,14 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
 }
 
 }  // namespace
+
+int decode_resident_ctas(int gqa, int group, int n_sm) {
+  if (gqa == 4 && group == 128) return resident_ctas<4, 128>(n_sm);
+  if (gqa == 4 && group == 32) return resident_ctas<4, 32>(n_sm);
+  if (gqa == 8 && group == 128) return resident_ctas<8, 128>(n_sm);
+  if (gqa == 8 && group == 32) return resident_ctas<8, 32>(n_sm);
+  return n_sm;
+}
 
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                   const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {

@@ -585,10 +585,34 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
         }
     total_pages += (long long)Hkv * pages_needed(c, Ls[i], Hs[i]);
   }
+  // Work items: per (request, kv-head) the BF16 sink+ring items and INT2 page ranges of
+  // `chunk` pages.  Automatic chunk: the smallest that lets one wave of resident CTAs hold
+  // every item (a second, partial wave would double the time of a latency-bound step).
+  std::vector<int> np_of(n_req), nbf_of(n_req);
+  long long n_bf_items = 0;
+  int max_np = 1;
+  for (int i = 0; i < n_req; ++i) {
+    np_of[i] = pages_needed(c, Ls[i], Hs[i]);
+    nbf_of[i] = is_int2(c) ? std::min(Ls[i], S) + std::max(0, Ls[i] - Hs[i]) : 0;
+    n_bf_items += (long long)Hkv * (nbf_of[i] > 0 ? ceil_div(nbf_of[i], kBf16ItemTokens) : 0);
+    max_np = std::max(max_np, np_of[i]);
+  }
+  auto count_items = [&](int ch) {
+    long long n = n_bf_items;
+    for (int i = 0; i < n_req; ++i) {
+      const int per = (np_of[i] > 0 ? ceil_div(np_of[i], ch) : 0) + (nbf_of[i] > 0 ? ceil_div(nbf_of[i], kBf16ItemTokens) : 0);
+      n += (long long)Hkv * (per > 0 ? (np_of[i] > 0 ? ceil_div(np_of[i], ch) : 0) : 1);
+    }
+    return n;
+  };
   int chunk = max_split_pages;
   if (chunk == 0) {
-    const long long target = 2LL * c->n_sm;
-    chunk = int(std::max<long long>(4, (total_pages + target - 1) / target));
+    const int G = c->cfg.n_q_heads / Hkv;
+    int resident = is_int2(c) ? decode_resident_ctas(G, c->cfg.group, c->n_sm) : bf16_decode_resident_ctas(G, c->n_sm);
+    if (resident <= 0) resident = 2 * c->n_sm;
+    const long long slots = std::max<long long>(1, resident - n_bf_items);
+    chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
+    while (chunk < max_np && count_items(chunk) > resident) ++chunk;
   }
   std::vector<DecodeReq> reqs(n_req);
   std::vector<DecodeItem> items;

@@ -103,6 +103,11 @@ int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, f
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                        const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
 
+// CTAs of the decode kernel of this shape that fit on the GPU at once (occupancy x SMs);
+// the planner sizes work items so that one wave holds them all.
+int decode_resident_ctas(int gqa, int group, int n_sm);
+int bf16_decode_resident_ctas(int gqa, int n_sm);
+
 // Decode with the library's own fixed device scratch instead of a caller workspace
 // (decode.cu).  Returns a cudaError_t as int; `too_big` is set when the plan's workspace
 // exceeds static_scratch_bytes().
