@@ -141,18 +141,27 @@ __device__ void quantize_tokens(Smem& sm, const float (&x)[kTokPer], int which) 
 // (positions are plain arithmetic on the item), so all loads of the 16 tokens are issued
 // together; thread j only ever touches channel j of a ring slot, so reading an evicted
 // token's value before writing the slot's new token needs no barrier.
+// Per-thread state of one item between its two halves.
+struct ItemState {
+  AppendReq a;
+  float clip;
+  int ev[kTokPer], nw[kTokPer];
+  float xe[kTokPer];
+  bool ok;
+};
+
+// First half of an item: everything that does not depend on the preceding kernel in the
+// stream (the plan and page table were uploaded before it; the ring tokens it evicts were
+// written by this layer's previous append, long complete), so it may run before the PDL
+// wait: positions, INT2 row pointers, evicted ring values.
 template <int GROUP>
-__device__ void append_item(Smem& sm, const float* Rs, const KernelParams& kp, int layer, const AppendItem& it,
-                            const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new) {
-  const AppendReq a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];
+__device__ void prepare_item(Smem& sm, const KernelParams& kp, int layer, const AppendItem& it, ItemState& st) {
+  st.a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];
+  const AppendReq& a = st.a;
   const int kvh = blockIdx.y, kv = blockIdx.z, tid = threadIdx.x, j = tid & 127, tg = tid >> 7;
-  if (a.slot < 0 || a.slot >= kp.max_requests) {
-    if (tid == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
-    return;
-  }
-  const uint16_t* X = kv ? v_new : k_new;
-  const float clip =
-      reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.clip_V : kp.lay.clip_K))[layer * kp.n_kv_heads + kvh];
+  st.ok = a.slot >= 0 && a.slot < kp.max_requests;
+  if (!st.ok) return;
+  st.clip = reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.clip_V : kp.lay.clip_K))[layer * kp.n_kv_heads + kvh];
   const int W = kp.window, S = kp.n_sink;
   const int e0 = a.H0, e1 = min(a.L0, a.H1);  // evicted ring positions
   const int n0 = max(a.L0, a.H1), n1 = a.L1;  // new ring positions
@@ -170,7 +179,7 @@ __device__ void append_item(Smem& sm, const float* Rs, const KernelParams& kp, i
     const int p = n0 + ((s - n0 % W) % W + W) % W;
     return p < n1 ? p : -1;
   };
-  // ---- INT2 row pointers, one thread per (token, evicted|new)
+  // INT2 row pointers, one thread per (token, evicted|new)
   if (tid < 2 * kTok) {
     const int t = tid & (kTok - 1), which = tid >> 4;
     const int p = position(t, which);
@@ -180,44 +189,72 @@ __device__ void append_item(Smem& sm, const float* Rs, const KernelParams& kp, i
     sm.code_row[which][t] = rp.code;
     sm.sz_row[which][t] = rp.sz;
   }
-  // ---- my 4 tokens: all loads at once (evicted ring values, new input rows), channel j
-  int ev[kTokPer], nw[kTokPer];
-  float xe[kTokPer], xn[kTokPer];
 #pragma unroll
   for (int u = 0; u < kTokPer; ++u) {
-    ev[u] = position(kTokPer * tg + u, 0);
-    nw[u] = position(kTokPer * tg + u, 1);
-    xe[u] = ev[u] >= 0 ? bf16_f32(ring_ptr(kp, a.slot, layer, kvh, kv, ev[u])[j]) : 0.f;
-    xn[u] = nw[u] >= 0 ? bf16_f32(X[(size_t(a.x_offset + nw[u] - a.L0) * kp.n_kv_heads + kvh) * kHeadDim + j]) : 0.f;
+    st.ev[u] = position(kTokPer * tg + u, 0);
+    st.nw[u] = position(kTokPer * tg + u, 1);
+    st.xe[u] = st.ev[u] >= 0 ? bf16_f32(ring_ptr(kp, a.slot, layer, kvh, kv, st.ev[u])[j]) : 0.f;
   }
+}
+
+// Second half: new input rows (written by the caller, so after the PDL wait), eviction into
+// INT2, rotation of the new tokens, routing.  Thread j only ever touches channel j of a
+// ring slot, so reading an evicted token's value before writing the slot's new token
+// needs no barrier.
+template <int GROUP>
+__device__ void finish_item(Smem& sm, const float* Rs, const KernelParams& kp, int layer, const AppendItem& it,
+                            ItemState& st, const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new) {
+  const AppendReq& a = st.a;
+  const int kvh = blockIdx.y, kv = blockIdx.z, tid = threadIdx.x, j = tid & 127, tg = tid >> 7;
+  if (!st.ok) {
+    if (tid == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+    return;
+  }
+  const uint16_t* X = kv ? v_new : k_new;
+  const float clip = st.clip;
+  const int S = kp.n_sink;
+  float xn[kTokPer];
+#pragma unroll
+  for (int u = 0; u < kTokPer; ++u)
+    xn[u] = st.nw[u] >= 0 ? bf16_f32(X[(size_t(a.x_offset + st.nw[u] - a.L0) * kp.n_kv_heads + kvh) * kHeadDim + j])
+                          : 0.f;
+  float xe[kTokPer];
 #pragma unroll
   for (int u = 0; u < kTokPer; ++u) {
     sm.xs[j][kTokPer * tg + u] = xn[u];
-    xe[u] = fmaxf(fminf(xe[u], clip), -clip);
+    xe[u] = fmaxf(fminf(st.xe[u], clip), -clip);
   }
   __syncthreads();
   // ---- evicted ring tokens -> INT2 (their stored bf16 value, clipped)
-  if (it.kind == 0 && e1 > e0) quantize_tokens<GROUP>(sm, xe, 0);
-  // ---- rotate my new tokens: one fixed-order fp32 fma chain per output channel
+  if (it.kind == 0 && min(a.L0, a.H1) > a.H0) quantize_tokens<GROUP>(sm, xe, 0);
+  // ---- rotate my new tokens: one fixed-order fp32 fma chain per output channel; the
+  // shared-memory loads of 16 steps are issued ahead of their FMAs
   float acc[kTokPer];
 #pragma unroll
   for (int u = 0; u < kTokPer; ++u) acc[u] = 0.0f;
   const float* Rc = Rs + j;  // column j of R, in shared memory
-#pragma unroll 8
-  for (int i = 0; i < kHeadDim; ++i) {
-    const float rij = Rc[i * kHeadDim];
-    const float4 x4 = *reinterpret_cast<const float4*>(&sm.xs[i][kTokPer * tg]);
-    acc[0] = __fmaf_rn(rij, x4.x, acc[0]);
-    acc[1] = __fmaf_rn(rij, x4.y, acc[1]);
-    acc[2] = __fmaf_rn(rij, x4.z, acc[2]);
-    acc[3] = __fmaf_rn(rij, x4.w, acc[3]);
+  for (int i0 = 0; i0 < kHeadDim; i0 += 16) {
+    float r[16];
+    float4 x4[16];
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      r[k] = Rc[(i0 + k) * kHeadDim];
+      x4[k] = *reinterpret_cast<const float4*>(&sm.xs[i0 + k][kTokPer * tg]);
+    }
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      acc[0] = __fmaf_rn(r[k], x4[k].x, acc[0]);
+      acc[1] = __fmaf_rn(r[k], x4[k].y, acc[1]);
+      acc[2] = __fmaf_rn(r[k], x4[k].z, acc[2]);
+      acc[3] = __fmaf_rn(r[k], x4[k].w, acc[3]);
+    }
   }
   // ---- route: sink / ring (bf16 r) or INT2 (clip + quantise)
   float xq[kTokPer];
   bool any_q = false;
 #pragma unroll
   for (int u = 0; u < kTokPer; ++u) {
-    const int p = nw[u];
+    const int p = st.nw[u];
     const uint16_t rb = bf16_rne(acc[u]);
     xq[u] = fmaxf(fminf(bf16_f32(rb), clip), -clip);
     if (p < 0) continue;
@@ -256,18 +293,28 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
     mbar_expect_tx(smem_u32(bar), kRBytes);
     bulk_g2s(smem_u32(Rs), R, kRBytes, smem_u32(bar));
   }
+  ItemState st;
+  AppendItem it{};
+  if (work) {
+    it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[blockIdx.x];
+    prepare_item<GROUP>(sm, kp, layer, it, st);
+  }
   pdl_wait();
   pdl_trigger();
   if (!work) return;
-  __syncthreads();  // barrier initialised
+  __syncthreads();  // barrier initialised, row pointers visible
   if (!mbar_wait(smem_u32(bar), 0)) {
     if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
     mbar_wait(smem_u32(bar), 0);  // drain (bounded) before exit
     return;
   }
   for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
-    const AppendItem it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
-    append_item<GROUP>(sm, Rs, kp, layer, it, k_new, v_new);
+    if (ix != int(blockIdx.x)) {
+      it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
+      prepare_item<GROUP>(sm, kp, layer, it, st);
+      __syncthreads();
+    }
+    finish_item<GROUP>(sm, Rs, kp, layer, it, st, k_new, v_new);
     __syncthreads();  // shared memory is reused by the next item
   }
 }

@@ -119,14 +119,18 @@ __global__ void __launch_bounds__(512) qrot_kernel(KernelParams kp, int layer, c
   float acc[HPT];
 #pragma unroll
   for (int k = 0; k < HPT; ++k) acc[k] = 0.f;
-#pragma unroll 8
-  for (int i = 0; i < kHeadDim; i += 4) {
-    const float r0 = Rs[(i + 0) * kHeadDim + c], r1 = Rs[(i + 1) * kHeadDim + c];
-    const float r2 = Rs[(i + 2) * kHeadDim + c], r3 = Rs[(i + 3) * kHeadDim + c];
+  for (int i0 = 0; i0 < kHeadDim; i0 += 16) {  // shared-memory loads of 16 steps ahead of the FMAs
+    float r[16];
+#pragma unroll
+    for (int u = 0; u < 16; ++u) r[u] = Rs[(i0 + u) * kHeadDim + c];
 #pragma unroll
     for (int k = 0; k < HPT; ++k) {
-      const float4 x = *reinterpret_cast<const float4*>(qs + (hg + 4 * k) * kHeadDim + i);
-      acc[k] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[k]))));
+      float4 x[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) x[u] = *reinterpret_cast<const float4*>(qs + (hg + 4 * k) * kHeadDim + i0 + 4 * u);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        acc[k] = fmaf(r[4 * u + 3], x[u].w, fmaf(r[4 * u + 2], x[u].z, fmaf(r[4 * u + 1], x[u].y, fmaf(r[4 * u], x[u].x, acc[k]))));
     }
   }
   const int lane = tid & 31, wq = (tid >> 5) & 3;  // warp wq of this head group covers channels 32wq..
@@ -193,11 +197,14 @@ __device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeI
   }
   const int n = it.head_count;
   const float* base = partials + size_t(it.head_first) * G * P;
-  // ---- pass 1: running (max, sum of exponentials) per head, one load round for m and l
+  // ---- pass 1: running (max, sum of exponentials) per head, one load round for m and l;
+  // the m values stay in shared memory for the weights (when they fit)
+  const bool cache_m = n * G <= kMergeChunk * G;
   float mloc = -INFINITY, lloc = 0.f;
   for (int e = t; e < n * G; e += kThreads) {
     const float* ph = base + size_t(e / G) * G * P + hh * P;
     const float m = __ldcg(ph), l = __ldcg(ph + 1);
+    if (cache_m) ws[e] = m;
     if (m == -INFINITY) continue;
     const float mn = fmaxf(mloc, m);
     lloc = lloc * ex2(mloc - mn) + l * ex2(m - mn);
@@ -225,7 +232,8 @@ __device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeI
     stat[G + t] = ls;
   }
   __syncthreads();
-  // ---- pass 2: weights in chunks; channel c of heads hb, hb + 2, .., 8 partials' loads per round
+  // ---- pass 2: weights in chunks; channel c of heads hb, hb + 2, .., 16 partials' loads per round
+  constexpr int kRound = 16;
   float o[HPT];
 #pragma unroll
   for (int k = 0; k < HPT; ++k) o[k] = 0.f;
@@ -233,20 +241,20 @@ __device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeI
     const int cnt = min(kMergeChunk, n - i0);
     for (int e = t; e < cnt * G; e += kThreads) {
       const int h = e % G;
-      const float m = __ldcg(base + size_t(i0 + e / G) * G * P + h * P);
+      const float m = cache_m ? ws[e] : __ldcg(base + size_t(i0 + e / G) * G * P + h * P);
       const float l = stat[G + h];
       ws[e] = (m == -INFINITY || !(l > 0.f)) ? 0.f : ex2(m - stat[h]) / l;
     }
     __syncthreads();
-    for (int i = 0; i < cnt; i += 8) {
-      float v[8][HPT];
+    for (int i = 0; i < cnt; i += kRound) {
+      float v[kRound][HPT];
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < kRound; ++k)
 #pragma unroll
         for (int q = 0; q < HPT; ++q)
           v[k][q] = i + k < cnt ? __ldcg(base + size_t(i0 + i + k) * G * P + (hb + 2 * q) * P + 2 + c) : 0.f;
 #pragma unroll
-      for (int k = 0; k < 8; ++k)
+      for (int k = 0; k < kRound; ++k)
 #pragma unroll
         for (int q = 0; q < HPT; ++q)
           if (i + k < cnt) o[q] = fmaf(ws[(i + k) * G + hb + 2 * q], v[k][q], o[q]);
