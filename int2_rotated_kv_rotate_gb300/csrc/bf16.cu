@@ -24,11 +24,13 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
   extern __shared__ __align__(128) uint8_t smem[];
   float* qs = reinterpret_cast<float*>(smem + Bf16Rows<4, 2>::kSmemBytes);
   int* s_last_p = reinterpret_cast<int*>(smem + Bf16Rows<4, 2>::kSmemBytes + G * kHeadDim * 4);
-  int& s_last = *s_last_p;
   pdl_wait();
   pdl_trigger();
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
-  for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
+  const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
+                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items};
+  int* s_next = s_last_p + 1;
+  for (int ix = wq.first(); ix >= 0; ix = wq.next(s_next)) {
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
@@ -59,41 +61,21 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
     bf16_rows_mma<G, 4, 2>(rowK, rowV, t0, t1, qs, part, smem);
 
-    __threadfence();
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned* ctr = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
-      const unsigned prev = atomicAdd(ctr, 1u);
-      s_last = prev == unsigned(it.head_count - 1);
-      if (s_last) *ctr = 0u;
-    }
-    __syncthreads();
-    if (s_last) {
-      __threadfence();
+    MergeAcc<G, 128> acc;
+    if (merge_partial<G, 128>(kp, it, ix, partials, acc, s_last_p, [] {}) == kMergeFinal) {
       const int c = threadIdx.x;
+#pragma unroll
       for (int h = 0; h < G; ++h) {
-        float ms = -INFINITY;
-        for (int i = 0; i < it.head_count; ++i)
-          ms = fmaxf(ms, __ldcg(partials + size_t(it.head_first + i) * G * (kHeadDim + 2) + h * (kHeadDim + 2)));
-        float l = 0.f, o = 0.f;
-        for (int i = 0; i < it.head_count; ++i) {
-          const float* ph = partials + size_t(it.head_first + i) * G * (kHeadDim + 2) + h * (kHeadDim + 2);
-          const float m = __ldcg(ph);
-          if (m == -INFINITY) continue;
-          const float w = ex2(m - ms);
-          l = fmaf(w, __ldcg(ph + 1), l);
-          o = fmaf(w, __ldcg(ph + 2 + c), o);
-        }
-        const float r = l > 0.f ? o / l : 0.f;
+        const float r = acc.L[h] > 0.f ? acc.O[h] / acc.L[h] : 0.f;
         out[(head0 + h) * kHeadDim + c] = bf16_rne(r);
         if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = r;
       }
     }
-    __syncthreads();
   }
+  wq.leave();
 }
 
-constexpr int kBf16KernelSmem(int G) { return Bf16Rows<4, 2>::kSmemBytes + G * kHeadDim * 4 + 16; }
+constexpr int kBf16KernelSmem(int G) { return Bf16Rows<4, 2>::kSmemBytes + G * kHeadDim * 4 + 32; }
 
 template <int G>
 int resident_ctas(int n_sm) {

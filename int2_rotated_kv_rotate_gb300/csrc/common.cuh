@@ -314,6 +314,164 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
   __syncthreads();
 }
 
+// Counter increment that publishes the CTA's prior global writes and observes those of
+// earlier incrementers: callers put a __syncthreads() before it (CTA-scope ordering of the
+// other threads' writes, made cumulative by this gpu-scope release) and after it (so the
+// acquire orders the whole CTA's later reads).
+__device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* p, unsigned v) {
+  unsigned old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// ---------------------------------------------------------------- merging partials
+// A partial slot holds, for each of the G heads of a kv group: m (log2 units), l, then the
+// unnormalised o[kHeadDim].  Thread (c, hb) of an NTH-thread CTA owns channel c of heads
+// hb, hb + NTH/128, ...; every thread reads the (m, l) words it needs itself (the same
+// addresses across a warp), so a merge of up to kRound partials takes one round of loads
+// and no block barrier.
+template <int G, int NTH>
+struct MergeAcc {
+  static constexpr int kStride = NTH / kHeadDim;
+  static constexpr int HPT = G / kStride;
+  static_assert(NTH % kHeadDim == 0 && G % kStride == 0, "thread count and group size");
+  float M[HPT], L[HPT], O[HPT];
+};
+
+// acc = online-softmax merge of the partial slots first, first + stride, ... (count slots).
+template <int G, int NTH>
+__device__ void merge_slots(const float* partials, int first, int stride, int count, MergeAcc<G, NTH>& acc) {
+  using A = MergeAcc<G, NTH>;
+  constexpr int P = kHeadDim + 2, HPT = A::HPT, kRound = 16 / HPT > 0 ? 16 / HPT : 1;
+  const int c = threadIdx.x & (kHeadDim - 1), hb = threadIdx.x / kHeadDim;
+#pragma unroll
+  for (int q = 0; q < HPT; ++q) {
+    acc.M[q] = -INFINITY;
+    acc.L[q] = 0.f;
+    acc.O[q] = 0.f;
+  }
+  for (int i0 = 0; i0 < count; i0 += kRound) {
+    float mv[kRound][HPT], lv[kRound][HPT], ov[kRound][HPT];
+#pragma unroll
+    for (int k = 0; k < kRound; ++k)
+#pragma unroll
+      for (int q = 0; q < HPT; ++q) {
+        const bool in = i0 + k < count;
+        const float* ph = partials + (size_t(first) + size_t(i0 + k) * stride) * G * P + (hb + A::kStride * q) * P;
+        mv[k][q] = in ? __ldcg(ph) : -INFINITY;
+        lv[k][q] = in ? __ldcg(ph + 1) : 0.f;
+        ov[k][q] = in ? __ldcg(ph + 2 + c) : 0.f;
+      }
+#pragma unroll
+    for (int k = 0; k < kRound; ++k)
+#pragma unroll
+      for (int q = 0; q < HPT; ++q) {
+        if (mv[k][q] == -INFINITY) continue;
+        const float mn = fmaxf(acc.M[q], mv[k][q]);
+        const float a = ex2(acc.M[q] - mn), b = ex2(mv[k][q] - mn);  // acc.M = -inf gives a = 0
+        acc.L[q] = fmaf(acc.L[q], a, lv[k][q] * b);
+        acc.O[q] = fmaf(acc.O[q], a, ov[k][q] * b);
+        acc.M[q] = mn;
+      }
+  }
+}
+
+template <int G, int NTH>
+__device__ void store_partial(float* slot, const MergeAcc<G, NTH>& acc) {
+  using A = MergeAcc<G, NTH>;
+  constexpr int P = kHeadDim + 2;
+  const int c = threadIdx.x & (kHeadDim - 1), hb = threadIdx.x / kHeadDim;
+#pragma unroll
+  for (int q = 0; q < A::HPT; ++q) {
+    float* ph = slot + (hb + A::kStride * q) * P;
+    if (c == 0) {
+      ph[0] = acc.M[q];
+      ph[1] = acc.L[q];
+    }
+    ph[2 + c] = acc.O[q];
+  }
+}
+
+// Roles of a CTA after merge_partial.
+constexpr int kMergeNone = 0;       // not the last of its group: nothing to do
+constexpr int kMergeGroupOnly = 1;  // merged its group into the group's first slot
+constexpr int kMergeFinal = 2;      // holds the whole (request, kv-head) merge in acc
+
+// After the partial of item `it` (slot ix) is written, by every thread: the last finisher
+// of each group of kMergeGroup consecutive items merges the group; the last group merger
+// merges the groups.  on_group_last() runs (all threads) as soon as this CTA knows it
+// merges a group.  s_flag: one int of shared memory.
+template <int G, int NTH, typename OnGroupLast>
+__device__ int merge_partial(const KernelParams& kp, const DecodeItem& it, int ix, float* partials,
+                             MergeAcc<G, NTH>& acc, int* s_flag, OnGroupLast on_group_last) {
+  __syncthreads();  // the partial is written (published by the release below)
+  const int grp = (ix - it.head_first) / kMergeGroup;
+  const int n_groups = (it.head_count + kMergeGroup - 1) / kMergeGroup;
+  const int grp_first = it.head_first + grp * kMergeGroup;
+  const int grp_size = min(kMergeGroup, it.head_count - grp * kMergeGroup);
+  if (threadIdx.x == 0) {
+    unsigned* gc = reinterpret_cast<unsigned*>(kp.base + kp.lay.group_counters) + it.gcounter;
+    const unsigned prev = atomic_add_acq_rel(gc, 1u);
+    *s_flag = prev == unsigned(grp_size - 1);
+    if (*s_flag) *gc = 0u;  // every partial of the group has arrived
+  }
+  __syncthreads();
+  if (!*s_flag) return kMergeNone;
+  on_group_last();
+  merge_slots<G, NTH>(partials, grp_first, 1, grp_size, acc);
+  if (n_groups == 1) return kMergeFinal;
+  __syncthreads();  // every thread has read the group's slots before the first is overwritten
+  store_partial<G, NTH>(partials + size_t(grp_first) * G * (kHeadDim + 2), acc);
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned* hc = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
+    const unsigned prev = atomic_add_acq_rel(hc, 1u);
+    *s_flag = prev == unsigned(n_groups - 1);
+    if (*s_flag) *hc = 0u;
+  }
+  __syncthreads();
+  if (!*s_flag) return kMergeGroupOnly;
+  merge_slots<G, NTH>(partials, it.head_first, kMergeGroup, n_groups, acc);
+  return kMergeFinal;
+}
+
+// Dynamic work distribution of a persistent-style decode grid: CTA b first takes
+// order[b] (known before any wait, so its copies can be issued early), then the next free
+// position gridDim.x + atomicAdd(work counter).  The last CTA to leave resets both counters
+// for the next launch (launches of one cache never overlap).  A plan of at most one item
+// per CTA uses neither counter.  Call from all threads.
+struct WorkQueue {
+  const int* order;
+  unsigned* counters;  // [0] work, [1] exit
+  int n;
+  // One wave (every item has its own CTA): no counters, item b is CTA b's.
+  __device__ bool one_wave() const { return n <= int(gridDim.x); }
+  __device__ int first() const {
+    if (int(blockIdx.x) >= n) return -1;
+    return one_wave() ? int(blockIdx.x) : order[blockIdx.x];
+  }
+  __device__ int next(int* s_slot) const {
+    if (one_wave()) return -1;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      const int pos = int(gridDim.x) + int(atomicAdd(&counters[0], 1u));
+      *s_slot = pos < n ? order[pos] : -1;
+    }
+    __syncthreads();
+    return *s_slot;
+  }
+  __device__ void leave() const {
+    if (one_wave()) return;
+    if (threadIdx.x == 0) {
+      __threadfence();  // this CTA's work-counter updates precede its exit
+      if (atomicAdd(&counters[1], 1u) == gridDim.x - 1) {
+        atomicExch(&counters[0], 0u);
+        atomicExch(&counters[1], 0u);
+      }
+    }
+  }
+};
+
 // Launch with programmatic stream serialization (PDL) allowed.
 template <typename Kern, typename... Args>
 int launch_ex(Kern kernel, dim3 grid, dim3 block, size_t smem, void* stream, Args... args) {

@@ -165,115 +165,41 @@ struct Cfg {
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
   static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers (128 B), merge flag and merge barrier
   static_assert(kPipeBytes >= Bf16Rows<kWarps, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
-  static_assert(kPipeBytes >= (kHeadDim * kHeadDim + G * kHeadDim + 64 * G + kWarps * G + (2 + kWarps) * G) * 4,
-                "the merge reuses the page pipeline memory");
+  static_assert(kPipeBytes >= (kHeadDim * kHeadDim + G * kHeadDim) * 4, "the merge reuses the page pipeline memory");
 };
 
-// Merge all partials of (request, kv-head), rotate back and store.  128 threads.
-// R_V^T (64 KB) comes into shared memory by one bulk copy while the partials merge:
-// pass 1 finds the max and the sum of exponentials per head (thread t owns head t % G,
-// loads spread over all threads), pass 2 forms the weights of up to kMergeChunk partials
-// at a time in shared memory and accumulates channel t of every head.
-constexpr int kMergeChunk = 64;
-
-template <int G>
-__device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeItem& it, const float* partials,
-                                uint16_t* out, float* out_f32, uint8_t* smem, uint32_t mbar, uint32_t& mphase) {
-  const int t = threadIdx.x, warp = t >> 5, lane = t & 31, hh = t % G;
-  const int c = t & (kHeadDim - 1), hb = t >> 7;  // pass 2 and the rotation: channel c, heads hb, hb + 2, ..
-  constexpr int HPT = G / (kThreads / kHeadDim);
-  constexpr int P = kHeadDim + 2;
-  float* Rs = reinterpret_cast<float*>(smem);      // R_V^T [128][128]
-  float* os = Rs + kHeadDim * kHeadDim;            // o~ [G][128]
-  float* ws = os + G * kHeadDim;                   // weights [kMergeChunk][G]
-  float* red = ws + kMergeChunk * G;               // [4 warps][G]
-  float* stat = red + kWarps * G;                  // m*[G], l*[G], per-warp sums [kWarps][G]
-  const float* RVt = reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
-                     (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim;
-  if (t == 0) {
+// Start the bulk copy of R_V^T (64 KB) of (layer, kv-head) into smem[0, 64 KB).
+__device__ void fetch_rvt(const KernelParams& kp, int layer, int kvh, uint8_t* smem, uint32_t mbar) {
+  if (threadIdx.x == 0) {
+    const float* RVt = reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
+                       (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
     fence_proxy_async();
     mbar_expect_tx(mbar, kHeadDim * kHeadDim * 4);
-    bulk_g2s(smem_u32(Rs), RVt, kHeadDim * kHeadDim * 4, mbar);
+    bulk_g2s(smem_u32(smem), RVt, kHeadDim * kHeadDim * 4, mbar);
   }
-  const int n = it.head_count;
-  const float* base = partials + size_t(it.head_first) * G * P;
-  // ---- pass 1: running (max, sum of exponentials) per head, one load round for m and l;
-  // the m values stay in shared memory for the weights (when they fit)
-  const bool cache_m = n * G <= kMergeChunk * G;
-  float mloc = -INFINITY, lloc = 0.f;
-  for (int e = t; e < n * G; e += kThreads) {
-    const float* ph = base + size_t(e / G) * G * P + hh * P;
-    const float m = __ldcg(ph), l = __ldcg(ph + 1);
-    if (cache_m) ws[e] = m;
-    if (m == -INFINITY) continue;
-    const float mn = fmaxf(mloc, m);
-    lloc = lloc * ex2(mloc - mn) + l * ex2(m - mn);
-    mloc = mn;
-  }
-  for (int off = G; off < 32; off <<= 1) {
-    const float mo = __shfl_xor_sync(0xffffffffu, mloc, off), lo = __shfl_xor_sync(0xffffffffu, lloc, off);
-    const float mn = fmaxf(mloc, mo);
-    lloc = (mloc == -INFINITY ? 0.f : lloc * ex2(mloc - mn)) + (mo == -INFINITY ? 0.f : lo * ex2(mo - mn));
-    mloc = mn;
-  }
-  if (lane < G) {
-    red[warp * G + lane] = mloc;
-    stat[2 * G + warp * G + lane] = lloc;  // scratch for the per-warp sums
-  }
-  __syncthreads();
-  if (t < G) {
-    float ms = -INFINITY, ls = 0.f;
-    for (int w = 0; w < kWarps; ++w) ms = fmaxf(ms, red[w * G + t]);
-    for (int w = 0; w < kWarps; ++w) {
-      const float mw = red[w * G + t];
-      if (mw != -INFINITY) ls += stat[2 * G + w * G + t] * ex2(mw - ms);
-    }
-    stat[t] = ms;
-    stat[G + t] = ls;
-  }
-  __syncthreads();
-  // ---- pass 2: weights in chunks; channel c of heads hb, hb + 2, .., 16 partials' loads per round
-  constexpr int kRound = 16;
-  float o[HPT];
+}
+
+// Final merge: o~ = O / L, then o = R_V o~ with R_V^T in smem (fetched by fetch_rvt; this
+// waits for it), bf16 and optional fp32 store.
+template <int G>
+__device__ void finish_output(const KernelParams& kp, const DecodeItem& it, const MergeAcc<G, kThreads>& acc, uint16_t* out,
+                              float* out_f32, uint8_t* smem, uint32_t mbar, uint32_t& mphase) {
+  constexpr int HPT = MergeAcc<G, kThreads>::HPT;
+  const int t = threadIdx.x, c = t & (kHeadDim - 1), hb = t >> 7;
+  const float* Rs = reinterpret_cast<const float*>(smem);   // R_V^T [128][128]
+  float* os = reinterpret_cast<float*>(smem) + kHeadDim * kHeadDim;  // o~ [G][128]
 #pragma unroll
-  for (int k = 0; k < HPT; ++k) o[k] = 0.f;
-  for (int i0 = 0; i0 < n; i0 += kMergeChunk) {
-    const int cnt = min(kMergeChunk, n - i0);
-    for (int e = t; e < cnt * G; e += kThreads) {
-      const int h = e % G;
-      const float m = cache_m ? ws[e] : __ldcg(base + size_t(i0 + e / G) * G * P + h * P);
-      const float l = stat[G + h];
-      ws[e] = (m == -INFINITY || !(l > 0.f)) ? 0.f : ex2(m - stat[h]) / l;
-    }
-    __syncthreads();
-    for (int i = 0; i < cnt; i += kRound) {
-      float v[kRound][HPT];
-#pragma unroll
-      for (int k = 0; k < kRound; ++k)
-#pragma unroll
-        for (int q = 0; q < HPT; ++q)
-          v[k][q] = i + k < cnt ? __ldcg(base + size_t(i0 + i + k) * G * P + (hb + 2 * q) * P + 2 + c) : 0.f;
-#pragma unroll
-      for (int k = 0; k < kRound; ++k)
-#pragma unroll
-        for (int q = 0; q < HPT; ++q)
-          if (i + k < cnt) o[q] = fmaf(ws[(i + k) * G + hb + 2 * q], v[k][q], o[q]);
-    }
-    __syncthreads();
-  }
-#pragma unroll
-  for (int q = 0; q < HPT; ++q) os[(hb + 2 * q) * kHeadDim + c] = o[q];
-  __syncthreads();
+  for (int q = 0; q < HPT; ++q) os[(hb + 2 * q) * kHeadDim + c] = acc.L[q] > 0.f ? acc.O[q] / acc.L[q] : 0.f;
   const bool ok = mbar_wait(mbar, mphase);
   if (!ok) {
     if (t == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
     mbar_wait(mbar, mphase);  // drain (bounded) before the memory is reused
   }
   mphase ^= 1u;
-  // ---- o = R_V o~: thread reads column c of R_V^T (conflict-free), o~ broadcast
-  float acc[HPT];
+  __syncthreads();
+  float r[HPT];
 #pragma unroll
-  for (int q = 0; q < HPT; ++q) acc[q] = 0.f;
+  for (int q = 0; q < HPT; ++q) r[q] = 0.f;
 #pragma unroll 4
   for (int j = 0; j < kHeadDim; j += 4) {
     const float r0 = Rs[(j + 0) * kHeadDim + c], r1 = Rs[(j + 1) * kHeadDim + c];
@@ -281,18 +207,17 @@ __device__ void merge_and_store(const KernelParams& kp, int layer, const DecodeI
 #pragma unroll
     for (int q = 0; q < HPT; ++q) {
       const float4 x = *reinterpret_cast<const float4*>(os + (hb + 2 * q) * kHeadDim + j);
-      acc[q] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, acc[q]))));
+      r[q] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, r[q]))));
     }
   }
   const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
 #pragma unroll
   for (int q = 0; q < HPT; ++q) {
     const int h = hb + 2 * q;
-    out[(head0 + h) * kHeadDim + c] = bf16_rne(ok ? acc[q] : 0.f);
-    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = ok ? acc[q] : 0.f;
+    out[(head0 + h) * kHeadDim + c] = bf16_rne(ok ? r[q] : 0.f);
+    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = ok ? r[q] : 0.f;
   }
 }
-
 
 // BF16 tokens of the sink + ring list: list index u < min(L, S) is sink u, otherwise
 // position H + u - min(L, S) in ring slot p % W.
@@ -666,10 +591,14 @@ __global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int la
   // right before this one) only lets this grid start after its own wait on the append:
   // the first INT2 item's page copies can be issued before waiting for the rotated q.
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
+  const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
+                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items};
+  int* s_next = s_last + 1;
+  const int first_ix = wq.first();
   bool pre_issued = false;
   uint32_t pre_mask = 0;
-  if (int(blockIdx.x) < n_items) {
-    const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[blockIdx.x];
+  if (first_ix >= 0) {
+    const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[first_ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     if (it.kind == 0 && dr.slot >= 0 && dr.slot < kp.max_requests) {
       const int warp = threadIdx.x >> 5;
@@ -682,7 +611,7 @@ __global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int la
   pdl_wait();
   pdl_trigger();
   uint32_t phase_bits = 0, merge_phase = 0;
-  for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
+  for (int ix = first_ix; ix >= 0; ix = wq.next(s_next)) {
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     float* part = partials + size_t(ix) * G * (kHeadDim + 2);
@@ -692,30 +621,29 @@ __global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int la
       for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += kThreads)
         part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
     } else if (it.kind == 0) {
-      const bool pre = pre_issued && ix == int(blockIdx.x);
+      const bool pre = pre_issued && ix == first_ix;
+      pre_issued = false;
       int2_pages_item<G, GROUP>(kp, layer, it, dr, qt + head0 * kHeadDim, qsum + head0 * 4, part, smem, phase_bits,
                                 pre, pre_mask);
     } else {
       bf16_tokens_item<G>(kp, layer, it, dr, qt + head0 * kHeadDim, part, smem);
     }
-    // ---- the last CTA of this (request, kv-head) merges and stores
-    __threadfence();  // this thread's partial stores are visible device-wide before the count
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned* ctr = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
-      const unsigned prev = atomicAdd(ctr, 1u);
-      *s_last = prev == unsigned(it.head_count - 1);
-      if (*s_last) *ctr = 0u;  // every partial has arrived; ready for the next launch
-    }
-    __syncthreads();
-    if (*s_last) {
-      __threadfence();
-      merge_and_store<G>(kp, layer, it, partials, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
+    // ---- two-level merge of the partials; R_V^T is fetched as soon as this CTA knows it
+    // merges a group (it may then finish the head)
+    MergeAcc<G, kThreads> acc;
+    const int role = merge_partial<G, kThreads>(kp, it, ix, partials, acc, s_last,
+                                                [&] { fetch_rvt(kp, layer, it.kvh, smem, smem_u32(merge_bar)); });
+    if (role == kMergeFinal) {
+      finish_output<G>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
+    } else if (role == kMergeGroupOnly) {
+      // drain the speculative R_V^T copy before the memory is reused (bounded)
+      if (!mbar_wait(smem_u32(merge_bar), merge_phase)) mbar_wait(smem_u32(merge_bar), merge_phase);
+      merge_phase ^= 1u;
     }
     // generic-proxy use of the stage memory is over before the next item's bulk copies
     fence_proxy_async();
-    __syncthreads();
   }
+  wq.leave();
 }
 
 template <int G, int GROUP>

@@ -114,6 +114,7 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.page_table = take(reqs * size_t(c.max_pages_per_request) * 4);
   L.status = take(256);
   L.counters = take(reqs * Hkv * 4);
+  L.group_counters = 0;  // placed after the decode items (its size depends on them)
   L.plan_counts = take(16);
   L.max_append_items = kMaxAppendTokenItems + reqs * (kMaxWindow / kAppendChunk);
   L.max_decode_items = reqs * Hkv * (2 + kMaxWindow / kBf16ItemTokens) + 16384;
@@ -121,6 +122,9 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.append_items = take(L.max_append_items * sizeof(AppendItem));
   L.decode_reqs = take(reqs * sizeof(DecodeReq));
   L.decode_items = take(L.max_decode_items * sizeof(DecodeItem));
+  L.decode_order = take(L.max_decode_items * 4);
+  L.sched = take(16);
+  L.group_counters = take(L.max_decode_items * 4);
   L.total = off;
   return L;
 }
@@ -252,7 +256,8 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   for (int p = cfg->max_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
   const size_t pt_bytes = size_t(cfg->max_requests) * cfg->max_pages_per_request * 4;
   c->staging_bytes = align256(size_t(cfg->max_requests) * std::max(sizeof(AppendReq), sizeof(DecodeReq))) +
-                     std::max(lay.max_append_items * sizeof(AppendItem), lay.max_decode_items * sizeof(DecodeItem));
+                     std::max(lay.max_append_items * sizeof(AppendItem),
+                              align256(lay.max_decode_items * sizeof(DecodeItem)) + lay.max_decode_items * 4);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_page_table), pt_bytes);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_staging), c->staging_bytes);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_status), 256);
@@ -266,6 +271,8 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   }
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.status, 0, 256);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.counters, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.group_counters, 0, lay.max_decode_items * 4);
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.sched, 0, 16);
   if (e == cudaSuccess && is_int2(c)) {
     // layer params start as zeros until oscar_set_layer_params
     e = cudaMemset(c->base + lay.R_K, 0, lay.clip_K - lay.R_K);
@@ -585,17 +592,25 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
         }
     total_pages += (long long)Hkv * pages_needed(c, Ls[i], Hs[i]);
   }
-  // Work items: per (request, kv-head) the BF16 sink+ring items and INT2 page ranges of
-  // `chunk` pages.  Automatic chunk: the smallest that lets one wave of resident CTAs hold
-  // every item (a second, partial wave would double the time of a latency-bound step).
+  // Work items: per (request, kv-head) the BF16 sink+ring items and page ranges of
+  // `chunk` pages.  Automatic chunk, from the bytes each resident CTA would stream:
+  //  - small steps (latency-bound): the smallest chunk that lets one wave of resident CTAs
+  //    hold every item (a second, partial wave would add a whole item's latency);
+  //  - large steps: about kWaves items per resident CTA (at least kItemBytes each), taken
+  //    dynamically by the CTAs, largest first, so the ragged tail stays short while the
+  //    per-item costs (pipeline fill, partial store and merge) stay small.
   std::vector<int> np_of(n_req), nbf_of(n_req);
   long long n_bf_items = 0;
   int max_np = 1;
+  const int ng = kHeadDim / (is_int2(c) ? c->cfg.group : kHeadDim);
+  const long long page_bytes = is_int2(c) ? 2LL * kPage * (kRowBytes + 4 * ng) : 2LL * kPage * kHeadDim * 2;
+  long long total_bytes = 0;
   for (int i = 0; i < n_req; ++i) {
     np_of[i] = pages_needed(c, Ls[i], Hs[i]);
     nbf_of[i] = is_int2(c) ? std::min(Ls[i], S) + std::max(0, Ls[i] - Hs[i]) : 0;
     n_bf_items += (long long)Hkv * (nbf_of[i] > 0 ? ceil_div(nbf_of[i], kBf16ItemTokens) : 0);
     max_np = std::max(max_np, np_of[i]);
+    total_bytes += (long long)Hkv * (np_of[i] * page_bytes + nbf_of[i] * 2LL * kHeadDim * 2);
   }
   auto count_items = [&](int ch) {
     long long n = n_bf_items;
@@ -605,14 +620,24 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     }
     return n;
   };
+  constexpr long long kItemBytes = 512 << 10;
+  constexpr long long kWaves = 4;
   int chunk = max_split_pages;
   if (chunk == 0) {
     const int G = c->cfg.n_q_heads / Hkv;
     int resident = is_int2(c) ? decode_resident_ctas(G, c->cfg.group, c->n_sm) : bf16_decode_resident_ctas(G, c->n_sm);
     if (resident <= 0) resident = 2 * c->n_sm;
-    const long long slots = std::max<long long>(1, resident - n_bf_items);
-    chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
-    while (chunk < max_np && count_items(chunk) > resident) ++chunk;
+    if (total_bytes <= kItemBytes * resident) {
+      const long long slots = std::max<long long>(1, resident - n_bf_items);
+      chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
+      while (chunk < max_np && count_items(chunk) > resident) ++chunk;
+    } else {
+      const long long item_bytes = std::max(kItemBytes, total_bytes / (kWaves * resident));
+      chunk = int(std::max<long long>(4, item_bytes / page_bytes));
+    }
+    // the plan must fit the item buffers
+    while (chunk < max_np && count_items(chunk) > (long long)c->lay.max_decode_items)
+      chunk = std::min(max_np, chunk + chunk / 4 + 1);
   }
   std::vector<DecodeReq> reqs(n_req);
   std::vector<DecodeItem> items;
@@ -632,16 +657,19 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     q.items_per_head = per_head;
     for (int h = 0; h < Hkv; ++h) {
       const int first = int(items.size());
+      const int gc_base = first;  // group g of this (req, kv-head) counts on group_counters[first + g]
       if (n_bf_items + n_pg_items == 0) {
-        items.push_back({i, h, 1, 0, 0, first, per_head, 0});
+        items.push_back({i, h, 1, 0, 0, first, per_head, gc_base});
         continue;
       }
       for (int t = 0; t < n_bf; t += kBf16ItemTokens) {
-        items.push_back({i, h, 1, t, std::min(n_bf, t + kBf16ItemTokens), first, per_head, 0});
+        items.push_back({i, h, 1, t, std::min(n_bf, t + kBf16ItemTokens), first, per_head,
+                         gc_base + (int(items.size()) - first) / kMergeGroup});
         ++n_bf16;
       }
       for (int p = 0; p < np; p += chunk) {
-        items.push_back({i, h, 0, p, std::min(np, p + chunk), first, per_head, 0});
+        items.push_back({i, h, 0, p, std::min(np, p + chunk), first, per_head,
+                         gc_base + (int(items.size()) - first) / kMergeGroup});
         max_pages = std::max(max_pages, std::min(np, p + chunk) - p);
       }
     }
@@ -649,12 +677,22 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   if (items.size() > c->lay.max_decode_items)
     return fail(OSCAR_ERR_INVALID_ARG, "plan of %zu items exceeds %zu; raise max_split_pages", items.size(),
                 c->lay.max_decode_items);
+  // the order CTAs take items in: largest first (stable)
+  std::vector<int> order(items.size());
+  for (size_t k = 0; k < items.size(); ++k) order[k] = int(k);
+  auto cost = [&](const DecodeItem& d) {
+    return d.kind == 0 ? (long long)(d.end - d.begin) * page_bytes : (long long)(d.end - d.begin) * 2LL * kHeadDim * 2;
+  };
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost(items[a]) > cost(items[b]); });
   oscar_status st = wait_uploads(c);
   if (st) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const size_t rb = reqs.size() * sizeof(DecodeReq);
   std::memcpy(c->h_staging, reqs.data(), rb);
   std::memcpy(c->h_staging + align256(rb), items.data(), items.size() * sizeof(DecodeItem));
+  uint8_t* h_order = c->h_staging + align256(rb) + align256(items.size() * sizeof(DecodeItem));
+  std::memcpy(h_order, order.data(), order.size() * 4);
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_order, h_order, order.size() * 4, cudaMemcpyHostToDevice, s));
   c->h_counts[1] = int(items.size());
   c->h_counts[2] = n_req;
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.plan_counts + 4, c->h_counts + 1, 8, cudaMemcpyHostToDevice, s));

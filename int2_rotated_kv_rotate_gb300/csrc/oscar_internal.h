@@ -43,6 +43,11 @@ struct DecodeReq {
 // One split-K work item: pages [p0, p1) of the INT2 history (kind 0) or BF16 tokens
 // [t0, t1) of the sink+ring list (kind 1; index < S is sink j, else ring position H + j - S)
 // of request `req` (plan index), kv-head `kvh`.  Partial results go to slot `item`.
+// Partials of one (request, kv-head) merge in two levels: each group of kMergeGroup
+// consecutive items is merged by its last finisher (into the group's first slot), then the
+// last group merger combines the group results.
+constexpr int kMergeGroup = 8;
+
 struct DecodeItem {
   int req;
   int kvh;
@@ -51,7 +56,7 @@ struct DecodeItem {
   int end;
   int head_first;  // first partial slot of this (req, kvh)
   int head_count;  // number of partial slots of this (req, kvh)
-  int pad;
+  int gcounter;    // merge-group counter of this item (groups of kMergeGroup consecutive items)
 };
 
 struct DeviceLayout {
@@ -67,9 +72,12 @@ struct DeviceLayout {
   // control
   size_t page_table;  // int32 [max_requests][max_pages_per_request]
   size_t status;      // uint32 flags
-  size_t counters;    // uint32 [max_requests][H_kv] merge counters
+  size_t counters;    // uint32 [max_requests][H_kv] merge counters (second level)
+  size_t group_counters;  // uint32 [max_decode_items] first-level merge counters
   size_t plan_counts; // int32 [4]: append items, decode items, decode requests, unused
   size_t append_reqs, append_items, decode_reqs, decode_items;
+  size_t decode_order;  // int32 [max_decode_items]: items in the order CTAs take them (largest first)
+  size_t sched;         // uint32 [4]: dynamic work counter, CTA exit counter (self-resetting)
   size_t max_append_items, max_decode_items;
   size_t total;
 };

@@ -201,6 +201,27 @@ def test_shared_prefix_bit_identical_to_private_copy():
 
 
 @pytest.mark.parametrize("gqa", [4, 8])
+def test_plans_larger_than_one_wave(gqa):
+    """Single-page items, several times more than the CTAs resident at once: the CTAs take
+    items from the shared work counter, merge in two levels, and leave the counters reset
+    for the next launch (three decodes in a row, with plans of different sizes)."""
+    w = wl.scaled(wl.WORKLOADS["tiny"], name=f"waves_{gqa}", n_q_heads=8 * gqa, n_kv_heads=8, context=3000,
+                  lognormal_sigma=0.5)
+    lens = [3000, 2100, 900]
+    cache, oc, _ = make_pair(w, SEED, 1, len(lens), 3000)
+    slots = [cache.alloc() for _ in lens]
+    cache.reserve(slots, lens)
+    append_both(cache, oc, w, 0, slots, list(range(len(lens))), [0] * len(lens), lens)
+    cache.commit()
+    torch.cuda.synchronize()
+    for step, msp in enumerate((1, 2, 1)):
+        decode_and_compare(cache, oc, w, 0, slots, list(range(len(lens))), step, f"waves msp {msp}",
+                           max_split_pages=msp)
+        n_items, n_bf16, _ = cache.plan_info()
+        assert n_items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+
+
+@pytest.mark.parametrize("gqa", [4, 8])
 def test_bf16_comparison_path(gqa):
     """Uncompressed BF16 pages: decode equals plain softmax attention on the bf16 tokens."""
     w = wl.scaled(wl.WORKLOADS["tiny"], name=f"bf16_{gqa}", n_q_heads=2 * gqa, lognormal_sigma=0.5)
@@ -215,15 +236,17 @@ def test_bf16_comparison_path(gqa):
     cache.reserve(slots, lens)
     cache.bf16_append(0, torch.cat(Ks).contiguous(), torch.cat(Vs).contiguous())
     cache.commit()
-    cache.plan(slots, max_split_pages=4)
-    q = wl.gen_q(w, SEED, 0, 0, 3, device="cuda")
-    out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
-    out = cache.decode(0, q, out_f32=out32)
-    torch.cuda.synchronize()
-    qb = bits(q)
-    for r in range(3):
-        ref = bf16_reference(qb[r], bits(Ks[r]), bits(Vs[r]))
-        compare_decode(out32[r], out[r], ref, f"bf16 req {r}")
+    # a few multi-page items (one wave), then single-page items: more than one wave
+    for step, msp in enumerate((4, 1, 1)):
+        cache.plan(slots, max_split_pages=msp)
+        q = wl.gen_q(w, SEED, 0, step, 3, device="cuda")
+        out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        out = cache.decode(0, q, out_f32=out32)
+        torch.cuda.synchronize()
+        qb = bits(q)
+        for r in range(3):
+            ref = bf16_reference(qb[r], bits(Ks[r]), bits(Vs[r]))
+            compare_decode(out32[r], out[r], ref, f"bf16 msp {msp} req {r}")
 
 
 def test_bad_page_entry_is_flagged_not_faulting():
