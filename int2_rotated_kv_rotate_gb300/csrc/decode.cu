@@ -4,13 +4,12 @@
 // unpacks and dequantises the INT2 history, works in the rotated basis and applies the
 // inverse rotation, over paged KV with prefix sharing, without extra memory traffic.
 //
-// Launches per layer:
-//   1. qrot_kernel     q~ = R_K^T q per query head (fp32) and per-group sums of q~.
-//   2. split_kernel    one CTA per work item (plan): either INT2 pages [p0, p1) of one
-//                      (request, kv-head), or BF16 sink/ring tokens.  Writes a partial
-//                      (m, l, o~) in the rotated basis; the last CTA of each (request,
-//                      kv-head) merges the partials (log-sum-exp), applies o = R_V o~ and
-//                      stores bf16 (and optional fp32) output.
+// One launch per layer: split_kernel, a persistent-style grid whose CTAs take work items
+// (plan): either INT2 pages [p0, p1) of one (request, kv-head), or BF16 sink/ring tokens.
+// Each item first rotates its query heads, q~ = R_K^T q (fp32, R_K columns loaded into
+// registers before the wait on the preceding kernel), then writes a partial (m, l, o~) in
+// the rotated basis; the last CTA of each (request, kv-head) merges the partials
+// (log-sum-exp), applies o = R_V o~ and stores bf16 (and optional fp32) output.
 //
 // INT2 page pipeline (per warp, no block barriers): lane 0 issues cp.async.bulk copies of
 // the page's code block (K 2 KB + V 2 KB) and scale/zero block into a private ring of
@@ -75,83 +74,63 @@ __device__ __forceinline__ uint32_t field(uint32_t w, uint32_t w_shr8, int f) {
 __device__ __forceinline__ int tau8(int m) { return (m >> 1) + 4 * (m & 1); }
 
 // ---------------------------------------------------------------- q rotation
-// One CTA per (request, kv-head): R_K (64 KB) arrives in shared memory by one bulk copy,
-// issued before the wait on the preceding kernel (R_K is written long before by
-// oscar_set_layer_params); R_V^T is prefetched into L2 for the merge of this layer.
-template <int G>
-struct QrotSmem {
-  static constexpr int kR = kHeadDim * kHeadDim * 4;  // R_K, fp32
-  static constexpr int kQ = G * kHeadDim * 4;
-  static constexpr int kBytes = kR + kQ + G * 4 * 4 + 16;
-};
+// Thread (c, half) of a split CTA holds column c of R_K, rows 64 half .. 64 half + 63
+// (R_K is written long before by oscar_set_layer_params, so this runs before the wait on
+// the preceding kernel).
+__device__ __forceinline__ void load_rk_cols(const KernelParams& kp, int layer, int kvh, float (&rk)[64]) {
+  const int c = threadIdx.x & (kHeadDim - 1), i0 = (threadIdx.x >> 7) * 64;
+  const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) +
+                   (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim + size_t(i0) * kHeadDim + c;
+#pragma unroll
+  for (int u = 0; u < 64; ++u) rk[u] = __ldg(R + u * kHeadDim);
+}
 
-template <int G>
-__global__ void __launch_bounds__(512) qrot_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
-                                                   float* __restrict__ qt, float* __restrict__ qsum) {
-  extern __shared__ __align__(128) uint8_t smem[];
-  using SM = QrotSmem<G>;
-  constexpr int HPT = G / 4;  // heads per thread: thread (c, hg) takes heads hg, hg + 4
-  float* Rs = reinterpret_cast<float*>(smem);
-  float* qs = reinterpret_cast<float*>(smem + SM::kR);
-  float* red = qs + G * kHeadDim;  // [G][4]
-  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + SM::kR + SM::kQ + G * 4 * 4);
-  const int req = blockIdx.x / kp.n_kv_heads, kvh = blockIdx.x % kp.n_kv_heads;
-  const int tid = threadIdx.x, c = tid & 127, hg = tid >> 7;
-  const size_t mat = size_t(kHeadDim) * kHeadDim;
-  const size_t lh = size_t(layer) * kp.n_kv_heads + kvh;
-  const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) + lh * mat;
-  if (tid == 0) {
-    mbar_init(smem_u32(bar), 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    mbar_expect_tx(smem_u32(bar), SM::kR);
-    bulk_g2s(smem_u32(Rs), R, SM::kR, smem_u32(bar));
-    bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) + lh * mat, SM::kR);
-  }
-  pdl_wait();
-  pdl_trigger();
-  const size_t head0 = size_t(req) * kp.n_q_heads + size_t(kvh) * G;
-  for (int e = tid; e < G * kHeadDim; e += 512) qs[e] = bf16_f32(q[head0 * kHeadDim + e]);
+// q~ = R_K^T q (fp32) for the G query heads at q_head0 into qts[G][d] (shared), and the
+// sums of q~ over each 32-channel quarter into qss[G][4] (GROUP = 128: qss[h][0] holds the
+// whole sum, the rest 0).  qin: G * d floats of shared staging.  All threads.
+template <int G, int GROUP>
+__device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)[64], float* qin, float* qts,
+                         float* qss) {
+  const int tid = threadIdx.x, c = tid & (kHeadDim - 1), half = tid >> 7;
+  for (int e = tid; e < G * kHeadDim; e += kThreads) qin[e] = bf16_f32(q_head0[e]);
   __syncthreads();
-  if (!mbar_wait(smem_u32(bar), 0)) {
-    if (tid == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
-    mbar_wait(smem_u32(bar), 0);
-  }
-  float acc[HPT];
+  float acc[G];
 #pragma unroll
-  for (int k = 0; k < HPT; ++k) acc[k] = 0.f;
-  for (int i0 = 0; i0 < kHeadDim; i0 += 16) {  // shared-memory loads of 16 steps ahead of the FMAs
-    float r[16];
+  for (int h = 0; h < G; ++h) acc[h] = 0.f;
 #pragma unroll
-    for (int u = 0; u < 16; ++u) r[u] = Rs[(i0 + u) * kHeadDim + c];
+  for (int u = 0; u < 64; u += 4)
 #pragma unroll
-    for (int k = 0; k < HPT; ++k) {
-      float4 x[4];
+    for (int h = 0; h < G; ++h) {
+      const float4 x = *reinterpret_cast<const float4*>(qin + h * kHeadDim + 64 * half + u);
+      acc[h] = fmaf(rk[u + 3], x.w, fmaf(rk[u + 2], x.z, fmaf(rk[u + 1], x.y, fmaf(rk[u], x.x, acc[h]))));
+    }
+  if (half == 1)
 #pragma unroll
-      for (int u = 0; u < 4; ++u) x[u] = *reinterpret_cast<const float4*>(qs + (hg + 4 * k) * kHeadDim + i0 + 4 * u);
+    for (int h = 0; h < G; ++h) qts[h * kHeadDim + c] = acc[h];
+  __syncthreads();
+  if (half == 0)
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        acc[k] = fmaf(r[4 * u + 3], x[u].w, fmaf(r[4 * u + 2], x[u].z, fmaf(r[4 * u + 1], x[u].y, fmaf(r[4 * u], x[u].x, acc[k]))));
+    for (int h = 0; h < G; ++h) qts[h * kHeadDim + c] += acc[h];
+  __syncthreads();
+  const int warp = tid >> 5, lane = tid & 31;
+  if (warp < G) {
+    float sq[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      sq[k] = qts[warp * kHeadDim + 32 * k + lane];
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) sq[k] += __shfl_xor_sync(0xffffffffu, sq[k], off);
+    }
+    if (lane < 4) {
+      float v;
+      if (GROUP == 32)
+        v = lane == 0 ? sq[0] : lane == 1 ? sq[1] : lane == 2 ? sq[2] : sq[3];
+      else
+        v = lane == 0 ? (sq[0] + sq[1]) + (sq[2] + sq[3]) : 0.f;
+      qss[warp * 4 + lane] = v;
     }
   }
-  const int lane = tid & 31, wq = (tid >> 5) & 3;  // warp wq of this head group covers channels 32wq..
-#pragma unroll
-  for (int k = 0; k < HPT; ++k) {
-    const int h = hg + 4 * k;
-    qt[(head0 + h) * kHeadDim + c] = acc[k];
-    float sum = acc[k];
-    for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
-    if (lane == 0) red[h * 4 + wq] = sum;
-  }
   __syncthreads();
-  if (tid < G * 4) {
-    const int h = tid >> 2, grp = tid & 3;
-    float v;
-    if (kp.group == 32)
-      v = red[h * 4 + grp];
-    else
-      v = grp == 0 ? (red[h * 4 + 0] + red[h * 4 + 1]) + (red[h * 4 + 2] + red[h * 4 + 3]) : 0.f;
-    qsum[(head0 + h) * 4 + grp] = v;
-  }
 }
 
 // ---------------------------------------------------------------- split kernel
@@ -163,7 +142,11 @@ struct Cfg {
   static constexpr int kSzBytes = 2 * kPage * NG * 4;       // K then V (scale, zero)
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
-  static constexpr int kSmemBytes = kPipeBytes + 256;  // + barriers (128 B), merge flag and merge barrier
+  static constexpr int kCtlBytes = 256;                // barriers (128 B), merge flag, next item, merge barrier
+  static constexpr int kQin = kPipeBytes + kCtlBytes;  // fp32 [G][d] query staging
+  static constexpr int kQts = kQin + G * kHeadDim * 4;  // fp32 [G][d] q~
+  static constexpr int kQss = kQts + G * kHeadDim * 4;  // fp32 [G][4] sums of q~ per 32 channels
+  static constexpr int kSmemBytes = kQss + G * 16;
   static_assert(kPipeBytes >= Bf16Rows<kWarps, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
   static_assert(kPipeBytes >= (kHeadDim * kHeadDim + G * kHeadDim) * 4, "the merge reuses the page pipeline memory");
 };
@@ -223,7 +206,7 @@ __device__ void finish_output(const KernelParams& kp, const DecodeItem& it, cons
 // position H + u - min(L, S) in ring slot p % W.
 template <int G>
 __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
-                                 const float* qt_head0, float* part, uint8_t* smem) {
+                                 const float* qts, float* part, uint8_t* smem) {
   const int S = kp.n_sink;
   const int n_s = min(dr.L, S);
   const uint16_t* sinkK = reinterpret_cast<const uint16_t*>(
@@ -241,7 +224,7 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
   auto rowV = [=](int u) {
     return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t((H + u - n_s) % W) * kHeadDim;
   };
-  bf16_rows_mma<G, kWarps, 1>(rowK, rowV, it.begin, it.end, qt_head0, part, smem);
+  bf16_rows_mma<G, kWarps, 1>(rowK, rowV, it.begin, it.end, qts, part, smem);
 }
 
 // Issue (lane 0 of the calling warp) the bulk copies of the warp's k-th page of an INT2
@@ -277,8 +260,8 @@ __device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeI
 // [S, H) inside those pages are masked.  Warp w takes pages begin + w, + kWarps, ...
 template <int G, int GROUP>
 __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
-                                const float* qt_head0, const float* qsum_head0, float* part, uint8_t* smem,
-                                uint32_t& phase_bits, bool pre_issued, uint32_t pre_mask) {
+                                const float* qts, const float* qss, float* part, uint8_t* smem,
+                                uint32_t& phase_bits, uint32_t pre_mask) {
   using C = Cfg<G, GROUP>;
   constexpr int NG = C::NG, NT = C::NT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -291,15 +274,11 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
   auto issue = [&](int k) -> bool { return int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem); };
   // ok_mask bit st: stage st has a copy in flight; phase_bits (kept across items):
-  // bit st = parity of the next completion of stage st.  The first item of a CTA may
-  // have been issued before the wait on the preceding kernel (pre_mask).
-  uint32_t ok_mask = 0;
-  if (pre_issued) {
-    ok_mask = pre_mask;
-  } else {
-    for (int k = 0; k < min(kStages, n_my); ++k)
-      if (issue(k)) ok_mask |= 1u << k;
-  }
+  // bit st = parity of the next completion of stage st.  The caller issued the first
+  // stages it could (pre_mask); the rest are issued here.
+  uint32_t ok_mask = pre_mask;
+  for (int k = 0; k < min(kStages, n_my); ++k)
+    if (!((pre_mask >> k) & 1u) && issue(k)) ok_mask |= 1u << k;
 
   // ---- B fragments of q~ (hi/lo fp16 columns), scaled by 4^-(kc & 3) for field kc
   uint32_t bq[8][NT][2];
@@ -309,7 +288,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const int head = 4 * j + (gid >> 1), part_lo = gid & 1;
-      const float4 v4 = *reinterpret_cast<const float4*>(qt_head0 + head * kHeadDim + 16 * kc + 4 * tig);
+      const float4 v4 = *reinterpret_cast<const float4*>(qts + head * kHeadDim + 16 * kc + 4 * tig);
       const float v[4] = {v4.x * fs, v4.y * fs, v4.z * fs, v4.w * fs};
       float o4[4];
 #pragma unroll
@@ -327,7 +306,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
-    for (int g = 0; g < NG; ++g) qs_scaled[j][g] = qsum_head0[(4 * j + tig) * 4 + g] * scale;
+    for (int g = 0; g < NG; ++g) qs_scaled[j][g] = qss[(4 * j + tig) * 4 + g] * scale;
 
   float m_run[NT], l_part[NT], zv[NT][NG];
   float oacc[8][4];
@@ -573,13 +552,17 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
 }
 
 template <int G, int GROUP>
-__global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int layer, const float* __restrict__ qt,
-                                                    const float* __restrict__ qsum, float* __restrict__ partials,
-                                                    uint16_t* __restrict__ out, float* __restrict__ out_f32) {
+__global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
+                                                    float* __restrict__ partials, uint16_t* __restrict__ out,
+                                                    float* __restrict__ out_f32) {
   extern __shared__ __align__(128) uint8_t smem[];
   using C = Cfg<G, GROUP>;
   int* s_last = reinterpret_cast<int*>(smem + C::kPipeBytes + kWarps * kStages * 8);
+  int* s_next = s_last + 1;
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes + kWarps * kStages * 8 + 8);
+  float* qin = reinterpret_cast<float*>(smem + C::kQin);
+  float* qts = reinterpret_cast<float*>(smem + C::kQts);
+  float* qss = reinterpret_cast<float*>(smem + C::kQss);
   if (threadIdx.x == 0) {
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
     for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
@@ -587,46 +570,50 @@ __global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int la
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  // The plan was uploaded before the preceding kernels, and the q rotation (the kernel
-  // right before this one) only lets this grid start after its own wait on the append:
-  // the first INT2 item's page copies can be issued before waiting for the rotated q.
+  // The plan, the page table and R_K were uploaded before the preceding kernels; of the
+  // pages, only those wholly below H_pre are final before the wait (the preceding append
+  // may still be writing the rest), so the first item copies those early.
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
   const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
                      reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items};
-  int* s_next = s_last + 1;
-  const int first_ix = wq.first();
-  bool pre_issued = false;
-  uint32_t pre_mask = 0;
-  if (first_ix >= 0) {
-    const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[first_ix];
-    const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
-    if (it.kind == 0 && dr.slot >= 0 && dr.slot < kp.max_requests) {
-      const int warp = threadIdx.x >> 5;
-      const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
-      for (int k = 0; k < min(kStages, n_my); ++k)
-        if (int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem)) pre_mask |= 1u << k;
-      pre_issued = true;
-    }
-  }
-  pdl_wait();
-  pdl_trigger();
+  bool waited = false;
   uint32_t phase_bits = 0, merge_phase = 0;
-  for (int ix = first_ix; ix >= 0; ix = wq.next(s_next)) {
+  for (int ix = wq.first(); ix >= 0; ix = wq.next(s_next)) {
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
-    float* part = partials + size_t(ix) * G * (kHeadDim + 2);
+    const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
+    uint32_t pre_mask = 0;
+    if (it.kind == 0 && slot_ok) {
+      const int warp = threadIdx.x >> 5;
+      const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
+      for (int k = 0; k < min(kStages, n_my); ++k) {
+        const int lp = it.begin + warp + kWarps * k;
+        if ((waited || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem))
+          pre_mask |= 1u << k;
+      }
+    }
+    if (threadIdx.x == 0 && ix == it.head_first)  // R_V^T for the merge of this (request, kv-head)
+      bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
+                           (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim,
+                       kHeadDim * kHeadDim * 4);
+    float rk[64];
+    load_rk_cols(kp, layer, it.kvh, rk);
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-    if (dr.slot < 0 || dr.slot >= kp.max_requests) {
+    rotate_q<G, GROUP>(q + head0 * kHeadDim, rk, qin, qts, qss);
+    float* part = partials + size_t(ix) * G * (kHeadDim + 2);
+    if (!slot_ok) {
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
       for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += kThreads)
         part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
     } else if (it.kind == 0) {
-      const bool pre = pre_issued && ix == first_ix;
-      pre_issued = false;
-      int2_pages_item<G, GROUP>(kp, layer, it, dr, qt + head0 * kHeadDim, qsum + head0 * 4, part, smem, phase_bits,
-                                pre, pre_mask);
+      int2_pages_item<G, GROUP>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask);
     } else {
-      bf16_tokens_item<G>(kp, layer, it, dr, qt + head0 * kHeadDim, part, smem);
+      bf16_tokens_item<G>(kp, layer, it, dr, qts, part, smem);
     }
     // ---- two-level merge of the partials; R_V^T is fetched as soon as this CTA knows it
     // merges a group (it may then finish the head)
@@ -651,9 +638,7 @@ int resident_ctas(int n_sm) {
   using C = Cfg<G, GROUP>;
   static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
   if (resident == 0) {
-    int e = int(cudaFuncSetAttribute(qrot_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, QrotSmem<G>::kBytes));
-    if (!e)
-      e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     int per_sm = 0;
     if (!e)
       e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP>, kThreads, C::kSmemBytes));
@@ -667,21 +652,15 @@ template <int G, int GROUP>
 int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                     const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
   using C = Cfg<G, GROUP>;
-  float* qt = reinterpret_cast<float*>(ws + wl.qt);
-  float* qsum = reinterpret_cast<float*>(ws + wl.qsum);
   float* partials = reinterpret_cast<float*>(ws + wl.partials);
   const int resident = resident_ctas<G, GROUP>(n_sm);
   if (resident < 0) return -resident;
-  int e = launch_ex(qrot_kernel<G>, dim3(n_req * kp.n_kv_heads), dim3(512), size_t(QrotSmem<G>::kBytes), stream, kp,
-                    layer, static_cast<const uint16_t*>(q), qt, qsum);
-  if (e) return e;
-  *launches += 1;
   // persistent-style grid: every resident CTA slot, each looping over work items, so a
   // captured launch serves later plans with other item counts
+  (void)n_req;
   (void)n_items;
-  e = launch_ex(split_kernel<G, GROUP>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes), stream, kp, layer,
-                static_cast<const float*>(qt), static_cast<const float*>(qsum), partials, static_cast<uint16_t*>(out),
-                out_f32);
+  int e = launch_ex(split_kernel<G, GROUP>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes), stream, kp, layer,
+                    static_cast<const uint16_t*>(q), partials, static_cast<uint16_t*>(out), out_f32);
   if (!e) *launches += 1;
   return e;
 }
@@ -711,7 +690,7 @@ int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, f
 
 
 // ---------------------------------------------------------------- no-allocation variant
-// Decode scratch (rotated queries, per-group query sums, split partials) owned by the
+// Decode scratch (the split partials) owned by the
 // library itself, for callers that cannot allocate device memory.  Every GPU that loads
 // the library holds this array until the process exits; all calls share it.
 constexpr size_t kStaticScratchBytes = size_t(8) << 20;  // 8 MiB
@@ -752,8 +731,8 @@ int launch_decode_static_scratch(const KernelParams& kp, int layer, const void* 
   uint8_t* ws = nullptr;
   int e = scratch_address(&ws);
   if (e) return e;
-  // Nothing in the scratch has to start at zero: the q rotation writes the rotated
-  // queries and sums, and every work item writes its partial before the merge reads it.
+  // Nothing in the scratch has to start at zero: every work item writes its partial
+  // before the merge reads it.
   return launch_decode(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
 }
 

@@ -574,7 +574,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   std::vector<char> seen(c->cfg.max_requests, 0);
   const int Hkv = c->cfg.n_kv_heads, S = is_int2(c) ? c->cfg.n_sink : 0;
   // lengths the decode will see: a pending reservation's tokens count (append before decode)
-  std::vector<int> Ls(n_req), Hs(n_req);
+  std::vector<int> Ls(n_req), Hs(n_req), Hpre(n_req);
   long long total_pages = 0;
   for (int i = 0; i < n_req; ++i) {
     oscar_status st = check_slot(c, slots[i]);
@@ -584,11 +584,13 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     const Request& r = c->reqs[slots[i]];
     Ls[i] = r.L;
     Hs[i] = r.H;
+    Hpre[i] = r.H;
     if (c->reserved)
       for (const AppendReq& a : c->app_reqs)
         if (a.slot == slots[i]) {
           Ls[i] = a.L1;
           Hs[i] = a.H1;
+          Hpre[i] = std::min(r.H, a.H0);
         }
     total_pages += (long long)Hkv * pages_needed(c, Ls[i], Hs[i]);
   }
@@ -647,6 +649,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     q.slot = slots[i];
     q.L = Ls[i];
     q.H = is_int2(c) ? Hs[i] : Ls[i];
+    q.H_pre = is_int2(c) ? Hpre[i] : 0;
     const int np = pages_needed(c, q.L, q.H);
     const int n_bf = is_int2(c) ? std::min(q.L, S) + std::max(0, q.L - q.H) : 0;
     const int n_bf_items = n_bf > 0 ? ceil_div(n_bf, kBf16ItemTokens) : 0;
@@ -704,10 +707,6 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   const int G = c->cfg.n_q_heads / Hkv;
   DecodeWorkspace w;
   size_t off = 0;
-  w.qt = off;
-  off = align256(off + size_t(n_req) * c->cfg.n_q_heads * kHeadDim * 4);
-  w.qsum = off;
-  off = align256(off + size_t(n_req) * c->cfg.n_q_heads * 4 * 4);
   w.partials = off;
   off = align256(off + items.size() * size_t(G) * (kHeadDim + 2) * 4);
   w.total = off;

@@ -36,6 +36,9 @@ struct AppendItem {
 struct DecodeReq {
   int slot;
   int L, H;          // length, history end (INT2 format); H = L for BF16 format
+  int H_pre;         // history end before this step's append: no kernel of the step writes
+                     // the INT2 pages wholly below it, so they may be copied before the wait
+                     // on the preceding kernel
   int first_item;    // items of this request, kv-head-major: first_item + kvh*items_per_head ..
   int items_per_head;
 };
@@ -92,8 +95,6 @@ struct KernelParams {
 
 // Decode workspace layout (per plan).
 struct DecodeWorkspace {
-  size_t qt;        // fp32 [n_req][H_q][d] rotated queries
-  size_t qsum;      // fp32 [n_req][H_q][4] per-group sums of q~
   size_t partials;  // fp32 [n_items][G][d + 2] (m, l, o~)
   size_t total;
 };
