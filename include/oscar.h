@@ -178,6 +178,21 @@ oscar_status oscar_plan_info(const oscar_cache* cache, int* n_items, int* n_bf16
 oscar_status oscar_decode_attention(oscar_cache* cache, int layer, const void* q, void* out, void* workspace,
                                     size_t ws_bytes, float* out_f32, void* stream);
 
+/* Quantize-append and decode in one launch (device, per layer): oscar_quantize_append of
+ * the pending reservation's tokens for `layer` (same k_new / v_new layout) followed by
+ * oscar_decode_attention of q over the cache that includes them, as a single kernel: the
+ * append tasks run first and each decode work item waits only for the append tasks of
+ * its own (request, kv-head) before it reads a ring or sink row or an INT2 page that the
+ * append writes ([OSCAR] §2.2-B: quantize on append, then fused decode over the
+ * mixed-precision cache; one launch per layer is this library's scheduling, not the
+ * paper's).  Requires a reservation and a plan made after it that lists every reserved
+ * slot (OSCAR_ERR_STATE otherwise); oscar_commit_append afterwards as usual.  Results are
+ * those of the two separate calls.  Waits are bounded: a wait that runs out sets
+ * OSCAR_FLAG_TIMEOUT. */
+oscar_status oscar_append_decode_attention(oscar_cache* cache, int layer, const void* k_new, const void* v_new,
+                                           const void* q, void* out, void* workspace, size_t ws_bytes,
+                                           float* out_f32, void* stream);
+
 /* Uncompressed comparison path (format OSCAR_FORMAT_BF16, same page tables and calls
  * for requests, reserve, commit and plan): append writes plain bf16 K and V rows into
  * pages; decode is softmax(q K^T / sqrt(d)) V over all L tokens, with no rotation. */

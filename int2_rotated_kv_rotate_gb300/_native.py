@@ -47,7 +47,7 @@ EXPORTS = [
     "oscar_set_layer_params", "oscar_request_alloc", "oscar_request_free", "oscar_request_info",
     "oscar_request_pages", "oscar_request_share_prefix", "oscar_reserve", "oscar_quantize_append",
     "oscar_commit_append", "oscar_plan_decode", "oscar_decode_workspace_bytes", "oscar_plan_info",
-    "oscar_decode_attention", "oscar_decode_attention_noalloc", "oscar_bf16_append", "oscar_bf16_decode_attention", "oscar_get_status",
+    "oscar_decode_attention", "oscar_append_decode_attention", "oscar_decode_attention_noalloc", "oscar_bf16_append", "oscar_bf16_decode_attention", "oscar_get_status",
     "oscar_last_error", "oscar_last_launch_count",
 ]
 
@@ -84,6 +84,7 @@ def lib() -> ctypes.CDLL:
                 "oscar_decode_workspace_bytes": (S, [P]),
                 "oscar_plan_info": (I, [P, IP, IP, IP]),
                 "oscar_decode_attention": (I, [P, I, P, P, P, S, P, P]),
+                "oscar_append_decode_attention": (I, [P, I, P, P, P, P, P, S, P, P]),
                 "oscar_decode_attention_noalloc": (I, [P, I, P, P, P, P]),
                 "oscar_bf16_append": (I, [P, I, P, P, P]),
                 "oscar_bf16_decode_attention": (I, [P, I, P, P, P, S, P, P]),
@@ -220,6 +221,13 @@ def oscar_decode_attention(handle: int, layer: int, q, out, workspace, out_f32=N
     _check(lib().oscar_decode_attention(handle, layer, _ptr(q), _ptr(out), _ptr(workspace),
                                         workspace.numel() * workspace.element_size(), _ptr(out_f32),
                                         _stream(stream)))
+
+
+def oscar_append_decode_attention(handle: int, layer: int, k_new, v_new, q, out, workspace, out_f32=None,
+                                  stream=None) -> None:
+    _check(lib().oscar_append_decode_attention(handle, layer, _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(out),
+                                               _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                               _ptr(out_f32), _stream(stream)))
 
 
 def oscar_decode_attention_noalloc(handle: int, layer: int, q, out, out_f32=None, stream=None) -> None:

@@ -103,7 +103,7 @@ class KVCache:
     def plan_info(self):
         return N.oscar_plan_info(self.handle)
 
-    def decode(self, layer: int, q, out=None, out_f32=None, stream=None):
+    def _check_decode(self, q, out, out_f32):
         shape = (self._n_plan, self.cfg.n_q_heads, self.cfg.head_dim)
         if tuple(q.shape) != shape or q.dtype != torch.bfloat16 or not q.is_contiguous() or q.device != self.mem.device:
             raise ValueError(f"q must be contiguous bf16 {shape} on {self.mem.device}")
@@ -114,10 +114,22 @@ class KVCache:
         if out_f32 is not None and (tuple(out_f32.shape) != shape or out_f32.dtype != torch.float32
                                     or not out_f32.is_contiguous()):
             raise ValueError("out_f32 must be contiguous fp32 like q")
+        return out
+
+    def decode(self, layer: int, q, out=None, out_f32=None, stream=None):
+        out = self._check_decode(q, out, out_f32)
         if self.fmt == N.OSCAR_FORMAT_INT2:
             N.oscar_decode_attention(self.handle, layer, q, out, self.workspace, out_f32, stream)
         else:
             N.oscar_bf16_decode_attention(self.handle, layer, q, out, self.workspace, out_f32, stream)
+        return out
+
+    def append_decode(self, layer: int, k_new, v_new, q, out=None, out_f32=None, stream=None):
+        """quantize_append then decode of `layer` in one launch (INT2 format; plan made
+        during the reservation over every reserved slot)."""
+        self._check_tokens(k_new, v_new)
+        out = self._check_decode(q, out, out_f32)
+        N.oscar_append_decode_attention(self.handle, layer, k_new, v_new, q, out, self.workspace, out_f32, stream)
         return out
 
     def status(self, stream=None):

@@ -443,20 +443,21 @@ __device__ int merge_partial(const KernelParams& kp, const DecodeItem& it, int i
 struct WorkQueue {
   const int* order;
   unsigned* counters;  // [0] work, [1] exit
-  int n;
-  // One wave (every item has its own CTA): no counters, item b is CTA b's.
+  int n;               // positions: n_pre leading ones taken in order, then order[] entries
+  int n_pre;
+  // One wave (every position has its own CTA): no counters, position b is CTA b's.
   __device__ bool one_wave() const { return n <= int(gridDim.x); }
-  __device__ int first() const {
-    if (int(blockIdx.x) >= n) return -1;
-    return one_wave() ? int(blockIdx.x) : order[blockIdx.x];
+  // Work id of position p: p itself for the leading positions (and in one wave), else
+  // n_pre + order[p - n_pre].
+  __device__ int id_of(int p) const {
+    if (p >= n) return -1;
+    return (p < n_pre || one_wave()) ? p : n_pre + order[p - n_pre];
   }
+  __device__ int first() const { return id_of(int(blockIdx.x)); }
   __device__ int next(int* s_slot) const {
     if (one_wave()) return -1;
     __syncthreads();
-    if (threadIdx.x == 0) {
-      const int pos = int(gridDim.x) + int(atomicAdd(&counters[0], 1u));
-      *s_slot = pos < n ? order[pos] : -1;
-    }
+    if (threadIdx.x == 0) *s_slot = id_of(int(gridDim.x) + int(atomicAdd(&counters[0], 1u)));
     __syncthreads();
     return *s_slot;
   }
@@ -471,6 +472,23 @@ struct WorkQueue {
     }
   }
 };
+
+// Bounded wait (one thread) until *ctr >= expect, with acquire semantics: false after about
+// a second of polling.
+constexpr uint32_t kCounterSpinLimit = 1u << 22;
+__device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned expect) {
+  for (uint32_t i = 0; i < kCounterSpinLimit; ++i) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= expect) return true;
+    __nanosleep(128);
+  }
+  return false;
+}
+
+// Generic-proxy writes made visible to this thread (e.g. by an acquire) are ordered before
+// its later async-proxy (bulk copy) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() { asm volatile("fence.proxy.async.global;" ::: "memory"); }
 
 // Launch with programmatic stream serialization (PDL) allowed.
 template <typename Kern, typename... Args>

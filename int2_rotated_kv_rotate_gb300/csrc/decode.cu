@@ -30,6 +30,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "append_dev.cuh"
 #include "common.cuh"
 #include "oscar_internal.h"
 
@@ -142,8 +143,13 @@ struct Cfg {
   static constexpr int kSzBytes = 2 * kPage * NG * 4;       // K then V (scale, zero)
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
   static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
-  static constexpr int kCtlBytes = 256;                // barriers (128 B), merge flag, next item, merge barrier
-  static constexpr int kQin = kPipeBytes + kCtlBytes;  // fp32 [G][d] query staging
+  // fused append tasks: R (fp32 [d][d]) then the append scratch, in the same memory
+  static constexpr int kAppendR = kHeadDim * kHeadDim * 4;
+  static constexpr int kAppendBytes = kAppendR + int(sizeof(append_dev::Smem));
+  static constexpr int kWorkBytes = kPipeBytes > kAppendBytes ? kPipeBytes : ((kAppendBytes + 127) / 128) * 128;
+  static constexpr int kCtl = kWorkBytes;           // control area
+  static constexpr int kCtlBytes = 256;             // barriers (128 B), merge flag, next item, merge barrier
+  static constexpr int kQin = kCtl + kCtlBytes;     // fp32 [G][d] query staging
   static constexpr int kQts = kQin + G * kHeadDim * 4;  // fp32 [G][d] q~
   static constexpr int kQss = kQts + G * kHeadDim * 4;  // fp32 [G][4] sums of q~ per 32 channels
   static constexpr int kSmemBytes = kQss + G * 16;
@@ -241,7 +247,7 @@ __device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeI
   if (phys < 0 || phys >= kp.max_pages) return false;
   if (lane == 0) {
     const int st = k % kStages;
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes) + warp * kStages;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kCtl) + warp * kStages;
     const uint32_t bar = smem_u32(&bars[st]);
     uint8_t* dst = smem + size_t(warp) * kStages * C::kStageBytes + size_t(st) * C::kStageBytes;
     const uint8_t* code = kp.base + kp.lay.codes + size_t(layer) * kp.lay.codes_layer_stride +
@@ -267,7 +273,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
   uint8_t* pipe = smem + size_t(warp) * kStages * C::kStageBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes) + warp * kStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kCtl) + warp * kStages;
   const int S = kp.n_sink, H = dr.H;
 
   // my pages: it.begin + warp + kWarps * k
@@ -551,44 +557,106 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   }
 }
 
+// One fused append task: append item `item` of the pending reservation for (kv-head kvh,
+// K|V kv), as the append kernel does it, with release-increments of the request's
+// app_done counters once its sink / ring rows are stored and once it is complete.  R arrives by bulk copy on `bar` (parity phase), issued before the
+// wait on the preceding kernel when this is the CTA's first work.
 template <int G, int GROUP>
-__global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
-                                                    float* __restrict__ partials, uint16_t* __restrict__ out,
-                                                    float* __restrict__ out_f32) {
+__device__ void fused_append_task(const KernelParams& kp, int layer, int id, uint8_t* smem, uint32_t bar,
+                                  uint32_t& phase, bool& waited, const uint16_t* k_new, const uint16_t* v_new) {
+  using C = Cfg<G, GROUP>;
+  using namespace append_dev;
+  const int item = id / (2 * kp.n_kv_heads), kvh = (id >> 1) % kp.n_kv_heads, kv = id & 1;
+  float* Rs = reinterpret_cast<float*>(smem);
+  Smem& sm = *reinterpret_cast<Smem*>(smem + C::kAppendR);
+  if (threadIdx.x == 0) {
+    const float* R = reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.R_V : kp.lay.R_K)) +
+                     (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
+    fence_proxy_async();
+    mbar_expect_tx(bar, C::kAppendR);
+    bulk_g2s(smem_u32(Rs), R, C::kAppendR, bar);
+  }
+  const AppendItem ait = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[item];
+  ItemState<kThreads> st;
+  prepare_item<GROUP, kThreads>(sm, kp, layer, ait, kvh, kv, st);
+  if (!waited) {
+    pdl_wait();
+    pdl_trigger();
+    waited = true;
+  }
+  __syncthreads();  // row pointers visible
+  const bool ok = mbar_wait(bar, phase);
+  if (!ok) {
+    if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+    mbar_wait(bar, phase);  // drain (bounded) before the memory is reused
+  }
+  phase ^= 1u;
+  unsigned* done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done) +
+                   (size_t(st.ok ? st.a.slot : 0) * kp.n_kv_heads + kvh) * 2;
+  // [0]: the task's sink and ring rows are stored; [1]: all of its rows
+  auto signal = [&](int which) {
+    __syncthreads();  // every store so far precedes the release below
+    if (threadIdx.x == 0 && st.ok) atomic_add_acq_rel(done + which, 1u);
+  };
+  if (ok) finish_item<GROUP, kThreads>(sm, Rs, kp, layer, ait, kvh, kv, st, k_new, v_new, [&] { signal(0); });
+  else signal(0);
+  signal(1);
+}
+
+template <int G, int GROUP, bool FUSED>
+__global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
+    split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q, float* __restrict__ partials,
+                 uint16_t* __restrict__ out, float* __restrict__ out_f32, const uint16_t* __restrict__ k_new,
+                 const uint16_t* __restrict__ v_new) {
+  constexpr bool fused = FUSED;
   extern __shared__ __align__(128) uint8_t smem[];
   using C = Cfg<G, GROUP>;
-  int* s_last = reinterpret_cast<int*>(smem + C::kPipeBytes + kWarps * kStages * 8);
+  int* s_last = reinterpret_cast<int*>(smem + C::kCtl + kWarps * kStages * 8);
   int* s_next = s_last + 1;
-  uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes + kWarps * kStages * 8 + 8);
+  uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + C::kCtl + kWarps * kStages * 8 + 8);
   float* qin = reinterpret_cast<float*>(smem + C::kQin);
   float* qts = reinterpret_cast<float*>(smem + C::kQts);
   float* qss = reinterpret_cast<float*>(smem + C::kQss);
   if (threadIdx.x == 0) {
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kPipeBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kCtl);
     for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
     mbar_init(smem_u32(merge_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
   // The plan, the page table and R_K were uploaded before the preceding kernels; of the
-  // pages, only those wholly below H_pre are final before the wait (the preceding append
-  // may still be writing the rest), so the first item copies those early.
-  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
+  // pages, only those wholly below H_pre are final before the wait (a preceding append may
+  // still be writing the rest), so the first item copies those early.  Fused launches put
+  // the reservation's append tasks (item x kv-head x K|V) ahead of the decode items.
+  const int* counts = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts);
+  const int n_items = counts[1];
+  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 : 0;
   const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
-                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items};
+                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_app + n_items, n_app};
+  unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
   bool waited = false;
   uint32_t phase_bits = 0, merge_phase = 0;
-  for (int ix = wq.first(); ix >= 0; ix = wq.next(s_next)) {
+  for (int id = wq.first(); id >= 0; id = wq.next(s_next)) {
+    if constexpr (FUSED) {
+      if (id < n_app) {
+        fused_append_task<G, GROUP>(kp, layer, id, smem, smem_u32(merge_bar), merge_phase, waited, k_new, v_new);
+        fence_proxy_async();  // generic use of the memory is over before later bulk copies
+        continue;
+      }
+    }
+    const int ix = id - n_app;
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
+    // rows this launch's append tasks of (request, kv-head) write: wait for them first
+    const bool dep = fused && slot_ok && it.dep != kDepNone && dr.app_expect > 0;
     uint32_t pre_mask = 0;
     if (it.kind == 0 && slot_ok) {
       const int warp = threadIdx.x >> 5;
       const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
       for (int k = 0; k < min(kStages, n_my); ++k) {
         const int lp = it.begin + warp + kWarps * k;
-        if ((waited || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem))
+        if (((waited && !dep) || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem))
           pre_mask |= 1u << k;
       }
     }
@@ -605,6 +673,12 @@ __global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int la
     }
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
     rotate_q<G, GROUP>(q + head0 * kHeadDim, rk, qin, qts, qss);
+    if (dep) {
+      const unsigned* ctr = app_done + (size_t(dr.slot) * kp.n_kv_heads + it.kvh) * 2 + (it.dep == kDepPages ? 1 : 0);
+      if (threadIdx.x == 0 && !wait_counter(ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
+      __syncthreads();
+      fence_proxy_async_global();  // the append's rows, seen through the acquire, before bulk copies
+    }
     float* part = partials + size_t(ix) * G * (kHeadDim + 2);
     if (!slot_ok) {
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
@@ -621,6 +695,12 @@ __global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int la
     const int role = merge_partial<G, kThreads>(kp, it, ix, partials, acc, s_last,
                                                 [&] { fetch_rvt(kp, layer, it.kvh, smem, smem_u32(merge_bar)); });
     if (role == kMergeFinal) {
+      // every item of (request, kv-head) is done, so are its waits: ready for the next launch
+      if (fused && slot_ok && dr.app_expect > 0 && threadIdx.x == 0) {
+        unsigned* ctr = app_done + (size_t(dr.slot) * kp.n_kv_heads + it.kvh) * 2;
+        ctr[0] = 0u;
+        ctr[1] = 0u;
+      }
       finish_output<G>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
     } else if (role == kMergeGroupOnly) {
       // drain the speculative R_V^T copy before the memory is reused (bounded)
@@ -633,24 +713,37 @@ __global__ void __launch_bounds__(kThreads) split_kernel(KernelParams kp, int la
   wq.leave();
 }
 
-template <int G, int GROUP>
-int resident_ctas(int n_sm) {
+template <int G, int GROUP, bool FUSED>
+int resident_ctas_t(int n_sm) {
   using C = Cfg<G, GROUP>;
   static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
   if (resident == 0) {
-    int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     C::kSmemBytes));
     int per_sm = 0;
     if (!e)
-      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP>, kThreads, C::kSmemBytes));
+      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED>, kThreads,
+                                                            C::kSmemBytes));
     if (e) return -e;
     resident = (per_sm > 0 ? per_sm : 1) * n_sm;
   }
   return resident;
 }
 
+// The decode and the fused append + decode kernels of a shape get one plan: the smaller
+// resident count of the two.
+template <int G, int GROUP>
+int resident_ctas(int n_sm) {
+  const int a = resident_ctas_t<G, GROUP, false>(n_sm), b = resident_ctas_t<G, GROUP, true>(n_sm);
+  if (a < 0) return a;
+  if (b < 0) return b;
+  return a < b ? a : b;
+}
+
 template <int G, int GROUP>
 int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                    const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
+                    const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches,
+                    const void* k_new, const void* v_new, bool fused) {
   using C = Cfg<G, GROUP>;
   float* partials = reinterpret_cast<float*>(ws + wl.partials);
   const int resident = resident_ctas<G, GROUP>(n_sm);
@@ -659,8 +752,14 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
   // captured launch serves later plans with other item counts
   (void)n_req;
   (void)n_items;
-  int e = launch_ex(split_kernel<G, GROUP>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes), stream, kp, layer,
-                    static_cast<const uint16_t*>(q), partials, static_cast<uint16_t*>(out), out_f32);
+  const uint16_t* qb = static_cast<const uint16_t*>(q);
+  uint16_t* ob = static_cast<uint16_t*>(out);
+  const uint16_t* kb = static_cast<const uint16_t*>(k_new);
+  const uint16_t* vb = static_cast<const uint16_t*>(v_new);
+  int e = fused ? launch_ex(split_kernel<G, GROUP, true>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes), stream,
+                            kp, layer, qb, partials, ob, out_f32, kb, vb)
+                : launch_ex(split_kernel<G, GROUP, false>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes),
+                            stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
   if (!e) *launches += 1;
   return e;
 }
@@ -676,15 +775,17 @@ int decode_resident_ctas(int gqa, int group, int n_sm) {
 }
 
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
-  if (kp.gqa == 4 && kp.group == 128)
-    return launch_decode_t<4, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
-  if (kp.gqa == 4 && kp.group == 32)
-    return launch_decode_t<4, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
-  if (kp.gqa == 8 && kp.group == 128)
-    return launch_decode_t<8, 128>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
-  if (kp.gqa == 8 && kp.group == 32)
-    return launch_decode_t<8, 32>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
+                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches,
+                  const void* k_new, const void* v_new, bool fused) {
+#define OSCAR_DECODE_CASE(G_, GROUP_)                                                                                 \
+  if (kp.gqa == G_ && kp.group == GROUP_)                                                                             \
+    return launch_decode_t<G_, GROUP_>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches, \
+                                       k_new, v_new, fused);
+  OSCAR_DECODE_CASE(4, 128)
+  OSCAR_DECODE_CASE(4, 32)
+  OSCAR_DECODE_CASE(8, 128)
+  OSCAR_DECODE_CASE(8, 32)
+#undef OSCAR_DECODE_CASE
   return int(cudaErrorInvalidValue);
 }
 

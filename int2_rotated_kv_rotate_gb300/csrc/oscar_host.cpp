@@ -124,6 +124,7 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.decode_items = take(L.max_decode_items * sizeof(DecodeItem));
   L.decode_order = take(L.max_decode_items * 4);
   L.sched = take(16);
+  L.app_done = take(size_t(reqs) * Hkv * 8);
   L.group_counters = take(L.max_decode_items * 4);
   L.total = off;
   return L;
@@ -156,7 +157,9 @@ struct oscar_cache {
   // pending append
   bool reserved = false;
   std::vector<AppendReq> app_reqs;
+  std::vector<int> app_req_items;  // append items of each reservation request
   int app_items = 0, app_rows = 0;
+  bool plan_covers_reservation = false;  // the plan lists every slot of the pending reservation
   // decode plan
   bool planned = false;
   bool planned_with_reservation = false;  // the plan already counts the reserved tokens
@@ -273,6 +276,7 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.counters, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 4);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.group_counters, 0, lay.max_decode_items * 4);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.sched, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.app_done, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 8);
   if (e == cudaSuccess && is_int2(c)) {
     // layer params start as zeros until oscar_set_layer_params
     e = cudaMemset(c->base + lay.R_K, 0, lay.clip_K - lay.R_K);
@@ -519,6 +523,8 @@ oscar_status oscar_reserve(oscar_cache* c, const int* slots, const int* n_new, i
   CUDA_TRY(cudaEventRecord(c->upload_done, s));
   c->upload_pending = true;
   c->app_reqs = reqs;
+  c->app_req_items.assign(reqs.size(), 0);
+  for (const AppendItem& it : items) ++c->app_req_items[it.req];
   c->app_items = int(items.size());
   c->app_rows = int(rows);
   c->reserved = true;
@@ -537,6 +543,7 @@ oscar_status oscar_commit_append(oscar_cache* c) {
   c->reserved = false;
   if (!c->planned_with_reservation) c->planned = false;
   c->planned_with_reservation = false;
+  c->plan_covers_reservation = false;
   return OSCAR_OK;
 }
 
@@ -574,7 +581,8 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   std::vector<char> seen(c->cfg.max_requests, 0);
   const int Hkv = c->cfg.n_kv_heads, S = is_int2(c) ? c->cfg.n_sink : 0;
   // lengths the decode will see: a pending reservation's tokens count (append before decode)
-  std::vector<int> Ls(n_req), Hs(n_req), Hpre(n_req);
+  std::vector<int> Ls(n_req), Hs(n_req), Hpre(n_req), Lpre(n_req), app_expect(n_req, 0);
+  int n_reserved_planned = 0;
   long long total_pages = 0;
   for (int i = 0; i < n_req; ++i) {
     oscar_status st = check_slot(c, slots[i]);
@@ -585,13 +593,18 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     Ls[i] = r.L;
     Hs[i] = r.H;
     Hpre[i] = r.H;
+    Lpre[i] = r.L;
     if (c->reserved)
-      for (const AppendReq& a : c->app_reqs)
+      for (size_t k = 0; k < c->app_reqs.size(); ++k) {
+        const AppendReq& a = c->app_reqs[k];
         if (a.slot == slots[i]) {
           Ls[i] = a.L1;
           Hs[i] = a.H1;
           Hpre[i] = std::min(r.H, a.H0);
+          app_expect[i] = 2 * c->app_req_items[k];  // K and V task of each item, per kv-head
+          ++n_reserved_planned;
         }
+      }
     total_pages += (long long)Hkv * pages_needed(c, Ls[i], Hs[i]);
   }
   // Work items: per (request, kv-head) the BF16 sink+ring items and page ranges of
@@ -601,8 +614,12 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   //  - large steps: about kWaves items per resident CTA (at least kItemBytes each), taken
   //    dynamically by the CTAs, largest first, so the ragged tail stays short while the
   //    per-item costs (pipeline fill, partial store and merge) stay small.
-  std::vector<int> np_of(n_req), nbf_of(n_req);
-  long long n_bf_items = 0;
+  // Per request: INT2 pages np, BF16 sink+ring tokens n_bf, and where this step's new
+  // tokens start in each (bf_new: BF16 list index; index < min(L, S) is a sink, else ring
+  // position H + index - min(L, S); pg_new: first INT2 page the append writes).  Items are
+  // split there, so that in a fused append + decode launch only the items after the split
+  // wait for the append tasks.
+  std::vector<int> np_of(n_req), nbf_of(n_req), bfnew_of(n_req), pgnew_of(n_req);
   int max_np = 1;
   const int ng = kHeadDim / (is_int2(c) ? c->cfg.group : kHeadDim);
   const long long page_bytes = is_int2(c) ? 2LL * kPage * (kRowBytes + 4 * ng) : 2LL * kPage * kHeadDim * 2;
@@ -610,15 +627,25 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   for (int i = 0; i < n_req; ++i) {
     np_of[i] = pages_needed(c, Ls[i], Hs[i]);
     nbf_of[i] = is_int2(c) ? std::min(Ls[i], S) + std::max(0, Ls[i] - Hs[i]) : 0;
-    n_bf_items += (long long)Hkv * (nbf_of[i] > 0 ? ceil_div(nbf_of[i], kBf16ItemTokens) : 0);
+    bfnew_of[i] = nbf_of[i];
+    pgnew_of[i] = np_of[i];
+    if (app_expect[i] > 0) {
+      const int n_s = std::min(Ls[i], S);
+      bfnew_of[i] = std::min(nbf_of[i], Lpre[i] < n_s ? Lpre[i] : n_s + std::max(0, Lpre[i] - Hs[i]));
+      if (Hs[i] > Hpre[i]) pgnew_of[i] = std::min(np_of[i], Hpre[i] / kPage);  // INT2 rows written
+    }
     max_np = std::max(max_np, np_of[i]);
     total_bytes += (long long)Hkv * (np_of[i] * page_bytes + nbf_of[i] * 2LL * kHeadDim * 2);
   }
+  auto split_count = [](int a, int b, int step) { return (a > 0 ? ceil_div(a, step) : 0) + (b > a ? ceil_div(b - a, step) : 0); };
+  long long n_bf_items = 0;
+  for (int i = 0; i < n_req; ++i) n_bf_items += (long long)Hkv * split_count(bfnew_of[i], nbf_of[i], kBf16ItemTokens);
   auto count_items = [&](int ch) {
     long long n = n_bf_items;
     for (int i = 0; i < n_req; ++i) {
-      const int per = (np_of[i] > 0 ? ceil_div(np_of[i], ch) : 0) + (nbf_of[i] > 0 ? ceil_div(nbf_of[i], kBf16ItemTokens) : 0);
-      n += (long long)Hkv * (per > 0 ? (np_of[i] > 0 ? ceil_div(np_of[i], ch) : 0) : 1);
+      const int pg = split_count(pgnew_of[i], np_of[i], ch);
+      const int bf = split_count(bfnew_of[i], nbf_of[i], kBf16ItemTokens);
+      n += (long long)Hkv * (pg + bf > 0 ? pg : 1);
     }
     return n;
   };
@@ -630,9 +657,11 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     int resident = is_int2(c) ? decode_resident_ctas(G, c->cfg.group, c->n_sm) : bf16_decode_resident_ctas(G, c->n_sm);
     if (resident <= 0) resident = 2 * c->n_sm;
     if (total_bytes <= kItemBytes * resident) {
-      const long long slots = std::max<long long>(1, resident - n_bf_items);
+      // a fused append + decode launch runs the reservation's append tasks in the same wave
+      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 2 : 0;
+      const long long slots = std::max<long long>(1, resident - n_bf_items - n_app_tasks);
       chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
-      while (chunk < max_np && count_items(chunk) > resident) ++chunk;
+      while (chunk < max_np && count_items(chunk) + n_app_tasks > resident) ++chunk;
     } else {
       const long long item_bytes = std::max(kItemBytes, total_bytes / (kWaves * resident));
       chunk = int(std::max<long long>(4, item_bytes / page_bytes));
@@ -650,32 +679,36 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     q.L = Ls[i];
     q.H = is_int2(c) ? Hs[i] : Ls[i];
     q.H_pre = is_int2(c) ? Hpre[i] : 0;
-    const int np = pages_needed(c, q.L, q.H);
-    const int n_bf = is_int2(c) ? std::min(q.L, S) + std::max(0, q.L - q.H) : 0;
-    const int n_bf_items = n_bf > 0 ? ceil_div(n_bf, kBf16ItemTokens) : 0;
-    const int n_pg_items = np > 0 ? ceil_div(np, chunk) : 0;
-    int per_head = n_bf_items + n_pg_items;
-    if (per_head == 0) per_head = 1;  // empty request: one empty item writes zeros
+    q.app_expect = is_int2(c) ? app_expect[i] : 0;
+    const int np = np_of[i], n_bf = nbf_of[i], bf_new = bfnew_of[i], pg_new = pgnew_of[i];
     q.first_item = int(items.size());
-    q.items_per_head = per_head;
     for (int h = 0; h < Hkv; ++h) {
       const int first = int(items.size());
       const int gc_base = first;  // group g of this (req, kv-head) counts on group_counters[first + g]
-      if (n_bf_items + n_pg_items == 0) {
-        items.push_back({i, h, 1, 0, 0, first, per_head, gc_base});
-        continue;
+      auto add = [&](int kind, int b, int e, int dep) {
+        items.push_back({i, h, kind, b, e, first, 0, gc_base + (int(items.size()) - first) / kMergeGroup, dep});
+      };
+      if (n_bf == 0 && np == 0) add(1, 0, 0, kDepNone);  // empty request: one empty item writes zeros
+      // BF16 sink+ring list, split where this step's new tokens start (those items wait for
+      // a fused launch's append tasks; the others do not)
+      for (int part = 0; part < 2; ++part) {
+        const int b0 = part == 0 ? 0 : bf_new, b1 = part == 0 ? bf_new : n_bf;
+        for (int t = b0; t < b1; t += kBf16ItemTokens) {
+          add(1, t, std::min(b1, t + kBf16ItemTokens), part == 0 ? kDepNone : kDepRing);
+          ++n_bf16;
+        }
       }
-      for (int t = 0; t < n_bf; t += kBf16ItemTokens) {
-        items.push_back({i, h, 1, t, std::min(n_bf, t + kBf16ItemTokens), first, per_head,
-                         gc_base + (int(items.size()) - first) / kMergeGroup});
-        ++n_bf16;
+      // INT2 pages, split where pages that this step's append writes begin
+      for (int part = 0; part < 2; ++part) {
+        const int p0 = part == 0 ? 0 : pg_new, p1 = part == 0 ? pg_new : np;
+        for (int p = p0; p < p1; p += chunk) {
+          add(0, p, std::min(p1, p + chunk), part == 0 ? kDepNone : kDepPages);
+          max_pages = std::max(max_pages, std::min(p1, p + chunk) - p);
+        }
       }
-      for (int p = 0; p < np; p += chunk) {
-        items.push_back({i, h, 0, p, std::min(np, p + chunk), first, per_head,
-                         gc_base + (int(items.size()) - first) / kMergeGroup});
-        max_pages = std::max(max_pages, std::min(np, p + chunk) - p);
-      }
+      for (size_t k = first; k < items.size(); ++k) items[k].head_count = int(items.size()) - first;
     }
+    q.items_per_head = (int(items.size()) - q.first_item) / Hkv;
   }
   if (items.size() > c->lay.max_decode_items)
     return fail(OSCAR_ERR_INVALID_ARG, "plan of %zu items exceeds %zu; raise max_split_pages", items.size(),
@@ -717,6 +750,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   c->dec_max_pages = max_pages;
   c->planned = true;
   c->planned_with_reservation = c->reserved;
+  c->plan_covers_reservation = c->reserved && n_reserved_planned == int(c->app_reqs.size());
   return OSCAR_OK;
 }
 
@@ -750,6 +784,23 @@ oscar_status oscar_decode_attention(oscar_cache* c, int layer, const void* q, vo
   int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_n_req,
                         c->dec_items, c->n_sm, stream, &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "decode launch: %s", cudaGetErrorString(cudaError_t(e)));
+  return OSCAR_OK;
+}
+
+oscar_status oscar_append_decode_attention(oscar_cache* c, int layer, const void* k_new, const void* v_new,
+                                           const void* q, void* out, void* workspace, size_t ws_bytes, float* out_f32,
+                                           void* stream) {
+  g_launches = 0;
+  oscar_status st = check_decode(c, layer, q, out, workspace, ws_bytes);
+  if (st) return st;
+  if (!is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_append_decode_attention needs the INT2 format");
+  if (!c->reserved) return fail(OSCAR_ERR_STATE, "no reservation");
+  if (!c->plan_covers_reservation)
+    return fail(OSCAR_ERR_STATE, "plan the decode after the reservation, over every reserved slot");
+  if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
+  int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_n_req,
+                        c->dec_items, c->n_sm, stream, &g_launches, k_new, v_new, true);
+  if (e) return fail(OSCAR_ERR_CUDA, "append + decode launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }
 

@@ -39,6 +39,8 @@ struct DecodeReq {
   int H_pre;         // history end before this step's append: no kernel of the step writes
                      // the INT2 pages wholly below it, so they may be copied before the wait
                      // on the preceding kernel
+  int app_expect;    // fused append + decode: append tasks of this request per kv-head (K and
+                     // V tasks of each of its append items); 0 = nothing to wait for
   int first_item;    // items of this request, kv-head-major: first_item + kvh*items_per_head ..
   int items_per_head;
 };
@@ -60,7 +62,11 @@ struct DecodeItem {
   int head_first;  // first partial slot of this (req, kvh)
   int head_count;  // number of partial slots of this (req, kvh)
   int gcounter;    // merge-group counter of this item (groups of kMergeGroup consecutive items)
+  int dep;         // fused append + decode: what the item reads that this launch's append tasks
+                   // write (kDepNone, kDepRing: BF16 rows of new tokens, kDepPages: INT2 pages
+                   // that receive evicted or new tokens)
 };
+constexpr int kDepNone = 0, kDepRing = 1, kDepPages = 2;
 
 struct DeviceLayout {
   // pools (byte offsets in the device block)
@@ -81,6 +87,9 @@ struct DeviceLayout {
   size_t append_reqs, append_items, decode_reqs, decode_items;
   size_t decode_order;  // int32 [max_decode_items]: items in the order CTAs take them (largest first)
   size_t sched;         // uint32 [4]: dynamic work counter, CTA exit counter (self-resetting)
+  size_t app_done;      // uint32 [max_requests][H_kv][2]: append tasks of the running fused launch
+                        // that have written their ring and sink rows ([0]) and everything ([1])
+                        // (reset by the request's final merge)
   size_t max_append_items, max_decode_items;
   size_t total;
 };
@@ -107,8 +116,11 @@ int launch_append(const KernelParams& kp, int layer, const void* k_new, const vo
                   int* launches);
 int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid, void* stream,
                        int* launches);
+// Decode; with `fused`, the same launch first runs the pending reservation's append tasks
+// (k_new, v_new as for launch_append) and decode items wait for the ones they depend on.
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
+                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches,
+                  const void* k_new = nullptr, const void* v_new = nullptr, bool fused = false);
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                        const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
 

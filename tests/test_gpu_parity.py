@@ -200,6 +200,98 @@ def test_shared_prefix_bit_identical_to_private_copy():
     assert torch.equal(o, outs[0])
 
 
+def kv_rows(w, layer, reqs, starts, counts):
+    ks, vs = [], []
+    for r, s0, n in zip(reqs, starts, counts):
+        k, v = wl.gen_kv(w, SEED, layer, r, s0, n, device="cuda")
+        ks.append(k)
+        vs.append(v)
+    return torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
+
+
+@pytest.mark.parametrize("gqa,group,msp", [(4, 128, 0), (4, 32, 1), (8, 128, 1), (8, 32, 0)])
+def test_fused_append_decode(gqa, group, msp):
+    """One-launch append + decode: the stored rows match the oracle bit for bit, and the
+    outputs equal those of the separate quantize_append and decode calls bit for bit (and
+    the oracle within tolerance).  Steps of 1 and 16 tokens evict ring tokens into INT2
+    pages that the same launch's decode items read; msp = 1 makes more work than one wave
+    of CTAs, so the append tasks and decode items are taken from the shared counter."""
+    w = wl.scaled(wl.WORKLOADS["tiny"], name=f"fused_{gqa}_{group}", n_q_heads=4 * gqa, n_kv_heads=4, group=group,
+                  window=64, lognormal_sigma=0.5)
+    n_layers, reqs, lens = 2, [0, 1, 2], [4000, 1200, 40]
+    steps = [[16, 1, 16], [16, 16, 1], [1, 16, 16]]
+    cap = max(lens) + 64
+    fused, oc, params = make_pair(w, SEED, n_layers, 3, cap)
+    sep, _, _ = make_pair(w, SEED, n_layers, 3, cap, params=params)
+    fs, ss = [fused.alloc() for _ in reqs], [sep.alloc() for _ in reqs]
+    fused.reserve(fs, lens)
+    sep.reserve(ss, lens)
+    for layer in range(n_layers):
+        K, V = kv_rows(w, layer, reqs, [0] * 3, lens)
+        fused.quantize_append(layer, K, V)
+        sep.quantize_append(layer, K, V)
+        kb, vb = bits(K), bits(V)
+        off = 0
+        for r, n in zip(reqs, lens):
+            oc.append(layer, r, kb[off:off + n], vb[off:off + n])
+            off += n
+    fused.commit()
+    sep.commit()
+    pos = list(lens)
+    for step, counts in enumerate(steps):
+        fused.reserve(fs, counts)
+        sep.reserve(ss, counts)
+        fused.plan(fs, max_split_pages=msp)
+        sep.plan(ss, max_split_pages=msp)
+        for layer in range(n_layers):
+            K, V = kv_rows(w, layer, reqs, pos, counts)
+            q = wl.gen_q(w, SEED, layer, step, 3, device="cuda")
+            o1 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+            o2 = torch.empty_like(o1)
+            out1 = fused.append_decode(layer, K, V, q, out_f32=o1)
+            assert N.oscar_last_launch_count() == 1
+            sep.quantize_append(layer, K, V)
+            sep.decode(layer, q, out_f32=o2)
+            torch.cuda.synchronize()
+            kb, vb = bits(K), bits(V)
+            off = 0
+            for r, n in zip(reqs, counts):
+                oc.append(layer, r, kb[off:off + n], vb[off:off + n])
+                off += n
+            assert torch.equal(o1, o2), f"step {step} layer {layer}: fused and separate outputs differ"
+            qb = bits(q)
+            for i, r in enumerate(reqs):
+                compare_decode(o1[i], out1[i], oc.decode(layer, r, qb[i]), f"fused step {step} layer {layer} req {r}")
+        fused.commit()
+        sep.commit()
+        pos = [p + n for p, n in zip(pos, counts)]
+        for st_, fl in (fused.status(), sep.status()):
+            assert st_ == 0 and fl == 0, f"device flags {fl:#x}"
+    if msp == 1:
+        n_items, _, _ = fused.plan_info()
+        assert n_items > torch.cuda.get_device_properties(0).multi_processor_count * (2 if gqa == 4 else 1)
+    for layer in range(n_layers):
+        for i, r in enumerate(reqs):
+            check_pages(fused, oc, layer, fs[i], r)
+
+
+def test_fused_append_decode_needs_a_covering_plan():
+    w = wl.WORKLOADS["tiny"]
+    cache, _, _ = make_pair(w, SEED, 1, 2, 512)
+    a, b = cache.alloc(), cache.alloc()
+    cache.reserve([a, b], [100, 100])
+    K, V = kv_rows(w, 0, [0, 1], [0, 0], [100, 100])
+    cache.quantize_append(0, K, V)
+    cache.commit()
+    cache.reserve([a, b], [1, 1])
+    cache.plan([a])  # b is reserved but not planned
+    K, V = kv_rows(w, 0, [0, 1], [100, 100], [1, 1])
+    q = wl.gen_q(w, SEED, 0, 0, 1, device="cuda")
+    with pytest.raises(N.OscarError) as ei:
+        cache.append_decode(0, K, V, q)
+    assert ei.value.status == 7  # OSCAR_ERR_STATE
+
+
 @pytest.mark.parametrize("gqa", [4, 8])
 def test_plans_larger_than_one_wave(gqa):
     """Single-page items, several times more than the CTAs resident at once: the CTAs take
