@@ -42,16 +42,18 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
     mbar_expect_tx(smem_u32(bar), kRBytes);
     bulk_g2s(smem_u32(Rs), R, kRBytes, smem_u32(bar));
   }
-  ItemState<kThreads> st;
+  ItemState st;
   AppendItem it{};
   if (work) {
     it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[blockIdx.x];
     prepare_item<GROUP, kThreads>(sm, kp, layer, it, kvh, kv, st);
+    __syncthreads();  // row pointers visible
+    evict_item<GROUP, kThreads>(sm, it, st);
   }
   pdl_wait();
   pdl_trigger();
   if (!work) return;
-  __syncthreads();  // barrier initialised, row pointers visible
+  __syncthreads();  // barrier initialised
   if (!mbar_wait(smem_u32(bar), 0)) {
     if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
     mbar_wait(smem_u32(bar), 0);  // drain (bounded) before exit
@@ -62,6 +64,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
       it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
       prepare_item<GROUP, kThreads>(sm, kp, layer, it, kvh, kv, st);
       __syncthreads();
+      evict_item<GROUP, kThreads>(sm, it, st);
     }
     finish_item<GROUP, kThreads>(sm, Rs, kp, layer, it, kvh, kv, st, k_new, v_new, [] {});
     __syncthreads();  // shared memory is reused by the next item

@@ -25,14 +25,16 @@
 namespace oscar {
 namespace append_dev {
 
-constexpr int kTok = 16;  // tokens (or ring slots) per item
+constexpr int kTok = 16;   // tokens (or ring slots) per item
+constexpr int kTokPer = 4;  // tokens per thread
 
-// Threads of a CTA working on one item: thread (g, j) owns rotated channel j of the
-// item's tokens kTokPer g .. kTokPer g + kTokPer - 1.
+// Threads of a CTA working on (part of) one item: thread (g, j) owns rotated channel j of
+// tokens kTokPer g .. kTokPer g + kTokPer - 1, so NTH threads cover kTokPer NTH / 128
+// tokens (512 threads: a whole item; 256: half an item).
 template <int NTH>
 struct AppendShape {
-  static constexpr int kTokPer = kTok * kHeadDim / NTH;
-  static_assert(NTH % kHeadDim == 0 && kTokPer % 4 == 0, "whole token groups of float4 width");
+  static constexpr int kTokens = kTokPer * NTH / kHeadDim;
+  static_assert(NTH % kHeadDim == 0 && kTokens <= kTok, "whole channel groups, at most one item");
 };
 
 struct Smem {
@@ -93,8 +95,7 @@ __device__ __forceinline__ uint16_t* sink_ptr(const KernelParams& kp, int slot, 
 // Format: per group s = bf16((max-min)/3), z = bf16(min), code = s == 0 ? 0 :
 // clamp(rint((x - z) / s), 0, 3); channel c = 16f + 2w + h at bit 16h + 2f of word w.
 template <int GROUP, int NTH>
-__device__ void quantize_tokens(Smem& sm, const float (&x)[AppendShape<NTH>::kTokPer], int which) {
-  constexpr int kTokPer = AppendShape<NTH>::kTokPer;
+__device__ void quantize_tokens(Smem& sm, const float (&x)[kTokPer], int which) {
   const int tid = threadIdx.x, j = tid & 127, tg = tid >> 7, warp = tid >> 5, lane = tid & 31;
   if (tid < kTok * 8) (&sm.words[0][0])[tid] = 0u;
   float mn[kTokPer], mx[kTokPer];
@@ -150,9 +151,7 @@ __device__ void quantize_tokens(Smem& sm, const float (&x)[AppendShape<NTH>::kTo
 // together; thread j only ever touches channel j of a ring slot, so reading an evicted
 // token's value before writing the slot's new token needs no barrier.
 // Per-thread state of one item between its two halves.
-template <int NTH>
 struct ItemState {
-  static constexpr int kTokPer = AppendShape<NTH>::kTokPer;
   AppendReq a;
   float clip;
   int ev[kTokPer], nw[kTokPer];
@@ -166,8 +165,7 @@ struct ItemState {
 // wait: positions, INT2 row pointers, evicted ring values.
 template <int GROUP, int NTH>
 __device__ void prepare_item(Smem& sm, const KernelParams& kp, int layer, const AppendItem& it, int kvh, int kv,
-                             ItemState<NTH>& st) {
-  constexpr int kTokPer = AppendShape<NTH>::kTokPer;
+                             ItemState& st) {
   st.a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];
   const AppendReq& a = st.a;
   const int tid = threadIdx.x, j = tid & 127, tg = tid >> 7;
@@ -209,19 +207,34 @@ __device__ void prepare_item(Smem& sm, const KernelParams& kp, int layer, const 
   }
 }
 
+// Eviction: the ring tokens that leave the window go to INT2 from their stored bf16 value,
+// clipped (read by prepare_item before this step's new tokens overwrite their slots).
+// Needs only what prepare_item read, so it may run before the PDL wait as well (it writes
+// INT2 rows of this layer at positions >= H0, which no kernel still running reads or
+// writes).  All threads, after a barrier that follows prepare_item.
+template <int GROUP, int NTH>
+__device__ void evict_item(Smem& sm, const AppendItem& it, const ItemState& st) {
+  const AppendReq& a = st.a;
+  if (!st.ok || it.kind != 0 || min(a.L0, a.H1) <= a.H0) return;
+  float xe[kTokPer];
+#pragma unroll
+  for (int u = 0; u < kTokPer; ++u) xe[u] = fmaxf(fminf(st.xe[u], st.clip), -st.clip);
+  quantize_tokens<GROUP, NTH>(sm, xe, 0);
+}
+
 // Second half: new input rows (written by the caller, so after the PDL wait), rotation of
-// the new tokens and their sink / ring rows, then eviction into INT2 and new INT2 rows.  Thread j only ever touches channel j of a
-// ring slot, so reading an evicted token's value before writing the slot's new token
-// needs no barrier.
+// the new tokens and their sink / ring rows, then new tokens that go straight to INT2.
+// Thread j only ever touches channel j of a ring slot, so reading an evicted token's value
+// (prepare_item) before writing the slot's new token needs no barrier.
 template <int GROUP, int NTH, typename OnRowsWritten>
 __device__ void finish_item(Smem& sm, const float* Rs, const KernelParams& kp, int layer, const AppendItem& it,
-                            int kvh, int kv, ItemState<NTH>& st, const uint16_t* __restrict__ k_new,
+                            int kvh, int kv, ItemState& st, const uint16_t* __restrict__ k_new,
                             const uint16_t* __restrict__ v_new, OnRowsWritten on_rows_written) {
-  constexpr int kTokPer = AppendShape<NTH>::kTokPer;
   const AppendReq& a = st.a;
   const int tid = threadIdx.x, j = tid & 127, tg = tid >> 7;
   if (!st.ok) {
     if (tid == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+    on_rows_written();
     return;
   }
   const uint16_t* X = kv ? v_new : k_new;
@@ -232,12 +245,8 @@ __device__ void finish_item(Smem& sm, const float* Rs, const KernelParams& kp, i
   for (int u = 0; u < kTokPer; ++u)
     xn[u] = st.nw[u] >= 0 ? bf16_f32(X[(size_t(a.x_offset + st.nw[u] - a.L0) * kp.n_kv_heads + kvh) * kHeadDim + j])
                           : 0.f;
-  float xe[kTokPer];
 #pragma unroll
-  for (int u = 0; u < kTokPer; ++u) {
-    sm.xs[j][kTokPer * tg + u] = xn[u];
-    xe[u] = fmaxf(fminf(st.xe[u], clip), -clip);
-  }
+  for (int u = 0; u < kTokPer; ++u) sm.xs[j][kTokPer * tg + u] = xn[u];
   __syncthreads();
   // ---- rotate my new tokens: one fixed-order fp32 fma chain per output channel; the
   // shared-memory loads of 16 steps are issued ahead of their FMAs
@@ -245,26 +254,21 @@ __device__ void finish_item(Smem& sm, const float* Rs, const KernelParams& kp, i
 #pragma unroll
   for (int u = 0; u < kTokPer; ++u) acc[u] = 0.0f;
   const float* Rc = Rs + j;  // column j of R, in shared memory
-  constexpr int kStep = kTokPer == 4 ? 16 : 4;  // rows of R per batch of shared-memory loads
-  for (int i0 = 0; i0 < kHeadDim; i0 += kStep) {
-    float r[kStep];
-    float4 x4[kStep][kTokPer / 4];
+  for (int i0 = 0; i0 < kHeadDim; i0 += 16) {
+    float r[16];
+    float4 x4[16];
 #pragma unroll
-    for (int k = 0; k < kStep; ++k) {
+    for (int k = 0; k < 16; ++k) {
       r[k] = Rc[(i0 + k) * kHeadDim];
-#pragma unroll
-      for (int v = 0; v < kTokPer / 4; ++v)
-        x4[k][v] = *reinterpret_cast<const float4*>(&sm.xs[i0 + k][kTokPer * tg + 4 * v]);
+      x4[k] = *reinterpret_cast<const float4*>(&sm.xs[i0 + k][kTokPer * tg]);
     }
 #pragma unroll
-    for (int k = 0; k < kStep; ++k)
-#pragma unroll
-      for (int v = 0; v < kTokPer / 4; ++v) {
-        acc[4 * v + 0] = __fmaf_rn(r[k], x4[k][v].x, acc[4 * v + 0]);
-        acc[4 * v + 1] = __fmaf_rn(r[k], x4[k][v].y, acc[4 * v + 1]);
-        acc[4 * v + 2] = __fmaf_rn(r[k], x4[k][v].z, acc[4 * v + 2]);
-        acc[4 * v + 3] = __fmaf_rn(r[k], x4[k][v].w, acc[4 * v + 3]);
-      }
+    for (int k = 0; k < 16; ++k) {
+      acc[0] = __fmaf_rn(r[k], x4[k].x, acc[0]);
+      acc[1] = __fmaf_rn(r[k], x4[k].y, acc[1]);
+      acc[2] = __fmaf_rn(r[k], x4[k].z, acc[2]);
+      acc[3] = __fmaf_rn(r[k], x4[k].w, acc[3]);
+    }
   }
   // ---- route: sink / ring (bf16 r) or INT2 (clip + quantise)
   float xq[kTokPer];
@@ -285,9 +289,6 @@ __device__ void finish_item(Smem& sm, const float* Rs, const KernelParams& kp, i
   }
   // the bf16 rows of the step are in place (all threads call this)
   on_rows_written();
-  // ---- evicted ring tokens -> INT2 (their stored bf16 value, clipped; read before the
-  // slot's new token was written), then new tokens that go straight to INT2
-  if (it.kind == 0 && min(a.L0, a.H1) > a.H0) quantize_tokens<GROUP, NTH>(sm, xe, 0);
   if (__syncthreads_or(any_q)) quantize_tokens<GROUP, NTH>(sm, xq, 1);
 }
 

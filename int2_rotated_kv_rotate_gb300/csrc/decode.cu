@@ -557,16 +557,22 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   }
 }
 
-// One fused append task: append item `item` of the pending reservation for (kv-head kvh,
-// K|V kv), as the append kernel does it, with release-increments of the request's
-// app_done counters once its sink / ring rows are stored and once it is complete.  R arrives by bulk copy on `bar` (parity phase), issued before the
-// wait on the preceding kernel when this is the CTA's first work.
+// One fused append task: half `half` (8 of the 16 tokens or ring slots) of append item
+// `item` of the pending reservation, for (kv-head kvh, K|V kv), as the append kernel does
+// it, with release-increments of the (layer, request, kv-head) counters app_done[0] once
+// its sink and ring rows are stored and app_done[1] once its INT2 rows are.  Before the
+// wait on the preceding kernel (when this is the CTA's first work): R's bulk copy, the
+// item's positions and evicted ring values, and the eviction into INT2 with its signal
+// (ring items write no other INT2 rows).
+constexpr int kAppendSplit = 2;  // CTAs per append item and kv-head and K|V
 template <int G, int GROUP>
 __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uint8_t* smem, uint32_t bar,
                                   uint32_t& phase, bool& waited, const uint16_t* k_new, const uint16_t* v_new) {
   using C = Cfg<G, GROUP>;
   using namespace append_dev;
-  const int item = id / (2 * kp.n_kv_heads), kvh = (id >> 1) % kp.n_kv_heads, kv = id & 1;
+  static_assert(AppendShape<kThreads>::kTokens * kAppendSplit == kTok, "the halves cover an item");
+  const int half = id % kAppendSplit, rest = id / kAppendSplit;
+  const int kv = rest & 1, kvh = (rest >> 1) % kp.n_kv_heads, item = (rest >> 1) / kp.n_kv_heads;
   float* Rs = reinterpret_cast<float*>(smem);
   Smem& sm = *reinterpret_cast<Smem*>(smem + C::kAppendR);
   if (threadIdx.x == 0) {
@@ -576,31 +582,36 @@ __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uin
     mbar_expect_tx(bar, C::kAppendR);
     bulk_g2s(smem_u32(Rs), R, C::kAppendR, bar);
   }
-  const AppendItem ait = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[item];
-  ItemState<kThreads> st;
+  AppendItem ait = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[item];
+  constexpr int kHalf = AppendShape<kThreads>::kTokens;
+  ait.begin += kHalf * half;
+  ait.count = max(0, min(kHalf, ait.count - kHalf * half));
+  ItemState st;
   prepare_item<GROUP, kThreads>(sm, kp, layer, ait, kvh, kv, st);
+  unsigned* done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done) +
+                   ((size_t(layer) * kp.max_requests + (st.ok ? st.a.slot : 0)) * kp.n_kv_heads + kvh) * 2;
+  auto signal = [&](int which) {
+    __syncthreads();  // every store so far precedes the release below
+    if (threadIdx.x == 0 && st.ok) atomic_add_acq_rel(done + which, 1u);
+  };
+  __syncthreads();  // row pointers visible
+  evict_item<GROUP, kThreads>(sm, ait, st);
+  if (ait.kind == 0) signal(1);
   if (!waited) {
     pdl_wait();
     pdl_trigger();
     waited = true;
   }
-  __syncthreads();  // row pointers visible
   const bool ok = mbar_wait(bar, phase);
   if (!ok) {
     if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
     mbar_wait(bar, phase);  // drain (bounded) before the memory is reused
   }
   phase ^= 1u;
-  unsigned* done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done) +
-                   (size_t(st.ok ? st.a.slot : 0) * kp.n_kv_heads + kvh) * 2;
-  // [0]: the task's sink and ring rows are stored; [1]: all of its rows
-  auto signal = [&](int which) {
-    __syncthreads();  // every store so far precedes the release below
-    if (threadIdx.x == 0 && st.ok) atomic_add_acq_rel(done + which, 1u);
-  };
+  __syncthreads();
   if (ok) finish_item<GROUP, kThreads>(sm, Rs, kp, layer, ait, kvh, kv, st, k_new, v_new, [&] { signal(0); });
   else signal(0);
-  signal(1);
+  if (ait.kind != 0) signal(1);
 }
 
 template <int G, int GROUP, bool FUSED>
@@ -630,7 +641,7 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
   // the reservation's append tasks (item x kv-head x K|V) ahead of the decode items.
   const int* counts = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts);
   const int n_items = counts[1];
-  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 : 0;
+  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * kAppendSplit : 0;
   const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
                      reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_app + n_items, n_app};
   unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
@@ -674,7 +685,8 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
     rotate_q<G, GROUP>(q + head0 * kHeadDim, rk, qin, qts, qss);
     if (dep) {
-      const unsigned* ctr = app_done + (size_t(dr.slot) * kp.n_kv_heads + it.kvh) * 2 + (it.dep == kDepPages ? 1 : 0);
+      const unsigned* ctr = app_done + ((size_t(layer) * kp.max_requests + dr.slot) * kp.n_kv_heads + it.kvh) * 2 +
+                            (it.dep == kDepPages ? 1 : 0);
       if (threadIdx.x == 0 && !wait_counter(ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
       __syncthreads();
       fence_proxy_async_global();  // the append's rows, seen through the acquire, before bulk copies
@@ -696,10 +708,11 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
                                                 [&] { fetch_rvt(kp, layer, it.kvh, smem, smem_u32(merge_bar)); });
     if (role == kMergeFinal) {
       // every item of (request, kv-head) is done, so are its waits: ready for the next launch
+      // (subtracting the launch's count: a task's last increment may still be on its way)
       if (fused && slot_ok && dr.app_expect > 0 && threadIdx.x == 0) {
-        unsigned* ctr = app_done + (size_t(dr.slot) * kp.n_kv_heads + it.kvh) * 2;
-        ctr[0] = 0u;
-        ctr[1] = 0u;
+        unsigned* ctr = app_done + ((size_t(layer) * kp.max_requests + dr.slot) * kp.n_kv_heads + it.kvh) * 2;
+        atomicSub(ctr, unsigned(dr.app_expect));
+        atomicSub(ctr + 1, unsigned(dr.app_expect));
       }
       finish_output<G>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
     } else if (role == kMergeGroupOnly) {

@@ -114,7 +114,6 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.page_table = take(reqs * size_t(c.max_pages_per_request) * 4);
   L.status = take(256);
   L.counters = take(reqs * Hkv * 4);
-  L.group_counters = 0;  // placed after the decode items (its size depends on them)
   L.plan_counts = take(16);
   L.max_append_items = kMaxAppendTokenItems + reqs * (kMaxWindow / kAppendChunk);
   L.max_decode_items = reqs * Hkv * (2 + kMaxWindow / kBf16ItemTokens) + 16384;
@@ -123,9 +122,9 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.decode_reqs = take(reqs * sizeof(DecodeReq));
   L.decode_items = take(L.max_decode_items * sizeof(DecodeItem));
   L.decode_order = take(L.max_decode_items * 4);
-  L.sched = take(16);
-  L.app_done = take(size_t(reqs) * Hkv * 8);
   L.group_counters = take(L.max_decode_items * 4);
+  L.sched = take(16);
+  L.app_done = take(layers * reqs * Hkv * 8);
   L.total = off;
   return L;
 }
@@ -276,7 +275,8 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.counters, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 4);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.group_counters, 0, lay.max_decode_items * 4);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.sched, 0, 16);
-  if (e == cudaSuccess) e = cudaMemset(c->base + lay.app_done, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 8);
+  if (e == cudaSuccess)
+    e = cudaMemset(c->base + lay.app_done, 0, size_t(cfg->n_layers) * cfg->max_requests * cfg->n_kv_heads * 8);
   if (e == cudaSuccess && is_int2(c)) {
     // layer params start as zeros until oscar_set_layer_params
     e = cudaMemset(c->base + lay.R_K, 0, lay.clip_K - lay.R_K);
@@ -601,7 +601,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
           Ls[i] = a.L1;
           Hs[i] = a.H1;
           Hpre[i] = std::min(r.H, a.H0);
-          app_expect[i] = 2 * c->app_req_items[k];  // K and V task of each item, per kv-head
+          app_expect[i] = 4 * c->app_req_items[k];  // K and V halves of each item, per kv-head
           ++n_reserved_planned;
         }
       }
@@ -658,7 +658,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     if (resident <= 0) resident = 2 * c->n_sm;
     if (total_bytes <= kItemBytes * resident) {
       // a fused append + decode launch runs the reservation's append tasks in the same wave
-      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 2 : 0;
+      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 4 : 0;
       const long long slots = std::max<long long>(1, resident - n_bf_items - n_app_tasks);
       chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
       while (chunk < max_np && count_items(chunk) + n_app_tasks > resident) ++chunk;
@@ -684,9 +684,9 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     q.first_item = int(items.size());
     for (int h = 0; h < Hkv; ++h) {
       const int first = int(items.size());
-      const int gc_base = first;  // group g of this (req, kv-head) counts on group_counters[first + g]
       auto add = [&](int kind, int b, int e, int dep) {
-        items.push_back({i, h, kind, b, e, first, 0, gc_base + (int(items.size()) - first) / kMergeGroup, dep});
+        // group g of this (req, kv-head) counts on group_counters[first + g]
+        items.push_back({i, h, kind, b, e, first, 0, first + (int(items.size()) - first) / kMergeGroup, dep});
       };
       if (n_bf == 0 && np == 0) add(1, 0, 0, kDepNone);  // empty request: one empty item writes zeros
       // BF16 sink+ring list, split where this step's new tokens start (those items wait for

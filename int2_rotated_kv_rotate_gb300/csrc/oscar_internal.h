@@ -39,8 +39,8 @@ struct DecodeReq {
   int H_pre;         // history end before this step's append: no kernel of the step writes
                      // the INT2 pages wholly below it, so they may be copied before the wait
                      // on the preceding kernel
-  int app_expect;    // fused append + decode: append tasks of this request per kv-head (K and
-                     // V tasks of each of its append items); 0 = nothing to wait for
+  int app_expect;    // fused append + decode: append tasks of this request per kv-head (the
+                     // K and V halves of each of its append items); 0 = nothing to wait for
   int first_item;    // items of this request, kv-head-major: first_item + kvh*items_per_head ..
   int items_per_head;
 };
@@ -49,10 +49,9 @@ struct DecodeReq {
 // [t0, t1) of the sink+ring list (kind 1; index < S is sink j, else ring position H + j - S)
 // of request `req` (plan index), kv-head `kvh`.  Partial results go to slot `item`.
 // Partials of one (request, kv-head) merge in two levels: each group of kMergeGroup
-// consecutive items is merged by its last finisher (into the group's first slot), then the
-// last group merger combines the group results.
+// consecutive items is merged by its last finisher into the group's first slot, then the
+// last group merger merges the groups.
 constexpr int kMergeGroup = 8;
-
 struct DecodeItem {
   int req;
   int kvh;
@@ -82,14 +81,14 @@ struct DeviceLayout {
   size_t page_table;  // int32 [max_requests][max_pages_per_request]
   size_t status;      // uint32 flags
   size_t counters;    // uint32 [max_requests][H_kv] merge counters (second level)
-  size_t group_counters;  // uint32 [max_decode_items] first-level merge counters
   size_t plan_counts; // int32 [4]: append items, decode items, decode requests, unused
   size_t append_reqs, append_items, decode_reqs, decode_items;
   size_t decode_order;  // int32 [max_decode_items]: items in the order CTAs take them (largest first)
   size_t sched;         // uint32 [4]: dynamic work counter, CTA exit counter (self-resetting)
-  size_t app_done;      // uint32 [max_requests][H_kv][2]: append tasks of the running fused launch
-                        // that have written their ring and sink rows ([0]) and everything ([1])
-                        // (reset by the request's final merge)
+  size_t group_counters;  // uint32 [max_decode_items] first-level merge counters
+  size_t app_done;      // uint32 [layer][max_requests][H_kv][2]: append tasks of the running fused
+                        // launch that have stored their sink and ring rows ([0]) and their INT2
+                        // rows ([1]); the request's final merge takes the launch's count off again
   size_t max_append_items, max_decode_items;
   size_t total;
 };
