@@ -257,6 +257,55 @@ def int2_bytes_per_layer(w, L_list, H_list):
     return total
 
 
+def append_bytes_per_layer(w, L0, H0, L1, H1):
+    """Algorithmic bytes of one layer's quantize-append: new K/V rows in, their bf16 sink or
+    ring rows out (or INT2 rows when they go straight to the history), evicted ring rows in
+    and their INT2 rows out, and R_V (R_K is already counted by the decode)."""
+    ng = w.head_dim // w.group
+    per_int2 = 2 * (w.head_dim // 4 + ng * 4)
+    row2 = 2 * w.head_dim * 2  # K and V bf16 rows
+    total = w.n_kv_heads * w.head_dim * w.head_dim * 4
+    for l0, h0, l1, h1 in zip(L0, H0, L1, H1):
+        new = l1 - l0
+        direct = max(0, min(l1, h1) - max(l0, w.n_sink))  # new tokens that go straight to INT2
+        evicted = max(0, min(l0, h1) - h0)
+        total += w.n_kv_heads * (new * row2 + (new - direct) * row2 + direct * per_int2 + evicted * (row2 + per_int2))
+    return total
+
+
+def source_digest() -> str:
+    """sha256 over the kernel sources: a profile's counters apply while this is unchanged."""
+    import hashlib
+
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "int2_rotated_kv_rotate_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h", ".cpp")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the step's kernel from the committed ncu summary of this
+    workload, if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"split_kernel_fused_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    with open(path) as f:
+        for line in f:
+            if line.startswith("- ") and ": " in line:
+                k, v = line[2:].strip().split(": ", 1)
+                fields[k.strip("`")] = v.strip().strip("`")
+    if fields.get("source_sha256") != source_digest():
+        return None
+    try:
+        return int(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
 def bf16_bytes_per_layer(w, L_list):
     return sum(w.n_kv_heads * L * 2 * w.head_dim * 2 for L in L_list) + 2 * len(L_list) * w.n_q_heads * w.head_dim * 2
 
@@ -276,7 +325,7 @@ def run_ours(args, world, rank, local):
     seed = args.seed + 1000 * rank  # each replica holds its own requests
     total_steps = args.warmup + args.steps
     E2E_STEPS = 10
-    plan = Plan(w, seed, n_layers, total_steps + 1 + E2E_STEPS)  # sizes the page pool for every step
+    plan = Plan(w, seed, n_layers, total_steps + 2 + E2E_STEPS)  # sizes the page pool for every step
     B = plan.B
     ppr = (plan.max_len() + 63) // 64 + 2
     # page pool: private pages of every request (shared prefixes counted once per group)
@@ -394,7 +443,34 @@ def run_ours(args, world, rank, local):
     st, flags = cache.status()
     assert st == 0, f"device status {flags:#x}"
 
-    # ---- decode-only timing (36 back-to-back decode calls, captured): the dominant kernels
+    # ---- the step's kernel alone (the roofline's duration): one reservation, the n_layers
+    # fused append + decode launches captured and replayed back to back (replays rewrite
+    # the same rows), CUDA events on the capturing stream
+    n_new_k = steps_in[total_steps][3]
+    L_pre = [cache.info(sl)[0] for sl in slots]
+    H_pre = [cache.info(sl)[1] for sl in slots]
+    cache.reserve(slots, n_new_k)
+    cache.plan(slots)
+    fgraph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(fgraph):
+        device_step()
+    for _ in range(3):
+        fgraph.replay()
+    torch.cuda.synchronize()
+    reps = max(5, args.steps)
+    e0.record()
+    for _ in range(reps):
+        fgraph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    fused_us = e0.elapsed_time(e1) * 1000.0 / (reps * n_layers)
+    cache.commit()
+    L_now, H_now = zip(*[cache.info(sl)[:2] for sl in slots])
+    fused_bytes = int2_bytes_per_layer(w, L_now, H_now) + append_bytes_per_layer(w, L_pre, H_pre, L_now, H_now)
+    st, flags = cache.status()
+    assert st == 0, f"device status {flags:#x} after the fused timing"
+
+    # ---- decode-only timing (n_layers back-to-back decode calls, captured)
     dgraph = torch.cuda.CUDAGraph()
     cache.plan(slots)
     with torch.cuda.graph(dgraph):
@@ -410,7 +486,6 @@ def run_ours(args, world, rank, local):
     e1.record()
     torch.cuda.synchronize()
     decode_us = e0.elapsed_time(e1) * 1000.0 / (reps * n_layers)
-    L_now, H_now = zip(*[cache.info(sl)[:2] for sl in slots])
     bytes_layer = int2_bytes_per_layer(w, L_now, H_now)
     n_items, n_bf16_items, _ = cache.plan_info()
 
@@ -452,6 +527,7 @@ def run_ours(args, world, rank, local):
         bf16 = bf16_comparison(w, seed, n_layers, [cache.info(sl)[0] for sl in slots], qin, dev, reps)
     cache.close()
     return dict(step_ms=step_ms, clocks=clk, decode_us=decode_us, bytes_layer=bytes_layer, n_layers=n_layers, B=B,
+                fused_us=fused_us, fused_bytes=fused_bytes,
                 launches=launches_per_step * args.steps, e2e=e2e, bf16=bf16, n_items=n_items,
                 n_bf16_items=n_bf16_items, t_cal=t_cal, t_fill=t_fill, world=world, w=w)
 
@@ -608,7 +684,7 @@ def main(argv=None):
     n_layers = r["n_layers"]
     us_layer_step = r["step_ms"] * 1000.0 / n_layers
     peak, peak_kind = measured_peaks()
-    achieved = r["bytes_layer"] / (r["decode_us"] * 1e-6) / 1e9
+    achieved = r["fused_bytes"] / (r["fused_us"] * 1e-6) / 1e9
     line = {
         "metric": METRIC,
         "value": round(us_layer_step, 3),
@@ -625,9 +701,10 @@ def main(argv=None):
         "config": config_of(w, n_layers),
         "decode_us_per_layer": round(r["decode_us"], 3),
         "append_decode_tokens_per_s": round(r["B"] * world / (r["step_ms"] * 1e-3), 1),
-        "roofline": {"bound": "hbm", "kernel": "decode (split_kernel), per layer",
+        "roofline": {"bound": "hbm", "kernel": "split_kernel (fused quantize-append + decode), one launch per layer",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                     "peak_kind": peak_kind, "traffic": None, "algorithmic_bytes": r["bytes_layer"]},
+                     "traffic": profiled_traffic(w.name), "peak_kind": peak_kind,
+                     "algorithmic_bytes": r["fused_bytes"], "launch_us": round(r["fused_us"], 3)},
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "plan": {"items": r["n_items"], "bf16_items": r["n_bf16_items"]},

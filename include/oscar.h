@@ -185,10 +185,12 @@ oscar_status oscar_decode_attention(oscar_cache* cache, int layer, const void* q
  * its own (request, kv-head) before it reads a ring or sink row or an INT2 page that the
  * append writes ([OSCAR] §2.2-B: quantize on append, then fused decode over the
  * mixed-precision cache; one launch per layer is this library's scheduling, not the
- * paper's).  Requires a reservation and a plan made after it that lists every reserved
- * slot (OSCAR_ERR_STATE otherwise); oscar_commit_append afterwards as usual.  Results are
- * those of the two separate calls.  Waits are bounded: a wait that runs out sets
- * OSCAR_FLAG_TIMEOUT. */
+ * paper's).  When the reservation has more append work than one wave of decode CTAs
+ * holds (long chunks, many requests), the call launches the append kernel and then the
+ * decode kernel instead (oscar_last_launch_count tells which).  Requires a reservation
+ * and a plan made after it that lists every reserved slot (OSCAR_ERR_STATE otherwise);
+ * oscar_commit_append afterwards as usual.  Results are those of the two separate calls.
+ * Waits are bounded: a wait that runs out sets OSCAR_FLAG_TIMEOUT. */
 oscar_status oscar_append_decode_attention(oscar_cache* cache, int layer, const void* k_new, const void* v_new,
                                            const void* q, void* out, void* workspace, size_t ws_bytes,
                                            float* out_f32, void* stream);

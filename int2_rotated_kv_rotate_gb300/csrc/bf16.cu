@@ -28,7 +28,7 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
   pdl_trigger();
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
   const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
-                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items};
+                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, 0, n_items};
   int* s_next = s_last_p + 1;
   for (int ix = wq.first(); ix >= 0; ix = wq.next(s_next)) {
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];

@@ -643,7 +643,7 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
   const int n_items = counts[1];
   const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * kAppendSplit : 0;
   const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
-                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_app + n_items, n_app};
+                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, n_app, counts[3]};
   unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
   bool waited = false;
   uint32_t phase_bits = 0, merge_phase = 0;

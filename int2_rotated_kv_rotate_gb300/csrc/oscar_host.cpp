@@ -150,7 +150,7 @@ struct oscar_cache {
   uint8_t* h_staging = nullptr;
   size_t staging_bytes = 0;
   uint32_t* h_status = nullptr;
-  int32_t* h_counts = nullptr;  // pinned: [append items, decode items, decode requests, 0]
+  int32_t* h_counts = nullptr;  // pinned: plan_counts as uploaded
   cudaEvent_t upload_done = nullptr;
   bool upload_pending = false;
   // pending append
@@ -713,13 +713,20 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   if (items.size() > c->lay.max_decode_items)
     return fail(OSCAR_ERR_INVALID_ARG, "plan of %zu items exceeds %zu; raise max_split_pages", items.size(),
                 c->lay.max_decode_items);
-  // the order CTAs take items in: largest first (stable)
+  // the order CTAs take items in (when they are more than one wave): the items that wait
+  // on no append task first, then those that may wait; largest first within each (stable)
   std::vector<int> order(items.size());
   for (size_t k = 0; k < items.size(); ++k) order[k] = int(k);
   auto cost = [&](const DecodeItem& d) {
     return d.kind == 0 ? (long long)(d.end - d.begin) * page_bytes : (long long)(d.end - d.begin) * 2LL * kHeadDim * 2;
   };
-  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cost(items[a]) > cost(items[b]); });
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) {
+    const bool wa = items[a].dep != kDepNone, wb = items[b].dep != kDepNone;
+    if (wa != wb) return wb;
+    return cost(items[a]) > cost(items[b]);
+  });
+  int n_front = 0;
+  while (n_front < int(order.size()) && items[order[n_front]].dep == kDepNone) ++n_front;
   oscar_status st = wait_uploads(c);
   if (st) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -731,7 +738,8 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_order, h_order, order.size() * 4, cudaMemcpyHostToDevice, s));
   c->h_counts[1] = int(items.size());
   c->h_counts[2] = n_req;
-  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.plan_counts + 4, c->h_counts + 1, 8, cudaMemcpyHostToDevice, s));
+  c->h_counts[3] = n_front;
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.plan_counts + 4, c->h_counts + 1, 12, cudaMemcpyHostToDevice, s));
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_reqs, c->h_staging, rb, cudaMemcpyHostToDevice, s));
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_items, c->h_staging + align256(rb), items.size() * sizeof(DecodeItem),
                            cudaMemcpyHostToDevice, s));
@@ -798,8 +806,20 @@ oscar_status oscar_append_decode_attention(oscar_cache* c, int layer, const void
   if (!c->plan_covers_reservation)
     return fail(OSCAR_ERR_STATE, "plan the decode after the reservation, over every reserved slot");
   if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
+  // The append tasks run in the same wave as the decode when they fit in it (4 per append
+  // item and kv-head: K and V halves); more of them (long chunks, many requests) would hold
+  // back the decode, so those go to the append kernel, which is launched first.
+  const int G = c->cfg.n_q_heads / c->cfg.n_kv_heads;
+  const int resident = decode_resident_ctas(G, c->cfg.group, c->n_sm);
+  const long long n_tasks = (long long)c->app_items * c->cfg.n_kv_heads * 4;
+  const bool fused = n_tasks <= (long long)resident;
+  if (!fused && c->app_items > 0) {
+    int e = launch_append(kernel_params(c), layer, k_new, v_new, std::min(c->app_items, 4 * c->n_sm), stream,
+                          &g_launches);
+    if (e) return fail(OSCAR_ERR_CUDA, "append launch: %s", cudaGetErrorString(cudaError_t(e)));
+  }
   int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_n_req,
-                        c->dec_items, c->n_sm, stream, &g_launches, k_new, v_new, true);
+                        c->dec_items, c->n_sm, stream, &g_launches, k_new, v_new, fused);
   if (e) return fail(OSCAR_ERR_CUDA, "append + decode launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }

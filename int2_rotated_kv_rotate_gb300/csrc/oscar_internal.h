@@ -81,7 +81,8 @@ struct DeviceLayout {
   size_t page_table;  // int32 [max_requests][max_pages_per_request]
   size_t status;      // uint32 flags
   size_t counters;    // uint32 [max_requests][H_kv] merge counters (second level)
-  size_t plan_counts; // int32 [4]: append items, decode items, decode requests, unused
+  size_t plan_counts; // int32 [4]: append items, decode items, decode requests, decode items
+                      // that wait on no append task (the first entries of decode_order)
   size_t append_reqs, append_items, decode_reqs, decode_items;
   size_t decode_order;  // int32 [max_decode_items]: items in the order CTAs take them (largest first)
   size_t sched;         // uint32 [4]: dynamic work counter, CTA exit counter (self-resetting)
