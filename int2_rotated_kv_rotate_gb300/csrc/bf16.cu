@@ -17,13 +17,24 @@
 namespace oscar {
 namespace {
 
+// The merge stages partial slots over the row buffers.
+template <int G>
+constexpr int kBf16SlabSlots = Bf16Rows<4, 2>::kSmemBytes / PartialSlot<G>::kBytes;
+
 template <int G>
 __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
-                                                         float* __restrict__ partials, uint16_t* __restrict__ out,
+                                                         uint8_t* __restrict__ partials, uint16_t* __restrict__ out,
                                                          float* __restrict__ out_f32) {
   extern __shared__ __align__(128) uint8_t smem[];
   float* qs = reinterpret_cast<float*>(smem + Bf16Rows<4, 2>::kSmemBytes);
-  int* s_last_p = reinterpret_cast<int*>(smem + Bf16Rows<4, 2>::kSmemBytes + G * kHeadDim * 4);
+  int* s_last_p = reinterpret_cast<int*>(smem + Bf16Rows<4, 2>::kSmemBytes + G * kQRow * 4);
+  uint64_t* slab_bar = reinterpret_cast<uint64_t*>(smem + Bf16Rows<4, 2>::kSmemBytes + G * kQRow * 4 + 16);
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(slab_bar), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  uint32_t slab_phase = 0;
   pdl_wait();
   pdl_trigger();
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
@@ -34,8 +45,8 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-    float* part = partials + size_t(ix) * G * (kHeadDim + 2);
-    for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[e] = bf16_f32(q[head0 * kHeadDim + e]);
+    uint8_t* part = partials + size_t(ix) * PartialSlot<G>::kBytes;
+    for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[(e / kHeadDim) * kQRow + e % kHeadDim] = bf16_f32(q[head0 * kHeadDim + e]);
     __syncthreads();
     const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
     if (!slot_ok && threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
@@ -62,7 +73,8 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     bf16_rows_mma<G, 4, 2>(rowK, rowV, t0, t1, qs, part, smem);
 
     MergeAcc<G, 128> acc;
-    if (merge_partial<G, 128>(kp, it, ix, partials, acc, s_last_p, [] {}) == kMergeFinal) {
+    if (merge_partial<G, 128>(kp, it, partials, acc, s_last_p, smem, kBf16SlabSlots<G>, smem_u32(slab_bar), slab_phase,
+                              [] {})) {
       const int c = threadIdx.x;
 #pragma unroll
       for (int h = 0; h < G; ++h) {
@@ -71,11 +83,12 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
         if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = r;
       }
     }
+    fence_proxy_async();  // generic use of the buffers is over before later bulk copies
   }
   wq.leave();
 }
 
-constexpr int kBf16KernelSmem(int G) { return Bf16Rows<4, 2>::kSmemBytes + G * kHeadDim * 4 + 32; }
+constexpr int kBf16KernelSmem(int G) { return Bf16Rows<4, 2>::kSmemBytes + G * kQRow * 4 + 32; }  // + flags, barrier
 
 template <int G>
 int resident_ctas(int n_sm) {
@@ -94,7 +107,7 @@ int resident_ctas(int n_sm) {
 template <int G>
 int launch_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
              const DecodeWorkspace& wl, int n_items, int n_sm, void* stream, int* launches) {
-  float* partials = reinterpret_cast<float*>(ws + wl.partials);
+  uint8_t* partials = ws + wl.partials;
   const int resident = resident_ctas<G>(n_sm);
   if (resident < 0) return -resident;
   (void)n_items;

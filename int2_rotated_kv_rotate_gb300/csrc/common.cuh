@@ -108,9 +108,32 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
   return y;
 }
-// Two floats as bf16 (round to nearest even), first in the low half.
+// Two floats as bf16 (round to nearest even), first in the low half (one conversion).
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-  return uint32_t(bf16_rne(lo)) | (uint32_t(bf16_rne(hi)) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+// x rounded to the nearest bf16 (even on ties), as fp32 (finite x: the splits below).
+__device__ __forceinline__ float bf16_round(float x) { return __uint_as_float(pack_bf16(0.f, x) & 0xffff0000u); }
+
+// ---------------------------------------------------------------- partial slots
+// The partial of one work item for the G heads of its kv group: float2 (m, l) per head
+// (m in log2 units, l the softmax denominator), then the normalised output o~ / l per head
+// and channel in fp32 (0 where l = 0).  fp16 here was measured to exceed the output
+// tolerance on large values (its error is relative to the value).
+template <int G>
+struct PartialSlot {
+  static constexpr int kMlBytes = G * 8;
+  static constexpr int kBytes = G * (8 + 4 * kHeadDim);
+  static_assert(kBytes % 16 == 0, "slots are bulk-copied");
+};
+
+// Store head h, channel c of a partial (unnormalised o); c == 0 also stores (m, l).
+template <int G>
+__device__ __forceinline__ void store_slot(uint8_t* slot, int h, int c, float m, float l, float o) {
+  if (c == 0) reinterpret_cast<float2*>(slot)[h] = make_float2(m, l);
+  reinterpret_cast<float*>(slot + PartialSlot<G>::kMlBytes)[h * kHeadDim + c] = l > 0.f ? o / l : 0.f;
 }
 
 // ---------------------------------------------------------------- BF16 rows on tensor cores
@@ -121,20 +144,24 @@ template <int NW, int NBUF>
 struct Bf16Rows {
   static constexpr int kChunk = 16 * NW;                   // tokens per chunk
   static constexpr int kBufBytes = 2 * kChunk * kRowPad;   // K and V rows of one chunk
-  static constexpr int kSmemBytes = NBUF * kBufBytes;
+  static constexpr int kPtrBytes = 2 * 2 * kChunk * 8;     // row pointers of two chunks
+  static constexpr int kSmemBytes = NBUF * kBufBytes + kPtrBytes;
 };
+
+// Row stride (floats) of a CTA's q / q~ staging: the 4 heads of an MMA n-tile fall in
+// different banks.
+constexpr int kQRow = kHeadDim + 4;
 
 // Softmax attention of G query heads over bf16 token rows u in [begin, end) (row pointers
 // from rowK(u), rowV(u): 128 bf16 channels each), CTA of NW warps.  qg is fp32 [G][128]
-// (global or shared).  Chunks of 16 NW tokens are staged by cp.async (zero-filled past
-// `end`) into NBUF buffers (2 = double buffered); warp w takes tokens 16w..16w+15 of each
-// chunk.  Scores and values use mma.sync bf16 with q split into bf16 hi + lo columns
+// (shared, rows kQRow floats apart).  Chunks of 16 NW tokens are staged by cp.async
+// (zero-filled past `end`) into NBUF buffers (2 = double buffered); warp w takes tokens
+// 16w..16w+15 of each chunk.  Scores and values use mma.sync bf16 with q split into bf16 hi + lo columns
 // (4 heads per n-tile) and p split the same way, so both products keep ~16 significant
-// bits.  Writes the partial m (log2 units), l, o~ (unnormalised) per head to
-// part[G][2 + d].  smem must hold Bf16Rows<NW, NBUF>::kSmemBytes and NW * G * (d + 2)
-// floats (the two may alias).
+// bits.  Writes the partial slot (PartialSlot<G>) at part.  smem must hold
+// Bf16Rows<NW, NBUF>::kSmemBytes and NW * G * (d + 2) floats (the two may alias).
 template <int G, int NW, int NBUF, typename RowK, typename RowV>
-__device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const float* qg, float* part, uint8_t* smem) {
+__device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const float* qg, uint8_t* part, uint8_t* smem) {
   constexpr int NT = G / 4;
   using B = Bf16Rows<NW, NBUF>;
   constexpr int kChunkTok = B::kChunk;
@@ -149,11 +176,11 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
     for (int j = 0; j < NT; ++j) {
       const int head = 4 * j + (gid >> 1);
       const bool lo = gid & 1;
-      const float* qh = qg + head * kHeadDim + 16 * kc + 2 * tig;
+      const float* qh = qg + head * kQRow + 16 * kc + 2 * tig;
       float v[4] = {qh[0], qh[1], qh[8], qh[9]};
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const float hi = bf16_f32(bf16_rne(v[e]));
+        const float hi = bf16_round(v[e]);
         v[e] = lo ? v[e] - hi : hi;
       }
       bq[kc][j][0] = pack_bf16(v[0], v[1]);
@@ -172,17 +199,25 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
   const uint32_t sbase = smem_u32(smem);
   const int n_chunks = end > begin ? (end - begin + kChunkTok - 1) / kChunkTok : 0;
   // stage chunk c into buffer c & 1: thread t copies 16-byte segment (t & 15) of rows t/16 + 8k
+  // row pointers of chunk c (thread t: row t, K rows then V rows; null past `end`), two
+  // chunks' worth so that filling the next never races with issuing the current
+  const uint16_t** rptr = reinterpret_cast<const uint16_t**>(smem + NBUF * kBf16BufBytes);
+  static_assert(2 * kChunkTok == 32 * NW, "one row per thread");
   auto stage = [&](int c) {
+    const uint16_t** rp = rptr + (c & 1) * 2 * kChunkTok;
+    {
+      const int tok = t & (kChunkTok - 1), u = begin + c * kChunkTok + tok;
+      rp[t] = u < end ? (t < kChunkTok ? rowK(u) : rowV(u)) : nullptr;
+    }
+    __syncthreads();
     const uint32_t buf = sbase + (c % NBUF) * kBf16BufBytes;
     const int seg = t & 15;
+    const uint16_t* any = rp[0];  // a valid row of the chunk (the chunk has one)
 #pragma unroll 4
     for (int k = 0; k < 16; ++k) {
       const int row = (t >> 4) + 2 * NW * k;  // K rows then V rows
-      const int tok = row & (kChunkTok - 1);
-      const int u = begin + c * kChunkTok + tok;
-      const bool ok = u < end;
-      const uint16_t* src = ok ? (row < kChunkTok ? rowK(u) : rowV(u)) : rowK(begin);
-      cp_async16(buf + row * kRowPad + seg * 16, src + seg * 8, ok ? 16u : 0u);
+      const uint16_t* src = rp[row];
+      cp_async16(buf + row * kRowPad + seg * 16, (src ? src : any) + seg * 8, src ? 16u : 0u);
     }
     cp_async_commit();
   };
@@ -248,7 +283,7 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
       const float p0 = lg[j][0] == -INFINITY ? 0.f : ex2(lg[j][0] - muse[j]);
       const float p1 = lg[j][1] == -INFINITY ? 0.f : ex2(lg[j][1] - muse[j]);
       l_part[j] += p0 + p1;
-      const float h0 = bf16_f32(bf16_rne(p0)), h1 = bf16_f32(bf16_rne(p1));
+      const float h0 = bf16_round(p0), h1 = bf16_round(p1);
       bp[j][0] = movmatrix_trans(pack_bf16(h0, p0 - h0));
       bp[j][1] = movmatrix_trans(pack_bf16(h1, p1 - h1));
     }
@@ -304,12 +339,7 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
       l = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 1], l);
       o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + c], o);
     }
-    float* ph = part + size_t(h) * (kHeadDim + 2);
-    if (c == 0) {
-      ph[0] = ms;
-      ph[1] = l;
-    }
-    ph[2 + c] = o;
+    store_slot<G>(part, h, c, ms, l, o);
   }
   __syncthreads();
 }
@@ -325,114 +355,89 @@ __device__ __forceinline__ unsigned atomic_add_acq_rel(unsigned* p, unsigned v) 
 }
 
 // ---------------------------------------------------------------- merging partials
-// A partial slot holds, for each of the G heads of a kv group: m (log2 units), l, then the
-// unnormalised o[kHeadDim].  Thread (c, hb) of an NTH-thread CTA owns channel c of heads
-// hb, hb + NTH/128, ...; every thread reads the (m, l) words it needs itself (the same
-// addresses across a warp), so a merge of up to kRound partials takes one round of loads
-// and no block barrier.
+// Thread (c, hb) of an NTH-thread CTA owns channel c of heads hb, hb + NTH/128, ...
 template <int G, int NTH>
 struct MergeAcc {
   static constexpr int kStride = NTH / kHeadDim;
   static constexpr int HPT = G / kStride;
   static_assert(NTH % kHeadDim == 0 && G % kStride == 0, "thread count and group size");
-  float M[HPT], L[HPT], O[HPT];
+  float M[HPT], L[HPT], O[HPT];  // running max (log2), sum of weights, weighted sum of o~ / l
 };
 
-// acc = online-softmax merge of the partial slots first, first + stride, ... (count slots).
+// Online merge of n partial slots staged in shared memory into acc.
 template <int G, int NTH>
-__device__ void merge_slots(const float* partials, int first, int stride, int count, MergeAcc<G, NTH>& acc) {
+__device__ void merge_slab(const uint8_t* slab, int n, MergeAcc<G, NTH>& acc) {
   using A = MergeAcc<G, NTH>;
-  constexpr int P = kHeadDim + 2, HPT = A::HPT, kRound = 16 / HPT > 0 ? 16 / HPT : 1;
+  constexpr int S = PartialSlot<G>::kBytes;
   const int c = threadIdx.x & (kHeadDim - 1), hb = threadIdx.x / kHeadDim;
 #pragma unroll
-  for (int q = 0; q < HPT; ++q) {
+  for (int q = 0; q < A::HPT; ++q) {
+    const int h = hb + A::kStride * q;
+    float mx = acc.M[q];
+    for (int i = 0; i < n; ++i) mx = fmaxf(mx, reinterpret_cast<const float2*>(slab + i * S)[h].x);
+    if (mx == -INFINITY) continue;  // nothing but empty partials so far
+    const float a = ex2(acc.M[q] - mx);  // acc.M = -inf gives 0
+    float L = acc.L[q] * a, O = acc.O[q] * a;
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+      const float2 ml = reinterpret_cast<const float2*>(slab + i * S)[h];
+      if (ml.x == -INFINITY) continue;
+      const float w = ex2(ml.x - mx) * ml.y;
+      L += w;
+      O = fmaf(w, reinterpret_cast<const float*>(slab + i * S + PartialSlot<G>::kMlBytes)[h * kHeadDim + c], O);
+    }
+    acc.M[q] = mx;
+    acc.L[q] = L;
+    acc.O[q] = O;
+  }
+}
+
+// After the partial of item `it` is written, by every thread: the last CTA to finish an
+// item of (request, kv-head) merges all of its partial slots into acc (true); the others
+// return false.  on_last() runs (all threads) as soon as this CTA knows it merges.  The
+// slots are bulk-copied into slab (shared, slab_slots of them per round) on the mbarrier
+// slab_bar (phase tracked in slab_phase); waits are bounded.  s_flag: one int of shared
+// memory.
+template <int G, int NTH, typename OnLast>
+__device__ bool merge_partial(const KernelParams& kp, const DecodeItem& it, const uint8_t* partials,
+                              MergeAcc<G, NTH>& acc, int* s_flag, uint8_t* slab, int slab_slots, uint32_t slab_bar,
+                              uint32_t& slab_phase, OnLast on_last) {
+  constexpr int S = PartialSlot<G>::kBytes;
+  fence_proxy_async();  // this thread's generic shared-memory accesses precede the bulk copies below
+  __syncthreads();      // the partial is written (published by the release below)
+  if (threadIdx.x == 0) {
+    unsigned* hc = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
+    const unsigned prev = atomic_add_acq_rel(hc, 1u);
+    *s_flag = prev == unsigned(it.head_count - 1);
+    if (*s_flag) *hc = 0u;  // every partial of (request, kv-head) has arrived
+  }
+  __syncthreads();
+  if (!*s_flag) return false;
+  on_last();
+#pragma unroll
+  for (int q = 0; q < MergeAcc<G, NTH>::HPT; ++q) {
     acc.M[q] = -INFINITY;
     acc.L[q] = 0.f;
     acc.O[q] = 0.f;
   }
-  for (int i0 = 0; i0 < count; i0 += kRound) {
-    float mv[kRound][HPT], lv[kRound][HPT], ov[kRound][HPT];
-#pragma unroll
-    for (int k = 0; k < kRound; ++k)
-#pragma unroll
-      for (int q = 0; q < HPT; ++q) {
-        const bool in = i0 + k < count;
-        const float* ph = partials + (size_t(first) + size_t(i0 + k) * stride) * G * P + (hb + A::kStride * q) * P;
-        mv[k][q] = in ? __ldcg(ph) : -INFINITY;
-        lv[k][q] = in ? __ldcg(ph + 1) : 0.f;
-        ov[k][q] = in ? __ldcg(ph + 2 + c) : 0.f;
-      }
-#pragma unroll
-    for (int k = 0; k < kRound; ++k)
-#pragma unroll
-      for (int q = 0; q < HPT; ++q) {
-        if (mv[k][q] == -INFINITY) continue;
-        const float mn = fmaxf(acc.M[q], mv[k][q]);
-        const float a = ex2(acc.M[q] - mn), b = ex2(mv[k][q] - mn);  // acc.M = -inf gives a = 0
-        acc.L[q] = fmaf(acc.L[q], a, lv[k][q] * b);
-        acc.O[q] = fmaf(acc.O[q], a, ov[k][q] * b);
-        acc.M[q] = mn;
-      }
-  }
-}
-
-template <int G, int NTH>
-__device__ void store_partial(float* slot, const MergeAcc<G, NTH>& acc) {
-  using A = MergeAcc<G, NTH>;
-  constexpr int P = kHeadDim + 2;
-  const int c = threadIdx.x & (kHeadDim - 1), hb = threadIdx.x / kHeadDim;
-#pragma unroll
-  for (int q = 0; q < A::HPT; ++q) {
-    float* ph = slot + (hb + A::kStride * q) * P;
-    if (c == 0) {
-      ph[0] = acc.M[q];
-      ph[1] = acc.L[q];
+  for (int base = 0; base < it.head_count; base += slab_slots) {
+    const int n = min(slab_slots, it.head_count - base);
+    if (threadIdx.x == 0) {
+      fence_proxy_async();
+      mbar_expect_tx(slab_bar, uint32_t(n * S));
+      bulk_g2s(smem_u32(slab), partials + size_t(it.head_first + base) * S, uint32_t(n * S), slab_bar);
     }
-    ph[2 + c] = acc.O[q];
+    const bool ok = mbar_wait(slab_bar, slab_phase);
+    if (!ok) {
+      if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+      mbar_wait(slab_bar, slab_phase);  // drain (bounded) before the memory is reused
+    }
+    slab_phase ^= 1u;
+    if (ok) merge_slab<G, NTH>(slab, n, acc);
+    fence_proxy_async();
+    __syncthreads();  // the slab is refilled by the next round
   }
-}
-
-// Roles of a CTA after merge_partial.
-constexpr int kMergeNone = 0;       // not the last of its group: nothing to do
-constexpr int kMergeGroupOnly = 1;  // merged its group into the group's first slot
-constexpr int kMergeFinal = 2;      // holds the whole (request, kv-head) merge in acc
-
-// After the partial of item `it` (slot ix) is written, by every thread: the last finisher
-// of each group of kMergeGroup consecutive items merges the group; the last group merger
-// merges the groups.  on_group_last() runs (all threads) as soon as this CTA knows it
-// merges a group.  s_flag: one int of shared memory.
-template <int G, int NTH, typename OnGroupLast>
-__device__ int merge_partial(const KernelParams& kp, const DecodeItem& it, int ix, float* partials,
-                             MergeAcc<G, NTH>& acc, int* s_flag, OnGroupLast on_group_last) {
-  __syncthreads();  // the partial is written (published by the release below)
-  const int grp = (ix - it.head_first) / kMergeGroup;
-  const int n_groups = (it.head_count + kMergeGroup - 1) / kMergeGroup;
-  const int grp_first = it.head_first + grp * kMergeGroup;
-  const int grp_size = min(kMergeGroup, it.head_count - grp * kMergeGroup);
-  if (threadIdx.x == 0) {
-    unsigned* gc = reinterpret_cast<unsigned*>(kp.base + kp.lay.group_counters) + it.gcounter;
-    const unsigned prev = atomic_add_acq_rel(gc, 1u);
-    *s_flag = prev == unsigned(grp_size - 1);
-    if (*s_flag) *gc = 0u;  // every partial of the group has arrived
-  }
-  __syncthreads();
-  if (!*s_flag) return kMergeNone;
-  on_group_last();
-  merge_slots<G, NTH>(partials, grp_first, 1, grp_size, acc);
-  if (n_groups == 1) return kMergeFinal;
-  __syncthreads();  // every thread has read the group's slots before the first is overwritten
-  store_partial<G, NTH>(partials + size_t(grp_first) * G * (kHeadDim + 2), acc);
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    unsigned* hc = reinterpret_cast<unsigned*>(kp.base + kp.lay.counters) + size_t(it.req) * kp.n_kv_heads + it.kvh;
-    const unsigned prev = atomic_add_acq_rel(hc, 1u);
-    *s_flag = prev == unsigned(n_groups - 1);
-    if (*s_flag) *hc = 0u;
-  }
-  __syncthreads();
-  if (!*s_flag) return kMergeGroupOnly;
-  merge_slots<G, NTH>(partials, it.head_first, kMergeGroup, n_groups, acc);
-  return kMergeFinal;
+  return true;
 }
 
 // Dynamic work distribution of a persistent-style decode grid: CTA b first takes position

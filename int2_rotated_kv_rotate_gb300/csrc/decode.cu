@@ -37,9 +37,21 @@
 namespace oscar {
 namespace {
 
-constexpr int kWarps = 8;   // warps per split-kernel CTA
 constexpr int kStages = 2;  // page stages per warp
-constexpr int kThreads = 32 * kWarps;
+
+// CTA shape of the split kernel: one CTA per SM, 16 warps at GQA 4 (128 registers a
+// thread fill the register file), 8 warps at GQA 8 (more registers a thread).  Each
+// channel of the q rotation has kParts threads, each summing 128 / kParts rows of R_K.
+template <int G>
+struct Shape {
+  static constexpr int NW = decode_warps(G);
+  static constexpr int NTH = 32 * NW;
+  static constexpr int kParts = NTH / kHeadDim;
+  static constexpr int kRows = kHeadDim / kParts;     // rows of R_K per thread
+  static constexpr int kQinRow = kHeadDim + 4 * kParts;  // padded staging row of q
+  static_assert(append_task_split(G) * append_dev::AppendShape<NTH>::kTokens == append_dev::kTok,
+                "append tasks cover an item");
+};
 
 // ---------------------------------------------------------------- MMA helpers
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3, uint32_t b0,
@@ -75,61 +87,62 @@ __device__ __forceinline__ uint32_t field(uint32_t w, uint32_t w_shr8, int f) {
 __device__ __forceinline__ int tau8(int m) { return (m >> 1) + 4 * (m & 1); }
 
 // ---------------------------------------------------------------- q rotation
-// Thread (c, half) of a split CTA holds column c of R_K, rows 64 half .. 64 half + 63
-// (R_K is written long before by oscar_set_layer_params, so this runs before the wait on
-// the preceding kernel).
-__device__ __forceinline__ void load_rk_cols(const KernelParams& kp, int layer, int kvh, float (&rk)[64]) {
-  const int c = threadIdx.x & (kHeadDim - 1), i0 = (threadIdx.x >> 7) * 64;
+// Thread t of a split CTA holds column c = t / kParts of R_K, rows kRows (t % kParts) ..
+// + kRows - 1, so the parts of a column sit in neighbouring lanes (R_K is written long
+// before by oscar_set_layer_params, so this runs before the wait on the preceding kernel).
+template <int G>
+__device__ __forceinline__ void load_rk_cols(const KernelParams& kp, int layer, int kvh,
+                                             float (&rk)[Shape<G>::kRows]) {
+  using Sh = Shape<G>;
+  const int c = threadIdx.x / Sh::kParts, i0 = (threadIdx.x % Sh::kParts) * Sh::kRows;
   const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) +
                    (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim + size_t(i0) * kHeadDim + c;
 #pragma unroll
-  for (int u = 0; u < 64; ++u) rk[u] = __ldg(R + u * kHeadDim);
+  for (int u = 0; u < Sh::kRows; ++u) rk[u] = __ldg(R + u * kHeadDim);
 }
 
-// q~ = R_K^T q (fp32) for the G query heads at q_head0 into qts[G][d] (shared), and the
-// sums of q~ over each 32-channel quarter into qss[G][4] (GROUP = 128: qss[h][0] holds the
-// whole sum, the rest 0).  qin: G * d floats of shared staging.  All threads.
-template <int G, int GROUP>
-__device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)[64], float* qin, float* qts,
-                         float* qss) {
-  const int tid = threadIdx.x, c = tid & (kHeadDim - 1), half = tid >> 7;
-  for (int e = tid; e < G * kHeadDim; e += kThreads) qin[e] = bf16_f32(q_head0[e]);
+// q~ = R_K^T q (fp32) for the G query heads at q_head0 into qts[G][kQRow] (shared), and per
+// warp w the sum of q~ over its kHeadDim / NW channels into qpart[w][G] (shared).  qin:
+// G * kQinRow floats of shared staging (channel i of a head at i + 4 (i / kRows), so that
+// the parts a warp reads together fall in different banks).  All threads; two barriers.
+template <int G>
+__device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)[Shape<G>::kRows], float* qin,
+                         float* qts, float* qpart) {
+  using Sh = Shape<G>;
+  constexpr int KP = Sh::kParts, KR = Sh::kRows;
+  const int tid = threadIdx.x, c = tid / KP, part = tid % KP, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < G * kHeadDim; e += Sh::NTH) {
+    const int h = e / kHeadDim, i = e % kHeadDim;
+    qin[h * Sh::kQinRow + i + 4 * (i / KR)] = bf16_f32(q_head0[e]);
+  }
   __syncthreads();
   float acc[G];
 #pragma unroll
   for (int h = 0; h < G; ++h) acc[h] = 0.f;
 #pragma unroll
-  for (int u = 0; u < 64; u += 4)
+  for (int u = 0; u < KR; u += 4)
 #pragma unroll
     for (int h = 0; h < G; ++h) {
-      const float4 x = *reinterpret_cast<const float4*>(qin + h * kHeadDim + 64 * half + u);
+      const float4 x = *reinterpret_cast<const float4*>(qin + h * Sh::kQinRow + (KR + 4) * part + u);
       acc[h] = fmaf(rk[u + 3], x.w, fmaf(rk[u + 2], x.z, fmaf(rk[u + 1], x.y, fmaf(rk[u], x.x, acc[h]))));
     }
-  if (half == 1)
 #pragma unroll
-    for (int h = 0; h < G; ++h) qts[h * kHeadDim + c] = acc[h];
-  __syncthreads();
-  if (half == 0)
-#pragma unroll
-    for (int h = 0; h < G; ++h) qts[h * kHeadDim + c] += acc[h];
-  __syncthreads();
-  const int warp = tid >> 5, lane = tid & 31;
-  if (warp < G) {
-    float sq[4];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      sq[k] = qts[warp * kHeadDim + 32 * k + lane];
-#pragma unroll
-      for (int off = 16; off > 0; off >>= 1) sq[k] += __shfl_xor_sync(0xffffffffu, sq[k], off);
+  for (int h = 0; h < G; ++h) {
+    // the parts of the channel in ascending row order; every lane of the group gets the sum
+    float v = acc[h];
+    if (KP == 2) {
+      const float o = __shfl_xor_sync(0xffffffffu, v, 1);
+      v = part ? o + v : v + o;
+    } else {
+      const float p0 = __shfl_sync(0xffffffffu, v, lane & ~3), p1 = __shfl_sync(0xffffffffu, v, (lane & ~3) | 1);
+      const float p2 = __shfl_sync(0xffffffffu, v, (lane & ~3) | 2), p3 = __shfl_sync(0xffffffffu, v, (lane & ~3) | 3);
+      v = ((p0 + p1) + p2) + p3;
     }
-    if (lane < 4) {
-      float v;
-      if (GROUP == 32)
-        v = lane == 0 ? sq[0] : lane == 1 ? sq[1] : lane == 2 ? sq[2] : sq[3];
-      else
-        v = lane == 0 ? (sq[0] + sq[1]) + (sq[2] + sq[3]) : 0.f;
-      qss[warp * 4 + lane] = v;
-    }
+    if (part == 0) qts[h * kQRow + c] = v;
+    float sw = part == 0 ? v : 0.f;  // the warp's channels, each counted once
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) sw += __shfl_xor_sync(0xffffffffu, sw, off);
+    if (lane == 0) qpart[warp * G + h] = sw;
   }
   __syncthreads();
 }
@@ -137,24 +150,34 @@ __device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)
 // ---------------------------------------------------------------- split kernel
 template <int G, int GROUP>
 struct Cfg {
+  static constexpr int NW = Shape<G>::NW, NTH = Shape<G>::NTH;
   static constexpr int NG = kHeadDim / GROUP;           // groups per token
   static constexpr int NT = G / 4;                      // score n-tiles (4 heads x hi/lo each)
   static constexpr int kCodeBytes = 2 * kPage * kRowBytes;  // K then V codes
   static constexpr int kSzBytes = 2 * kPage * NG * 4;       // K then V (scale, zero)
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
-  static constexpr int kPipeBytes = kWarps * kStages * kStageBytes;
+  static constexpr int kPipeBytes = NW * kStages * kStageBytes;
   // fused append tasks: R (fp32 [d][d]) then the append scratch, in the same memory
   static constexpr int kAppendR = kHeadDim * kHeadDim * 4;
   static constexpr int kAppendBytes = kAppendR + int(sizeof(append_dev::Smem));
-  static constexpr int kWorkBytes = kPipeBytes > kAppendBytes ? kPipeBytes : ((kAppendBytes + 127) / 128) * 128;
+  // the merge: R_V^T (64 KB) then a slab of at least 32 partial slots
+  static constexpr int kSlabOff = kHeadDim * kHeadDim * 4;
+  static constexpr int kMergeBytes = kSlabOff + 32 * PartialSlot<G>::kBytes;
+  static constexpr int kWorkBytes0 = kPipeBytes > kAppendBytes ? kPipeBytes : kAppendBytes;
+  static constexpr int kWorkBytes = (((kWorkBytes0 > kMergeBytes ? kWorkBytes0 : kMergeBytes) + 127) / 128) * 128;
+  static constexpr int kSlabSlots = (kWorkBytes - kSlabOff) / PartialSlot<G>::kBytes;
   static constexpr int kCtl = kWorkBytes;           // control area
-  static constexpr int kCtlBytes = 256;             // barriers (128 B), merge flag, next item, merge barrier
-  static constexpr int kQin = kCtl + kCtlBytes;     // fp32 [G][d] query staging
-  static constexpr int kQts = kQin + G * kHeadDim * 4;  // fp32 [G][d] q~
-  static constexpr int kQss = kQts + G * kHeadDim * 4;  // fp32 [G][4] sums of q~ per 32 channels
-  static constexpr int kSmemBytes = kQss + G * 16;
-  static_assert(kPipeBytes >= Bf16Rows<kWarps, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
-  static_assert(kPipeBytes >= (kHeadDim * kHeadDim + G * kHeadDim) * 4, "the merge reuses the page pipeline memory");
+  // control: page barriers (NW x kStages), merge flag, next item, R_V^T and slab barriers
+  static constexpr int kCtlBytes = ((NW * kStages * 8 + 24 + 127) / 128) * 128;
+  static constexpr int kQin = kCtl + kCtlBytes;     // fp32 [G][kQinRow] query staging
+  static constexpr int kQts = kQin + G * Shape<G>::kQinRow * 4;  // fp32 [G][kQRow] q~
+  static constexpr int kQss = kQts + G * kQRow * 4;  // fp32 [NW][G] sums of q~ per warp's channels
+  static constexpr int kSmemBytes = kQss + NW * G * 4;
+  static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
+  static_assert(kWorkBytes >= Bf16Rows<NW, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
+  static_assert(kWorkBytes >= NW * G * (kHeadDim + 2) * 4, "per-warp results reuse the page pipeline memory");
+  static_assert(kSlabOff + (1 + Shape<G>::NTH / kHeadDim) * G * kHeadDim * 4 <= kMergeBytes,
+                "o~ and the partial sums of the output rotation are staged over the slab");
 };
 
 // Start the bulk copy of R_V^T (64 KB) of (layer, kv-head) into smem[0, 64 KB).
@@ -171,14 +194,16 @@ __device__ void fetch_rvt(const KernelParams& kp, int layer, int kvh, uint8_t* s
 // Final merge: o~ = O / L, then o = R_V o~ with R_V^T in smem (fetched by fetch_rvt; this
 // waits for it), bf16 and optional fp32 store.
 template <int G>
-__device__ void finish_output(const KernelParams& kp, const DecodeItem& it, const MergeAcc<G, kThreads>& acc, uint16_t* out,
+__device__ void finish_output(const KernelParams& kp, const DecodeItem& it, const MergeAcc<G, Shape<G>::NTH>& acc, uint16_t* out,
                               float* out_f32, uint8_t* smem, uint32_t mbar, uint32_t& mphase) {
-  constexpr int HPT = MergeAcc<G, kThreads>::HPT;
+  using A = MergeAcc<G, Shape<G>::NTH>;
+  constexpr int HPT = A::HPT, KS = A::kStride, JR = kHeadDim / KS;
   const int t = threadIdx.x, c = t & (kHeadDim - 1), hb = t >> 7;
   const float* Rs = reinterpret_cast<const float*>(smem);   // R_V^T [128][128]
   float* os = reinterpret_cast<float*>(smem) + kHeadDim * kHeadDim;  // o~ [G][128]
+  float* red = os + G * kHeadDim;                                      // [KS][G][128] partial sums
 #pragma unroll
-  for (int q = 0; q < HPT; ++q) os[(hb + 2 * q) * kHeadDim + c] = acc.L[q] > 0.f ? acc.O[q] / acc.L[q] : 0.f;
+  for (int q = 0; q < HPT; ++q) os[(hb + KS * q) * kHeadDim + c] = acc.L[q] > 0.f ? acc.O[q] / acc.L[q] : 0.f;
   const bool ok = mbar_wait(mbar, mphase);
   if (!ok) {
     if (t == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
@@ -186,25 +211,33 @@ __device__ void finish_output(const KernelParams& kp, const DecodeItem& it, cons
   }
   mphase ^= 1u;
   __syncthreads();
-  float r[HPT];
+  // thread (c, hb): rows j of R_V^T in [JR hb, JR hb + JR) for every head, then the KS
+  // partial sums of a (head, channel) are added in ascending row order
+  float r[G];
 #pragma unroll
-  for (int q = 0; q < HPT; ++q) r[q] = 0.f;
-#pragma unroll 4
-  for (int j = 0; j < kHeadDim; j += 4) {
+  for (int h = 0; h < G; ++h) r[h] = 0.f;
+#pragma unroll 2
+  for (int j = JR * hb; j < JR * hb + JR; j += 4) {
     const float r0 = Rs[(j + 0) * kHeadDim + c], r1 = Rs[(j + 1) * kHeadDim + c];
     const float r2 = Rs[(j + 2) * kHeadDim + c], r3 = Rs[(j + 3) * kHeadDim + c];
 #pragma unroll
-    for (int q = 0; q < HPT; ++q) {
-      const float4 x = *reinterpret_cast<const float4*>(os + (hb + 2 * q) * kHeadDim + j);
-      r[q] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, r[q]))));
+    for (int h = 0; h < G; ++h) {
+      const float4 x = *reinterpret_cast<const float4*>(os + h * kHeadDim + j);
+      r[h] = fmaf(r3, x.w, fmaf(r2, x.z, fmaf(r1, x.y, fmaf(r0, x.x, r[h]))));
     }
   }
+#pragma unroll
+  for (int h = 0; h < G; ++h) red[(hb * G + h) * kHeadDim + c] = r[h];
+  __syncthreads();
   const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
 #pragma unroll
   for (int q = 0; q < HPT; ++q) {
-    const int h = hb + 2 * q;
-    out[(head0 + h) * kHeadDim + c] = bf16_rne(ok ? r[q] : 0.f);
-    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = ok ? r[q] : 0.f;
+    const int h = hb + KS * q;
+    float v = 0.f;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) v += red[(k * G + h) * kHeadDim + c];
+    out[(head0 + h) * kHeadDim + c] = bf16_rne(ok ? v : 0.f);
+    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = ok ? v : 0.f;
   }
 }
 
@@ -212,7 +245,7 @@ __device__ void finish_output(const KernelParams& kp, const DecodeItem& it, cons
 // position H + u - min(L, S) in ring slot p % W.
 template <int G>
 __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
-                                 const float* qts, float* part, uint8_t* smem) {
+                                 const float* qts, uint8_t* part, uint8_t* smem) {
   const int S = kp.n_sink;
   const int n_s = min(dr.L, S);
   const uint16_t* sinkK = reinterpret_cast<const uint16_t*>(
@@ -230,7 +263,7 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
   auto rowV = [=](int u) {
     return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t((H + u - n_s) % W) * kHeadDim;
   };
-  bf16_rows_mma<G, kWarps, 1>(rowK, rowV, it.begin, it.end, qts, part, smem);
+  bf16_rows_mma<G, Shape<G>::NW, 1>(rowK, rowV, it.begin, it.end, qts, part, smem);
 }
 
 // Issue (lane 0 of the calling warp) the bulk copies of the warp's k-th page of an INT2
@@ -240,7 +273,7 @@ __device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeI
                                 uint8_t* smem) {
   using C = Cfg<G, GROUP>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int lp = it.begin + warp + kWarps * k;
+  const int lp = it.begin + warp + C::NW * k;
   const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
   int phys = -1;
   if (lp < kp.max_pages_per_request) phys = ptab[lp];
@@ -263,11 +296,11 @@ __device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeI
 }
 
 // INT2 history pages [it.begin, it.end) of one (request, kv-head).  Positions outside
-// [S, H) inside those pages are masked.  Warp w takes pages begin + w, + kWarps, ...
+// [S, H) inside those pages are masked.  Warp w takes pages begin + w, + NW, ...
 template <int G, int GROUP>
 __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
-                                const float* qts, const float* qss, float* part, uint8_t* smem,
-                                uint32_t& phase_bits, uint32_t pre_mask) {
+                                const float* qts, const float* qss, uint8_t* part, uint8_t* smem,
+                                uint32_t& phase_bits, uint32_t pre_mask, const unsigned* pages_ctr) {
   using C = Cfg<G, GROUP>;
   constexpr int NG = C::NG, NT = C::NT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -276,9 +309,22 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kCtl) + warp * kStages;
   const int S = kp.n_sink, H = dr.H;
 
-  // my pages: it.begin + warp + kWarps * k
-  const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
-  auto issue = [&](int k) -> bool { return int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem); };
+  // my pages: it.begin + warp + C::NW * k
+  const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + C::NW - 1) / C::NW : 0;
+  // fused append: a page not wholly below H_pre may hold rows this launch's append tasks
+  // write; the warp waits (once) for their signal before copying such a page
+  bool pages_ready = pages_ctr == nullptr;
+  auto issue = [&](int k) -> bool {
+    if (!pages_ready && (it.begin + warp + C::NW * k + 1) * kPage > dr.H_pre) {
+      if (lane == 0) {
+        if (!wait_counter(pages_ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
+        fence_proxy_async_global();
+      }
+      __syncwarp();
+      pages_ready = true;
+    }
+    return int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem);
+  };
   // ok_mask bit st: stage st has a copy in flight; phase_bits (kept across items):
   // bit st = parity of the next completion of stage st.  The caller issued the first
   // stages it could (pre_mask); the rest are issued here.
@@ -294,7 +340,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
       const int head = 4 * j + (gid >> 1), part_lo = gid & 1;
-      const float4 v4 = *reinterpret_cast<const float4*>(qts + head * kHeadDim + 16 * kc + 4 * tig);
+      const float4 v4 = *reinterpret_cast<const float4*>(qts + head * kQRow + 16 * kc + 4 * tig);
       const float v[4] = {v4.x * fs, v4.y * fs, v4.z * fs, v4.w * fs};
       float o4[4];
 #pragma unroll
@@ -312,7 +358,13 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
 #pragma unroll
   for (int j = 0; j < NT; ++j)
 #pragma unroll
-    for (int g = 0; g < NG; ++g) qs_scaled[j][g] = qss[(4 * j + tig) * 4 + g] * scale;
+    for (int g = 0; g < NG; ++g) {  // sum of q~ over group g: warps 8g / NG .. 8(g + 1) / NG - 1
+      constexpr int WPG = C::NW / NG;
+      float sq = 0.f;
+#pragma unroll
+      for (int w = 0; w < WPG; ++w) sq += qss[(WPG * g + w) * G + 4 * j + tig];
+      qs_scaled[j][g] = sq * scale;
+    }
 
   float m_run[NT], l_part[NT], zv[NT][NG];
   float oacc[8][4];
@@ -329,11 +381,12 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     for (int e = 0; e < 4; ++e) oacc[f][e] = 0.f;
 
   const float two24 = 16777216.0f;
+  const float scale24 = scale * two24;  // undoes the 2^-24 of the subnormal key codes
   const int tok_a = tau8(gid);  // rows gid and gid + 8 of the score tile: tokens tok_a, tok_a + 8
   bool broken = false;
   for (int k = 0; k < n_my; ++k) {
     const int st = k % kStages;
-    const int lp = it.begin + warp + kWarps * k;
+    const int lp = it.begin + warp + C::NW * k;
     const bool have = (ok_mask >> st) & 1u;
     if (have) {
       if (!mbar_wait(smem_u32(&bars[st]), (phase_bits >> st) & 1u)) {
@@ -346,6 +399,8 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     } else if (lane == 0) {
       flag(kp, OSCAR_FLAG_BAD_PAGE);
     }
+    // positions [S, H) of the page: tokens t with t - vlo < vn (unsigned); none if no copy
+    const int vlo = max(S - lp * kPage, 0), vn = have ? max(0, min(H - lp * kPage, kPage) - vlo) : 0;
     const uint8_t* stage = pipe + size_t(st) * C::kStageBytes;
     const uint8_t* kcodes = stage;
     const uint8_t* vcodes = stage + kPage * kRowBytes;
@@ -360,9 +415,12 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       const uint2 wa = *reinterpret_cast<const uint2*>(kcodes + t0 * kRowBytes + 8 * tig);
       const uint2 wb = *reinterpret_cast<const uint2*>(kcodes + t1 * kRowBytes + 8 * tig);
       const uint32_t wa0s = wa.x >> 8, wa1s = wa.y >> 8, wb0s = wb.x >> 8, wb1s = wb.y >> 8;
-      float acc[4][NT][4];
+      // accumulators: one per group of 32 channels (fields 2g, 2g+1) at g = 32; two
+      // (even / odd fields) at g = 128
+      constexpr int NA = NG == 1 ? 2 : 4;
+      float acc[NA][NT][4];
 #pragma unroll
-      for (int p = 0; p < 4; ++p)
+      for (int p = 0; p < NA; ++p)
 #pragma unroll
         for (int j = 0; j < NT; ++j)
 #pragma unroll
@@ -372,10 +430,10 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
         const uint32_t a0 = field(wa.x, wa0s, kc), a1 = field(wb.x, wb0s, kc);
         const uint32_t a2 = field(wa.y, wa1s, kc), a3 = field(wb.y, wb1s, kc);
 #pragma unroll
-        for (int j = 0; j < NT; ++j) mma16816(acc[kc >> 1][j], a0, a1, a2, a3, bq[kc][j][0], bq[kc][j][1]);
+        for (int j = 0; j < NT; ++j)
+          mma16816(acc[NG == 1 ? (kc & 1) : (kc >> 1)][j], a0, a1, a2, a3, bq[kc][j][0], bq[kc][j][1]);
       }
-      const int pos0 = lp * kPage + t0, pos1 = lp * kPage + t1;
-      const bool v0 = have && pos0 >= S && pos0 < H, v1 = have && pos1 >= S && pos1 < H;
+      const bool v0 = unsigned(t0 - vlo) < unsigned(vn), v1 = unsigned(t1 - vlo) < unsigned(vn);
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         float s0 = 0.f, s1 = 0.f;
@@ -383,17 +441,15 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
         for (int g = 0; g < NG; ++g) {
           float T0, T1;
           if (NG == 1) {
-            T0 = ((acc[0][j][0] + acc[0][j][1]) + (acc[1][j][0] + acc[1][j][1])) +
-                 ((acc[2][j][0] + acc[2][j][1]) + (acc[3][j][0] + acc[3][j][1]));
-            T1 = ((acc[0][j][2] + acc[0][j][3]) + (acc[1][j][2] + acc[1][j][3])) +
-                 ((acc[2][j][2] + acc[2][j][3]) + (acc[3][j][2] + acc[3][j][3]));
+            T0 = (acc[0][j][0] + acc[0][j][1]) + (acc[1][j][0] + acc[1][j][1]);
+            T1 = (acc[0][j][2] + acc[0][j][3]) + (acc[1][j][2] + acc[1][j][3]);
           } else {
             T0 = acc[g][j][0] + acc[g][j][1];
             T1 = acc[g][j][2] + acc[g][j][3];
           }
           const uint32_t sz0 = ksz[t0 * NG + g], sz1 = ksz[t1 * NG + g];
-          s0 += fmaf(T0 * two24, bf16_lo(sz0) * scale, bf16_hi(sz0) * qs_scaled[j][g]);
-          s1 += fmaf(T1 * two24, bf16_lo(sz1) * scale, bf16_hi(sz1) * qs_scaled[j][g]);
+          s0 += fmaf(T0, bf16_lo(sz0) * scale24, bf16_hi(sz0) * qs_scaled[j][g]);
+          s1 += fmaf(T1, bf16_lo(sz1) * scale24, bf16_hi(sz1) * qs_scaled[j][g]);
         }
         lg[b][j][0] = v0 ? s0 : -INFINITY;
         lg[b][j][1] = v1 ? s1 : -INFINITY;
@@ -446,8 +502,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
         p[j][1] = ex2(lg[b][j][1] - muse[j]);
         l_part[j] += p[j][0] + p[j][1];
       }
-      const int pos0 = lp * kPage + t0, pos1 = lp * kPage + t1;
-      const bool v0 = have && pos0 >= S && pos0 < H, v1 = have && pos1 >= S && pos1 < H;
+      const bool v0 = unsigned(t0 - vlo) < unsigned(vn), v1 = unsigned(t1 - vlo) < unsigned(vn);
       // B fragments of P' = p * s_V per group (movmatrix turns score rows into value k-rows);
       // scale/zero of masked rows may hold anything, so they are selected away, not multiplied
       uint32_t bp[NG][2];
@@ -507,7 +562,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     }
   }
   __syncthreads();  // every warp is done with its stages: reuse the pipeline memory
-  float* wres = reinterpret_cast<float*>(smem);  // [kWarps][G][2 + d]
+  float* wres = reinterpret_cast<float*>(smem);  // [C::NW][G][2 + d]
   float* mine = wres + size_t(warp) * G * (kHeadDim + 2);
   if (gid == 0) {
 #pragma unroll
@@ -534,44 +589,39 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     }
   }
   __syncthreads();
-  for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) {
+  for (int e = threadIdx.x; e < G * kHeadDim; e += C::NTH) {
     const int h = e / kHeadDim, c = e % kHeadDim;
     float ms = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) ms = fmaxf(ms, wres[(w * G + h) * (kHeadDim + 2)]);
+    for (int w = 0; w < C::NW; ++w) ms = fmaxf(ms, wres[(w * G + h) * (kHeadDim + 2)]);
     float l = 0.f, o = 0.f;
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) {
+    for (int w = 0; w < C::NW; ++w) {
       const float mw = wres[(w * G + h) * (kHeadDim + 2)];
       if (mw == -INFINITY) continue;
       const float a = ex2(mw - ms);
       l = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 1], l);
       o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + c], o);
     }
-    float* ph = part + size_t(h) * (kHeadDim + 2);
-    if (c == 0) {
-      ph[0] = ms;
-      ph[1] = l;
-    }
-    ph[2 + c] = o;
+    store_slot<G>(part, h, c, ms, l, o);
   }
 }
 
-// One fused append task: half `half` (8 of the 16 tokens or ring slots) of append item
-// `item` of the pending reservation, for (kv-head kvh, K|V kv), as the append kernel does
+// One fused append task: part `half` (all 16 tokens or ring slots of the item at GQA 4, 8
+// of them at GQA 8) of append item `item` of the pending reservation, for (kv-head kvh,
+// K|V kv), as the append kernel does
 // it, with release-increments of the (layer, request, kv-head) counters app_done[0] once
 // its sink and ring rows are stored and app_done[1] once its INT2 rows are.  Before the
 // wait on the preceding kernel (when this is the CTA's first work): R's bulk copy, the
 // item's positions and evicted ring values, and the eviction into INT2 with its signal
 // (ring items write no other INT2 rows).
-constexpr int kAppendSplit = 2;  // CTAs per append item and kv-head and K|V
 template <int G, int GROUP>
 __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uint8_t* smem, uint32_t bar,
                                   uint32_t& phase, bool& waited, const uint16_t* k_new, const uint16_t* v_new) {
   using C = Cfg<G, GROUP>;
   using namespace append_dev;
-  static_assert(AppendShape<kThreads>::kTokens * kAppendSplit == kTok, "the halves cover an item");
-  const int half = id % kAppendSplit, rest = id / kAppendSplit;
+  constexpr int NTH = Shape<G>::NTH, kSplit = append_task_split(G);
+  const int half = id % kSplit, rest = id / kSplit;
   const int kv = rest & 1, kvh = (rest >> 1) % kp.n_kv_heads, item = (rest >> 1) / kp.n_kv_heads;
   float* Rs = reinterpret_cast<float*>(smem);
   Smem& sm = *reinterpret_cast<Smem*>(smem + C::kAppendR);
@@ -583,11 +633,11 @@ __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uin
     bulk_g2s(smem_u32(Rs), R, C::kAppendR, bar);
   }
   AppendItem ait = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[item];
-  constexpr int kHalf = AppendShape<kThreads>::kTokens;
+  constexpr int kHalf = AppendShape<NTH>::kTokens;
   ait.begin += kHalf * half;
   ait.count = max(0, min(kHalf, ait.count - kHalf * half));
   ItemState st;
-  prepare_item<GROUP, kThreads>(sm, kp, layer, ait, kvh, kv, st);
+  prepare_item<GROUP, NTH>(sm, kp, layer, ait, kvh, kv, st);
   unsigned* done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done) +
                    ((size_t(layer) * kp.max_requests + (st.ok ? st.a.slot : 0)) * kp.n_kv_heads + kvh) * 2;
   auto signal = [&](int which) {
@@ -595,7 +645,7 @@ __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uin
     if (threadIdx.x == 0 && st.ok) atomic_add_acq_rel(done + which, 1u);
   };
   __syncthreads();  // row pointers visible
-  evict_item<GROUP, kThreads>(sm, ait, st);
+  evict_item<GROUP, NTH>(sm, ait, st);
   if (ait.kind == 0) signal(1);
   if (!waited) {
     pdl_wait();
@@ -609,22 +659,24 @@ __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uin
   }
   phase ^= 1u;
   __syncthreads();
-  if (ok) finish_item<GROUP, kThreads>(sm, Rs, kp, layer, ait, kvh, kv, st, k_new, v_new, [&] { signal(0); });
+  if (ok) finish_item<GROUP, NTH>(sm, Rs, kp, layer, ait, kvh, kv, st, k_new, v_new, [&] { signal(0); });
   else signal(0);
   if (ait.kind != 0) signal(1);
 }
 
 template <int G, int GROUP, bool FUSED>
-__global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
-    split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q, float* __restrict__ partials,
+__global__ void __launch_bounds__(Shape<G>::NTH, 1)
+    split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q, uint8_t* __restrict__ partials,
                  uint16_t* __restrict__ out, float* __restrict__ out_f32, const uint16_t* __restrict__ k_new,
                  const uint16_t* __restrict__ v_new) {
   constexpr bool fused = FUSED;
   extern __shared__ __align__(128) uint8_t smem[];
   using C = Cfg<G, GROUP>;
+  constexpr int kWarps = C::NW, kThreads = C::NTH;
   int* s_last = reinterpret_cast<int*>(smem + C::kCtl + kWarps * kStages * 8);
   int* s_next = s_last + 1;
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + C::kCtl + kWarps * kStages * 8 + 8);
+  uint64_t* slab_bar = merge_bar + 1;
   float* qin = reinterpret_cast<float*>(smem + C::kQin);
   float* qts = reinterpret_cast<float*>(smem + C::kQts);
   float* qss = reinterpret_cast<float*>(smem + C::kQss);
@@ -632,6 +684,7 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kCtl);
     for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
     mbar_init(smem_u32(merge_bar), 1);
+    mbar_init(smem_u32(slab_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -641,12 +694,12 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
   // the reservation's append tasks (item x kv-head x K|V) ahead of the decode items.
   const int* counts = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts);
   const int n_items = counts[1];
-  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * kAppendSplit : 0;
+  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * append_task_split(G) : 0;
   const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
                      reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, n_app, counts[3]};
   unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
   bool waited = false;
-  uint32_t phase_bits = 0, merge_phase = 0;
+  uint32_t phase_bits = 0, merge_phase = 0, slab_phase = 0;
   for (int id = wq.first(); id >= 0; id = wq.next(s_next)) {
     if constexpr (FUSED) {
       if (id < n_app) {
@@ -659,15 +712,18 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
-    // rows this launch's append tasks of (request, kv-head) write: wait for them first
-    const bool dep = fused && slot_ok && it.dep != kDepNone && dr.app_expect > 0;
+    // rows this launch's append tasks of (request, kv-head) write: an item marked dependent
+    // waits for them first; INT2 pages at or above H_pre are waited for per warp
+    const bool pending = fused && slot_ok && dr.app_expect > 0;
+    const bool dep = pending && it.dep != kDepNone;
+    const unsigned* ctrs = app_done + ((size_t(layer) * kp.max_requests + (slot_ok ? dr.slot : 0)) * kp.n_kv_heads + it.kvh) * 2;
     uint32_t pre_mask = 0;
     if (it.kind == 0 && slot_ok) {
       const int warp = threadIdx.x >> 5;
       const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
       for (int k = 0; k < min(kStages, n_my); ++k) {
         const int lp = it.begin + warp + kWarps * k;
-        if (((waited && !dep) || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem))
+        if (((waited && !pending) || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem))
           pre_mask |= 1u << k;
       }
     }
@@ -675,38 +731,37 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
       bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                            (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim,
                        kHeadDim * kHeadDim * 4);
-    float rk[64];
-    load_rk_cols(kp, layer, it.kvh, rk);
+    float rk[Shape<G>::kRows];
+    load_rk_cols<G>(kp, layer, it.kvh, rk);
     if (!waited) {
       pdl_wait();
       pdl_trigger();
       waited = true;
     }
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-    rotate_q<G, GROUP>(q + head0 * kHeadDim, rk, qin, qts, qss);
+    rotate_q<G>(q + head0 * kHeadDim, rk, qin, qts, qss);
     if (dep) {
-      const unsigned* ctr = app_done + ((size_t(layer) * kp.max_requests + dr.slot) * kp.n_kv_heads + it.kvh) * 2 +
-                            (it.dep == kDepPages ? 1 : 0);
+      const unsigned* ctr = ctrs + (it.dep == kDepPages ? 1 : 0);
       if (threadIdx.x == 0 && !wait_counter(ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
       __syncthreads();
       fence_proxy_async_global();  // the append's rows, seen through the acquire, before bulk copies
     }
-    float* part = partials + size_t(ix) * G * (kHeadDim + 2);
+    uint8_t* part = partials + size_t(ix) * PartialSlot<G>::kBytes;
     if (!slot_ok) {
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
-      for (int e = threadIdx.x; e < G * (kHeadDim + 2); e += kThreads)
-        part[e] = (e % (kHeadDim + 2)) == 0 ? -INFINITY : 0.f;
+      for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) store_slot<G>(part, e / kHeadDim, e % kHeadDim, -INFINITY, 0.f, 0.f);
     } else if (it.kind == 0) {
-      int2_pages_item<G, GROUP>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask);
+      int2_pages_item<G, GROUP>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask,
+                                pending && it.dep == kDepNone ? ctrs + 1 : nullptr);
     } else {
       bf16_tokens_item<G>(kp, layer, it, dr, qts, part, smem);
     }
-    // ---- two-level merge of the partials; R_V^T is fetched as soon as this CTA knows it
-    // merges a group (it may then finish the head)
+    // ---- merge by the last CTA of (request, kv-head): R_V^T is fetched as soon as this CTA
+    // knows it merges, the partial slots are bulk-copied after it
     MergeAcc<G, kThreads> acc;
-    const int role = merge_partial<G, kThreads>(kp, it, ix, partials, acc, s_last,
-                                                [&] { fetch_rvt(kp, layer, it.kvh, smem, smem_u32(merge_bar)); });
-    if (role == kMergeFinal) {
+    if (merge_partial<G, kThreads>(kp, it, partials, acc, s_last, smem + C::kSlabOff, C::kSlabSlots,
+                                   smem_u32(slab_bar), slab_phase,
+                                   [&] { fetch_rvt(kp, layer, it.kvh, smem, smem_u32(merge_bar)); })) {
       // every item of (request, kv-head) is done, so are its waits: ready for the next launch
       // (subtracting the launch's count: a task's last increment may still be on its way)
       if (fused && slot_ok && dr.app_expect > 0 && threadIdx.x == 0) {
@@ -715,10 +770,6 @@ __global__ void __launch_bounds__(kThreads, G == 4 ? 2 : 1)
         atomicSub(ctr + 1, unsigned(dr.app_expect));
       }
       finish_output<G>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
-    } else if (role == kMergeGroupOnly) {
-      // drain the speculative R_V^T copy before the memory is reused (bounded)
-      if (!mbar_wait(smem_u32(merge_bar), merge_phase)) mbar_wait(smem_u32(merge_bar), merge_phase);
-      merge_phase ^= 1u;
     }
     // generic-proxy use of the stage memory is over before the next item's bulk copies
     fence_proxy_async();
@@ -735,7 +786,7 @@ int resident_ctas_t(int n_sm) {
                                      C::kSmemBytes));
     int per_sm = 0;
     if (!e)
-      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED>, kThreads,
+      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED>, C::NTH,
                                                             C::kSmemBytes));
     if (e) return -e;
     resident = (per_sm > 0 ? per_sm : 1) * n_sm;
@@ -758,7 +809,7 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
                     const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches,
                     const void* k_new, const void* v_new, bool fused) {
   using C = Cfg<G, GROUP>;
-  float* partials = reinterpret_cast<float*>(ws + wl.partials);
+  uint8_t* partials = ws + wl.partials;
   const int resident = resident_ctas<G, GROUP>(n_sm);
   if (resident < 0) return -resident;
   // persistent-style grid: every resident CTA slot, each looping over work items, so a
@@ -769,9 +820,9 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
   uint16_t* ob = static_cast<uint16_t*>(out);
   const uint16_t* kb = static_cast<const uint16_t*>(k_new);
   const uint16_t* vb = static_cast<const uint16_t*>(v_new);
-  int e = fused ? launch_ex(split_kernel<G, GROUP, true>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes), stream,
+  int e = fused ? launch_ex(split_kernel<G, GROUP, true>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes), stream,
                             kp, layer, qb, partials, ob, out_f32, kb, vb)
-                : launch_ex(split_kernel<G, GROUP, false>, dim3(resident), dim3(kThreads), size_t(C::kSmemBytes),
+                : launch_ex(split_kernel<G, GROUP, false>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
                             stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
   if (!e) *launches += 1;
   return e;

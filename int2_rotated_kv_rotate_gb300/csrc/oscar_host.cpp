@@ -46,7 +46,7 @@ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 constexpr int kAppendChunk = 16;     // tokens (or ring slots) per append work item
 constexpr int kMaxAppendTokenItems = 65536;
-constexpr int kBf16ItemTokens = 128;  // sink+ring tokens per decode work item
+constexpr int kBf16ItemTokens = 128;  // sink+ring tokens per decode work item (at least; one chunk of the CTA)
 
 bool config_ok(const oscar_config* c, std::string* why) {
   auto bad = [&](const char* m) {
@@ -122,7 +122,6 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.decode_reqs = take(reqs * sizeof(DecodeReq));
   L.decode_items = take(L.max_decode_items * sizeof(DecodeItem));
   L.decode_order = take(L.max_decode_items * 4);
-  L.group_counters = take(L.max_decode_items * 4);
   L.sched = take(16);
   L.app_done = take(layers * reqs * Hkv * 8);
   L.total = off;
@@ -273,7 +272,6 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   }
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.status, 0, 256);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.counters, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 4);
-  if (e == cudaSuccess) e = cudaMemset(c->base + lay.group_counters, 0, lay.max_decode_items * 4);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.sched, 0, 16);
   if (e == cudaSuccess)
     e = cudaMemset(c->base + lay.app_done, 0, size_t(cfg->n_layers) * cfg->max_requests * cfg->n_kv_heads * 8);
@@ -601,7 +599,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
           Ls[i] = a.L1;
           Hs[i] = a.H1;
           Hpre[i] = std::min(r.H, a.H0);
-          app_expect[i] = 4 * c->app_req_items[k];  // K and V halves of each item, per kv-head
+          app_expect[i] = 2 * append_task_split(c->cfg.n_q_heads / Hkv) * c->app_req_items[k];  // per kv-head
           ++n_reserved_planned;
         }
       }
@@ -614,11 +612,9 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   //  - large steps: about kWaves items per resident CTA (at least kItemBytes each), taken
   //    dynamically by the CTAs, largest first, so the ragged tail stays short while the
   //    per-item costs (pipeline fill, partial store and merge) stay small.
-  // Per request: INT2 pages np, BF16 sink+ring tokens n_bf, and where this step's new
-  // tokens start in each (bf_new: BF16 list index; index < min(L, S) is a sink, else ring
-  // position H + index - min(L, S); pg_new: first INT2 page the append writes).  Items are
-  // split there, so that in a fused append + decode launch only the items after the split
-  // wait for the append tasks.
+  // Per request: INT2 pages np, BF16 sink+ring tokens n_bf, and the split points of the
+  // items that do not (before) and may (after) read rows of this step's append: bf_new in
+  // the BF16 list, pg_new in the pages.
   std::vector<int> np_of(n_req), nbf_of(n_req), bfnew_of(n_req), pgnew_of(n_req);
   int max_np = 1;
   const int ng = kHeadDim / (is_int2(c) ? c->cfg.group : kHeadDim);
@@ -629,22 +625,25 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     nbf_of[i] = is_int2(c) ? std::min(Ls[i], S) + std::max(0, Ls[i] - Hs[i]) : 0;
     bfnew_of[i] = nbf_of[i];
     pgnew_of[i] = np_of[i];
-    if (app_expect[i] > 0) {
-      const int n_s = std::min(Ls[i], S);
-      bfnew_of[i] = std::min(nbf_of[i], Lpre[i] < n_s ? Lpre[i] : n_s + std::max(0, Lpre[i] - Hs[i]));
-      if (Hs[i] > Hpre[i]) pgnew_of[i] = std::min(np_of[i], Hpre[i] / kPage);  // INT2 rows written
-    }
+    // A fused launch's BF16 items of an appending request wait for its rows as a whole (the
+    // new rows are a small part of the list); its INT2 items are not split: the append's
+    // eviction rows are signalled before the launch's wait, and the one warp whose page
+    // holds them waits for that signal before copying it.
+    if (app_expect[i] > 0) bfnew_of[i] = 0;
+    (void)Lpre;
     max_np = std::max(max_np, np_of[i]);
     total_bytes += (long long)Hkv * (np_of[i] * page_bytes + nbf_of[i] * 2LL * kHeadDim * 2);
   }
   auto split_count = [](int a, int b, int step) { return (a > 0 ? ceil_div(a, step) : 0) + (b > a ? ceil_div(b - a, step) : 0); };
   long long n_bf_items = 0;
-  for (int i = 0; i < n_req; ++i) n_bf_items += (long long)Hkv * split_count(bfnew_of[i], nbf_of[i], kBf16ItemTokens);
+  // BF16 items of one CTA chunk: 16 tokens per warp
+  const int bf_item = is_int2(c) ? 16 * decode_warps(c->cfg.n_q_heads / Hkv) : kBf16ItemTokens;
+  for (int i = 0; i < n_req; ++i) n_bf_items += (long long)Hkv * split_count(bfnew_of[i], nbf_of[i], bf_item);
   auto count_items = [&](int ch) {
     long long n = n_bf_items;
     for (int i = 0; i < n_req; ++i) {
       const int pg = split_count(pgnew_of[i], np_of[i], ch);
-      const int bf = split_count(bfnew_of[i], nbf_of[i], kBf16ItemTokens);
+      const int bf = split_count(bfnew_of[i], nbf_of[i], bf_item);
       n += (long long)Hkv * (pg + bf > 0 ? pg : 1);
     }
     return n;
@@ -658,7 +657,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     if (resident <= 0) resident = 2 * c->n_sm;
     if (total_bytes <= kItemBytes * resident) {
       // a fused append + decode launch runs the reservation's append tasks in the same wave
-      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 4 : 0;
+      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 2 * append_task_split(G) : 0;
       const long long slots = std::max<long long>(1, resident - n_bf_items - n_app_tasks);
       chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
       while (chunk < max_np && count_items(chunk) + n_app_tasks > resident) ++chunk;
@@ -685,16 +684,15 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     for (int h = 0; h < Hkv; ++h) {
       const int first = int(items.size());
       auto add = [&](int kind, int b, int e, int dep) {
-        // group g of this (req, kv-head) counts on group_counters[first + g]
-        items.push_back({i, h, kind, b, e, first, 0, first + (int(items.size()) - first) / kMergeGroup, dep});
+        items.push_back({i, h, kind, b, e, first, 0, dep});
       };
       if (n_bf == 0 && np == 0) add(1, 0, 0, kDepNone);  // empty request: one empty item writes zeros
       // BF16 sink+ring list, split where this step's new tokens start (those items wait for
       // a fused launch's append tasks; the others do not)
       for (int part = 0; part < 2; ++part) {
         const int b0 = part == 0 ? 0 : bf_new, b1 = part == 0 ? bf_new : n_bf;
-        for (int t = b0; t < b1; t += kBf16ItemTokens) {
-          add(1, t, std::min(b1, t + kBf16ItemTokens), part == 0 ? kDepNone : kDepRing);
+        for (int t = b0; t < b1; t += bf_item) {
+          add(1, t, std::min(b1, t + bf_item), part == 0 ? kDepNone : kDepRing);
           ++n_bf16;
         }
       }
@@ -749,7 +747,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   DecodeWorkspace w;
   size_t off = 0;
   w.partials = off;
-  off = align256(off + items.size() * size_t(G) * (kHeadDim + 2) * 4);
+  off = align256(off + items.size() * size_t(G) * (8 + 4 * kHeadDim));  // partial slots
   w.total = off;
   c->ws = w;
   c->dec_n_req = n_req;
@@ -806,12 +804,12 @@ oscar_status oscar_append_decode_attention(oscar_cache* c, int layer, const void
   if (!c->plan_covers_reservation)
     return fail(OSCAR_ERR_STATE, "plan the decode after the reservation, over every reserved slot");
   if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
-  // The append tasks run in the same wave as the decode when they fit in it (4 per append
-  // item and kv-head: K and V halves); more of them (long chunks, many requests) would hold
-  // back the decode, so those go to the append kernel, which is launched first.
+  // The append tasks run in the same wave as the decode when they fit in it; more of them
+  // (long chunks, many requests) would hold back the decode, so those go to the append
+  // kernel, which is launched first.
   const int G = c->cfg.n_q_heads / c->cfg.n_kv_heads;
   const int resident = decode_resident_ctas(G, c->cfg.group, c->n_sm);
-  const long long n_tasks = (long long)c->app_items * c->cfg.n_kv_heads * 4;
+  const long long n_tasks = (long long)c->app_items * c->cfg.n_kv_heads * 2 * append_task_split(G);
   const bool fused = n_tasks <= (long long)resident;
   if (!fused && c->app_items > 0) {
     int e = launch_append(kernel_params(c), layer, k_new, v_new, std::min(c->app_items, 4 * c->n_sm), stream,

@@ -39,19 +39,16 @@ struct DecodeReq {
   int H_pre;         // history end before this step's append: no kernel of the step writes
                      // the INT2 pages wholly below it, so they may be copied before the wait
                      // on the preceding kernel
-  int app_expect;    // fused append + decode: append tasks of this request per kv-head (the
-                     // K and V halves of each of its append items); 0 = nothing to wait for
+  int app_expect;    // fused append + decode: append tasks of this request per kv-head (K and
+                     // V, times append_task_split, per append item); 0 = nothing to wait for
   int first_item;    // items of this request, kv-head-major: first_item + kvh*items_per_head ..
   int items_per_head;
 };
 
 // One split-K work item: pages [p0, p1) of the INT2 history (kind 0) or BF16 tokens
 // [t0, t1) of the sink+ring list (kind 1; index < S is sink j, else ring position H + j - S)
-// of request `req` (plan index), kv-head `kvh`.  Partial results go to slot `item`.
-// Partials of one (request, kv-head) merge in two levels: each group of kMergeGroup
-// consecutive items is merged by its last finisher into the group's first slot, then the
-// last group merger merges the groups.
-constexpr int kMergeGroup = 8;
+// of request `req` (plan index), kv-head `kvh`.  Partial results go to slot `item`; the
+// last CTA to finish an item of (req, kvh) merges the head_count slots from head_first.
 struct DecodeItem {
   int req;
   int kvh;
@@ -60,12 +57,22 @@ struct DecodeItem {
   int end;
   int head_first;  // first partial slot of this (req, kvh)
   int head_count;  // number of partial slots of this (req, kvh)
-  int gcounter;    // merge-group counter of this item (groups of kMergeGroup consecutive items)
   int dep;         // fused append + decode: what the item reads that this launch's append tasks
                    // write (kDepNone, kDepRing: BF16 rows of new tokens, kDepPages: INT2 pages
                    // that receive evicted or new tokens)
 };
 constexpr int kDepNone = 0, kDepRing = 1, kDepPages = 2;
+
+// Fused append + decode: CTAs per append item and kv-head and K|V (a split-kernel CTA
+// covers 16 tokens at GQA 4, 8 at GQA 8).
+#ifdef __CUDACC__
+#define OSCAR_HOST_DEVICE __host__ __device__
+#else
+#define OSCAR_HOST_DEVICE
+#endif
+OSCAR_HOST_DEVICE constexpr int append_task_split(int gqa) { return gqa == 4 ? 1 : 2; }
+// Warps of a split-kernel CTA (one CTA per SM): 16 at GQA 4, 8 at GQA 8.
+OSCAR_HOST_DEVICE constexpr int decode_warps(int gqa) { return gqa == 4 ? 16 : 8; }
 
 struct DeviceLayout {
   // pools (byte offsets in the device block)
@@ -86,7 +93,6 @@ struct DeviceLayout {
   size_t append_reqs, append_items, decode_reqs, decode_items;
   size_t decode_order;  // int32 [max_decode_items]: items in the order CTAs take them (largest first)
   size_t sched;         // uint32 [4]: dynamic work counter, CTA exit counter (self-resetting)
-  size_t group_counters;  // uint32 [max_decode_items] first-level merge counters
   size_t app_done;      // uint32 [layer][max_requests][H_kv][2]: append tasks of the running fused
                         // launch that have stored their sink and ring rows ([0]) and their INT2
                         // rows ([1]); the request's final merge takes the launch's count off again
@@ -104,7 +110,7 @@ struct KernelParams {
 
 // Decode workspace layout (per plan).
 struct DecodeWorkspace {
-  size_t partials;  // fp32 [n_items][G][d + 2] (m, l, o~)
+  size_t partials;  // [n_items] slots of G x (fp32 m, l) then G x d fp32 o~ / l
   size_t total;
 };
 
