@@ -161,6 +161,13 @@ oscar_status oscar_commit_append(oscar_cache* cache);
  * (0 = automatic, balanced over the SMs). */
 oscar_status oscar_plan_decode(oscar_cache* cache, const int* slots, int n_req, int max_split_pages, void* stream);
 
+/* oscar_plan_decode with plan flags (OSCAR_PLAN_*, or-ed).  OSCAR_PLAN_NARROW plans for
+ * the 8-warp CTA shape (two CTAs per SM at GQA 4), which the automatic choice takes only
+ * for steps larger than one wave of 16-warp CTAs; results are the same either way. */
+#define OSCAR_PLAN_NARROW 0x1u
+oscar_status oscar_plan_decode_ex(oscar_cache* cache, const int* slots, int n_req, int max_split_pages, uint32_t flags,
+                                  void* stream);
+
 /* Decode workspace bytes for the current plan (0 without a plan). */
 size_t oscar_decode_workspace_bytes(const oscar_cache* cache);
 

@@ -92,8 +92,8 @@ class KVCache:
         self._n_plan = None
 
     # ------------------------------------------------------------------ decode
-    def plan(self, slots, max_split_pages: int = 0, stream=None) -> int:
-        N.oscar_plan_decode(self.handle, slots, max_split_pages, stream)
+    def plan(self, slots, max_split_pages: int = 0, stream=None, flags: int = 0) -> int:
+        N.oscar_plan_decode_ex(self.handle, slots, max_split_pages, flags, stream)
         self._n_plan = len(list(slots))
         need = N.oscar_decode_workspace_bytes(self.handle)
         if self.workspace is None or self.workspace.numel() < need:

@@ -39,17 +39,19 @@ namespace {
 
 constexpr int kStages = 2;  // page stages per warp
 
-// CTA shape of the split kernel: one CTA per SM, 16 warps at GQA 4 (128 registers a
-// thread fill the register file), 8 warps at GQA 8 (more registers a thread).  Each
-// channel of the q rotation has kParts threads, each summing 128 / kParts rows of R_K.
-template <int G>
+// CTA shape of the split kernel.  NW = 16 (GQA 4, plans of one wave): one CTA per SM, 128
+// registers a thread fill the register file.  NW = 8: two CTAs per SM at GQA 4 (plans of
+// several waves: one CTA streams while the other is between items), one at GQA 8 (more
+// registers a thread).  Each channel of the q rotation has kParts threads, each summing
+// 128 / kParts rows of R_K.
+template <int NW_>
 struct Shape {
-  static constexpr int NW = decode_warps(G);
+  static constexpr int NW = NW_;
   static constexpr int NTH = 32 * NW;
   static constexpr int kParts = NTH / kHeadDim;
-  static constexpr int kRows = kHeadDim / kParts;     // rows of R_K per thread
+  static constexpr int kRows = kHeadDim / kParts;        // rows of R_K per thread
   static constexpr int kQinRow = kHeadDim + 4 * kParts;  // padded staging row of q
-  static_assert(append_task_split(G) * append_dev::AppendShape<NTH>::kTokens == append_dev::kTok,
+  static_assert(append_task_split(NW) * append_dev::AppendShape<NTH>::kTokens == append_dev::kTok,
                 "append tasks cover an item");
 };
 
@@ -90,10 +92,10 @@ __device__ __forceinline__ int tau8(int m) { return (m >> 1) + 4 * (m & 1); }
 // Thread t of a split CTA holds column c = t / kParts of R_K, rows kRows (t % kParts) ..
 // + kRows - 1, so the parts of a column sit in neighbouring lanes (R_K is written long
 // before by oscar_set_layer_params, so this runs before the wait on the preceding kernel).
-template <int G>
+template <int NW>
 __device__ __forceinline__ void load_rk_cols(const KernelParams& kp, int layer, int kvh,
-                                             float (&rk)[Shape<G>::kRows]) {
-  using Sh = Shape<G>;
+                                             float (&rk)[Shape<NW>::kRows]) {
+  using Sh = Shape<NW>;
   const int c = threadIdx.x / Sh::kParts, i0 = (threadIdx.x % Sh::kParts) * Sh::kRows;
   const float* R = reinterpret_cast<const float*>(kp.base + kp.lay.R_K) +
                    (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim + size_t(i0) * kHeadDim + c;
@@ -105,10 +107,10 @@ __device__ __forceinline__ void load_rk_cols(const KernelParams& kp, int layer, 
 // warp w the sum of q~ over its kHeadDim / NW channels into qpart[w][G] (shared).  qin:
 // G * kQinRow floats of shared staging (channel i of a head at i + 4 (i / kRows), so that
 // the parts a warp reads together fall in different banks).  All threads; two barriers.
-template <int G>
-__device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)[Shape<G>::kRows], float* qin,
+template <int G, int NW>
+__device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)[Shape<NW>::kRows], float* qin,
                          float* qts, float* qpart) {
-  using Sh = Shape<G>;
+  using Sh = Shape<NW>;
   constexpr int KP = Sh::kParts, KR = Sh::kRows;
   const int tid = threadIdx.x, c = tid / KP, part = tid % KP, warp = tid >> 5, lane = tid & 31;
   for (int e = tid; e < G * kHeadDim; e += Sh::NTH) {
@@ -148,9 +150,10 @@ __device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)
 }
 
 // ---------------------------------------------------------------- split kernel
-template <int G, int GROUP>
+template <int G, int GROUP, int NW_>
 struct Cfg {
-  static constexpr int NW = Shape<G>::NW, NTH = Shape<G>::NTH;
+  static constexpr int NW = NW_, NTH = Shape<NW>::NTH;
+  static constexpr int kPerSM = G == 4 && NW == 8 ? 2 : 1;  // resident CTAs per SM
   static constexpr int NG = kHeadDim / GROUP;           // groups per token
   static constexpr int NT = G / 4;                      // score n-tiles (4 heads x hi/lo each)
   static constexpr int kCodeBytes = 2 * kPage * kRowBytes;  // K then V codes
@@ -160,9 +163,9 @@ struct Cfg {
   // fused append tasks: R (fp32 [d][d]) then the append scratch, in the same memory
   static constexpr int kAppendR = kHeadDim * kHeadDim * 4;
   static constexpr int kAppendBytes = kAppendR + int(sizeof(append_dev::Smem));
-  // the merge: R_V^T (64 KB) then a slab of at least 32 partial slots
+  // the merge: R_V^T (64 KB) then a slab of at least 32 partial slots (16 at two CTAs per SM)
   static constexpr int kSlabOff = kHeadDim * kHeadDim * 4;
-  static constexpr int kMergeBytes = kSlabOff + 32 * PartialSlot<G>::kBytes;
+  static constexpr int kMergeBytes = kSlabOff + (kPerSM == 2 ? 16 : 32) * PartialSlot<G>::kBytes;
   static constexpr int kWorkBytes0 = kPipeBytes > kAppendBytes ? kPipeBytes : kAppendBytes;
   static constexpr int kWorkBytes = (((kWorkBytes0 > kMergeBytes ? kWorkBytes0 : kMergeBytes) + 127) / 128) * 128;
   static constexpr int kSlabSlots = (kWorkBytes - kSlabOff) / PartialSlot<G>::kBytes;
@@ -170,13 +173,13 @@ struct Cfg {
   // control: page barriers (NW x kStages), merge flag, next item, R_V^T and slab barriers
   static constexpr int kCtlBytes = ((NW * kStages * 8 + 24 + 127) / 128) * 128;
   static constexpr int kQin = kCtl + kCtlBytes;     // fp32 [G][kQinRow] query staging
-  static constexpr int kQts = kQin + G * Shape<G>::kQinRow * 4;  // fp32 [G][kQRow] q~
+  static constexpr int kQts = kQin + G * Shape<NW>::kQinRow * 4;  // fp32 [G][kQRow] q~
   static constexpr int kQss = kQts + G * kQRow * 4;  // fp32 [NW][G] sums of q~ per warp's channels
   static constexpr int kSmemBytes = kQss + NW * G * 4;
-  static_assert(kSmemBytes <= 227 * 1024, "one CTA per SM");
+  static_assert(kSmemBytes + 1024 <= 228 * 1024 / kPerSM, "resident CTAs per SM");
   static_assert(kWorkBytes >= Bf16Rows<NW, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
   static_assert(kWorkBytes >= NW * G * (kHeadDim + 2) * 4, "per-warp results reuse the page pipeline memory");
-  static_assert(kSlabOff + (1 + Shape<G>::NTH / kHeadDim) * G * kHeadDim * 4 <= kMergeBytes,
+  static_assert(kSlabOff + (1 + NTH / kHeadDim) * G * kHeadDim * 4 <= kMergeBytes,
                 "o~ and the partial sums of the output rotation are staged over the slab");
 };
 
@@ -193,10 +196,10 @@ __device__ void fetch_rvt(const KernelParams& kp, int layer, int kvh, uint8_t* s
 
 // Final merge: o~ = O / L, then o = R_V o~ with R_V^T in smem (fetched by fetch_rvt; this
 // waits for it), bf16 and optional fp32 store.
-template <int G>
-__device__ void finish_output(const KernelParams& kp, const DecodeItem& it, const MergeAcc<G, Shape<G>::NTH>& acc, uint16_t* out,
-                              float* out_f32, uint8_t* smem, uint32_t mbar, uint32_t& mphase) {
-  using A = MergeAcc<G, Shape<G>::NTH>;
+template <int G, int NW>
+__device__ void finish_output(const KernelParams& kp, const DecodeItem& it, const MergeAcc<G, Shape<NW>::NTH>& acc,
+                              uint16_t* out, float* out_f32, uint8_t* smem, uint32_t mbar, uint32_t& mphase) {
+  using A = MergeAcc<G, Shape<NW>::NTH>;
   constexpr int HPT = A::HPT, KS = A::kStride, JR = kHeadDim / KS;
   const int t = threadIdx.x, c = t & (kHeadDim - 1), hb = t >> 7;
   const float* Rs = reinterpret_cast<const float*>(smem);   // R_V^T [128][128]
@@ -243,7 +246,7 @@ __device__ void finish_output(const KernelParams& kp, const DecodeItem& it, cons
 
 // BF16 tokens of the sink + ring list: list index u < min(L, S) is sink u, otherwise
 // position H + u - min(L, S) in ring slot p % W.
-template <int G>
+template <int G, int NW>
 __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
                                  const float* qts, uint8_t* part, uint8_t* smem) {
   const int S = kp.n_sink;
@@ -263,15 +266,15 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
   auto rowV = [=](int u) {
     return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t((H + u - n_s) % W) * kHeadDim;
   };
-  bf16_rows_mma<G, Shape<G>::NW, 1>(rowK, rowV, it.begin, it.end, qts, part, smem);
+  bf16_rows_mma<G, NW, 1>(rowK, rowV, it.begin, it.end, qts, part, smem);
 }
 
 // Issue (lane 0 of the calling warp) the bulk copies of the warp's k-th page of an INT2
 // item into stage k % kStages; false (no copy) if the page id is out of range.
-template <int G, int GROUP>
+template <int G, int GROUP, int NW>
 __device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr, int k,
                                 uint8_t* smem) {
-  using C = Cfg<G, GROUP>;
+  using C = Cfg<G, GROUP, NW>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int lp = it.begin + warp + C::NW * k;
   const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
@@ -297,11 +300,11 @@ __device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeI
 
 // INT2 history pages [it.begin, it.end) of one (request, kv-head).  Positions outside
 // [S, H) inside those pages are masked.  Warp w takes pages begin + w, + NW, ...
-template <int G, int GROUP>
+template <int G, int GROUP, int NW>
 __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
                                 const float* qts, const float* qss, uint8_t* part, uint8_t* smem,
                                 uint32_t& phase_bits, uint32_t pre_mask, const unsigned* pages_ctr) {
-  using C = Cfg<G, GROUP>;
+  using C = Cfg<G, GROUP, NW>;
   constexpr int NG = C::NG, NT = C::NT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int gid = lane >> 2, tig = lane & 3;
@@ -323,7 +326,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       __syncwarp();
       pages_ready = true;
     }
-    return int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem);
+    return int2_issue_page<G, GROUP, NW>(kp, layer, it, dr, k, smem);
   };
   // ok_mask bit st: stage st has a copy in flight; phase_bits (kept across items):
   // bit st = parity of the next completion of stage st.  The caller issued the first
@@ -615,12 +618,12 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
 // wait on the preceding kernel (when this is the CTA's first work): R's bulk copy, the
 // item's positions and evicted ring values, and the eviction into INT2 with its signal
 // (ring items write no other INT2 rows).
-template <int G, int GROUP>
+template <int G, int GROUP, int NW>
 __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uint8_t* smem, uint32_t bar,
                                   uint32_t& phase, bool& waited, const uint16_t* k_new, const uint16_t* v_new) {
-  using C = Cfg<G, GROUP>;
+  using C = Cfg<G, GROUP, NW>;
   using namespace append_dev;
-  constexpr int NTH = Shape<G>::NTH, kSplit = append_task_split(G);
+  constexpr int NTH = Shape<NW>::NTH, kSplit = append_task_split(NW);
   const int half = id % kSplit, rest = id / kSplit;
   const int kv = rest & 1, kvh = (rest >> 1) % kp.n_kv_heads, item = (rest >> 1) / kp.n_kv_heads;
   float* Rs = reinterpret_cast<float*>(smem);
@@ -664,14 +667,14 @@ __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uin
   if (ait.kind != 0) signal(1);
 }
 
-template <int G, int GROUP, bool FUSED>
-__global__ void __launch_bounds__(Shape<G>::NTH, 1)
+template <int G, int GROUP, bool FUSED, int NW>
+__global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
     split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q, uint8_t* __restrict__ partials,
                  uint16_t* __restrict__ out, float* __restrict__ out_f32, const uint16_t* __restrict__ k_new,
                  const uint16_t* __restrict__ v_new) {
   constexpr bool fused = FUSED;
   extern __shared__ __align__(128) uint8_t smem[];
-  using C = Cfg<G, GROUP>;
+  using C = Cfg<G, GROUP, NW>;
   constexpr int kWarps = C::NW, kThreads = C::NTH;
   int* s_last = reinterpret_cast<int*>(smem + C::kCtl + kWarps * kStages * 8);
   int* s_next = s_last + 1;
@@ -694,7 +697,7 @@ __global__ void __launch_bounds__(Shape<G>::NTH, 1)
   // the reservation's append tasks (item x kv-head x K|V) ahead of the decode items.
   const int* counts = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts);
   const int n_items = counts[1];
-  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * append_task_split(G) : 0;
+  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * append_task_split(NW) : 0;
   const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
                      reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, n_app, counts[3]};
   unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
@@ -703,7 +706,7 @@ __global__ void __launch_bounds__(Shape<G>::NTH, 1)
   for (int id = wq.first(); id >= 0; id = wq.next(s_next)) {
     if constexpr (FUSED) {
       if (id < n_app) {
-        fused_append_task<G, GROUP>(kp, layer, id, smem, smem_u32(merge_bar), merge_phase, waited, k_new, v_new);
+        fused_append_task<G, GROUP, NW>(kp, layer, id, smem, smem_u32(merge_bar), merge_phase, waited, k_new, v_new);
         fence_proxy_async();  // generic use of the memory is over before later bulk copies
         continue;
       }
@@ -723,7 +726,7 @@ __global__ void __launch_bounds__(Shape<G>::NTH, 1)
       const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
       for (int k = 0; k < min(kStages, n_my); ++k) {
         const int lp = it.begin + warp + kWarps * k;
-        if (((waited && !pending) || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP>(kp, layer, it, dr, k, smem))
+        if (((waited && !pending) || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP, NW>(kp, layer, it, dr, k, smem))
           pre_mask |= 1u << k;
       }
     }
@@ -731,15 +734,15 @@ __global__ void __launch_bounds__(Shape<G>::NTH, 1)
       bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                            (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim,
                        kHeadDim * kHeadDim * 4);
-    float rk[Shape<G>::kRows];
-    load_rk_cols<G>(kp, layer, it.kvh, rk);
+    float rk[Shape<NW>::kRows];
+    load_rk_cols<NW>(kp, layer, it.kvh, rk);
     if (!waited) {
       pdl_wait();
       pdl_trigger();
       waited = true;
     }
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-    rotate_q<G>(q + head0 * kHeadDim, rk, qin, qts, qss);
+    rotate_q<G, NW>(q + head0 * kHeadDim, rk, qin, qts, qss);
     if (dep) {
       const unsigned* ctr = ctrs + (it.dep == kDepPages ? 1 : 0);
       if (threadIdx.x == 0 && !wait_counter(ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
@@ -751,10 +754,10 @@ __global__ void __launch_bounds__(Shape<G>::NTH, 1)
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
       for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) store_slot<G>(part, e / kHeadDim, e % kHeadDim, -INFINITY, 0.f, 0.f);
     } else if (it.kind == 0) {
-      int2_pages_item<G, GROUP>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask,
+      int2_pages_item<G, GROUP, NW>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask,
                                 pending && it.dep == kDepNone ? ctrs + 1 : nullptr);
     } else {
-      bf16_tokens_item<G>(kp, layer, it, dr, qts, part, smem);
+      bf16_tokens_item<G, NW>(kp, layer, it, dr, qts, part, smem);
     }
     // ---- merge by the last CTA of (request, kv-head): R_V^T is fetched as soon as this CTA
     // knows it merges, the partial slots are bulk-copied after it
@@ -769,7 +772,7 @@ __global__ void __launch_bounds__(Shape<G>::NTH, 1)
         atomicSub(ctr, unsigned(dr.app_expect));
         atomicSub(ctr + 1, unsigned(dr.app_expect));
       }
-      finish_output<G>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
+      finish_output<G, NW>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
     }
     // generic-proxy use of the stage memory is over before the next item's bulk copies
     fence_proxy_async();
@@ -777,16 +780,16 @@ __global__ void __launch_bounds__(Shape<G>::NTH, 1)
   wq.leave();
 }
 
-template <int G, int GROUP, bool FUSED>
+template <int G, int GROUP, bool FUSED, int NW>
 int resident_ctas_t(int n_sm) {
-  using C = Cfg<G, GROUP>;
+  using C = Cfg<G, GROUP, NW>;
   static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
   if (resident == 0) {
-    int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP, FUSED>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP, FUSED, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      C::kSmemBytes));
     int per_sm = 0;
     if (!e)
-      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED>, C::NTH,
+      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED, NW>, C::NTH,
                                                             C::kSmemBytes));
     if (e) return -e;
     resident = (per_sm > 0 ? per_sm : 1) * n_sm;
@@ -796,33 +799,31 @@ int resident_ctas_t(int n_sm) {
 
 // The decode and the fused append + decode kernels of a shape get one plan: the smaller
 // resident count of the two.
-template <int G, int GROUP>
+template <int G, int GROUP, int NW>
 int resident_ctas(int n_sm) {
-  const int a = resident_ctas_t<G, GROUP, false>(n_sm), b = resident_ctas_t<G, GROUP, true>(n_sm);
+  const int a = resident_ctas_t<G, GROUP, false, NW>(n_sm), b = resident_ctas_t<G, GROUP, true, NW>(n_sm);
   if (a < 0) return a;
   if (b < 0) return b;
   return a < b ? a : b;
 }
 
-template <int G, int GROUP>
+template <int G, int GROUP, int NW>
 int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                    const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches,
-                    const void* k_new, const void* v_new, bool fused) {
-  using C = Cfg<G, GROUP>;
+                    const DecodeWorkspace& wl, int n_sm, void* stream, int* launches, const void* k_new,
+                    const void* v_new, bool fused) {
+  using C = Cfg<G, GROUP, NW>;
   uint8_t* partials = ws + wl.partials;
-  const int resident = resident_ctas<G, GROUP>(n_sm);
+  const int resident = resident_ctas<G, GROUP, NW>(n_sm);
   if (resident < 0) return -resident;
   // persistent-style grid: every resident CTA slot, each looping over work items, so a
   // captured launch serves later plans with other item counts
-  (void)n_req;
-  (void)n_items;
   const uint16_t* qb = static_cast<const uint16_t*>(q);
   uint16_t* ob = static_cast<uint16_t*>(out);
   const uint16_t* kb = static_cast<const uint16_t*>(k_new);
   const uint16_t* vb = static_cast<const uint16_t*>(v_new);
-  int e = fused ? launch_ex(split_kernel<G, GROUP, true>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes), stream,
-                            kp, layer, qb, partials, ob, out_f32, kb, vb)
-                : launch_ex(split_kernel<G, GROUP, false>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
+  int e = fused ? launch_ex(split_kernel<G, GROUP, true, NW>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
+                            stream, kp, layer, qb, partials, ob, out_f32, kb, vb)
+                : launch_ex(split_kernel<G, GROUP, false, NW>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
                             stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
   if (!e) *launches += 1;
   return e;
@@ -830,25 +831,29 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
 
 }  // namespace
 
-int decode_resident_ctas(int gqa, int group, int n_sm) {
-  if (gqa == 4 && group == 128) return resident_ctas<4, 128>(n_sm);
-  if (gqa == 4 && group == 32) return resident_ctas<4, 32>(n_sm);
-  if (gqa == 8 && group == 128) return resident_ctas<8, 128>(n_sm);
-  if (gqa == 8 && group == 32) return resident_ctas<8, 32>(n_sm);
+int decode_resident_ctas(int gqa, int group, bool wide, int n_sm) {
+  const bool w = wide && gqa == 4;
+  if (gqa == 4 && group == 128) return w ? resident_ctas<4, 128, 16>(n_sm) : resident_ctas<4, 128, 8>(n_sm);
+  if (gqa == 4 && group == 32) return w ? resident_ctas<4, 32, 16>(n_sm) : resident_ctas<4, 32, 8>(n_sm);
+  if (gqa == 8 && group == 128) return resident_ctas<8, 128, 8>(n_sm);
+  if (gqa == 8 && group == 32) return resident_ctas<8, 32, 8>(n_sm);
   return n_sm;
 }
 
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches,
-                  const void* k_new, const void* v_new, bool fused) {
-#define OSCAR_DECODE_CASE(G_, GROUP_)                                                                                 \
-  if (kp.gqa == G_ && kp.group == GROUP_)                                                                             \
-    return launch_decode_t<G_, GROUP_>(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches, \
-                                       k_new, v_new, fused);
-  OSCAR_DECODE_CASE(4, 128)
-  OSCAR_DECODE_CASE(4, 32)
-  OSCAR_DECODE_CASE(8, 128)
-  OSCAR_DECODE_CASE(8, 32)
+                  const DecodeWorkspace& wl, bool wide, int n_sm, void* stream, int* launches, const void* k_new,
+                  const void* v_new, bool fused) {
+  const bool w = wide && kp.gqa == 4;
+#define OSCAR_DECODE_CASE(G_, GROUP_, NW_)                                                                       \
+  if (kp.gqa == G_ && kp.group == GROUP_ && (NW_ == 16) == w)                                                   \
+    return launch_decode_t<G_, GROUP_, NW_>(kp, layer, q, out, out_f32, ws, wl, n_sm, stream, launches, k_new, \
+                                            v_new, fused);
+  OSCAR_DECODE_CASE(4, 128, 16)
+  OSCAR_DECODE_CASE(4, 128, 8)
+  OSCAR_DECODE_CASE(4, 32, 16)
+  OSCAR_DECODE_CASE(4, 32, 8)
+  OSCAR_DECODE_CASE(8, 128, 8)
+  OSCAR_DECODE_CASE(8, 32, 8)
 #undef OSCAR_DECODE_CASE
   return int(cudaErrorInvalidValue);
 }
@@ -889,8 +894,8 @@ int scratch_address(uint8_t** out) {
 }  // namespace
 
 int launch_decode_static_scratch(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32,
-                                 const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream,
-                                 int* launches, bool* too_big) {
+                                 const DecodeWorkspace& wl, bool wide, int n_sm, void* stream, int* launches,
+                                 bool* too_big) {
   *too_big = wl.total > kStaticScratchBytes;
   if (*too_big) return int(cudaErrorInvalidValue);
   uint8_t* ws = nullptr;
@@ -898,7 +903,7 @@ int launch_decode_static_scratch(const KernelParams& kp, int layer, const void* 
   if (e) return e;
   // Nothing in the scratch has to start at zero: every work item writes its partial
   // before the merge reads it.
-  return launch_decode(kp, layer, q, out, out_f32, ws, wl, n_req, n_items, n_sm, stream, launches);
+  return launch_decode(kp, layer, q, out, out_f32, ws, wl, wide, n_sm, stream, launches);
 }
 
 }  // namespace oscar

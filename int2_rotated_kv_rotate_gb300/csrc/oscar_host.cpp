@@ -158,6 +158,7 @@ struct oscar_cache {
   std::vector<int> app_req_items;  // append items of each reservation request
   int app_items = 0, app_rows = 0;
   bool plan_covers_reservation = false;  // the plan lists every slot of the pending reservation
+  bool dec_wide = false;                  // the plan is for 16-warp split-kernel CTAs
   // decode plan
   bool planned = false;
   bool planned_with_reservation = false;  // the plan already counts the reserved tokens
@@ -573,13 +574,19 @@ oscar_status oscar_bf16_append(oscar_cache* c, int layer, const void* k_new, con
 }
 
 oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int max_split_pages, void* stream) {
+  return oscar_plan_decode_ex(c, slots, n_req, max_split_pages, 0u, stream);
+}
+
+oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, int max_split_pages, uint32_t flags,
+                                  void* stream) {
   if (!c || !slots || n_req <= 0 || n_req > c->cfg.max_requests)
     return fail(OSCAR_ERR_INVALID_ARG, "bad plan arguments");
+  if (flags & ~OSCAR_PLAN_NARROW) return fail(OSCAR_ERR_INVALID_ARG, "unknown plan flags %#x", flags);
   if (max_split_pages < 0) return fail(OSCAR_ERR_INVALID_ARG, "max_split_pages < 0");
   std::vector<char> seen(c->cfg.max_requests, 0);
   const int Hkv = c->cfg.n_kv_heads, S = is_int2(c) ? c->cfg.n_sink : 0;
   // lengths the decode will see: a pending reservation's tokens count (append before decode)
-  std::vector<int> Ls(n_req), Hs(n_req), Hpre(n_req), Lpre(n_req), app_expect(n_req, 0);
+  std::vector<int> Ls(n_req), Hs(n_req), Hpre(n_req), app_items(n_req, 0), app_expect(n_req, 0);
   int n_reserved_planned = 0;
   long long total_pages = 0;
   for (int i = 0; i < n_req; ++i) {
@@ -591,7 +598,6 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     Ls[i] = r.L;
     Hs[i] = r.H;
     Hpre[i] = r.H;
-    Lpre[i] = r.L;
     if (c->reserved)
       for (size_t k = 0; k < c->app_reqs.size(); ++k) {
         const AppendReq& a = c->app_reqs[k];
@@ -599,7 +605,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
           Ls[i] = a.L1;
           Hs[i] = a.H1;
           Hpre[i] = std::min(r.H, a.H0);
-          app_expect[i] = 2 * append_task_split(c->cfg.n_q_heads / Hkv) * c->app_req_items[k];  // per kv-head
+          app_items[i] = c->app_req_items[k];
           ++n_reserved_planned;
         }
       }
@@ -629,15 +635,26 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     // new rows are a small part of the list); its INT2 items are not split: the append's
     // eviction rows are signalled before the launch's wait, and the one warp whose page
     // holds them waits for that signal before copying it.
-    if (app_expect[i] > 0) bfnew_of[i] = 0;
-    (void)Lpre;
+    if (app_items[i] > 0) bfnew_of[i] = 0;
     max_np = std::max(max_np, np_of[i]);
     total_bytes += (long long)Hkv * (np_of[i] * page_bytes + nbf_of[i] * 2LL * kHeadDim * 2);
   }
+  // CTA shape: at GQA 4 a step that one wave of 16-warp CTAs holds (one per SM) is planned
+  // for them ("wide"); larger steps for 8-warp CTAs, two per SM.
+  constexpr long long kItemBytes = 512 << 10;
+  constexpr long long kWaves = 4;
+  const int G = c->cfg.n_q_heads / Hkv;
+  bool wide = false;
+  if (is_int2(c) && G == 4 && !(flags & OSCAR_PLAN_NARROW)) {
+    const int r_wide = decode_resident_ctas(G, c->cfg.group, true, c->n_sm);
+    wide = r_wide > 0 && total_bytes <= kItemBytes * r_wide;
+  }
+  const int nw = decode_warps(G, wide);
+  for (int i = 0; i < n_req; ++i) app_expect[i] = 2 * append_task_split(nw) * app_items[i];  // per kv-head
   auto split_count = [](int a, int b, int step) { return (a > 0 ? ceil_div(a, step) : 0) + (b > a ? ceil_div(b - a, step) : 0); };
   long long n_bf_items = 0;
   // BF16 items of one CTA chunk: 16 tokens per warp
-  const int bf_item = is_int2(c) ? 16 * decode_warps(c->cfg.n_q_heads / Hkv) : kBf16ItemTokens;
+  const int bf_item = is_int2(c) ? 16 * nw : kBf16ItemTokens;
   for (int i = 0; i < n_req; ++i) n_bf_items += (long long)Hkv * split_count(bfnew_of[i], nbf_of[i], bf_item);
   auto count_items = [&](int ch) {
     long long n = n_bf_items;
@@ -648,16 +665,14 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
     }
     return n;
   };
-  constexpr long long kItemBytes = 512 << 10;
-  constexpr long long kWaves = 4;
   int chunk = max_split_pages;
   if (chunk == 0) {
-    const int G = c->cfg.n_q_heads / Hkv;
-    int resident = is_int2(c) ? decode_resident_ctas(G, c->cfg.group, c->n_sm) : bf16_decode_resident_ctas(G, c->n_sm);
+    int resident =
+        is_int2(c) ? decode_resident_ctas(G, c->cfg.group, wide, c->n_sm) : bf16_decode_resident_ctas(G, c->n_sm);
     if (resident <= 0) resident = 2 * c->n_sm;
     if (total_bytes <= kItemBytes * resident) {
       // a fused append + decode launch runs the reservation's append tasks in the same wave
-      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 2 * append_task_split(G) : 0;
+      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 2 * append_task_split(nw) : 0;
       const long long slots = std::max<long long>(1, resident - n_bf_items - n_app_tasks);
       chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
       while (chunk < max_np && count_items(chunk) + n_app_tasks > resident) ++chunk;
@@ -743,7 +758,6 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
                            cudaMemcpyHostToDevice, s));
   CUDA_TRY(cudaEventRecord(c->upload_done, s));
   c->upload_pending = true;
-  const int G = c->cfg.n_q_heads / Hkv;
   DecodeWorkspace w;
   size_t off = 0;
   w.partials = off;
@@ -756,6 +770,7 @@ oscar_status oscar_plan_decode(oscar_cache* c, const int* slots, int n_req, int 
   c->dec_max_pages = max_pages;
   c->planned = true;
   c->planned_with_reservation = c->reserved;
+  c->dec_wide = wide;
   c->plan_covers_reservation = c->reserved && n_reserved_planned == int(c->app_reqs.size());
   return OSCAR_OK;
 }
@@ -787,8 +802,8 @@ oscar_status oscar_decode_attention(oscar_cache* c, int layer, const void* q, vo
   oscar_status st = check_decode(c, layer, q, out, workspace, ws_bytes);
   if (st) return st;
   if (!is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_decode_attention needs the INT2 format");
-  int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_n_req,
-                        c->dec_items, c->n_sm, stream, &g_launches);
+  int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_wide,
+                        c->n_sm, stream, &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "decode launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }
@@ -808,16 +823,17 @@ oscar_status oscar_append_decode_attention(oscar_cache* c, int layer, const void
   // (long chunks, many requests) would hold back the decode, so those go to the append
   // kernel, which is launched first.
   const int G = c->cfg.n_q_heads / c->cfg.n_kv_heads;
-  const int resident = decode_resident_ctas(G, c->cfg.group, c->n_sm);
-  const long long n_tasks = (long long)c->app_items * c->cfg.n_kv_heads * 2 * append_task_split(G);
+  const int resident = decode_resident_ctas(G, c->cfg.group, c->dec_wide, c->n_sm);
+  const long long n_tasks =
+      (long long)c->app_items * c->cfg.n_kv_heads * 2 * append_task_split(decode_warps(G, c->dec_wide));
   const bool fused = n_tasks <= (long long)resident;
   if (!fused && c->app_items > 0) {
     int e = launch_append(kernel_params(c), layer, k_new, v_new, std::min(c->app_items, 4 * c->n_sm), stream,
                           &g_launches);
     if (e) return fail(OSCAR_ERR_CUDA, "append launch: %s", cudaGetErrorString(cudaError_t(e)));
   }
-  int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_n_req,
-                        c->dec_items, c->n_sm, stream, &g_launches, k_new, v_new, fused);
+  int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_wide,
+                        c->n_sm, stream, &g_launches, k_new, v_new, fused);
   if (e) return fail(OSCAR_ERR_CUDA, "append + decode launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }
@@ -843,7 +859,7 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int layer, const voi
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (!q || !out) return fail(OSCAR_ERR_INVALID_ARG, "NULL q or out");
   bool too_big = false;
-  int e = launch_decode_static_scratch(kernel_params(c), layer, q, out, out_f32, c->ws, c->dec_n_req, c->dec_items,
+  int e = launch_decode_static_scratch(kernel_params(c), layer, q, out, out_f32, c->ws, c->dec_wide,
                                        c->n_sm, stream, &g_launches, &too_big);
   if (too_big)
     return fail(OSCAR_ERR_INVALID_ARG,

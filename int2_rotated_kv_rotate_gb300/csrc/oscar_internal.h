@@ -63,16 +63,16 @@ struct DecodeItem {
 };
 constexpr int kDepNone = 0, kDepRing = 1, kDepPages = 2;
 
-// Fused append + decode: CTAs per append item and kv-head and K|V (a split-kernel CTA
-// covers 16 tokens at GQA 4, 8 at GQA 8).
 #ifdef __CUDACC__
 #define OSCAR_HOST_DEVICE __host__ __device__
 #else
 #define OSCAR_HOST_DEVICE
 #endif
-OSCAR_HOST_DEVICE constexpr int append_task_split(int gqa) { return gqa == 4 ? 1 : 2; }
-// Warps of a split-kernel CTA (one CTA per SM): 16 at GQA 4, 8 at GQA 8.
-OSCAR_HOST_DEVICE constexpr int decode_warps(int gqa) { return gqa == 4 ? 16 : 8; }
+// Warps of a split-kernel CTA: 16 for one-wave plans at GQA 4 ("wide"), else 8.
+OSCAR_HOST_DEVICE constexpr int decode_warps(int gqa, bool wide) { return gqa == 4 && wide ? 16 : 8; }
+// Fused append + decode: CTAs per append item and kv-head and K|V (a CTA of nw warps
+// covers nw tokens of the item's 16).
+OSCAR_HOST_DEVICE constexpr int append_task_split(int nw) { return 16 / nw; }
 
 struct DeviceLayout {
   // pools (byte offsets in the device block)
@@ -124,15 +124,16 @@ int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, con
                        int* launches);
 // Decode; with `fused`, the same launch first runs the pending reservation's append tasks
 // (k_new, v_new as for launch_append) and decode items wait for the ones they depend on.
+// `wide`: the 16-warp CTA shape (GQA 4 only; the plan was made for it).
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                  const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches,
+                  const DecodeWorkspace& wl, bool wide, int n_sm, void* stream, int* launches,
                   const void* k_new = nullptr, const void* v_new = nullptr, bool fused = false);
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                        const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
 
 // CTAs of the decode kernel of this shape that fit on the GPU at once (occupancy x SMs);
 // the planner sizes work items so that one wave holds them all.
-int decode_resident_ctas(int gqa, int group, int n_sm);
+int decode_resident_ctas(int gqa, int group, bool wide, int n_sm);
 int bf16_decode_resident_ctas(int gqa, int n_sm);
 
 // Decode with the library's own fixed device scratch instead of a caller workspace
@@ -140,7 +141,7 @@ int bf16_decode_resident_ctas(int gqa, int n_sm);
 // exceeds static_scratch_bytes().
 size_t static_scratch_bytes();
 int launch_decode_static_scratch(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32,
-                                 const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream,
-                                 int* launches, bool* too_big);
+                                 const DecodeWorkspace& wl, bool wide, int n_sm, void* stream, int* launches,
+                                 bool* too_big);
 
 }  // namespace oscar

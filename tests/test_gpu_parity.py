@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 SEED = 1234
 
 
-def decode_and_compare(cache, oc, w, layer, slots, reqs, step, label, max_split_pages=0):
-    cache.plan(slots, max_split_pages=max_split_pages)
+def decode_and_compare(cache, oc, w, layer, slots, reqs, step, label, max_split_pages=0, flags=0):
+    cache.plan(slots, max_split_pages=max_split_pages, flags=flags)
     q = wl.gen_q(w, SEED, layer, step, len(slots), device="cuda")
     out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
     out = cache.decode(layer, q, out_f32=out32)
@@ -209,14 +209,16 @@ def kv_rows(w, layer, reqs, starts, counts):
     return torch.cat(ks).contiguous(), torch.cat(vs).contiguous()
 
 
-@pytest.mark.parametrize("gqa,group,msp", [(4, 128, 0), (4, 32, 1), (8, 128, 1), (8, 32, 0)])
-def test_fused_append_decode(gqa, group, msp):
+@pytest.mark.parametrize("gqa,group,msp,narrow", [(4, 128, 0, False), (4, 32, 1, False), (4, 128, 1, True),
+                                                 (4, 32, 0, True), (8, 128, 1, False), (8, 32, 0, False)])
+def test_fused_append_decode(gqa, group, msp, narrow):
     """One-launch append + decode: the stored rows match the oracle bit for bit, and the
     outputs equal those of the separate quantize_append and decode calls bit for bit (and
     the oracle within tolerance).  Steps of 1 and 16 tokens evict ring tokens into INT2
     pages that the same launch's decode items read; msp = 1 makes more work than one wave
     of CTAs, so the append tasks and decode items are taken from the shared counter.  A
-    512-token step has more append work than one wave and takes the two-launch path."""
+    512-token step has more append work than one wave and takes the two-launch path.
+    `narrow`: the 8-warp CTA shape (two per SM), otherwise taken only by large steps."""
     w = wl.scaled(wl.WORKLOADS["tiny"], name=f"fused_{gqa}_{group}", n_q_heads=4 * gqa, n_kv_heads=4, group=group,
                   window=64, lognormal_sigma=0.5)
     n_layers, reqs, lens = 2, [0, 1, 2], [4000, 1200, 40]
@@ -242,8 +244,9 @@ def test_fused_append_decode(gqa, group, msp):
     for step, counts in enumerate(steps):
         fused.reserve(fs, counts)
         sep.reserve(ss, counts)
-        fused.plan(fs, max_split_pages=msp)
-        sep.plan(ss, max_split_pages=msp)
+        flags = N.OSCAR_PLAN_NARROW if narrow else 0
+        fused.plan(fs, max_split_pages=msp, flags=flags)
+        sep.plan(ss, max_split_pages=msp, flags=flags)
         for layer in range(n_layers):
             K, V = kv_rows(w, layer, reqs, pos, counts)
             q = wl.gen_q(w, SEED, layer, step, 3, device="cuda")
@@ -270,7 +273,7 @@ def test_fused_append_decode(gqa, group, msp):
             assert st_ == 0 and fl == 0, f"device flags {fl:#x}"
     if msp == 1:
         n_items, _, _ = fused.plan_info()
-        assert n_items > torch.cuda.get_device_properties(0).multi_processor_count * (2 if gqa == 4 else 1)
+        assert n_items > torch.cuda.get_device_properties(0).multi_processor_count * (2 if narrow else 1)
     for layer in range(n_layers):
         for i, r in enumerate(reqs):
             check_pages(fused, oc, layer, fs[i], r)
@@ -293,8 +296,8 @@ def test_fused_append_decode_needs_a_covering_plan():
     assert ei.value.status == 7  # OSCAR_ERR_STATE
 
 
-@pytest.mark.parametrize("gqa", [4, 8])
-def test_plans_larger_than_one_wave(gqa):
+@pytest.mark.parametrize("gqa,narrow", [(4, False), (4, True), (8, False)])
+def test_plans_larger_than_one_wave(gqa, narrow):
     """Single-page items, several times more than the CTAs resident at once: the CTAs take
     items from the shared work counter, merge in two levels, and leave the counters reset
     for the next launch (three decodes in a row, with plans of different sizes)."""
@@ -309,7 +312,7 @@ def test_plans_larger_than_one_wave(gqa):
     torch.cuda.synchronize()
     for step, msp in enumerate((1, 2, 1)):
         decode_and_compare(cache, oc, w, 0, slots, list(range(len(lens))), step, f"waves msp {msp}",
-                           max_split_pages=msp)
+                           max_split_pages=msp, flags=N.OSCAR_PLAN_NARROW if narrow else 0)
         n_items, n_bf16, _ = cache.plan_info()
         assert n_items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
 
