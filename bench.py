@@ -391,11 +391,15 @@ def run_ours(args, world, rank, local):
         cache.reserve(slots, steps_in[s][3])
         cache.plan(slots)
 
-    def device_step():
+    # per-layer views, made once (the calls below are the step's whole host work per layer)
+    kin_l, vin_l = [kin[layer] for layer in range(n_layers)], [vin[layer] for layer in range(n_layers)]
+    qin_l, out_l = [qin[layer] for layer in range(n_layers)], [out[layer] for layer in range(n_layers)]
+
+    def device_step(strm=None):
         # per layer, one call: quantize-append of the step's tokens, then decode attention
         n = 0  # kernels the library put on the stream (its own count, per call)
         for layer in range(n_layers):
-            cache.append_decode(layer, kin[layer], vin[layer], qin[layer], out=out[layer])
+            cache.append_decode(layer, kin_l[layer], vin_l[layer], qin_l[layer], out=out_l[layer], stream=strm)
             n += N.oscar_last_launch_count()
         return n
 
@@ -498,6 +502,7 @@ def run_ours(args, world, rank, local):
         hout = torch.empty(out.shape, dtype=out.dtype).pin_memory()
         # roll the cache back is not possible; e2e continues the sequence on fresh steps
         n_e2e = min(args.steps, E2E_STEPS)
+        stream_handle = torch.cuda.current_stream().cuda_stream
         torch.cuda.synchronize()
         e0.record()
         for i in range(n_e2e):
@@ -507,7 +512,7 @@ def run_ours(args, world, rank, local):
             kin.copy_(hK[s], non_blocking=True)
             vin.copy_(hV[s], non_blocking=True)
             qin.copy_(hQ[s], non_blocking=True)
-            device_step()  # the public calls themselves, launched eagerly
+            device_step(stream_handle)  # the public calls themselves, launched eagerly
             hout.copy_(out, non_blocking=True)
             cache.commit()
         e1.record()

@@ -399,11 +399,15 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       }
       phase_bits ^= 1u << st;
       ok_mask &= ~(1u << st);
-    } else if (lane == 0) {
-      flag(kp, OSCAR_FLAG_BAD_PAGE);
+    } else {
+      // a page that was not copied (page id out of range) contributes nothing
+      if (lane == 0) flag(kp, OSCAR_FLAG_BAD_PAGE);
+      __syncwarp();
+      if (k + kStages < n_my && issue(k + kStages)) ok_mask |= 1u << st;
+      continue;
     }
-    // positions [S, H) of the page: tokens t with t - vlo < vn (unsigned); none if no copy
-    const int vlo = max(S - lp * kPage, 0), vn = have ? max(0, min(H - lp * kPage, kPage) - vlo) : 0;
+    // positions [S, H) of the page: tokens t with t - vlo < vn (unsigned)
+    const int vlo = max(S - lp * kPage, 0), vn = max(0, min(H - lp * kPage, kPage) - vlo);
     const uint8_t* stage = pipe + size_t(st) * C::kStageBytes;
     const uint8_t* kcodes = stage;
     const uint8_t* vcodes = stage + kPage * kRowBytes;
@@ -505,15 +509,15 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
         p[j][1] = ex2(lg[b][j][1] - muse[j]);
         l_part[j] += p[j][0] + p[j][1];
       }
-      const bool v0 = unsigned(t0 - vlo) < unsigned(vn), v1 = unsigned(t1 - vlo) < unsigned(vn);
-      // B fragments of P' = p * s_V per group (movmatrix turns score rows into value k-rows);
-      // scale/zero of masked rows may hold anything, so they are selected away, not multiplied
+      // B fragments of P' = p * s_V per group (movmatrix turns score rows into value k-rows).
+      // Masked rows have p = 0, and every scale/zero word of the pool is finite (the pool
+      // starts zeroed and only finite words are written), so they need no select.
       uint32_t bp[NG][2];
 #pragma unroll
       for (int g = 0; g < NG; ++g) {
         const uint32_t vz0 = vsz[t0 * NG + g], vz1 = vsz[t1 * NG + g];
-        const float sv0 = v0 ? bf16_lo(vz0) : 0.f, sv1 = v1 ? bf16_lo(vz1) : 0.f;
-        const float zv0 = v0 ? bf16_hi(vz0) : 0.f, zv1 = v1 ? bf16_hi(vz1) : 0.f;
+        const float sv0 = bf16_lo(vz0), sv1 = bf16_lo(vz1);
+        const float zv0 = bf16_hi(vz0), zv1 = bf16_hi(vz1);
         uint32_t x0, x1;
         if (NT == 1) {
           const float q0 = p[0][0] * sv0, q1 = p[0][1] * sv1;

@@ -274,6 +274,9 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.status, 0, 256);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.counters, 0, size_t(cfg->max_requests) * cfg->n_kv_heads * 4);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.sched, 0, 16);
+  // scale/zero words of rows no append has written yet (sink positions, the tail of a
+  // page) are read with p = 0 by the decode: they must be finite, so the pool starts at 0
+  if (e == cudaSuccess && is_int2(c)) e = cudaMemset(c->base + lay.sz, 0, size_t(cfg->n_layers) * lay.sz_layer_stride);
   if (e == cudaSuccess)
     e = cudaMemset(c->base + lay.app_done, 0, size_t(cfg->n_layers) * cfg->max_requests * cfg->n_kv_heads * 8);
   if (e == cudaSuccess && is_int2(c)) {
