@@ -38,6 +38,7 @@ namespace oscar {
 namespace {
 
 constexpr int kStages = 2;  // page stages per warp
+constexpr int kSpareSMs = 8;  // SMs a one-per-SM grid leaves free (see resident_ctas_t)
 
 // CTA shape of the split kernel.  NW = 16 (GQA 4, plans of one wave): one CTA per SM, 128
 // registers a thread fill the register file.  NW = 8: two CTAs per SM at GQA 4 (plans of
@@ -797,6 +798,9 @@ int resident_ctas_t(int n_sm) {
                                                             C::kSmemBytes));
     if (e) return -e;
     resident = (per_sm > 0 ? per_sm : 1) * n_sm;
+    // One CTA per SM (16-warp shape): leave a few SMs to the preceding launch's last CTAs
+    // (its final merges), so that no CTA of this launch waits for an SM to drain.
+    if (NW == 16 && resident > 4 * kSpareSMs) resident -= kSpareSMs;
   }
   return resident;
 }
