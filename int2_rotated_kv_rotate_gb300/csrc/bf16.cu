@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     };
     auto rowK = [=](int u) { return page_of(u) + size_t(u % kPage) * kHeadDim; };
     auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
-    bf16_rows_mma<G, 4, 2>(rowK, rowV, t0, t1, qs, part, smem);
+    bf16_rows_mma<G, 4, 2>(rowK, rowV, t0, t1, qs, part, smem, 0, [] {});
 
     MergeAcc<G, 128> acc;
     if (merge_partial<G, 128>(kp, it, partials, acc, s_last_p, smem, kBf16SlabSlots<G>, smem_u32(slab_bar), slab_phase,

@@ -245,29 +245,52 @@ __device__ void finish_output(const KernelParams& kp, const DecodeItem& it, cons
   }
 }
 
-// BF16 tokens of the sink + ring list: list index u < min(L, S) is sink u, otherwise
-// position H + u - min(L, S) in ring slot p % W.
-template <int G, int NW>
+// BF16 rows of the sink + ring list of (request, kv-head): list index u < min(L, S) is
+// sink u, otherwise position H + u - min(L, S) in ring slot p % W.
+struct SinkRingRows {
+  const uint16_t *sinkK, *sinkV, *ringK, *ringV;
+  int n_s, W, hw;  // hw = H % W
+  __device__ SinkRingRows(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr) {
+    const int S = kp.n_sink;
+    n_s = min(dr.L, S);
+    W = kp.window;
+    hw = W > 0 ? dr.H % W : 0;
+    sinkK = reinterpret_cast<const uint16_t*>(kp.base + kp.lay.sink + size_t(dr.slot) * kp.lay.sink_slot_stride +
+                                              size_t(layer) * kp.lay.sink_layer_stride +
+                                              size_t(it.kvh) * kp.lay.sink_head_stride);
+    sinkV = sinkK + size_t(S) * kHeadDim;
+    ringK = reinterpret_cast<const uint16_t*>(kp.base + kp.lay.ring + size_t(dr.slot) * kp.lay.ring_slot_stride +
+                                              size_t(layer) * kp.lay.ring_layer_stride +
+                                              size_t(it.kvh) * kp.lay.ring_head_stride);
+    ringV = ringK + size_t(W) * kHeadDim;
+  }
+  // ring slot of list index u >= n_s: (H + u - n_s) % W, with u - n_s < W
+  __device__ int slot(int u) const {
+    const int s = hw + u - n_s;
+    return s >= W ? s - W : s;
+  }
+  __device__ const uint16_t* K(int u) const { return u < n_s ? sinkK + size_t(u) * kHeadDim : ringK + size_t(slot(u)) * kHeadDim; }
+  __device__ const uint16_t* V(int u) const { return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t(slot(u)) * kHeadDim; }
+};
+
+// Copy the rows of BF16 item `it` that are final before the wait on the preceding kernel
+// (list indices below it.split) into the item's row buffer.
+template <int NW>
+__device__ void bf16_item_prestage(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
+                                   uint8_t* smem) {
+  const SinkRingRows rows(kp, layer, it, dr);
+  bf16_prestage<NW>([&](int u) { return rows.K(u); }, [&](int u) { return rows.V(u); }, it.begin, it.split, smem);
+}
+
+// BF16 tokens [it.begin, it.end) of the sink + ring list; the rows below it.split were
+// copied by bf16_item_prestage when `prestaged`; wait_rest() runs before the other rows
+// are copied.
+template <int G, int NW, typename WaitRest>
 __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
-                                 const float* qts, uint8_t* part, uint8_t* smem) {
-  const int S = kp.n_sink;
-  const int n_s = min(dr.L, S);
-  const uint16_t* sinkK = reinterpret_cast<const uint16_t*>(
-      kp.base + kp.lay.sink + size_t(dr.slot) * kp.lay.sink_slot_stride + size_t(layer) * kp.lay.sink_layer_stride +
-      size_t(it.kvh) * kp.lay.sink_head_stride);
-  const uint16_t* sinkV = sinkK + size_t(S) * kHeadDim;
-  const uint16_t* ringK = reinterpret_cast<const uint16_t*>(
-      kp.base + kp.lay.ring + size_t(dr.slot) * kp.lay.ring_slot_stride + size_t(layer) * kp.lay.ring_layer_stride +
-      size_t(it.kvh) * kp.lay.ring_head_stride);
-  const uint16_t* ringV = ringK + size_t(kp.window) * kHeadDim;
-  const int W = kp.window, H = dr.H;
-  auto rowK = [=](int u) {
-    return u < n_s ? sinkK + size_t(u) * kHeadDim : ringK + size_t((H + u - n_s) % W) * kHeadDim;
-  };
-  auto rowV = [=](int u) {
-    return u < n_s ? sinkV + size_t(u) * kHeadDim : ringV + size_t((H + u - n_s) % W) * kHeadDim;
-  };
-  bf16_rows_mma<G, NW, 1>(rowK, rowV, it.begin, it.end, qts, part, smem);
+                                 const float* qts, uint8_t* part, uint8_t* smem, bool prestaged, WaitRest wait_rest) {
+  const SinkRingRows rows(kp, layer, it, dr);
+  bf16_rows_mma<G, NW, 1>([&](int u) { return rows.K(u); }, [&](int u) { return rows.V(u); }, it.begin, it.end, qts,
+                          part, smem, prestaged ? it.split - it.begin : 0, wait_rest);
 }
 
 // Issue (lane 0 of the calling warp) the bulk copies of the warp's k-th page of an INT2
@@ -726,6 +749,11 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
     const bool dep = pending && it.dep != kDepNone;
     const unsigned* ctrs = app_done + ((size_t(layer) * kp.max_requests + (slot_ok ? dr.slot : 0)) * kp.n_kv_heads + it.kvh) * 2;
     uint32_t pre_mask = 0;
+    bool prestaged = false;
+    if (it.kind == 1 && slot_ok && it.split > it.begin) {
+      bf16_item_prestage<NW>(kp, layer, it, dr, smem);
+      prestaged = true;
+    }
     if (it.kind == 0 && slot_ok) {
       const int warp = threadIdx.x >> 5;
       const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
@@ -748,12 +776,15 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
     }
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
     rotate_q<G, NW>(q + head0 * kHeadDim, rk, qin, qts, qss);
-    if (dep) {
+    // rows this launch's append tasks write: wait for their signal (all threads)
+    auto wait_dep = [&] {
+      if (!dep) return;
       const unsigned* ctr = ctrs + (it.dep == kDepPages ? 1 : 0);
       if (threadIdx.x == 0 && !wait_counter(ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
       __syncthreads();
       fence_proxy_async_global();  // the append's rows, seen through the acquire, before bulk copies
-    }
+    };
+    if (it.kind == 0) wait_dep();
     uint8_t* part = partials + size_t(ix) * PartialSlot<G>::kBytes;
     if (!slot_ok) {
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
@@ -762,7 +793,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
       int2_pages_item<G, GROUP, NW>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask,
                                 pending && it.dep == kDepNone ? ctrs + 1 : nullptr);
     } else {
-      bf16_tokens_item<G, NW>(kp, layer, it, dr, qts, part, smem);
+      bf16_tokens_item<G, NW>(kp, layer, it, dr, qts, part, smem, prestaged, wait_dep);
     }
     // ---- merge by the last CTA of (request, kv-head): R_V^T is fetched as soon as this CTA
     // knows it merges, the partial slots are bulk-copied after it

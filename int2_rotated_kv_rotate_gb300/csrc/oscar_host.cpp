@@ -589,7 +589,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   std::vector<char> seen(c->cfg.max_requests, 0);
   const int Hkv = c->cfg.n_kv_heads, S = is_int2(c) ? c->cfg.n_sink : 0;
   // lengths the decode will see: a pending reservation's tokens count (append before decode)
-  std::vector<int> Ls(n_req), Hs(n_req), Hpre(n_req), app_items(n_req, 0), app_expect(n_req, 0);
+  std::vector<int> Ls(n_req), Hs(n_req), Hpre(n_req), Lpre(n_req), app_items(n_req, 0), app_expect(n_req, 0);
   int n_reserved_planned = 0;
   long long total_pages = 0;
   for (int i = 0; i < n_req; ++i) {
@@ -601,6 +601,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
     Ls[i] = r.L;
     Hs[i] = r.H;
     Hpre[i] = r.H;
+    Lpre[i] = r.L;
     if (c->reserved)
       for (size_t k = 0; k < c->app_reqs.size(); ++k) {
         const AppendReq& a = c->app_reqs[k];
@@ -608,6 +609,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
           Ls[i] = a.L1;
           Hs[i] = a.H1;
           Hpre[i] = std::min(r.H, a.H0);
+          Lpre[i] = std::min(r.L, a.L0);
           app_items[i] = c->app_req_items[k];
           ++n_reserved_planned;
         }
@@ -698,11 +700,18 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
     q.H_pre = is_int2(c) ? Hpre[i] : 0;
     q.app_expect = is_int2(c) ? app_expect[i] : 0;
     const int np = np_of[i], n_bf = nbf_of[i], bf_new = bfnew_of[i], pg_new = pgnew_of[i];
+    // BF16 list index of this step's first new row (index < min(L, S): sink, else ring
+    // position H + index - min(L, S)); rows before it are final before the launch's wait
+    int u_new = n_bf;
+    if (is_int2(c) && Lpre[i] < Ls[i]) {
+      const int n_s = std::min(q.L, S);
+      u_new = std::min(n_bf, Lpre[i] < n_s ? Lpre[i] : n_s + std::max(0, Lpre[i] - q.H));
+    }
     q.first_item = int(items.size());
     for (int h = 0; h < Hkv; ++h) {
       const int first = int(items.size());
       auto add = [&](int kind, int b, int e, int dep) {
-        items.push_back({i, h, kind, b, e, first, 0, dep});
+        items.push_back({i, h, kind, b, e, first, 0, dep, kind == 1 ? std::min(e, std::max(b, u_new)) : e});
       };
       if (n_bf == 0 && np == 0) add(1, 0, 0, kDepNone);  // empty request: one empty item writes zeros
       // BF16 sink+ring list, split where this step's new tokens start (those items wait for

@@ -60,6 +60,8 @@ struct DecodeItem {
   int dep;         // fused append + decode: what the item reads that this launch's append tasks
                    // write (kDepNone, kDepRing: BF16 rows of new tokens, kDepPages: INT2 pages
                    // that receive evicted or new tokens)
+  int split;       // BF16 items: list index from which rows may be written by this step's
+                   // append (rows before it may be copied before the wait); INT2 items: end
 };
 constexpr int kDepNone = 0, kDepRing = 1, kDepPages = 2;
 
