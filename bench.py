@@ -31,6 +31,9 @@ sys.path.insert(0, ROOT)
 METRIC = "INT2 decode-attn µs/layer/step & achieved HBM GB/s vs ~8 TB/s peak"
 
 
+FILL_CHUNK = 16384  # context tokens appended per request and call while filling
+
+
 def parse_args(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -342,23 +345,7 @@ def run_ours(args, world, rank, local):
 
     # ---- fill the context (prefix owners first, then sharers map the shared pages)
     t_fill = time.time()
-    shared = [0] * B
-    if w.prefix_tokens:
-        owners = [r for r in range(B) if r % w.prefix_group == 0]
-    else:
-        owners = list(range(B))
-    fill(cache, w, seed, n_layers, [slots[r] for r in owners], owners, [0] * len(owners),
-         [plan.lengths[r] for r in owners], dev)
-    if w.prefix_tokens:
-        sharers = [r for r in range(B) if r % w.prefix_group != 0]
-        for r in sharers:
-            src = r - r % w.prefix_group
-            n_sh = min(wl.shared_prefix_tokens(w, plan.lengths[r]), (cache.info(slots[src])[1] // 64) * 64)
-            if n_sh > 0:
-                cache.share_prefix(slots[r], slots[src], n_sh)
-                shared[r] = n_sh
-        fill(cache, w, seed, n_layers, [slots[r] for r in sharers], sharers, [shared[r] for r in sharers],
-             [plan.lengths[r] - shared[r] for r in sharers], dev)
+    fill_context(cache, w, seed, n_layers, slots, plan.lengths, dev)
     torch.cuda.synchronize()
     t_fill = time.time() - t_fill
 
@@ -537,7 +524,31 @@ def run_ours(args, world, rank, local):
                 n_bf16_items=n_bf16_items, t_cal=t_cal, t_fill=t_fill, world=world, w=w)
 
 
-def fill(cache, w, seed, n_layers, slots, reqs, starts, counts, dev, chunk=16384):
+def fill_context(cache, w, seed, n_layers, slots, lengths, dev):
+    """The workload's context: prefix owners are filled first, then each sharer maps its group
+    owner's prefix pages and appends the rest of its own context.  Returns the shared token
+    count of every request."""
+    from int2_rotated_kv_rotate_gb300 import workloads as wl
+
+    B = len(lengths)
+    shared = [0] * B
+    owners = [r for r in range(B) if r % w.prefix_group == 0] if w.prefix_tokens else list(range(B))
+    fill(cache, w, seed, n_layers, [slots[r] for r in owners], owners, [0] * len(owners),
+         [lengths[r] for r in owners], dev)
+    if w.prefix_tokens:
+        sharers = [r for r in range(B) if r % w.prefix_group != 0]
+        for r in sharers:
+            src = r - r % w.prefix_group
+            n_sh = min(wl.shared_prefix_tokens(w, lengths[r]), (cache.info(slots[src])[1] // 64) * 64)
+            if n_sh > 0:
+                cache.share_prefix(slots[r], slots[src], n_sh)
+                shared[r] = n_sh
+        fill(cache, w, seed, n_layers, [slots[r] for r in sharers], sharers, [shared[r] for r in sharers],
+             [lengths[r] - shared[r] for r in sharers], dev)
+    return shared
+
+
+def fill(cache, w, seed, n_layers, slots, reqs, starts, counts, dev, chunk=FILL_CHUNK):
     """Append the context of `reqs` in pieces of at most `chunk` tokens per request."""
     import torch
 
