@@ -176,10 +176,14 @@ struct Cfg {
   static constexpr int kQin = kCtl + kCtlBytes;     // fp32 [G][kQinRow] query staging
   static constexpr int kQts = kQin + G * Shape<NW>::kQinRow * 4;  // fp32 [G][kQRow] q~
   static constexpr int kQss = kQts + G * kQRow * 4;  // fp32 [NW][G] sums of q~ per warp's channels
-  static constexpr int kSmemBytes = kQss + NW * G * 4;
+  // packed B fragments of q~ for the INT2 pages: [4 NT chunks][32 lanes][4 words]
+  static constexpr int kQbWords = 16 * NT;  // per lane
+  static constexpr int kQb = ((kQss + NW * G * 4 + 15) / 16) * 16;
+  static constexpr int kSmemBytes = kQb + 32 * kQbWords * 4;
   static_assert(kSmemBytes + 1024 <= 228 * 1024 / kPerSM, "resident CTAs per SM");
   static_assert(kWorkBytes >= Bf16Rows<NW, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
-  static_assert(kWorkBytes >= NW * G * (kHeadDim + 2) * 4, "per-warp results reuse the page pipeline memory");
+  static_assert(kWorkBytes >= (NW * G * (kHeadDim + 4) + 4 * ((G + 3) / 4)) * 4,
+                "per-warp results reuse the page pipeline memory");
   static_assert(kSlabOff + (1 + NTH / kHeadDim) * G * kHeadDim * 4 <= kMergeBytes,
                 "o~ and the partial sums of the output rotation are staged over the slab");
 };
@@ -359,24 +363,31 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   for (int k = 0; k < min(kStages, n_my); ++k)
     if (!((pre_mask >> k) & 1u) && issue(k)) ok_mask |= 1u << k;
 
-  // ---- B fragments of q~ (hi/lo fp16 columns), scaled by 4^-(kc & 3) for field kc
+  // ---- B fragments of q~ (hi/lo fp16 columns), scaled by 4^-(kc & 3) for field kc: the
+  // same for every warp, so the CTA packs them once.  Lane (gid, tig) word w = 2(NT kc + j) + r
+  // holds head 4j + gid / 2, channels 16 kc + 4 tig + 2r, +1 (hi part for even gid, lo for odd).
+  uint32_t* qb = reinterpret_cast<uint32_t*>(smem + C::kQb);
+  for (int e = threadIdx.x; e < 32 * C::kQbWords; e += C::NTH) {
+    const int ln = e & 31, w = e >> 5;  // consecutive threads: consecutive lanes of one word
+    const int kc = w / (2 * NT), j = (w >> 1) % NT, r = w & 1;
+    const int g_ = ln >> 2, t_ = ln & 3;
+    const int head = 4 * j + (g_ >> 1);
+    const float fs = 1.0f / float(1 << (2 * (kc & 3)));
+    const float2 v2 = *reinterpret_cast<const float2*>(qts + head * kQRow + 16 * kc + 4 * t_ + 2 * r);
+    const float v0 = v2.x * fs, v1 = v2.y * fs;
+    const float h0 = __half2float(__float2half_rn(v0)), h1 = __half2float(__float2half_rn(v1));
+    qb[((w >> 2) * 32 + ln) * 4 + (w & 3)] = (g_ & 1) ? pack_h2(v0 - h0, v1 - h1) : pack_h2(h0, h1);
+  }
+  __syncthreads();
   uint32_t bq[8][NT][2];
 #pragma unroll
-  for (int kc = 0; kc < 8; ++kc) {
-    const float fs = 1.0f / float(1 << (2 * (kc & 3)));
+  for (int c4 = 0; c4 < 4 * NT; ++c4) {
+    const uint4 u = reinterpret_cast<const uint4*>(qb)[c4 * 32 + lane];
+    const uint32_t ws[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int head = 4 * j + (gid >> 1), part_lo = gid & 1;
-      const float4 v4 = *reinterpret_cast<const float4*>(qts + head * kQRow + 16 * kc + 4 * tig);
-      const float v[4] = {v4.x * fs, v4.y * fs, v4.z * fs, v4.w * fs};
-      float o4[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float hi = __half2float(__float2half_rn(v[e]));
-        o4[e] = part_lo ? v[e] - hi : hi;
-      }
-      bq[kc][j][0] = pack_h2(o4[0], o4[1]);
-      bq[kc][j][1] = pack_h2(o4[2], o4[3]);
+    for (int i = 0; i < 4; ++i) {
+      const int w = 4 * c4 + i;
+      bq[w / (2 * NT)][(w >> 1) % NT][w & 1] = ws[i];
     }
   }
   // per-thread heads: n-tile j gives head 4j + tig
@@ -593,14 +604,29 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     }
   }
   __syncthreads();  // every warp is done with its stages: reuse the pipeline memory
-  float* wres = reinterpret_cast<float*>(smem);  // [C::NW][G][2 + d]
-  float* mine = wres + size_t(warp) * G * (kHeadDim + 2);
+  // per-warp maxima, then every warp scales its (l, o) to the CTA's maximum and the
+  // scaled parts are added over the warps in ascending order
+  float* wm = reinterpret_cast<float*>(smem);  // [NW][G] maxima
+  float* wl = wm + C::NW * G;                   // [NW][G] scaled l
+  float* wmax = wl + C::NW * G;                 // [G] CTA maxima (4 floats reserved)
+  float* wo = wmax + 4 * ((G + 3) / 4);         // [NW][G][d + 2] scaled o (rows padded against bank conflicts)
+  constexpr int kRow = kHeadDim + 2;
   if (gid == 0) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const int head = 4 * j + tig;
-      mine[head * (kHeadDim + 2)] = broken ? -INFINITY : m_run[j];
-      mine[head * (kHeadDim + 2) + 1] = broken ? 0.f : l_part[j];
+    for (int j = 0; j < NT; ++j) wm[warp * G + 4 * j + tig] = broken ? -INFINITY : m_run[j];
+  }
+  __syncthreads();
+  float a[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    const int head = 4 * j + tig;
+    float ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < C::NW; ++w) ms = fmaxf(ms, wm[w * G + head]);
+    a[j] = broken || ms == -INFINITY ? 0.f : ex2(m_run[j] - ms);
+    if (gid == 0) {
+      wl[warp * G + head] = l_part[j] * a[j];
+      if (warp == 0) wmax[head] = ms;
     }
   }
 #pragma unroll
@@ -608,33 +634,27 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     const float us = two24 / float(1 << (2 * (f & 3)));
     const int ch0 = 16 * f + 2 * gid, ch1 = ch0 + 1;
     const int g = NG == 1 ? 0 : (f >> 1);
+    float* mine = wo + size_t(warp) * G * kRow;
     if (NT == 1) {
-      const int head = tig;
-      mine[head * (kHeadDim + 2) + 2 + ch0] = (oacc[f][0] + oacc[f][1]) * us + zv[0][g];
-      mine[head * (kHeadDim + 2) + 2 + ch1] = (oacc[f][2] + oacc[f][3]) * us + zv[0][g];
+      mine[tig * kRow + ch0] = ((oacc[f][0] + oacc[f][1]) * us + zv[0][g]) * a[0];
+      mine[tig * kRow + ch1] = ((oacc[f][2] + oacc[f][3]) * us + zv[0][g]) * a[0];
     } else {
-      mine[tig * (kHeadDim + 2) + 2 + ch0] = oacc[f][0] * us + zv[0][g];
-      mine[(4 + tig) * (kHeadDim + 2) + 2 + ch0] = oacc[f][1] * us + zv[NT - 1][g];
-      mine[tig * (kHeadDim + 2) + 2 + ch1] = oacc[f][2] * us + zv[0][g];
-      mine[(4 + tig) * (kHeadDim + 2) + 2 + ch1] = oacc[f][3] * us + zv[NT - 1][g];
+      mine[tig * kRow + ch0] = (oacc[f][0] * us + zv[0][g]) * a[0];
+      mine[(4 + tig) * kRow + ch0] = (oacc[f][1] * us + zv[NT - 1][g]) * a[NT - 1];
+      mine[tig * kRow + ch1] = (oacc[f][2] * us + zv[0][g]) * a[0];
+      mine[(4 + tig) * kRow + ch1] = (oacc[f][3] * us + zv[NT - 1][g]) * a[NT - 1];
     }
   }
   __syncthreads();
   for (int e = threadIdx.x; e < G * kHeadDim; e += C::NTH) {
     const int h = e / kHeadDim, c = e % kHeadDim;
-    float ms = -INFINITY;
-#pragma unroll
-    for (int w = 0; w < C::NW; ++w) ms = fmaxf(ms, wres[(w * G + h) * (kHeadDim + 2)]);
     float l = 0.f, o = 0.f;
 #pragma unroll
     for (int w = 0; w < C::NW; ++w) {
-      const float mw = wres[(w * G + h) * (kHeadDim + 2)];
-      if (mw == -INFINITY) continue;
-      const float a = ex2(mw - ms);
-      l = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 1], l);
-      o = fmaf(a, wres[(w * G + h) * (kHeadDim + 2) + 2 + c], o);
+      l += wl[w * G + h];
+      o += wo[(w * G + h) * kRow + c];
     }
-    store_slot<G>(part, h, c, ms, l, o);
+    store_slot<G>(part, h, c, wmax[h], l, o);
   }
 }
 
