@@ -41,9 +41,9 @@ constexpr int kStages = 2;  // page stages per warp
 constexpr int kSpareSMs = 8;  // SMs a one-per-SM grid leaves free (see resident_ctas_t)
 
 // CTA shape of the split kernel.  NW = 16 (GQA 4, plans of one wave): one CTA per SM, 128
-// registers a thread fill the register file.  NW = 8: two CTAs per SM at GQA 4 (plans of
-// several waves: one CTA streams while the other is between items), one at GQA 8 (more
-// registers a thread).  Each channel of the q rotation has kParts threads, each summing
+// registers a thread fill the register file.  NW = 8: two CTAs per SM, also 128 registers
+// a thread (plans of several waves, and every plan at GQA 8: one CTA streams while the
+// other is between items).  Each channel of the q rotation has kParts threads, each summing
 // 128 / kParts rows of R_K.
 template <int NW_>
 struct Shape {
@@ -154,7 +154,7 @@ __device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)
 template <int G, int GROUP, int NW_>
 struct Cfg {
   static constexpr int NW = NW_, NTH = Shape<NW>::NTH;
-  static constexpr int kPerSM = G == 4 && NW == 8 ? 2 : 1;  // resident CTAs per SM
+  static constexpr int kPerSM = NW == 8 ? 2 : 1;  // resident CTAs per SM (128 registers a thread)
   static constexpr int NG = kHeadDim / GROUP;           // groups per token
   static constexpr int NT = G / 4;                      // score n-tiles (4 heads x hi/lo each)
   static constexpr int kCodeBytes = 2 * kPage * kRowBytes;  // K then V codes
@@ -164,9 +164,9 @@ struct Cfg {
   // fused append tasks: R (fp32 [d][d]) then the append scratch, in the same memory
   static constexpr int kAppendR = kHeadDim * kHeadDim * 4;
   static constexpr int kAppendBytes = kAppendR + int(sizeof(append_dev::Smem));
-  // the merge: R_V^T (64 KB) then a slab of at least 32 partial slots (16 at two CTAs per SM)
+  // the merge: R_V^T (64 KB) then a slab of at least 32 partial slots (64 / G at two CTAs per SM)
   static constexpr int kSlabOff = kHeadDim * kHeadDim * 4;
-  static constexpr int kMergeBytes = kSlabOff + (kPerSM == 2 ? 16 : 32) * PartialSlot<G>::kBytes;
+  static constexpr int kMergeBytes = kSlabOff + (kPerSM == 2 ? 64 / G : 32) * PartialSlot<G>::kBytes;
   static constexpr int kWorkBytes0 = kPipeBytes > kAppendBytes ? kPipeBytes : kAppendBytes;
   static constexpr int kWorkBytes = (((kWorkBytes0 > kMergeBytes ? kWorkBytes0 : kMergeBytes) + 127) / 128) * 128;
   static constexpr int kSlabSlots = (kWorkBytes - kSlabOff) / PartialSlot<G>::kBytes;
