@@ -181,7 +181,6 @@ struct Cfg {
   static constexpr int kQb = ((kQss + NW * G * 4 + 15) / 16) * 16;
   static constexpr int kSmemBytes = kQb + 32 * kQbWords * 4;
   static_assert(kSmemBytes + 1024 <= 228 * 1024 / kPerSM, "resident CTAs per SM");
-  static_assert(NW * kStages <= kPrePages, "first-work pages cover every warp's first stages");
   static_assert(kWorkBytes >= Bf16Rows<NW, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
   static_assert(kWorkBytes >= (NW * G * (kHeadDim + 4) + 4 * ((G + 3) / 4)) * 4,
                 "per-warp results reuse the page pipeline memory");
@@ -301,10 +300,14 @@ __device__ void bf16_tokens_item(const KernelParams& kp, int layer, const Decode
 // Issue (lane 0 of the calling warp) the bulk copies of the warp's k-th page of an INT2
 // item into stage k % kStages; false (no copy) if the page id is out of range.
 template <int G, int GROUP, int NW>
-__device__ bool int2_issue_phys(const KernelParams& kp, int layer, const DecodeItem& it, int phys, int k,
+__device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr, int k,
                                 uint8_t* smem) {
   using C = Cfg<G, GROUP, NW>;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lp = it.begin + warp + C::NW * k;
+  const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
+  int phys = -1;
+  if (lp < kp.max_pages_per_request) phys = ptab[lp];
   if (phys < 0 || phys >= kp.max_pages) return false;
   if (lane == 0) {
     const int st = k % kStages;
@@ -321,16 +324,6 @@ __device__ bool int2_issue_phys(const KernelParams& kp, int layer, const DecodeI
     bulk_g2s(smem_u32(dst + C::kCodeBytes), sz, C::kSzBytes, bar);
   }
   return true;
-}
-
-// The same, with the physical page looked up in the request's page table.
-template <int G, int GROUP, int NW>
-__device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr, int k,
-                                uint8_t* smem) {
-  const int lp = it.begin + (threadIdx.x >> 5) + NW * k;
-  const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
-  const int phys = lp < kp.max_pages_per_request ? ptab[lp] : -1;
-  return int2_issue_phys<G, GROUP, NW>(kp, layer, it, phys, k, smem);
 }
 
 // INT2 history pages [it.begin, it.end) of one (request, kv-head).  Positions outside
@@ -750,11 +743,6 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
   // pages, only those wholly below H_pre are final before the wait (a preceding append may
   // still be writing the rest), so the first item copies those early.  Fused launches put
   // the reservation's append tasks (item x kv-head x K|V) ahead of the decode items.
-  // the CTA's first work comes self-contained from the plan's first-work table (one load,
-  // beside the counts); later work from the work queue
-  const bool have_first = blockIdx.x < unsigned(kMaxPositions);
-  const FirstWork* fwp = reinterpret_cast<const FirstWork*>(kp.base + kp.lay.first_work) +
-                         (fused ? kMaxPositions : 0) + (have_first ? blockIdx.x : 0);
   const int* counts = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts);
   const int n_items = counts[1];
   const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * append_task_split(NW) : 0;
@@ -763,19 +751,17 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
   unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
   bool waited = false;
   uint32_t phase_bits = 0, merge_phase = 0, slab_phase = 0;
-  bool first = have_first;
-  for (int id = first ? fwp->id : wq.first(); id >= 0; id = wq.next(s_next)) {
+  for (int id = wq.first(); id >= 0; id = wq.next(s_next)) {
     if constexpr (FUSED) {
       if (id < n_app) {
-        first = false;
         fused_append_task<G, GROUP, NW>(kp, layer, id, smem, smem_u32(merge_bar), merge_phase, waited, k_new, v_new);
         fence_proxy_async();  // generic use of the memory is over before later bulk copies
         continue;
       }
     }
     const int ix = id - n_app;
-    const DecodeItem it = first ? fwp->it : reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
-    const DecodeReq dr = first ? fwp->dr : reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
+    const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
+    const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
     // rows this launch's append tasks of (request, kv-head) write: an item marked dependent
     // waits for them first; INT2 pages at or above H_pre are waited for per warp
@@ -793,15 +779,10 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
       const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
       for (int k = 0; k < min(kStages, n_my); ++k) {
         const int lp = it.begin + warp + kWarps * k;
-        if (first) {  // the table holds the pages that may be copied before the wait
-          if (int2_issue_phys<G, GROUP, NW>(kp, layer, it, fwp->page[warp + kWarps * k], k, smem)) pre_mask |= 1u << k;
-        } else if (((waited && !pending) || (lp + 1) * kPage <= dr.H_pre) &&
-                   int2_issue_page<G, GROUP, NW>(kp, layer, it, dr, k, smem)) {
+        if (((waited && !pending) || (lp + 1) * kPage <= dr.H_pre) && int2_issue_page<G, GROUP, NW>(kp, layer, it, dr, k, smem))
           pre_mask |= 1u << k;
-        }
       }
     }
-    first = false;
     if (threadIdx.x == 0 && ix == it.head_first)  // R_V^T for the merge of this (request, kv-head)
       bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                            (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim,

@@ -123,7 +123,6 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.decode_items = take(L.max_decode_items * sizeof(DecodeItem));
   L.decode_order = take(L.max_decode_items * 4);
   L.sched = take(16);
-  L.first_work = take(2 * kMaxPositions * sizeof(FirstWork));
   L.app_done = take(layers * reqs * Hkv * 8);
   L.total = off;
   return L;
@@ -151,7 +150,6 @@ struct oscar_cache {
   size_t staging_bytes = 0;
   uint32_t* h_status = nullptr;
   int32_t* h_counts = nullptr;  // pinned: plan_counts as uploaded
-  FirstWork* h_first = nullptr;  // pinned: [2][kMaxPositions] first work of the planned launches
   cudaEvent_t upload_done = nullptr;
   bool upload_pending = false;
   // pending append
@@ -266,8 +264,6 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_staging), c->staging_bytes);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_status), 256);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_counts), 64);
-  if (e == cudaSuccess)
-    e = cudaMallocHost(reinterpret_cast<void**>(&c->h_first), 2 * kMaxPositions * sizeof(FirstWork));
   if (e == cudaSuccess) std::memset(c->h_counts, 0, 64);
   if (e == cudaSuccess) e = cudaMemset(c->base + lay.plan_counts, 0, 16);
   if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->upload_done, cudaEventDisableTiming);
@@ -306,7 +302,6 @@ void oscar_cache_destroy(oscar_cache* c) {
   if (c->h_staging) cudaFreeHost(c->h_staging);
   if (c->h_status) cudaFreeHost(c->h_status);
   if (c->h_counts) cudaFreeHost(c->h_counts);
-  if (c->h_first) cudaFreeHost(c->h_first);
   delete c;
 }
 
@@ -773,44 +768,6 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_reqs, c->h_staging, rb, cudaMemcpyHostToDevice, s));
   CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_items, c->h_staging + align256(rb), items.size() * sizeof(DecodeItem),
                            cudaMemcpyHostToDevice, s));
-  // the first work of every CTA position of the launches this plan serves (INT2 split
-  // kernel): a decode launch and, with a reservation, a fused one
-  if (is_int2(c)) {
-    const int resident = decode_resident_ctas(G, c->cfg.group, wide, c->n_sm);
-    const int npos = std::min(std::max(resident, 0), kMaxPositions);
-    for (int f = 0; f < (c->reserved ? 2 : 1); ++f) {
-      const int n_tasks = f ? c->app_items * Hkv * 2 * append_task_split(nw) : 0;
-      const int n_all = int(items.size()) + n_tasks;
-      const bool one_wave = n_all <= resident;
-      FirstWork* fw = c->h_first + size_t(f) * kMaxPositions;
-      for (int p = 0; p < npos; ++p) {
-        // the position's work id, as the kernel's work queue hands it out
-        int id = -1;
-        if (p < n_all) {
-          if (one_wave) id = p;
-          else if (p < n_front) id = n_tasks + order[p];
-          else if (p < n_front + n_tasks) id = p - n_front;
-          else id = n_tasks + order[p - n_tasks];
-        }
-        FirstWork& w = fw[p];
-        std::memset(&w, 0, sizeof(w));
-        w.id = id;
-        w.ix = id - n_tasks;
-        for (int i = 0; i < kPrePages; ++i) w.page[i] = -1;
-        if (id < n_tasks) continue;
-        w.it = items[w.ix];
-        w.dr = reqs[w.it.req];
-        if (w.it.kind != 0 || w.dr.slot < 0) continue;
-        const std::vector<int>& pg = c->reqs[w.dr.slot].pages;
-        for (int i = 0; i < kPrePages && w.it.begin + i < w.it.end; ++i) {
-          const int lp = w.it.begin + i;
-          if ((lp + 1) * kPage <= w.dr.H_pre && lp < int(pg.size())) w.page[i] = pg[lp];
-        }
-      }
-      CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.first_work + size_t(f) * kMaxPositions * sizeof(FirstWork), fw,
-                               size_t(npos) * sizeof(FirstWork), cudaMemcpyHostToDevice, s));
-    }
-  }
   CUDA_TRY(cudaEventRecord(c->upload_done, s));
   c->upload_pending = true;
   DecodeWorkspace w;

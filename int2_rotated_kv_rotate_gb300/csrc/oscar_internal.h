@@ -65,24 +65,6 @@ struct DecodeItem {
 };
 constexpr int kDepNone = 0, kDepRing = 1, kDepPages = 2;
 
-// The first work of each CTA position of a split-kernel launch, self-contained, so that a
-// CTA starts its first copies after one load (the CTAs of a launch mostly start as the
-// preceding kernel ends, and each dependent load in front of the wait on it delays the
-// whole launch).  Two tables: [0] for decode launches, [1] for fused append + decode
-// launches (the reservation's append tasks come first).
-constexpr int kMaxPositions = 512;  // CTAs of a launch (at most two per SM)
-constexpr int kPrePages = 32;       // the first two pages of each of at most 16 warps
-struct FirstWork {
-  int id;  // work id (task t < n_tasks, else n_tasks + item index), -1: no work
-  int ix;  // item index (items)
-  DecodeItem it;
-  DecodeReq dr;
-  int page[kPrePages];  // INT2 items: physical page of the item's page it.begin + i if it may
-                        // be copied before the wait, else -1 (warp w's stage k is i = w + NW k)
-  int pad[2];
-};
-static_assert(sizeof(FirstWork) % 16 == 0, "first-work entries are read as 16-byte words");
-
 #ifdef __CUDACC__
 #define OSCAR_HOST_DEVICE __host__ __device__
 #else
@@ -113,7 +95,6 @@ struct DeviceLayout {
   size_t append_reqs, append_items, decode_reqs, decode_items;
   size_t decode_order;  // int32 [max_decode_items]: items in the order CTAs take them (largest first)
   size_t sched;         // uint32 [4]: dynamic work counter, CTA exit counter (self-resetting)
-  size_t first_work;    // FirstWork [2][kMaxPositions]: decode launches, fused launches
   size_t app_done;      // uint32 [layer][max_requests][H_kv][2]: append tasks of the running fused
                         // launch that have stored their sink and ring rows ([0]) and their INT2
                         // rows ([1]); the request's final merge takes the launch's count off again

@@ -346,22 +346,19 @@ def test_bf16_comparison_path(gqa):
 
 
 def test_bad_page_entry_is_flagged_not_faulting():
-    """A page-table entry out of range (written on the host) is skipped and flagged.  The
-    pages a CTA copies before the wait on the preceding kernel come from the plan (the host's
-    page lists); the entry corrupted here is one that a warp looks up in the device table
-    (an item of 64 pages has more pages than the first two stages of its warps)."""
+    """A page-table entry out of range (written on the host) is skipped and flagged."""
     w = wl.WORKLOADS["tiny"]
-    cache, oc, _ = make_pair(w, SEED, 1, 1, 4096)
+    cache, oc, _ = make_pair(w, SEED, 1, 1, 1024)
     slot = cache.alloc()
-    cache.reserve([slot], [4096])
-    append_both(cache, oc, w, 0, [slot], [0], [0], [4096])
+    cache.reserve([slot], [1024])
+    append_both(cache, oc, w, 0, [slot], [0], [0], [1024])
     cache.commit()
     torch.cuda.synchronize()
-    # corrupt logical page 40 of the request in the device page table (host-side write)
+    # corrupt logical page 3 of the request in the device page table (host-side write)
     row = cache.layout.page_table + slot * cache.cfg.max_pages_per_request * 4
     bad = torch.tensor([cache.cfg.max_pages + 5], dtype=torch.int32).view(torch.uint8).cuda()
-    cache.mem[row + 40 * 4: row + 41 * 4] = bad
-    cache.plan([slot], max_split_pages=64)
+    cache.mem[row + 3 * 4: row + 4 * 4] = bad
+    cache.plan([slot], max_split_pages=2)
     q = wl.gen_q(w, SEED, 0, 0, 1, device="cuda")
     out = cache.decode(0, q)
     st, flags = cache.status()
