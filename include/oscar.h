@@ -171,6 +171,12 @@ oscar_status oscar_plan_decode_ex(oscar_cache* cache, const int* slots, int n_re
 /* Decode workspace bytes for the current plan (0 without a plan). */
 size_t oscar_decode_workspace_bytes(const oscar_cache* cache);
 
+/* Decode workspace bytes that cover every plan of this cache (0 for NULL).  A launch
+ * captured into a CUDA graph keeps the workspace pointer it was given, and a replay after
+ * a later plan writes that plan's partial results through it: a workspace of this size
+ * keeps such replays in bounds whatever the later plans are. */
+size_t oscar_decode_workspace_max_bytes(const oscar_cache* cache);
+
 /* Number of split-K work items of the current plan, and of them BF16 (sink/ring) items. */
 oscar_status oscar_plan_info(const oscar_cache* cache, int* n_items, int* n_bf16_items, int* max_item_pages);
 

@@ -46,7 +46,8 @@ EXPORTS = [
     "oscar_cache_device_bytes", "oscar_cache_create", "oscar_cache_destroy", "oscar_cache_layout",
     "oscar_set_layer_params", "oscar_request_alloc", "oscar_request_free", "oscar_request_info",
     "oscar_request_pages", "oscar_request_share_prefix", "oscar_reserve", "oscar_quantize_append",
-    "oscar_commit_append", "oscar_plan_decode", "oscar_plan_decode_ex", "oscar_decode_workspace_bytes", "oscar_plan_info",
+    "oscar_commit_append", "oscar_plan_decode", "oscar_plan_decode_ex", "oscar_decode_workspace_bytes",
+    "oscar_decode_workspace_max_bytes", "oscar_plan_info",
     "oscar_decode_attention", "oscar_append_decode_attention", "oscar_decode_attention_noalloc", "oscar_bf16_append", "oscar_bf16_decode_attention", "oscar_get_status",
     "oscar_last_error", "oscar_last_launch_count",
 ]
@@ -83,6 +84,7 @@ def lib() -> ctypes.CDLL:
                 "oscar_plan_decode": (I, [P, IP, I, I, P]),
                 "oscar_plan_decode_ex": (I, [P, IP, I, I, ctypes.c_uint32, P]),
                 "oscar_decode_workspace_bytes": (S, [P]),
+                "oscar_decode_workspace_max_bytes": (S, [P]),
                 "oscar_plan_info": (I, [P, IP, IP, IP]),
                 "oscar_decode_attention": (I, [P, I, P, P, P, S, P, P]),
                 "oscar_append_decode_attention": (I, [P, I, P, P, P, P, P, S, P, P]),
@@ -218,6 +220,10 @@ def oscar_plan_decode_ex(handle: int, slots, max_split_pages: int = 0, flags: in
 
 def oscar_decode_workspace_bytes(handle: int) -> int:
     return int(lib().oscar_decode_workspace_bytes(handle))
+
+
+def oscar_decode_workspace_max_bytes(handle: int) -> int:
+    return int(lib().oscar_decode_workspace_max_bytes(handle))
 
 
 def oscar_plan_info(handle: int):

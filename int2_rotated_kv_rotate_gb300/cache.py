@@ -97,7 +97,10 @@ class KVCache:
         self._n_plan = len(list(slots))
         need = N.oscar_decode_workspace_bytes(self.handle)
         if self.workspace is None or self.workspace.numel() < need:
-            self.workspace = torch.empty(max(need, 256), dtype=torch.uint8, device=self.device)
+            # sized for every plan of the cache, once: launches captured into a graph keep
+            # this pointer across later plans
+            full = N.oscar_decode_workspace_max_bytes(self.handle)
+            self.workspace = torch.empty(max(need, full, 256), dtype=torch.uint8, device=self.device)
         return need
 
     def plan_info(self):

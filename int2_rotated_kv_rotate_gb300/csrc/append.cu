@@ -34,7 +34,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
   const int kvh = blockIdx.y, kv = blockIdx.z;
   const float* R = reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.R_V : kp.lay.R_K)) +
                    (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
-  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[0];
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.append_counts)[0];
   const bool work = int(blockIdx.x) < n_items;
   if (threadIdx.x == 0 && work) {
     mbar_init(smem_u32(bar), 1);
@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(128) bf16_append_kernel(KernelParams kp, int l
                                                           const uint16_t* __restrict__ v_new) {
   pdl_wait();
   pdl_trigger();
-  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[0];
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.append_counts)[0];
   for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
   const AppendItem it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
   const AppendReq a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];

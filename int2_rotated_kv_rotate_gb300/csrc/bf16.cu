@@ -37,15 +37,14 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
   uint32_t slab_phase = 0;
   pdl_wait();
   pdl_trigger();
-  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts)[1];
-  const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
-                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, 0, n_items};
+  const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.decode_counts)[0];
+  const WorkQueue wq{reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, 0, n_items};
   int* s_next = s_last_p + 1;
   for (int ix = wq.first(); ix >= 0; ix = wq.next(s_next)) {
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-    uint8_t* part = partials + size_t(ix) * PartialSlot<G>::kBytes;
+    uint8_t* part = partials + size_t(it.slot) * PartialSlot<G>::kBytes;
     for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[(e / kHeadDim) * kQRow + e % kHeadDim] = bf16_f32(q[head0 * kHeadDim + e]);
     __syncthreads();
     const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;

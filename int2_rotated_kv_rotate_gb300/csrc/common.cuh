@@ -468,26 +468,24 @@ __device__ bool merge_partial(const KernelParams& kp, const DecodeItem& it, cons
 // b (known before any wait, so its copies can be issued early), then the next free
 // position gridDim.x + atomicAdd(work counter).  The last CTA to leave resets both counters
 // for the next launch (launches of one cache never overlap).  A plan of at most one
-// position per CTA uses neither counter.  Call from all threads.
+// position per CTA uses neither counter.  Items are stored in the order they are taken
+// (those that wait on no task first).  Call from all threads.
 struct WorkQueue {
-  const int* order;
   unsigned* counters;  // [0] work, [1] exit
-  int n_items;         // entries of order[]
+  int n_items;         // stored items
   int n_tasks;         // work ids 0 .. n_tasks - 1 that are not items (fused append tasks)
-  int n_front;         // order[] entries handed out before the tasks (items that wait on none)
+  int n_front;         // items that wait on no task (stored first)
   // One wave (every position has its own CTA): no counters, position b is CTA b's, tasks
-  // first.  Several waves: the items that wait on nothing (largest first), the tasks, then
-  // the items that wait on tasks, so that every task is handed out before any item that
-  // may wait on it.
+  // first.  Several waves: the items that wait on nothing, the tasks, then the items that
+  // wait on tasks, so that every task is handed out before any item that may wait on it.
   __device__ int n() const { return n_items + n_tasks; }
   __device__ bool one_wave() const { return n() <= int(gridDim.x); }
   // Work id of position p: a task t < n_tasks, or n_tasks + item index.
   __device__ int id_of(int p) const {
     if (p >= n()) return -1;
-    if (one_wave()) return p;
-    if (p < n_front) return n_tasks + order[p];
-    if (p < n_front + n_tasks) return p - n_front;
-    return n_tasks + order[p - n_tasks];
+    if (one_wave() || p >= n_front + n_tasks) return p;
+    if (p < n_front) return n_tasks + p;
+    return p - n_front;
   }
   __device__ int first() const { return id_of(int(blockIdx.x)); }
   __device__ int next(int* s_slot) const {

@@ -743,11 +743,12 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
   // pages, only those wholly below H_pre are final before the wait (a preceding append may
   // still be writing the rest), so the first item copies those early.  Fused launches put
   // the reservation's append tasks (item x kv-head x K|V) ahead of the decode items.
-  const int* counts = reinterpret_cast<const int*>(kp.base + kp.lay.plan_counts);
-  const int n_items = counts[1];
-  const int n_app = fused ? counts[0] * kp.n_kv_heads * 2 * append_task_split(NW) : 0;
-  const WorkQueue wq{reinterpret_cast<const int*>(kp.base + kp.lay.decode_order),
-                     reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, n_app, counts[3]};
+  const int* counts = reinterpret_cast<const int*>(kp.base + kp.lay.decode_counts);
+  const int n_items = counts[0];
+  const int n_app =
+      fused ? reinterpret_cast<const int*>(kp.base + kp.lay.append_counts)[0] * kp.n_kv_heads * 2 * append_task_split(NW)
+            : 0;
+  const WorkQueue wq{reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, n_app, counts[2]};
   unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
   bool waited = false;
   uint32_t phase_bits = 0, merge_phase = 0, slab_phase = 0;
@@ -783,7 +784,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
           pre_mask |= 1u << k;
       }
     }
-    if (threadIdx.x == 0 && ix == it.head_first)  // R_V^T for the merge of this (request, kv-head)
+    if (threadIdx.x == 0 && it.slot == it.head_first)  // R_V^T for the merge of this (request, kv-head)
       bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                            (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim,
                        kHeadDim * kHeadDim * 4);
@@ -805,7 +806,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
       fence_proxy_async_global();  // the append's rows, seen through the acquire, before bulk copies
     };
     if (it.kind == 0) wait_dep();
-    uint8_t* part = partials + size_t(ix) * PartialSlot<G>::kBytes;
+    uint8_t* part = partials + size_t(it.slot) * PartialSlot<G>::kBytes;
     if (!slot_ok) {
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
       for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) store_slot<G>(part, e / kHeadDim, e % kHeadDim, -INFINITY, 0.f, 0.f);

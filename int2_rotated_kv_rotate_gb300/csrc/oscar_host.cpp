@@ -19,6 +19,8 @@
 
 using namespace oscar;
 
+constexpr int kUploadSlots = 6;  // pinned upload buffers (two uploads per step: reserve, plan)
+
 namespace {
 
 thread_local std::string g_error;
@@ -42,6 +44,9 @@ oscar_status fail(oscar_status st, const char* fmt, ...) {
   } while (0)
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+// offsets of the items inside a plan block (counts at 0, requests at 256)
+size_t append_items_offset(size_t reqs) { return 256 + align256(reqs * sizeof(AppendReq)); }
+size_t decode_items_offset(size_t reqs) { return 256 + align256(reqs * sizeof(DecodeReq)); }
 int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 constexpr int kAppendChunk = 16;     // tokens (or ring slots) per append work item
@@ -114,14 +119,16 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.page_table = take(reqs * size_t(c.max_pages_per_request) * 4);
   L.status = take(256);
   L.counters = take(reqs * Hkv * 4);
-  L.plan_counts = take(16);
   L.max_append_items = kMaxAppendTokenItems + reqs * (kMaxWindow / kAppendChunk);
   L.max_decode_items = reqs * Hkv * (2 + kMaxWindow / kBf16ItemTokens) + 16384;
-  L.append_reqs = take(reqs * sizeof(AppendReq));
-  L.append_items = take(L.max_append_items * sizeof(AppendItem));
-  L.decode_reqs = take(reqs * sizeof(DecodeReq));
-  L.decode_items = take(L.max_decode_items * sizeof(DecodeItem));
-  L.decode_order = take(L.max_decode_items * 4);
+  L.append_plan = take(append_items_offset(reqs) + L.max_append_items * sizeof(AppendItem));
+  L.append_counts = L.append_plan;
+  L.append_reqs = L.append_plan + 256;
+  L.append_items = L.append_plan + append_items_offset(reqs);
+  L.decode_plan = take(decode_items_offset(reqs) + L.max_decode_items * sizeof(DecodeItem));
+  L.decode_counts = L.decode_plan;
+  L.decode_reqs = L.decode_plan + 256;
+  L.decode_items = L.decode_plan + decode_items_offset(reqs);
   L.sched = take(16);
   L.app_done = take(layers * reqs * Hkv * 8);
   L.total = off;
@@ -144,14 +151,16 @@ struct oscar_cache {
   std::vector<Request> reqs;
   std::vector<int> refcount;
   std::vector<int> free_pages;
-  // pinned host mirrors / staging
+  // host mirror of the page table, and a ring of pinned upload buffers: every upload copies
+  // what it sends into the next buffer first, so the host never rewrites memory that an
+  // enqueued copy still reads, and waits only when it runs kUploadSlots uploads ahead
   int32_t* h_page_table = nullptr;
-  uint8_t* h_staging = nullptr;
-  size_t staging_bytes = 0;
+  uint8_t* h_upload = nullptr;  // kUploadSlots x upload_bytes, pinned
+  size_t upload_bytes = 0, staging_bytes = 0;
+  cudaEvent_t upload_done[kUploadSlots] = {};
+  bool upload_pending[kUploadSlots] = {};
+  int upload_next = 0;
   uint32_t* h_status = nullptr;
-  int32_t* h_counts = nullptr;  // pinned: plan_counts as uploaded
-  cudaEvent_t upload_done = nullptr;
-  bool upload_pending = false;
   // pending append
   bool reserved = false;
   std::vector<AppendReq> app_reqs;
@@ -167,6 +176,13 @@ struct oscar_cache {
 };
 
 namespace {
+
+// One upload buffer: page-table rows (max_requests rows), then the image of a plan block.
+struct Upload {
+  int32_t* rows;
+  uint8_t* staging;
+  int slot;
+};
 
 KernelParams kernel_params(const oscar_cache* c) {
   KernelParams kp;
@@ -185,20 +201,45 @@ KernelParams kernel_params(const oscar_cache* c) {
   return kp;
 }
 
-// The pinned staging buffers are rewritten only after the previous uploads finished.
-oscar_status wait_uploads(oscar_cache* c) {
-  if (c->upload_pending) {
-    CUDA_TRY(cudaEventSynchronize(c->upload_done));
-    c->upload_pending = false;
+// The next upload buffer of the ring, once the copies that last read it have run.
+oscar_status begin_upload(oscar_cache* c, Upload* u) {
+  const int i = c->upload_next;
+  c->upload_next = (i + 1) % kUploadSlots;
+  if (c->upload_pending[i]) {
+    CUDA_TRY(cudaEventSynchronize(c->upload_done[i]));
+    c->upload_pending[i] = false;
   }
+  uint8_t* b = c->h_upload + size_t(i) * c->upload_bytes;
+  u->rows = reinterpret_cast<int32_t*>(b);
+  u->staging = b + align256(size_t(c->cfg.max_requests) * c->cfg.max_pages_per_request * 4);
+  u->slot = i;
   return OSCAR_OK;
 }
 
-oscar_status upload_rows(oscar_cache* c, const std::vector<int>& slots, cudaStream_t s) {
-  const size_t row = size_t(c->cfg.max_pages_per_request) * 4;
-  for (int slot : slots) {
-    CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.page_table + slot * row, c->h_page_table + size_t(slot) * c->cfg.max_pages_per_request,
-                             row, cudaMemcpyHostToDevice, s));
+// Record that the copies enqueued on s so far read upload buffer u.
+oscar_status end_upload(oscar_cache* c, const Upload& u, cudaStream_t s) {
+  CUDA_TRY(cudaEventRecord(c->upload_done[u.slot], s));
+  c->upload_pending[u.slot] = true;
+  return OSCAR_OK;
+}
+
+// Every upload buffer is free again (teardown).
+void drain_uploads(oscar_cache* c) {
+  for (int i = 0; i < kUploadSlots; ++i)
+    if (c->upload_pending[i]) {
+      cudaEventSynchronize(c->upload_done[i]);
+      c->upload_pending[i] = false;
+    }
+}
+
+// Page-table rows of `slots` from the host mirror, through upload buffer u.
+oscar_status upload_rows(oscar_cache* c, const Upload& u, const std::vector<int>& slots, cudaStream_t s) {
+  const size_t n = size_t(c->cfg.max_pages_per_request);
+  for (size_t k = 0; k < slots.size(); ++k) {
+    int32_t* dst = u.rows + k * n;
+    std::memcpy(dst, c->h_page_table + size_t(slots[k]) * n, n * 4);
+    CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.page_table + size_t(slots[k]) * n * 4, dst, n * 4,
+                             cudaMemcpyHostToDevice, s));
   }
   return OSCAR_OK;
 }
@@ -257,16 +298,17 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   c->free_pages.reserve(cfg->max_pages);
   for (int p = cfg->max_pages - 1; p >= 0; --p) c->free_pages.push_back(p);
   const size_t pt_bytes = size_t(cfg->max_requests) * cfg->max_pages_per_request * 4;
-  c->staging_bytes = align256(size_t(cfg->max_requests) * std::max(sizeof(AppendReq), sizeof(DecodeReq))) +
-                     std::max(lay.max_append_items * sizeof(AppendItem),
-                              align256(lay.max_decode_items * sizeof(DecodeItem)) + lay.max_decode_items * 4);
+  // a plan block's image (the larger of the two)
+  c->staging_bytes = std::max(append_items_offset(cfg->max_requests) + lay.max_append_items * sizeof(AppendItem),
+                              decode_items_offset(cfg->max_requests) + lay.max_decode_items * sizeof(DecodeItem));
+  c->upload_bytes = align256(pt_bytes) + align256(c->staging_bytes);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_page_table), pt_bytes);
-  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_staging), c->staging_bytes);
+  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_upload), kUploadSlots * c->upload_bytes);
   if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_status), 256);
-  if (e == cudaSuccess) e = cudaMallocHost(reinterpret_cast<void**>(&c->h_counts), 64);
-  if (e == cudaSuccess) std::memset(c->h_counts, 0, 64);
-  if (e == cudaSuccess) e = cudaMemset(c->base + lay.plan_counts, 0, 16);
-  if (e == cudaSuccess) e = cudaEventCreateWithFlags(&c->upload_done, cudaEventDisableTiming);
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.append_counts, 0, 16);
+  if (e == cudaSuccess) e = cudaMemset(c->base + lay.decode_counts, 0, 16);
+  for (int i = 0; i < kUploadSlots && e == cudaSuccess; ++i)
+    e = cudaEventCreateWithFlags(&c->upload_done[i], cudaEventDisableTiming);
   if (e == cudaSuccess) {
     std::memset(c->h_page_table, 0xff, pt_bytes);  // -1 = unmapped
     e = cudaMemcpy(c->base + lay.page_table, c->h_page_table, pt_bytes, cudaMemcpyHostToDevice);
@@ -294,14 +336,12 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
 
 void oscar_cache_destroy(oscar_cache* c) {
   if (!c) return;
-  if (c->upload_done) {
-    cudaEventSynchronize(c->upload_done);
-    cudaEventDestroy(c->upload_done);
-  }
+  drain_uploads(c);
+  for (int i = 0; i < kUploadSlots; ++i)
+    if (c->upload_done[i]) cudaEventDestroy(c->upload_done[i]);
   if (c->h_page_table) cudaFreeHost(c->h_page_table);
-  if (c->h_staging) cudaFreeHost(c->h_staging);
+  if (c->h_upload) cudaFreeHost(c->h_upload);
   if (c->h_status) cudaFreeHost(c->h_status);
-  if (c->h_counts) cudaFreeHost(c->h_counts);
   delete c;
 }
 
@@ -373,8 +413,6 @@ oscar_status oscar_request_free(oscar_cache* c, int slot) {
   for (int p : r.pages)
     if (--c->refcount[p] == 0) c->free_pages.push_back(p);
   // the device row keeps stale ids; it is rewritten before the slot is used again
-  st = wait_uploads(c);
-  if (st) return st;
   std::fill(c->h_page_table + size_t(slot) * c->cfg.max_pages_per_request,
             c->h_page_table + size_t(slot + 1) * c->cfg.max_pages_per_request, -1);
   r = Request();
@@ -416,7 +454,8 @@ oscar_status oscar_request_share_prefix(oscar_cache* c, int dst, int src, int n_
   if (n_tokens > limit)
     return fail(OSCAR_ERR_INVALID_ARG, "n_tokens %d exceeds the shareable prefix %d of src", n_tokens, limit);
   if (n_tokens / kPage > c->cfg.max_pages_per_request) return fail(OSCAR_ERR_INVALID_ARG, "prefix too long");
-  st = wait_uploads(c);
+  Upload u;
+  st = begin_upload(c, &u);
   if (st) return st;
   cudaStream_t strm = static_cast<cudaStream_t>(stream);
   const int n = n_tokens / kPage;
@@ -427,15 +466,15 @@ oscar_status oscar_request_share_prefix(oscar_cache* c, int dst, int src, int n_
   std::copy(d.pages.begin(), d.pages.end(), row);
   d.L = n_tokens;
   d.H = is_int2(c) ? n_tokens : n_tokens;
-  st = upload_rows(c, {dst}, strm);
+  st = upload_rows(c, u, {dst}, strm);
   if (st) return st;
   if (is_int2(c) && c->lay.sink_slot_stride > 0) {
     CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.sink + size_t(dst) * c->lay.sink_slot_stride,
                              c->base + c->lay.sink + size_t(src) * c->lay.sink_slot_stride, c->lay.sink_slot_stride,
                              cudaMemcpyDeviceToDevice, strm));
   }
-  CUDA_TRY(cudaEventRecord(c->upload_done, strm));
-  c->upload_pending = true;
+  st = end_upload(c, u, strm);
+  if (st) return st;
   c->planned = false;
   return OSCAR_OK;
 }
@@ -491,7 +530,8 @@ oscar_status oscar_reserve(oscar_cache* c, const int* slots, const int* n_new, i
   }
   if (items.size() > c->lay.max_append_items)
     return fail(OSCAR_ERR_INVALID_ARG, "append of %lld tokens is too large for one reservation; split it", rows);
-  oscar_status st = wait_uploads(c);
+  Upload u;
+  oscar_status st = begin_upload(c, &u);
   if (st) return st;
   // allocate pages and update the host mirror
   std::vector<int> changed;
@@ -511,19 +551,19 @@ oscar_status oscar_reserve(oscar_cache* c, const int* slots, const int* n_new, i
     }
   }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  st = upload_rows(c, changed, s);
+  st = upload_rows(c, u, changed, s);
   if (st) return st;
-  std::memcpy(c->h_staging, reqs.data(), reqs.size() * sizeof(AppendReq));
-  std::memcpy(c->h_staging + align256(reqs.size() * sizeof(AppendReq)), items.data(), items.size() * sizeof(AppendItem));
-  c->h_counts[0] = int(items.size());
-  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.plan_counts, c->h_counts, 4, cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.append_reqs, c->h_staging, reqs.size() * sizeof(AppendReq),
+  // the append plan block, one copy
+  const size_t items_off = append_items_offset(c->cfg.max_requests);
+  int32_t* counts = reinterpret_cast<int32_t*>(u.staging);
+  counts[0] = int(items.size());
+  counts[1] = counts[2] = counts[3] = 0;
+  std::memcpy(u.staging + 256, reqs.data(), reqs.size() * sizeof(AppendReq));
+  std::memcpy(u.staging + items_off, items.data(), items.size() * sizeof(AppendItem));
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.append_plan, u.staging, items_off + items.size() * sizeof(AppendItem),
                            cudaMemcpyHostToDevice, s));
-  if (!items.empty())
-    CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.append_items, c->h_staging + align256(reqs.size() * sizeof(AppendReq)),
-                             items.size() * sizeof(AppendItem), cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaEventRecord(c->upload_done, s));
-  c->upload_pending = true;
+  st = end_upload(c, u, s);
+  if (st) return st;
   c->app_reqs = reqs;
   c->app_req_items.assign(reqs.size(), 0);
   for (const AppendItem& it : items) ++c->app_req_items[it.req];
@@ -752,24 +792,28 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   });
   int n_front = 0;
   while (n_front < int(order.size()) && items[order[n_front]].dep == kDepNone) ++n_front;
-  oscar_status st = wait_uploads(c);
+  Upload u;
+  oscar_status st = begin_upload(c, &u);
   if (st) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const size_t rb = reqs.size() * sizeof(DecodeReq);
-  std::memcpy(c->h_staging, reqs.data(), rb);
-  std::memcpy(c->h_staging + align256(rb), items.data(), items.size() * sizeof(DecodeItem));
-  uint8_t* h_order = c->h_staging + align256(rb) + align256(items.size() * sizeof(DecodeItem));
-  std::memcpy(h_order, order.data(), order.size() * 4);
-  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_order, h_order, order.size() * 4, cudaMemcpyHostToDevice, s));
-  c->h_counts[1] = int(items.size());
-  c->h_counts[2] = n_req;
-  c->h_counts[3] = n_front;
-  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.plan_counts + 4, c->h_counts + 1, 12, cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_reqs, c->h_staging, rb, cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_items, c->h_staging + align256(rb), items.size() * sizeof(DecodeItem),
+  // the decode plan block, one copy: the items in the order CTAs take them, each with its
+  // partial slot (its index above)
+  const size_t items_off = decode_items_offset(c->cfg.max_requests);
+  int32_t* counts = reinterpret_cast<int32_t*>(u.staging);
+  counts[0] = int(items.size());
+  counts[1] = n_req;
+  counts[2] = n_front;
+  counts[3] = 0;
+  std::memcpy(u.staging + 256, reqs.data(), reqs.size() * sizeof(DecodeReq));
+  DecodeItem* staged = reinterpret_cast<DecodeItem*>(u.staging + items_off);
+  for (size_t k = 0; k < order.size(); ++k) {
+    staged[k] = items[order[k]];
+    staged[k].slot = order[k];
+  }
+  CUDA_TRY(cudaMemcpyAsync(c->base + c->lay.decode_plan, u.staging, items_off + items.size() * sizeof(DecodeItem),
                            cudaMemcpyHostToDevice, s));
-  CUDA_TRY(cudaEventRecord(c->upload_done, s));
-  c->upload_pending = true;
+  st = end_upload(c, u, s);
+  if (st) return st;
   DecodeWorkspace w;
   size_t off = 0;
   w.partials = off;
@@ -788,6 +832,12 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
 }
 
 size_t oscar_decode_workspace_bytes(const oscar_cache* c) { return (c && c->planned) ? c->ws.total : 0; }
+
+size_t oscar_decode_workspace_max_bytes(const oscar_cache* c) {
+  if (!c) return 0;
+  const size_t G = size_t(c->cfg.n_q_heads / c->cfg.n_kv_heads);
+  return align256(c->lay.max_decode_items * G * (8 + 4 * kHeadDim));
+}
 
 oscar_status oscar_plan_info(const oscar_cache* c, int* n_items, int* n_bf16_items, int* max_item_pages) {
   if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");

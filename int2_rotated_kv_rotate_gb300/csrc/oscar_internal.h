@@ -47,8 +47,10 @@ struct DecodeReq {
 
 // One split-K work item: pages [p0, p1) of the INT2 history (kind 0) or BF16 tokens
 // [t0, t1) of the sink+ring list (kind 1; index < S is sink j, else ring position H + j - S)
-// of request `req` (plan index), kv-head `kvh`.  Partial results go to slot `item`; the
-// last CTA to finish an item of (req, kvh) merges the head_count slots from head_first.
+// of request `req` (plan index), kv-head `kvh`.  Partial results go to partial slot
+// `slot`; the last CTA to finish an item of (req, kvh) merges the head_count slots from
+// head_first.  A plan stores its items in the order CTAs take them: the items that wait
+// on no append task first, largest first.
 struct DecodeItem {
   int req;
   int kvh;
@@ -62,6 +64,7 @@ struct DecodeItem {
                    // that receive evicted or new tokens)
   int split;       // BF16 items: list index from which rows may be written by this step's
                    // append (rows before it may be copied before the wait); INT2 items: end
+  int slot;        // partial slot: the item's index in the plan's (request, kv-head) order
 };
 constexpr int kDepNone = 0, kDepRing = 1, kDepPages = 2;
 
@@ -90,10 +93,11 @@ struct DeviceLayout {
   size_t page_table;  // int32 [max_requests][max_pages_per_request]
   size_t status;      // uint32 flags
   size_t counters;    // uint32 [max_requests][H_kv] merge counters (second level)
-  size_t plan_counts; // int32 [4]: append items, decode items, decode requests, decode items
-                      // that wait on no append task (the first entries of decode_order)
-  size_t append_reqs, append_items, decode_reqs, decode_items;
-  size_t decode_order;  // int32 [max_decode_items]: items in the order CTAs take them (largest first)
+  // the append and the decode plan, each one block that one copy uploads: int32 counts[4]
+  // at +0, the requests at +256, the items after them.  Append counts: items.  Decode
+  // counts: items, requests, items that wait on no append task (stored first).
+  size_t append_plan, append_counts, append_reqs, append_items;
+  size_t decode_plan, decode_counts, decode_reqs, decode_items;
   size_t sched;         // uint32 [4]: dynamic work counter, CTA exit counter (self-resetting)
   size_t app_done;      // uint32 [layer][max_requests][H_kv][2]: append tasks of the running fused
                         // launch that have stored their sink and ring rows ([0]) and their INT2
@@ -117,7 +121,7 @@ struct DecodeWorkspace {
 };
 
 // Launchers (defined in the .cu files); return a cudaError_t as int.
-// Work-item counts live in device memory (plan_counts); `grid` is the number of CTAs the
+// Work-item counts live in device memory (the plan blocks); `grid` is the number of CTAs the
 // host launches, each CTA loops over items blockIdx.x, + gridDim.x, ... so a captured
 // launch stays valid when a later plan has a different item count.
 int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid, void* stream,

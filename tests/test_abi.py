@@ -65,5 +65,7 @@ def test_device_bytes_and_invalid_configs(lib):
 def test_null_handles_are_rejected(lib):
     assert lib.oscar_commit_append(None) == 1
     assert lib.oscar_decode_workspace_bytes(None) == 0
+    lib.oscar_decode_workspace_max_bytes.restype = ctypes.c_size_t
+    assert lib.oscar_decode_workspace_max_bytes(None) == 0
     s = ctypes.c_int()
     assert lib.oscar_request_alloc(None, ctypes.byref(s)) == 1
