@@ -687,7 +687,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   // CTA shape: at GQA 4 a step that one wave of 16-warp CTAs holds (one per SM) is planned
   // for them ("wide"); larger steps for 8-warp CTAs, two per SM.
   constexpr long long kItemBytes = 512 << 10;
-  constexpr long long kWaves = 4;
+  constexpr long long kWaves = 2;
   const int G = c->cfg.n_q_heads / Hkv;
   bool wide = false;
   if (is_int2(c) && G == 4 && !(flags & OSCAR_PLAN_NARROW)) {

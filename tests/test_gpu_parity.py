@@ -299,7 +299,7 @@ def test_fused_append_decode_needs_a_covering_plan():
 @pytest.mark.parametrize("gqa,narrow", [(4, False), (4, True), (8, False)])
 def test_plans_larger_than_one_wave(gqa, narrow):
     """Single-page items, several times more than the CTAs resident at once: the CTAs take
-    items from the shared work counter, merge in two levels, and leave the counters reset
+    items from the shared work counter, merge, and leave the counters reset
     for the next launch (three decodes in a row, with plans of different sizes)."""
     w = wl.scaled(wl.WORKLOADS["tiny"], name=f"waves_{gqa}", n_q_heads=8 * gqa, n_kv_heads=8, context=3000,
                   lognormal_sigma=0.5)
