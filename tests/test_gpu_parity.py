@@ -98,11 +98,11 @@ def test_chunked_appends_with_eviction(name, gqa, group, window, sink):
 
 
 def test_short_contexts_and_empty_request():
-    """L < S (sinks only), L <= S + W (no INT2), L = 0 (zero output)."""
+    """L = 1 and L < S (sinks only), L <= S + W (no INT2), L = 0 (zero output)."""
     w = wl.scaled(wl.WORKLOADS["tiny"], name="short", lognormal_sigma=0.5)
     cache, oc, _ = make_pair(w, SEED, 1, 4, 512)
     slots = [cache.alloc() for _ in range(4)]
-    lens = [2, 4, 132, 0]
+    lens = [1, 4, 132, 0]
     cache.reserve(slots[:3], lens[:3])
     append_both(cache, oc, w, 0, slots[:3], [0, 1, 2], [0, 0, 0], lens[:3])
     cache.commit()
