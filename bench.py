@@ -245,14 +245,26 @@ class Plan:
         return max(self.final)
 
 
-def int2_bytes_per_layer(w, L_list, H_list):
+def percentile(xs, f):
+    """Linear-interpolated quantile f in [0, 1] of a non-empty list."""
+    v = sorted(xs)
+    k = f * (len(v) - 1)
+    lo = int(math.floor(k))
+    hi = min(lo + 1, len(v) - 1)
+    return v[lo] + (v[hi] - v[lo]) * (k - lo)
+
+
+def int2_bytes_per_layer(w, L_list, H_list, shared=None):
     """Algorithmic bytes of one layer's decode: INT2 codes + scale/zero of positions
-    [S, H), BF16 sinks and ring tokens, fp32 R_K and R_V, q and out."""
+    [S, H), BF16 sinks and ring tokens, fp32 R_K and R_V, q and out.  With `shared` (tokens
+    each request maps from its group owner's prefix pages), the shared INT2 rows count once,
+    with the owner: the unique bytes."""
     ng = w.head_dim // w.group
     per_int2 = 2 * (w.head_dim // 4 + ng * 4)
     total = 0
-    for L, H in zip(L_list, H_list):
-        n_int2 = max(0, H - w.n_sink)
+    shared = shared or [0] * len(L_list)
+    for L, H, sh in zip(L_list, H_list, shared):
+        n_int2 = max(0, H - max(w.n_sink, sh))
         n_bf16 = min(L, w.n_sink) + max(0, L - H)
         total += w.n_kv_heads * (n_int2 * per_int2 + n_bf16 * 2 * w.head_dim * 2)
     total += 2 * w.n_kv_heads * w.head_dim * w.head_dim * 4
@@ -345,7 +357,7 @@ def run_ours(args, world, rank, local):
 
     # ---- fill the context (prefix owners first, then sharers map the shared pages)
     t_fill = time.time()
-    fill_context(cache, w, seed, n_layers, slots, plan.lengths, dev)
+    shared = fill_context(cache, w, seed, n_layers, slots, plan.lengths, dev)
     torch.cuda.synchronize()
     t_fill = time.time() - t_fill
 
@@ -423,15 +435,20 @@ def run_ours(args, world, rank, local):
     barrier(world)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e0.record()
-    for s in range(s0, s0 + args.steps):
+    for i, s in enumerate(range(s0, s0 + args.steps)):
         if s > s0:
             host_plan(s)
         graphs[s].replay()
         cache.commit()
+        marks[i].record()
     e1.record()
     torch.cuda.synchronize()
     step_ms = e0.elapsed_time(e1) / args.steps
+    # per-step times (between consecutive step ends; the first from the region's start)
+    per_step = [e0.elapsed_time(marks[0])] + [marks[i - 1].elapsed_time(marks[i]) for i in range(1, args.steps)]
+    step_pct = [percentile(per_step, f) for f in (0.1, 0.5, 0.9)]
     barrier(world)
     step_ms = max_over_ranks(step_ms, world, dev)
     clk = clocks.stop()
@@ -461,7 +478,9 @@ def run_ours(args, world, rank, local):
     fused_us = e0.elapsed_time(e1) * 1000.0 / (reps * n_layers)
     cache.commit()
     L_now, H_now = zip(*[cache.info(sl)[:2] for sl in slots])
-    fused_bytes = int2_bytes_per_layer(w, L_now, H_now) + append_bytes_per_layer(w, L_pre, H_pre, L_now, H_now)
+    app_bytes = append_bytes_per_layer(w, L_pre, H_pre, L_now, H_now)
+    fused_bytes = int2_bytes_per_layer(w, L_now, H_now, shared) + app_bytes  # unique (shared prefixes once)
+    reader_bytes = int2_bytes_per_layer(w, L_now, H_now) + app_bytes  # every request's reads
     st, flags = cache.status()
     assert st == 0, f"device status {flags:#x} after the fused timing"
 
@@ -523,7 +542,7 @@ def run_ours(args, world, rank, local):
         bf16 = bf16_comparison(w, seed, n_layers, [cache.info(sl)[0] for sl in slots], qin, dev, reps)
     cache.close()
     return dict(step_ms=step_ms, clocks=clk, decode_us=decode_us, bytes_layer=bytes_layer, n_layers=n_layers, B=B,
-                fused_us=fused_us, fused_bytes=fused_bytes,
+                fused_us=fused_us, fused_bytes=fused_bytes, reader_bytes=reader_bytes, step_pct=step_pct,
                 launches=launches_per_step * args.steps, e2e=e2e, bf16=bf16, n_items=n_items,
                 n_bf16_items=n_bf16_items, t_cal=t_cal, t_fill=t_fill, world=world, w=w)
 
@@ -724,7 +743,9 @@ def main(argv=None):
         "roofline": {"bound": "hbm", "kernel": "split_kernel (fused quantize-append + decode), one launch per layer",
                      "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                      "traffic": profiled_traffic(w.name), "peak_kind": peak_kind,
-                     "algorithmic_bytes": r["fused_bytes"], "launch_us": round(r["fused_us"], 3)},
+                     "algorithmic_bytes": r["fused_bytes"], "algorithmic_bytes_per_reader": r["reader_bytes"],
+                     "launch_us": round(r["fused_us"], 3)},
+        "step_us_per_layer_p10_p50_p90": [round(x * 1000.0 / n_layers, 3) for x in r["step_pct"]],
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
         "plan": {"items": r["n_items"], "bf16_items": r["n_bf16_items"]},

@@ -46,33 +46,38 @@ def make_pair(w: wl.Workload, seed: int, n_layers: int, n_requests: int, max_len
     return cache, oc, params
 
 
+def check_stream(cache: KVCache, layer: int, slot: int, kvh: int, kv: int, st, label: str = "", positions=None):
+    """One (request, kv-head, K|V) stream of the cache against an oracle.Stream: INT2 rows,
+    scale/zero words, sinks and ring slots, bit-exact."""
+    L, H, S, W = st.length, st.history_end, st.S, st.W
+    gL, gH, _ = cache.info(slot)
+    assert (gL, gH) == (L, H), f"{label}: lengths {(gL, gH)} != {(L, H)}"
+    pos = list(range(S, H)) if positions is None else [p for p in positions if S <= p < H]
+    if pos:
+        rows, sz = cache.int2_rows(layer, slot, kvh, kv, pos)
+        exp_rows = st.rows[pos]
+        exp_sz = st.sz[pos].view(np.int16)
+        bad = np.nonzero((rows.numpy() != exp_rows).any(axis=1))[0]
+        assert bad.size == 0, f"{label} layer {layer} kvh {kvh} kv {kv}: {bad.size} code rows differ, first pos {pos[bad[0]]}"
+        badz = np.nonzero((sz.numpy() != exp_sz).any(axis=1))[0]
+        assert badz.size == 0, f"{label} layer {layer} kvh {kvh} kv {kv}: {badz.size} scale/zero differ, first pos {pos[badz[0]]}"
+    n_s = min(L, S)
+    if n_s:
+        got = cache.sink_tokens(layer, slot, kvh, kv)[:n_s].numpy().view(np.uint16)
+        assert np.array_equal(got, st.sink[:n_s]), f"{label}: sink tokens differ"
+    if L > H:
+        ring = cache.ring_tokens(layer, slot, kvh, kv).numpy().view(np.uint16)
+        idx = [p % W for p in range(H, L)]
+        assert np.array_equal(ring[idx], st.ring[idx]), f"{label}: ring tokens differ"
+
+
 def check_pages(cache: KVCache, oc: OracleCache, layer: int, slot: int, req: int, kvhs=None, positions=None):
     """INT2 rows, scale/zero words, sinks and ring slots: bit-exact."""
-    L, H = oc.length(req), oc.history_end(req)
-    gL, gH, _ = cache.info(slot)
-    assert (gL, gH) == (L, H)
-    S, W = oc.S, oc.W
+    assert cache.info(slot)[:2] == (oc.length(req), oc.history_end(req))
     kvhs = range(oc.Hkv) if kvhs is None else kvhs
     for kvh in kvhs:
         for kv in range(2):
-            st = oc.streams[layer][req][kvh][kv]
-            pos = list(range(S, H)) if positions is None else [p for p in positions if S <= p < H]
-            if pos:
-                rows, sz = cache.int2_rows(layer, slot, kvh, kv, pos)
-                exp_rows = st.rows[pos]
-                exp_sz = st.sz[pos].view(np.int16)
-                bad = np.nonzero((rows.numpy() != exp_rows).any(axis=1))[0]
-                assert bad.size == 0, f"layer {layer} kvh {kvh} kv {kv}: {bad.size} code rows differ, first pos {pos[bad[0]]}"
-                badz = np.nonzero((sz.numpy() != exp_sz).any(axis=1))[0]
-                assert badz.size == 0, f"layer {layer} kvh {kvh} kv {kv}: {badz.size} scale/zero differ, first pos {pos[badz[0]]}"
-            n_s = min(L, S)
-            if n_s:
-                got = cache.sink_tokens(layer, slot, kvh, kv)[:n_s].numpy().view(np.uint16)
-                assert np.array_equal(got, st.sink[:n_s]), "sink tokens differ"
-            if L > H:
-                ring = cache.ring_tokens(layer, slot, kvh, kv).numpy().view(np.uint16)
-                idx = [p % W for p in range(H, L)]
-                assert np.array_equal(ring[idx], st.ring[idx]), "ring tokens differ"
+            check_stream(cache, layer, slot, kvh, kv, oc.streams[layer][req][kvh][kv], positions=positions)
 
 
 def compare_decode(out_f32: torch.Tensor, out_bf16: torch.Tensor, ref: np.ndarray, label: str = ""):

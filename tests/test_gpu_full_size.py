@@ -5,11 +5,12 @@ times: the workload's whole batch at its context lengths, filled by the bench's 
 under the automatic plan, so the CTA shape, the schedule and the merge are the bench's.
 One layer is built: every layer of a step runs the same plan.
 
-The outputs are checked on samples the oracle can compute one by one: it rebuilds only
-the sampled (request, kv-head) streams from the same seeded tokens (a sharer's stream
-takes its prefix from the owner's, as the cache does) and computes their fp64 attention.
-The tolerance is the parity tests' (max-abs 2e-2, relative L2 5e-3 on the fp32 output,
-bf16 output = RNE of it).
+The cache is checked on samples the oracle can compute one by one: it rebuilds only the
+sampled (request, kv-head) streams from the same seeded tokens (a sharer's stream takes
+its prefix from the owner's, as the cache does).  Their stored K and V streams (INT2 rows,
+scale/zero words, sinks, ring) must match bit for bit, and their outputs the oracle's
+fp64 attention within the parity tests' tolerance (max-abs 2e-2, relative L2 5e-3 on the
+fp32 output, bf16 output = RNE of it).
 """
 import os
 import sys
@@ -23,7 +24,7 @@ from int2_rotated_kv_rotate_gb300 import KVCache, workloads as wl
 from oracle import calibration as ocal
 from oracle.model import as_bits
 
-from helpers import compare_decode
+from helpers import check_stream, compare_decode
 
 sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
 import bench  # noqa: E402  (the plan and the context fill are the bench's own)
@@ -111,8 +112,11 @@ def test_full_size_sampled_heads(name):
             _append_pieces(sk, sv, kb[:L - start], vb[:L - start], start, L)
             sk.append(np.ascontiguousarray(kb[L - start:]))  # the step's tokens, as one append
             sv.append(np.ascontiguousarray(vb[L - start:]))
+            label = f"{name} req {r} (L {L} + {n}, shared {shared[r]}) kv-head {h}"
+            # the stored stream after the step, bit for bit, then the step's output
+            check_stream(cache, 0, slots[r], h, 0, sk, label)
+            check_stream(cache, 0, slots[r], h, 1, sv, label)
             ref = oracle.decode(np.ascontiguousarray(qb[r, h * G:(h + 1) * G]), sk, sv, RK[h], RV[h])
-            compare_decode(out32[r, h * G:(h + 1) * G], out[r, h * G:(h + 1) * G], ref,
-                           f"{name} req {r} (L {L} + {n}, shared {shared[r]}) kv-head {h}")
+            compare_decode(out32[r, h * G:(h + 1) * G], out[r, h * G:(h + 1) * G], ref, label)
     finally:
         cache.close()
