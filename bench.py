@@ -46,6 +46,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rotation", default="oscar", choices=["oscar", "hadamard"],
+                    help="calibrated rotations: OSCAR's (default) or the Hadamard-only ablation")
     return ap.parse_args(argv)
 
 
@@ -350,7 +352,7 @@ def run_ours(args, world, rank, local):
     t_cal = time.time()
     for layer in range(n_layers):
         qc, kc, vc = wl.gen_calibration(w, seed, layer, device=dev)
-        RK, RV, cK, cV = calibrate.calibrate_layer_device(qc, kc, vc, w.clip_percentile)
+        RK, RV, cK, cV = calibrate.calibrate_layer_device(qc, kc, vc, w.clip_percentile, rotation=args.rotation)
         cache.set_layer_params(layer, RK, RV, cK, cV)
     t_cal = time.time() - t_cal
     slots = [cache.alloc() for _ in range(B)]
@@ -702,8 +704,9 @@ def cpu_baseline(w, seed, budget_s=20.0):
 
 
 # ---------------------------------------------------------------------------- output
-def config_of(w, n_layers):
+def config_of(w, n_layers, rotation="oscar"):
     return {"workload": w.name, "description": w.description, "layers": n_layers, "batch": w.batch,
+            "rotation": rotation,
             "context": w.context, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
             "group": w.group, "page": w.page, "sink": w.n_sink, "window": w.window,
             "l2": "inputs larger than L2: every layer's cache is distinct and the step cycles through all layers"}
@@ -737,7 +740,7 @@ def main(argv=None):
         "vs_baseline": None,
         "dtype": "int2 codes + bf16 scale/zero; fp16 mma, fp32 softmax",
         "data": "synthetic (seeded N(0,1) bf16 K/V/q with channel outliers and log-normal token norms)",
-        "config": config_of(w, n_layers),
+        "config": config_of(w, n_layers, args.rotation),
         "decode_us_per_layer": round(r["decode_us"], 3),
         "append_decode_tokens_per_s": round(r["B"] * world / (r["step_ms"] * 1e-3), 1),
         "roofline": {"bound": "hbm", "kernel": "split_kernel (fused quantize-append + decode), one launch per layer",

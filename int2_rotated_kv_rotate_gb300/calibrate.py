@@ -88,29 +88,46 @@ def _decimal_ratio(p: float):
     return int(whole + frac), den
 
 
-def calibrate_kv_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, percentile: float = 99.9):
-    """q [N, G, d], k and v [N, d] -> (R_K, R_V) fp32 [d, d], (clip_K, clip_V) fp32."""
+ROTATIONS = ("oscar", "hadamard")
+
+
+def _check_rotation(rotation: str) -> None:
+    if rotation not in ROTATIONS:
+        raise ValueError(f"rotation must be one of {ROTATIONS}, not {rotation!r}")
+
+
+def calibrate_kv_head(q: np.ndarray, k: np.ndarray, v: np.ndarray, percentile: float = 99.9,
+                      rotation: str = "oscar"):
+    """q [N, G, d], k and v [N, d] -> (R_K, R_V) fp32 [d, d], (clip_K, clip_V) fp32.
+    rotation "oscar": R = U H P with U the sorted eigenbasis of C_Q (keys) or C_S (values);
+    "hadamard": the ablation without the covariance basis, R = H P for both (the
+    Hadamard-only rotation that the OSCAR technical summary compares against, sections 1
+    and 4)."""
+    _check_rotation(rotation)
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     n, G, d = q.shape
-    flat_q = q.reshape(n * G, d)
-    C_Q = np.einsum("ni,nj->ij", flat_q, flat_q) / (n * G)
-    C_S = np.zeros((d, d))
-    for h in range(G):
-        O = causal_attention_outputs(q[:, h, :], k, v)
-        C_S += O.T @ O
-    C_S /= n * G
-    R_K = rotation_from_eigenbasis(sorted_eigenbasis(C_Q)).astype(np.float32)
-    R_V = rotation_from_eigenbasis(sorted_eigenbasis(C_S)).astype(np.float32)
+    if rotation == "hadamard":
+        R_K = R_V = rotation_from_eigenbasis(np.eye(d)).astype(np.float32)
+    else:
+        flat_q = q.reshape(n * G, d)
+        C_Q = np.einsum("ni,nj->ij", flat_q, flat_q) / (n * G)
+        C_S = np.zeros((d, d))
+        for h in range(G):
+            O = causal_attention_outputs(q[:, h, :], k, v)
+            C_S += O.T @ O
+        C_S /= n * G
+        R_K = rotation_from_eigenbasis(sorted_eigenbasis(C_Q)).astype(np.float32)
+        R_V = rotation_from_eigenbasis(sorted_eigenbasis(C_S)).astype(np.float32)
     clip_K = np.float32(nearest_rank(np.abs(k @ R_K.astype(np.float64)), percentile))
     clip_V = np.float32(nearest_rank(np.abs(v @ R_V.astype(np.float64)), percentile))
     return R_K, R_V, clip_K, clip_V
 
 
-def calibrate_layer(q, k, v, percentile: float = 99.9):
+def calibrate_layer(q, k, v, percentile: float = 99.9, rotation: str = "oscar"):
     """q [N, H_q, d], k and v [N, H_kv, d] (array-like) -> R_K, R_V [H_kv, d, d],
-    clip_K, clip_V [H_kv] (fp32 numpy)."""
+    clip_K, clip_V [H_kv] (fp32 numpy).  rotation: "oscar" or "hadamard" (the ablation)."""
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
@@ -122,17 +139,19 @@ def calibrate_layer(q, k, v, percentile: float = 99.9):
     cK = np.empty(Hkv, np.float32)
     cV = np.empty(Hkv, np.float32)
     for h in range(Hkv):
-        RK[h], RV[h], cK[h], cV[h] = calibrate_kv_head(q[:, h * G:(h + 1) * G], k[:, h], v[:, h], percentile)
+        RK[h], RV[h], cK[h], cV[h] = calibrate_kv_head(q[:, h * G:(h + 1) * G], k[:, h], v[:, h], percentile,
+                                                       rotation)
     return RK, RV, cK, cV
 
 
-def calibrate_layer_device(q, k, v, percentile: float = 99.9):
+def calibrate_layer_device(q, k, v, percentile: float = 99.9, rotation: str = "oscar"):
     """Same calibration with the heavy products on the tensors' device (torch): the causal
     attention in fp32, covariances and rotated activations in fp64, eigendecomposition
     on the host in fp64.  q [N, H_q, d], k and v [N, H_kv, d] torch tensors.
     Returns fp32 numpy R_K, R_V [H_kv, d, d] and clip_K, clip_V [H_kv]."""
     import torch
 
+    _check_rotation(rotation)
     n, Hq, d = q.shape
     Hkv = k.shape[1]
     G = Hq // Hkv
@@ -152,8 +171,11 @@ def calibrate_layer_device(q, k, v, percentile: float = 99.9):
         O = torch.softmax(logits, dim=-1) @ vf[:, h]
         Of = O.reshape(-1, d).double()
         C_S = (Of.T @ Of) / (n * G)
-        RK[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_Q.cpu().numpy())).astype(np.float32)
-        RV[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_S.cpu().numpy())).astype(np.float32)
+        if rotation == "hadamard":
+            RK[h] = RV[h] = rotation_from_eigenbasis(np.eye(d)).astype(np.float32)
+        else:
+            RK[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_Q.cpu().numpy())).astype(np.float32)
+            RV[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_S.cpu().numpy())).astype(np.float32)
         for R, X, out in ((RK[h], kf[:, h], cK), (RV[h], vf[:, h], cV)):
             rot = (X.double() @ torch.from_numpy(R).to(X.device).double()).abs().flatten()
             rank = max(1, -(-(num * rot.numel()) // (den * 100)))

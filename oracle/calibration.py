@@ -109,10 +109,15 @@ def clip_threshold(R: np.ndarray, X: np.ndarray, pct: float) -> float:
     return nearest_rank_percentile(np.abs(rotated), pct)
 
 
-def calibrate_head(Q: np.ndarray, K: np.ndarray, V: np.ndarray, pct: float):
-    """(R_K, R_V, clip_K, clip_V) for one kv-head; Q [N, G, d], K and V [N, d] (float)."""
-    _, U_Q = eig_desc(query_covariance(Q))
-    _, U_S = eig_desc(score_value_covariance(Q, K, V))
+def calibrate_head(Q: np.ndarray, K: np.ndarray, V: np.ndarray, pct: float, rotation: str = "oscar"):
+    """(R_K, R_V, clip_K, clip_V) for one kv-head; Q [N, G, d], K and V [N, d] (float).
+    rotation "hadamard" is the ablation without the covariance eigenbasis (U = I): the
+    Hadamard-only rotation of the OSCAR technical summary's sections 1 and 4."""
+    if rotation == "hadamard":
+        U_Q = U_S = np.eye(Q.shape[-1])
+    else:
+        _, U_Q = eig_desc(query_covariance(Q))
+        _, U_S = eig_desc(score_value_covariance(Q, K, V))
     R_K = compose_rotation(U_Q).astype(np.float32)
     R_V = compose_rotation(U_S).astype(np.float32)
     clip_K = np.float32(clip_threshold(R_K, K, pct))
@@ -120,7 +125,7 @@ def calibrate_head(Q: np.ndarray, K: np.ndarray, V: np.ndarray, pct: float):
     return R_K, R_V, float(clip_K), float(clip_V)
 
 
-def calibrate_layer(Q: np.ndarray, K: np.ndarray, V: np.ndarray, pct: float):
+def calibrate_layer(Q: np.ndarray, K: np.ndarray, V: np.ndarray, pct: float, rotation: str = "oscar"):
     """Per kv-head calibration of one layer.  Q [N, H_q, d]; K, V [N, H_kv, d].
 
     Returns R_K, R_V fp32 [H_kv, d, d] and clip_K, clip_V fp32 [H_kv].
@@ -133,5 +138,6 @@ def calibrate_layer(Q: np.ndarray, K: np.ndarray, V: np.ndarray, pct: float):
     cK = np.zeros(Hkv, np.float32)
     cV = np.zeros(Hkv, np.float32)
     for h in range(Hkv):
-        RK[h], RV[h], cK[h], cV[h] = calibrate_head(Q[:, h * G:(h + 1) * G, :], K[:, h, :], V[:, h, :], pct)
+        RK[h], RV[h], cK[h], cV[h] = calibrate_head(Q[:, h * G:(h + 1) * G, :], K[:, h, :], V[:, h, :], pct,
+                                                    rotation)
     return RK, RV, cK, cV

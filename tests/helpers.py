@@ -15,12 +15,13 @@ MAX_ABS = 2e-2
 REL_L2 = 5e-3
 
 
-def oracle_params(w: wl.Workload, seed: int, n_layers: int):
+def oracle_params(w: wl.Workload, seed: int, n_layers: int, rotation: str = "oscar"):
     """Rotations and clips per layer from the oracle's calibration (inputs to both sides)."""
     RK, RV, cK, cV = [], [], [], []
     for layer in range(n_layers):
         q, k, v = wl.gen_calibration(w, seed, layer)
-        a, b, c, d = ocal.calibrate_layer(q.float().numpy(), k.float().numpy(), v.float().numpy(), w.clip_percentile)
+        a, b, c, d = ocal.calibrate_layer(q.float().numpy(), k.float().numpy(), v.float().numpy(), w.clip_percentile,
+                                          rotation=rotation)
         RK.append(a)
         RV.append(b)
         cK.append(c)

@@ -13,7 +13,7 @@ from int2_rotated_kv_rotate_gb300 import workloads as wl
 from int2_rotated_kv_rotate_gb300 import _native as N
 from oracle.model import bf16_reference
 
-from helpers import bits, check_pages, compare_decode, make_pair
+from helpers import oracle_params, bits, check_pages, compare_decode, make_pair
 
 pytestmark = pytest.mark.gpu
 
@@ -65,6 +65,41 @@ def test_tiny_workload_full_context():
     # several split plans give the same answer within tolerance
     for msp in (1, 3, 64):
         decode_and_compare(cache, oc, w, 0, [slot], [0], 1, f"tiny split {msp}", max_split_pages=msp)
+
+
+def test_hadamard_only_rotation():
+    """The ablation's rotations (R = H_Had P_br for keys and values, no covariance basis)
+    through the same kernels: pages bit-exact, outputs within tolerance, fused step too."""
+    w = wl.scaled(wl.WORKLOADS["tiny"], name="hadamard_only", lognormal_sigma=0.5)
+    params = oracle_params(w, SEED, 1, rotation="hadamard")
+    cache, oc, _ = make_pair(w, SEED, 1, 2, 2600, params=params)
+    slots = [cache.alloc() for _ in range(2)]
+    lens = [2500, 700]
+    cache.reserve(slots, lens)
+    append_both(cache, oc, w, 0, slots, [0, 1], [0, 0], lens)
+    cache.commit()
+    torch.cuda.synchronize()
+    for i, s in enumerate(slots):
+        check_pages(cache, oc, 0, s, i)
+    decode_and_compare(cache, oc, w, 0, slots, [0, 1], 0, "hadamard only")
+    # one fused append + decode step
+    counts = [16, 1]
+    cache.reserve(slots, counts)
+    cache.plan(slots)
+    K, V = kv_rows(w, 0, [0, 1], lens, counts)
+    q = wl.gen_q(w, SEED, 0, 1, 2, device="cuda")
+    o32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    out = cache.append_decode(0, K, V, q, out_f32=o32)
+    torch.cuda.synchronize()
+    cache.commit()
+    kb, vb = bits(K), bits(V)
+    oc.append(0, 0, kb[:16], vb[:16])
+    oc.append(0, 1, kb[16:], vb[16:])
+    qb = bits(q)
+    for i, s_ in enumerate(slots):
+        check_pages(cache, oc, 0, s_, i)
+        compare_decode(o32[i], out[i], oc.decode(0, i, qb[i]), f"hadamard only fused req {i}")
+    cache.close()
 
 
 @pytest.mark.parametrize("name,gqa,group,window,sink", [
