@@ -681,10 +681,12 @@ def oracle_sample(w, seed, n_heads_sample: int, context: int):
 
 
 def cpu_baseline(w, seed, budget_s=20.0):
-    """Oracle (as it stands) on the host cores: µs per layer-step, scaled from a sample of
-    kv-heads of layer 0 of request 0."""
+    """Oracle (as it stands) on one host core: µs per layer-step, scaled from a sample of
+    kv-heads of layer 0 of request 0.  The oracle's decode is serial (only its rotation
+    runs on several threads), so the sample runs on one thread and says so."""
     import oracle
 
+    oracle.set_threads(1)
     context = min(w.context, 32768)
     n_heads = 2
     step = oracle_sample(w, seed, n_heads, context)
@@ -697,8 +699,8 @@ def cpu_baseline(w, seed, budget_s=20.0):
     per_head = statistics.median(times) / n_heads
     scale_layer = w.n_kv_heads * w.batch * (w.context / context)
     us = per_head * scale_layer * 1e6
-    return {"value": round(us, 1), "unit": "us/layer/step", "cores": oracle.max_threads(), "kind": "oracle",
-            "sample": f"{n_heads} of {w.n_kv_heads} kv-heads of one request, layer 0, context {context}: append "
+    return {"value": round(us, 1), "unit": "us/layer/step", "cores": 1, "kind": "oracle",
+            "sample": f"one thread; {n_heads} of {w.n_kv_heads} kv-heads of one request, layer 0, context {context}: append "
                       f"{w.append_per_step or 1} token(s) + decode 1 per step, {len(times)} steps, median, scaled "
                       f"x{scale_layer:.1f} to one layer-step of the workload"}
 
@@ -773,6 +775,7 @@ def main_reference(args, world, rank, w):
         return 0
     import oracle
 
+    oracle.set_threads(1)  # the oracle's decode is serial; its rotation alone would use more
     context = min(w.context, 32768)
     n_heads = 1
     step = oracle_sample(w, args.seed, n_heads, context)
@@ -785,9 +788,9 @@ def main_reference(args, world, rank, w):
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us * w.n_layers / 1000.0, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 quantizer",
             "data": "synthetic", "config": config_of(w, w.n_layers),
-            "cpu_baseline": {"value": round(us, 1), "unit": "us/layer/step", "cores": oracle.max_threads(),
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/layer/step", "cores": 1,
                              "kind": "oracle",
-                             "sample": f"{n_heads} kv-head of one request, layer 0, context {context}, append "
+                             "sample": f"one thread; {n_heads} kv-head of one request, layer 0, context {context}, append "
                                        f"{w.append_per_step or 1} + decode 1 per step, scaled x{scale:.1f}"},
             "e2e": {"value": round(us, 1), "unit": "us/layer/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
