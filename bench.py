@@ -503,7 +503,8 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize()
     decode_us = e0.elapsed_time(e1) * 1000.0 / (reps * n_layers)
     bytes_layer = int2_bytes_per_layer(w, L_now, H_now)
-    n_items, n_bf16_items, _ = cache.plan_info()
+    int2_pages = w.n_kv_heads * sum((H + 63) // 64 if H > w.n_sink else 0 for H in H_now)  # over all items
+    n_items, n_bf16_items, max_item_pages = cache.plan_info()
 
     # ---- end to end through the C ABI with host buffers (no graph: one call per layer).
     # Every step copies its inputs in from pinned host memory and its output out; the
@@ -580,6 +581,7 @@ def run_ours(args, world, rank, local):
     return dict(step_ms=step_ms, clocks=clk, decode_us=decode_us, bytes_layer=bytes_layer, n_layers=n_layers, B=B,
                 fused_us=fused_us, fused_bytes=fused_bytes, reader_bytes=reader_bytes, step_pct=step_pct,
                 launches=launches_per_step * args.steps, e2e=e2e, bf16=bf16, n_items=n_items,
+                max_item_pages=max_item_pages, int2_pages=int2_pages,
                 n_bf16_items=n_bf16_items, t_cal=t_cal, t_fill=t_fill, world=world, w=w)
 
 
@@ -787,7 +789,8 @@ def main(argv=None):
         "step_us_per_layer_p10_p50_p90": [round(x * 1000.0 / n_layers, 3) for x in r["step_pct"]],
         "gpu_launches": r["launches"],
         "clocks": r["clocks"],
-        "plan": {"items": r["n_items"], "bf16_items": r["n_bf16_items"]},
+        "plan": {"items": r["n_items"], "bf16_items": r["n_bf16_items"], "max_item_pages": r["max_item_pages"],
+                 "mean_int2_item_pages": round(r["int2_pages"] / max(1, r["n_items"] - r["n_bf16_items"]), 1)},
         "setup_s": {"calibration": round(r["t_cal"], 2), "fill": round(r["t_fill"], 2)},
     }
     if r["e2e"]:
