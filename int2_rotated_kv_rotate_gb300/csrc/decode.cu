@@ -522,7 +522,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
 #pragma unroll
         for (int g = 0; g < NG; ++g) zv[j][g] *= alpha[j];
       }
-      // value accumulator columns: G = 4 -> (hi, lo) of head tig; G = 8 -> heads tig, 4 + tig
+      // value accumulator columns: G = 4 -> head tig (and a column that stays 0); G = 8 -> heads tig, 4 + tig
 #pragma unroll
       for (int f = 0; f < 8; ++f) {
         const float a0 = alpha[0], a1 = NT == 2 ? alpha[NT - 1] : alpha[0];
@@ -554,11 +554,9 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
         const float sv0 = bf16_lo(vz0), sv1 = bf16_lo(vz1);
         const float zv0 = bf16_hi(vz0), zv1 = bf16_hi(vz1);
         uint32_t x0, x1;
-        if (NT == 1) {
-          const float q0 = p[0][0] * sv0, q1 = p[0][1] * sv1;
-          const float h0 = __half2float(__float2half_rn(q0)), h1 = __half2float(__float2half_rn(q1));
-          x0 = pack_h2(h0, q0 - h0);
-          x1 = pack_h2(h1, q1 - h1);
+        if (NT == 1) {  // heads in the even columns; the odd (second-part) columns stay 0
+          x0 = pack_h2(p[0][0] * sv0, 0.f);
+          x1 = pack_h2(p[0][1] * sv1, 0.f);
         } else {
           x0 = pack_h2(p[0][0] * sv0, p[NT - 1][0] * sv0);
           x1 = pack_h2(p[0][1] * sv1, p[NT - 1][1] * sv1);

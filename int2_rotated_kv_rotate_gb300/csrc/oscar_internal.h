@@ -92,7 +92,7 @@ struct DeviceLayout {
   // control
   size_t page_table;  // int32 [max_requests][max_pages_per_request]
   size_t status;      // uint32 flags
-  size_t counters;    // uint32 [max_requests][H_kv] merge counters (second level)
+  size_t counters;    // uint32 [max_requests][H_kv] merge counters (items of a head done)
   // the append and the decode plan, each one block that one copy uploads: int32 counts[4]
   // at +0, the requests at +256, the items after them.  Append counts: items.  Decode
   // counts: items, requests, items that wait on no append task (stored first).
