@@ -65,7 +65,7 @@ extern "C" {
 typedef enum {
   OSCAR_OK = 0,
   OSCAR_ERR_INVALID_ARG = 1,  /* a size, index or pointer is out of the documented range */
-  OSCAR_ERR_UNSUPPORTED = 2,  /* a shape this build has no kernel for */
+  OSCAR_ERR_UNSUPPORTED = 2,  /* a shape the library has no kernel for */
   OSCAR_ERR_OUT_OF_PAGES = 3, /* the page pool cannot hold the reservation; nothing changed */
   OSCAR_ERR_BAD_PAGE = 4,     /* device: a page-table entry or slot out of range was skipped */
   OSCAR_ERR_CUDA = 5,         /* a CUDA runtime call failed (text in oscar_last_error) */
