@@ -487,3 +487,173 @@ def test_decode_empty_context_is_zero():
     K = oracle.Stream(128, 128, 4, 8, 8, I, 1.0)
     V = oracle.Stream(128, 128, 4, 8, 8, I, 1.0)
     assert not oracle.decode(bits(np.ones((2, 128))), K, V, I, I).any()
+
+
+# ----------------------------------------------------------------------------- quantizer ties
+def test_quantizer_rounds_exact_ties_to_even():
+    """Groups whose (x - z) / s lands exactly on 0.5, 1.5 and 2.5 take codes 0, 2 and 2
+    (round half to even); rounding half away from zero would give 1, 2 and 3."""
+    inf = float("inf")
+    cases = [
+        ([0.0, 3.0] + [0.5, 1.5, 2.5] * 42, [1.0, 0.0]),  # s = 1, z = 0
+        ([0.0, 6.0] + [1.0, 3.0, 5.0] * 42, [2.0, 0.0]),  # s = 2, z = 0
+        ([-1.0, 2.0] + [-0.5, 0.5, 1.5] * 42, [1.0, -1.0]),  # s = 1, z = -1
+    ]
+    for vals, sz_expect in cases:
+        row, sz = oracle.quantize_token(group_token(vals), 128, inf)
+        assert list(sz) == list(bits(sz_expect))
+        codes = oracle.unpack_row(row)
+        assert codes[0] == 0 and codes[1] == 3
+        assert list(codes[2:]) == [0, 2, 2] * 42, vals[:5]
+    # g = 32: each group on its own, ties in every group
+    vals = []
+    for grp in range(4):
+        base = float(4 * grp)
+        vals += [base, base + 3.0] + [base + 0.5, base + 1.5, base + 2.5] * 10
+    row, sz = oracle.quantize_token(group_token(vals), 32, inf)
+    codes = oracle.unpack_row(row)
+    for grp in range(4):
+        assert list(codes[32 * grp:32 * grp + 32]) == [0, 3] + [0, 2, 2] * 10
+
+
+# ----------------------------------------------------------------------------- BF16 comparison decode
+def softmax_attention_loops(qf, Kf, Vf):
+    """softmax(q K^T / sqrt(d)) V spelled out token by token with Python floats."""
+    G, d = qf.shape
+    out = np.zeros((G, d))
+    for h in range(G):
+        logits = []
+        for t in range(Kf.shape[0]):
+            logits.append(math.fsum(float(qf[h, c]) * float(Kf[t, c]) for c in range(d)) / math.sqrt(d))
+        m = max(logits)
+        w = [math.exp(x - m) for x in logits]
+        tot = math.fsum(w)
+        for t in range(Kf.shape[0]):
+            out[h] += (w[t] / tot) * Vf[t]
+    return out
+
+
+@pytest.mark.parametrize("L,G", [(1, 4), (2, 8), (7, 4), (64, 8), (129, 4)])
+def test_bf16_comparison_decode_brute_force(L, G):
+    """The uncompressed comparison's reference: plain attention over every one of the L
+    tokens, with the 1/sqrt(d) logit scale (sharp logits make a dropped scale or a
+    dropped token visible)."""
+    rng = np.random.default_rng(100 + L)
+    K = bits(rng.standard_normal((L, 128)) * 4)
+    V = bits(rng.standard_normal((L, 128)) * np.where(np.arange(128) % 50 == 0, 8.0, 1.0))
+    q = bits(rng.standard_normal((G, 128)))
+    got = oracle.bf16_decode(q, K, V)
+    assert np.allclose(got, softmax_attention_loops(f64(q), f64(K), f64(V)), atol=1e-12, rtol=0)
+
+
+def test_bf16_comparison_decode_closed_forms():
+    rng = np.random.default_rng(120)
+    K = bits(rng.standard_normal((1, 128)) * 3)
+    V = bits(rng.standard_normal((1, 128)))
+    q = bits(rng.standard_normal((4, 128)) * 7)
+    # one token: every head's output is that token's value, exactly
+    assert np.array_equal(oracle.bf16_decode(q, K, V), np.repeat(f64(V), 4, axis=0))
+    # equal logits (q = 0): the mean of the values
+    K = bits(rng.standard_normal((37, 128)) * 3)
+    V = bits(rng.standard_normal((37, 128)))
+    got = oracle.bf16_decode(np.zeros((8, 128), np.uint16), K, V)
+    assert np.allclose(got, np.repeat(f64(V).mean(0)[None], 8, axis=0), atol=1e-14, rtol=0)
+    # two tokens with logits a and b: weights 1 / (1 + e^(b - a)) and the rest
+    K = np.zeros((2, 128), np.uint16)
+    K[0, 0] = bits([2.0])[0]
+    K[1, 0] = bits([-1.0])[0]
+    V = bits(rng.standard_normal((2, 128)))
+    q = np.zeros((1, 128), np.uint16)
+    q[0, 0] = bits([math.sqrt(128.0) * 0.5])[0]  # exact in bf16? sqrt(128)/2 is not: use its bf16 value
+    qv = float(f64(q)[0, 0])
+    a, b = qv * 2.0 / math.sqrt(128), qv * -1.0 / math.sqrt(128)
+    w0 = 1.0 / (1.0 + math.exp(b - a))
+    expect = w0 * f64(V)[0] + (1 - w0) * f64(V)[1]
+    assert np.allclose(oracle.bf16_decode(q, K, V)[0], expect, atol=1e-14, rtol=0)
+    # no tokens: zeros
+    assert not oracle.bf16_decode(q, np.zeros((0, 128), np.uint16), np.zeros((0, 128), np.uint16)).any()
+
+
+# ----------------------------------------------------------------------------- calibration wiring
+def independent_hadamard_bitrev(d):
+    """H_Had from its entries, (-1)^popcount(i & j) / sqrt(d), and the bit-reversal map."""
+    nbits = d.bit_length() - 1
+    H = np.array([[(-1) ** bin(i & j).count("1") for j in range(d)] for i in range(d)], np.float64) / math.sqrt(d)
+    rev = [int(format(j, f"0{nbits}b")[::-1], 2) for j in range(d)]
+    P = np.zeros((d, d))
+    P[rev, np.arange(d)] = 1.0  # column j of P_br is e_rev(j)
+    return H, P, rev
+
+
+def test_compose_rotation_order_with_a_general_basis():
+    """R = U H_Had P_br for a U that is not the identity: column j of R is U H e_rev(j),
+    and none of the other orders of the three factors gives the same matrix."""
+    d = 128
+    U = random_orthogonal(d, 31).astype(np.float64)
+    H, P, rev = independent_hadamard_bitrev(d)
+    R = cal.compose_rotation(U)
+    for j in range(d):
+        assert np.allclose(R[:, j], U @ H[:, rev[j]], atol=1e-13, rtol=0), j
+    # (H_Had and P_br commute, since H_Had[rev i][rev j] = H_Had[i][j], so U P_br H_Had is the
+    # same matrix; every order that moves U is not)
+    assert np.abs(U @ P @ H - U @ H @ P).max() < 1e-13
+    for wrong in (H @ U @ P, P @ H @ U, H @ P @ U, P @ U @ H):
+        assert np.abs(R - wrong).max() > 0.1
+
+
+def rows_with_covariance(U, sigma, n, seed):
+    """n rows x with (1/n) sum x^T x = U diag(sigma^2) U^T (exact up to fp64 rounding)."""
+    g = np.random.default_rng(seed)
+    Z, _ = np.linalg.qr(g.standard_normal((n, U.shape[0])))  # orthonormal columns
+    return math.sqrt(n) * Z @ np.diag(sigma) @ U.T
+
+
+def causal_softmax_rows(Qh, K):
+    """S[i, j] = exp(l_ij) / sum_{j' <= i} exp(l_ij') for j <= i, l = q_i . k_j / sqrt(d), row by row."""
+    n, d = Qh.shape
+    S = np.zeros((n, n))
+    for i in range(n):
+        l = K[:i + 1] @ Qh[i] / math.sqrt(d)
+        e = np.exp(l - l.max())
+        S[i, :i + 1] = e / e.sum()
+    return S
+
+
+def test_calibrate_head_recovers_the_key_eigenbasis_and_wires_values_to_c_s():
+    """Key queries with a known covariance U diag(sigma^2) U^T: the key rotation's basis
+    U_Q = R_K P_br^T H_Had^T is U with its columns in descending-variance order, each with its
+    largest-magnitude entry positive.  The value rotation's basis diagonalises C_S (built
+    here from its definition, V^T S^T S V / N pooled over the query heads) with the
+    eigenvalues descending, and it is not the key basis."""
+    d, N, G = 128, 384, 2
+    U_true = random_orthogonal(d, 40).astype(np.float64)
+    sigma = np.geomspace(4.0, 0.25, d)  # distinct, descending
+    Q = rows_with_covariance(U_true, sigma, N * G, 41).reshape(N, G, d)
+    g = np.random.default_rng(42)
+    K = g.standard_normal((N, d))
+    V = g.standard_normal((N, d)) * np.geomspace(6.0, 0.5, d)  # anisotropic values, a different basis
+    RK, RV, cK, cV = cal.calibrate_head(Q, K, V, 99.9)
+    H, P, _ = independent_hadamard_bitrev(d)
+    U_K = RK.astype(np.float64) @ P.T @ H.T
+    expect = U_true.copy()
+    for k in range(d):
+        i = int(np.argmax(np.abs(expect[:, k])))
+        if expect[i, k] < 0:
+            expect[:, k] = -expect[:, k]
+    assert np.abs(U_K - expect).max() < 1e-5
+    C_S = np.zeros((d, d))
+    for h in range(G):
+        O = causal_softmax_rows(Q[:, h], K) @ V
+        C_S += O.T @ O
+    C_S /= N * G
+    U_V = RV.astype(np.float64) @ P.T @ H.T
+    D = U_V.T @ C_S @ U_V
+    diag = np.diag(D)
+    assert np.abs(D - np.diag(diag)).max() < 1e-5 * diag.max()
+    assert np.all(np.diff(diag) <= 1e-6 * diag.max()) and diag[0] > 2 * diag[-1]
+    # wiring: the key basis does not diagonalise C_S, nor the value basis C_Q
+    C_Q = U_true @ np.diag(sigma ** 2) @ U_true.T
+    DK = U_K.T @ C_S @ U_K
+    DV = U_V.T @ C_Q @ U_V
+    assert np.abs(DK - np.diag(np.diag(DK))).max() > 1e-2 * diag.max()
+    assert np.abs(DV - np.diag(np.diag(DV))).max() > 1e-2 * sigma[0] ** 2

@@ -55,3 +55,17 @@ def test_the_two_rotations_differ_and_unknown_names_are_rejected():
     assert not np.array_equal(osc[0], had[0])
     with pytest.raises(ValueError):
         calibrate.calibrate_layer(q, k, v, w.clip_percentile, rotation="identity")
+
+
+def test_product_oscar_calibration_matches_the_oracle():
+    """The product's CPU calibration in OSCAR mode (covariance eigenbases) against the
+    oracle's: the same rotations to 1e-6 and the same clip thresholds."""
+    w = wl.scaled(wl.WORKLOADS["qwen3_8b_layer"], n_q_heads=8, n_kv_heads=2, calib_tokens=1024)
+    q, k, v = wl.gen_calibration(w, 17, 3)
+    q, k, v = q.float().numpy(), k.float().numpy(), v.float().numpy()
+    a = calibrate.calibrate_layer(q, k, v, w.clip_percentile)
+    b = ocal.calibrate_layer(q, k, v, w.clip_percentile)
+    assert np.abs(a[0] - b[0]).max() < 1e-6 and np.abs(a[1] - b[1]).max() < 1e-6
+    np.testing.assert_allclose(a[2], b[2], rtol=1e-6)
+    np.testing.assert_allclose(a[3], b[3], rtol=1e-6)
+    assert not np.array_equal(a[0], a[1])  # keys and values get their own bases
