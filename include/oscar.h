@@ -127,6 +127,9 @@ oscar_status oscar_set_layer_params(oscar_cache* cache, int layer, const float* 
 /* Request slots.  alloc gives an empty request (L = 0).  free drops its page references. */
 oscar_status oscar_request_alloc(oscar_cache* cache, int* slot);
 oscar_status oscar_request_free(oscar_cache* cache, int slot);
+/* Free physical pages of the pool and free request slots (host view; a page shared by
+ * several requests is free once the last of them is freed).  Either pointer may be NULL. */
+oscar_status oscar_cache_stats(const oscar_cache* cache, int* free_pages, int* free_slots);
 /* Host view of a request: length L, history end H (INT2 format), pages mapped. */
 oscar_status oscar_request_info(const oscar_cache* cache, int slot, int* length, int* history_end, int* n_pages);
 /* Host copy of a request's page-table row (n entries). */
@@ -225,16 +228,61 @@ oscar_status oscar_bf16_decode_attention(oscar_cache* cache, int layer, const vo
  *   - Returns OSCAR_ERR_INVALID_ARG, launching nothing, when the current plan needs more
  *     than 8 MiB (oscar_decode_workspace_bytes tells the need).
  *   - Allocates nothing: no cudaMalloc, cudaFree or allocating library call.
- *   - The first call on a device looks up the array's device address (with that device
- *     current); make that first call before any stream capture.
+ *   - The current device must be the cache's device (the one current at
+ *     oscar_cache_create): the array's address is looked up on the current device, on
+ *     every call; OSCAR_ERR_INVALID_ARG otherwise.  The first call on a device also loads
+ *     the library's device code there if nothing has yet; make that first call before any
+ *     stream capture.
  *   - Every call, on every cache and stream, shares the one array and leaves its
  *     contents behind; nothing in it needs to start at zero.  Calls that overlap on the
  *     GPU race on it: order them on one stream or serialise them. */
 oscar_status oscar_decode_attention_noalloc(oscar_cache* cache, int layer, const void* q, void* out, float* out_f32,
                                             void* stream);
 
+/* Offline calibration of one layer on the GPU ([OSCAR] §2.2-A.1 to A.4), in fp64:
+ *   A.1  C_Q = (1/(G N)) sum over tokens and the G query heads of each kv-head of q^T q;
+ *        C_S = (1/(G N)) sum_h O_h^T O_h, O_h = causal softmax(Q_h K^T / sqrt(d)) V
+ *        (the score-aware value target V^T S^T S V / N);
+ *   A.2  eigenbases by cyclic Jacobi: eigenvalues descending, each eigenvector's first
+ *        largest-magnitude entry positive;
+ *   A.3  R_K = U_Q H_Had P_br, R_V = U_S H_Had P_br (H_Had the Sylvester matrix / sqrt(d),
+ *        P_br sending e_j to e_rev(j)), rounded to fp32;
+ *   A.4  clip = the clip_rank-th smallest of |x R| over the N tokens x d channels of each
+ *        kv-head's keys (values), with R as rounded; a nearest-rank percentile p is
+ *        clip_rank = ceil(p / 100 * N * d).
+ * rotation OSCAR_ROTATION_HADAMARD skips A.1 and A.2 (U = I: the Hadamard-only rotation).
+ * q [dev] bf16 [N][H_q][d], k and v [dev] bf16 [N][H_kv][d] (d = 128); outputs [dev]:
+ * R_K, R_V fp32 [H_kv][d][d] row-major (the inputs of oscar_set_layer_params), clip_K,
+ * clip_V fp32 [H_kv]; covariances [dev] nullable fp64 [2 H_kv][d][d] (C_Q of every
+ * kv-head, then C_S; untouched in the Hadamard-only mode).  workspace [dev], 256-byte
+ * aligned, of oscar_calibration_workspace_bytes (0 for a bad shape).  Asynchronous on
+ * `stream`. */
+#define OSCAR_ROTATION_OSCAR 0
+#define OSCAR_ROTATION_HADAMARD 1
+size_t oscar_calibration_workspace_bytes(int n_tokens, int n_q_heads, int n_kv_heads);
+oscar_status oscar_calibrate_layer(const void* q, const void* k, const void* v, int n_tokens, int n_q_heads,
+                                   int n_kv_heads, long long clip_rank, int rotation, float* R_K, float* R_V,
+                                   float* clip_K, float* clip_V, double* covariances, void* workspace,
+                                   size_t ws_bytes, void* stream);
+
+/* Bounded waits: a work item of oscar_append_decode_attention that waits for the append
+ * tasks it depends on gives up after `counter_polls` polls of their counter (each poll
+ * sleeps about 0.1 us; 0 restores the default of 2^22 polls, about a second), sets
+ * OSCAR_FLAG_TIMEOUT and carries on.  Applies to launches made after the call. */
+oscar_status oscar_set_wait_limit(oscar_cache* cache, uint32_t counter_polls);
+
+/* Host-side fault injection, for tests of the failure paths (nothing faults on the GPU).
+ * OSCAR_FAULT_LOST_APPEND_SIGNAL: the next decode plan made while a reservation is pending
+ * expects one more append signal for its first appending request than the append tasks
+ * send, so that request's waits in oscar_append_decode_attention run out (a signal that
+ * never arrives); the kernel returns with OSCAR_FLAG_TIMEOUT set.  One-shot. */
+#define OSCAR_FAULT_LOST_APPEND_SIGNAL 0x1u
+oscar_status oscar_inject_fault(oscar_cache* cache, uint32_t faults);
+
 /* Synchronises `stream`, returns the device status word in *flags (OSCAR_FLAG_*) and
- * clears it.  Returns OSCAR_ERR_BAD_PAGE / OSCAR_ERR_TIMEOUT if a flag was set. */
+ * clears it.  Returns OSCAR_ERR_BAD_PAGE / OSCAR_ERR_TIMEOUT if a flag was set.  After a
+ * timeout it also resets the cache's append-dependency and merge counters, so the next
+ * step starts from a consistent state. */
 oscar_status oscar_get_status(oscar_cache* cache, void* stream, uint32_t* flags);
 
 /* Text of the last error on this thread ("" if none). */

@@ -19,6 +19,7 @@ OSCAR_FORMAT_BF16 = 1
 OSCAR_FLAG_BAD_PAGE = 0x1
 OSCAR_FLAG_TIMEOUT = 0x2
 OSCAR_FLAG_BAD_SLOT = 0x4
+OSCAR_FAULT_LOST_APPEND_SIGNAL = 0x1
 
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "OUT_OF_PAGES", 4: "BAD_PAGE", 5: "CUDA",
                 6: "TIMEOUT", 7: "STATE"}
@@ -44,11 +45,13 @@ class oscar_layout(ctypes.Structure):
 
 EXPORTS = [
     "oscar_cache_device_bytes", "oscar_cache_create", "oscar_cache_destroy", "oscar_cache_layout",
-    "oscar_set_layer_params", "oscar_request_alloc", "oscar_request_free", "oscar_request_info",
+    "oscar_set_layer_params", "oscar_cache_stats", "oscar_request_alloc", "oscar_request_free", "oscar_request_info",
     "oscar_request_pages", "oscar_request_share_prefix", "oscar_reserve", "oscar_quantize_append",
     "oscar_commit_append", "oscar_plan_decode", "oscar_plan_decode_ex", "oscar_decode_workspace_bytes",
     "oscar_decode_workspace_max_bytes", "oscar_plan_info",
-    "oscar_decode_attention", "oscar_append_decode_attention", "oscar_decode_attention_noalloc", "oscar_bf16_append", "oscar_bf16_decode_attention", "oscar_get_status",
+    "oscar_decode_attention", "oscar_append_decode_attention", "oscar_decode_attention_noalloc", "oscar_bf16_append",
+    "oscar_bf16_decode_attention", "oscar_calibration_workspace_bytes", "oscar_calibrate_layer",
+    "oscar_set_wait_limit", "oscar_inject_fault", "oscar_get_status",
     "oscar_last_error", "oscar_last_launch_count",
 ]
 
@@ -73,6 +76,7 @@ def lib() -> ctypes.CDLL:
                 "oscar_cache_destroy": (None, [P]),
                 "oscar_cache_layout": (I, [P, ctypes.POINTER(oscar_layout)]),
                 "oscar_set_layer_params": (I, [P, I, P, P, P, P, P]),
+                "oscar_cache_stats": (I, [P, IP, IP]),
                 "oscar_request_alloc": (I, [P, IP]),
                 "oscar_request_free": (I, [P, I]),
                 "oscar_request_info": (I, [P, I, IP, IP, IP]),
@@ -91,6 +95,10 @@ def lib() -> ctypes.CDLL:
                 "oscar_decode_attention_noalloc": (I, [P, I, P, P, P, P]),
                 "oscar_bf16_append": (I, [P, I, P, P, P]),
                 "oscar_bf16_decode_attention": (I, [P, I, P, P, P, S, P, P]),
+                "oscar_calibration_workspace_bytes": (S, [I, I, I]),
+                "oscar_calibrate_layer": (I, [P, P, P, I, I, I, ctypes.c_longlong, I, P, P, P, P, P, P, S, P]),
+                "oscar_set_wait_limit": (I, [P, ctypes.c_uint32]),
+                "oscar_inject_fault": (I, [P, ctypes.c_uint32]),
                 "oscar_get_status": (I, [P, P, ctypes.POINTER(ctypes.c_uint32)]),
                 "oscar_last_error": (ctypes.c_char_p, []),
                 "oscar_last_launch_count": (I, []),
@@ -158,6 +166,13 @@ def oscar_set_layer_params(handle: int, layer: int, R_K, R_V, clip_K, clip_V, st
         assert t.device.type == "cpu" and t.is_contiguous()
     _check(lib().oscar_set_layer_params(handle, layer, _ptr(R_K), _ptr(R_V), _ptr(clip_K), _ptr(clip_V),
                                         _stream(stream)))
+
+
+def oscar_cache_stats(handle: int):
+    """(free pages, free request slots)."""
+    p, r = ctypes.c_int(), ctypes.c_int()
+    _check(lib().oscar_cache_stats(handle, ctypes.byref(p), ctypes.byref(r)))
+    return p.value, r.value
 
 
 def oscar_request_alloc(handle: int) -> int:
@@ -265,3 +280,31 @@ def oscar_get_status(handle: int, stream=None):
 
 def oscar_last_launch_count() -> int:
     return int(lib().oscar_last_launch_count())
+
+
+def oscar_set_wait_limit(handle: int, counter_polls: int) -> None:
+    _check(lib().oscar_set_wait_limit(handle, int(counter_polls)))
+
+
+def oscar_inject_fault(handle: int, faults: int) -> None:
+    _check(lib().oscar_inject_fault(handle, int(faults)))
+
+
+OSCAR_ROTATION_OSCAR = 0
+OSCAR_ROTATION_HADAMARD = 1
+
+
+def oscar_calibration_workspace_bytes(n_tokens: int, n_q_heads: int, n_kv_heads: int) -> int:
+    return int(lib().oscar_calibration_workspace_bytes(n_tokens, n_q_heads, n_kv_heads))
+
+
+def oscar_calibrate_layer(q, k, v, clip_rank: int, rotation: int, R_K, R_V, clip_K, clip_V, workspace,
+                          covariances=None, stream=None) -> None:
+    """q [N, H_q, d], k and v [N, H_kv, d] bf16 device tensors -> R_K, R_V [H_kv, d, d], clip_K,
+    clip_V [H_kv] fp32 device tensors (and optionally the fp64 covariances [2 H_kv, d, d])."""
+    n, hq, _ = q.shape
+    hkv = k.shape[1]
+    _check(lib().oscar_calibrate_layer(_ptr(q), _ptr(k), _ptr(v), n, hq, hkv, int(clip_rank), int(rotation),
+                                       _ptr(R_K), _ptr(R_V), _ptr(clip_K), _ptr(clip_V), _ptr(covariances),
+                                       _ptr(workspace), workspace.numel() * workspace.element_size(),
+                                       _stream(stream)))

@@ -45,6 +45,10 @@ class KVCache:
         f = lambda t: torch.as_tensor(t, dtype=torch.float32).contiguous().cpu()  # noqa: E731
         N.oscar_set_layer_params(self.handle, layer, f(R_K), f(R_V), f(clip_K), f(clip_V), stream)
 
+    def stats(self):
+        """(free pages, free request slots)."""
+        return N.oscar_cache_stats(self.handle)
+
     def alloc(self) -> int:
         return N.oscar_request_alloc(self.handle)
 

@@ -507,11 +507,10 @@ struct WorkQueue {
   }
 };
 
-// Bounded wait (one thread) until *ctr >= expect, with acquire semantics: false after about
-// a second of polling.
-constexpr uint32_t kCounterSpinLimit = 1u << 22;
-__device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned expect) {
-  for (uint32_t i = 0; i < kCounterSpinLimit; ++i) {
+// Bounded wait (one thread) until *ctr >= expect, with acquire semantics: false after
+// `polls` polls (kp.counter_polls; about a second by default).
+__device__ __forceinline__ bool wait_counter(const unsigned* ctr, unsigned expect, uint32_t polls) {
+  for (uint32_t i = 0; i < polls; ++i) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
     if (v >= expect) return true;

@@ -28,7 +28,6 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
-#include <mutex>
 
 #include "append_dev.cuh"
 #include "common.cuh"
@@ -171,8 +170,9 @@ struct Cfg {
   static constexpr int kWorkBytes = (((kWorkBytes0 > kMergeBytes ? kWorkBytes0 : kMergeBytes) + 127) / 128) * 128;
   static constexpr int kSlabSlots = (kWorkBytes - kSlabOff) / PartialSlot<G>::kBytes;
   static constexpr int kCtl = kWorkBytes;           // control area
-  // control: page barriers (NW x kStages), merge flag, next item, R_V^T and slab barriers
-  static constexpr int kCtlBytes = ((NW * kStages * 8 + 24 + 127) / 128) * 128;
+  // control: page barriers (NW x kStages), merge flag, next item, R_V^T and slab barriers,
+  // poison flag
+  static constexpr int kCtlBytes = ((NW * kStages * 8 + 32 + 127) / 128) * 128;
   static constexpr int kQin = kCtl + kCtlBytes;     // fp32 [G][kQinRow] query staging
   static constexpr int kQts = kQin + G * Shape<NW>::kQinRow * 4;  // fp32 [G][kQRow] q~
   static constexpr int kQss = kQts + G * kQRow * 4;  // fp32 [NW][G] sums of q~ per warp's channels
@@ -331,7 +331,7 @@ __device__ bool int2_issue_page(const KernelParams& kp, int layer, const DecodeI
 template <int G, int GROUP, int NW>
 __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
                                 const float* qts, const float* qss, uint8_t* part, uint8_t* smem,
-                                uint32_t& phase_bits, uint32_t pre_mask, const unsigned* pages_ctr) {
+                                uint32_t& phase_bits, uint32_t pre_mask, const unsigned* pages_ctr, int* s_poison) {
   using C = Cfg<G, GROUP, NW>;
   constexpr int NG = C::NG, NT = C::NT;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -348,7 +348,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   auto issue = [&](int k) -> bool {
     if (!pages_ready && (it.begin + warp + C::NW * k + 1) * kPage > dr.H_pre) {
       if (lane == 0) {
-        if (!wait_counter(pages_ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
+        if (!wait_counter(pages_ctr, unsigned(dr.app_expect), kp.counter_polls)) flag(kp, OSCAR_FLAG_TIMEOUT);
         fence_proxy_async_global();
       }
       __syncwarp();
@@ -583,9 +583,16 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     if (k + kStages < n_my && issue(k + kStages)) ok_mask |= 1u << st;
   }
   if (broken) {
-    // drain copies still in flight (bounded) before the stages are reused or the CTA exits
+    // drain copies still in flight (bounded) before the stages are reused or the CTA exits;
+    // a stage whose copy does not land even then leaves its barrier phase unknown, so the
+    // CTA takes no further work (s_poison) once this item is done
+    bool drained = true;
     for (int st = 0; st < kStages; ++st)
-      if (((ok_mask >> st) & 1u) && mbar_wait(smem_u32(&bars[st]), (phase_bits >> st) & 1u)) phase_bits ^= 1u << st;
+      if ((ok_mask >> st) & 1u) {
+        if (mbar_wait(smem_u32(&bars[st]), (phase_bits >> st) & 1u)) phase_bits ^= 1u << st;
+        else drained = false;
+      }
+    if (!drained && lane == 0) *s_poison = 1;
   }
 
   // ---- per-warp results -> shared memory, then merge the 4 warps into the partial
@@ -726,6 +733,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
   int* s_next = s_last + 1;
   uint64_t* merge_bar = reinterpret_cast<uint64_t*>(smem + C::kCtl + kWarps * kStages * 8 + 8);
   uint64_t* slab_bar = merge_bar + 1;
+  int* s_poison = reinterpret_cast<int*>(slab_bar + 1);
   float* qin = reinterpret_cast<float*>(smem + C::kQin);
   float* qts = reinterpret_cast<float*>(smem + C::kQts);
   float* qss = reinterpret_cast<float*>(smem + C::kQss);
@@ -734,6 +742,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
     for (int i = 0; i < kWarps * kStages; ++i) mbar_init(smem_u32(&bars[i]), 1);
     mbar_init(smem_u32(merge_bar), 1);
     mbar_init(smem_u32(slab_bar), 1);
+    *s_poison = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -750,7 +759,9 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
   unsigned* app_done = reinterpret_cast<unsigned*>(kp.base + kp.lay.app_done);
   bool waited = false;
   uint32_t phase_bits = 0, merge_phase = 0, slab_phase = 0;
-  for (int id = wq.first(); id >= 0; id = wq.next(s_next)) {
+  // (a CTA whose page copies did not land takes no further work: *s_poison, written before
+  // the item's last barriers)
+  for (int id = wq.first(); id >= 0; id = *s_poison ? -1 : wq.next(s_next)) {
     if constexpr (FUSED) {
       if (id < n_app) {
         fused_append_task<G, GROUP, NW>(kp, layer, id, smem, smem_u32(merge_bar), merge_phase, waited, k_new, v_new);
@@ -799,7 +810,8 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
     auto wait_dep = [&] {
       if (!dep) return;
       const unsigned* ctr = ctrs + (it.dep == kDepPages ? 1 : 0);
-      if (threadIdx.x == 0 && !wait_counter(ctr, unsigned(dr.app_expect))) flag(kp, OSCAR_FLAG_TIMEOUT);
+      if (threadIdx.x == 0 && !wait_counter(ctr, unsigned(dr.app_expect), kp.counter_polls))
+        flag(kp, OSCAR_FLAG_TIMEOUT);
       __syncthreads();
       fence_proxy_async_global();  // the append's rows, seen through the acquire, before bulk copies
     };
@@ -810,7 +822,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
       for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) store_slot<G>(part, e / kHeadDim, e % kHeadDim, -INFINITY, 0.f, 0.f);
     } else if (it.kind == 0) {
       int2_pages_item<G, GROUP, NW>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask,
-                                pending && it.dep == kDepNone ? ctrs + 1 : nullptr);
+                                    pending && it.dep == kDepNone ? ctrs + 1 : nullptr, s_poison);
     } else {
       bf16_tokens_item<G, NW>(kp, layer, it, dr, qts, part, smem, prestaged, wait_dep);
     }
@@ -927,26 +939,15 @@ static __device__ __align__(256) uint8_t g_decode_scratch[kStaticScratchBytes];
 size_t static_scratch_bytes() { return kStaticScratchBytes; }
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mutex;
-uint8_t* g_scratch_ptr[kMaxDevices] = {};
-
 // Device address of g_decode_scratch on the current device.  The host-side name of the
-// array is only a stand-in, so the address is looked up once per device, with that
-// device current, and cached.
+// array is only a stand-in, so the address is looked up with the device current, on every
+// call (cheap after the first, which loads the module): a cached address would go stale
+// when a host framework tears the context down and makes a new one.
 int scratch_address(uint8_t** out) {
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t e = cudaGetSymbolAddress(&p, g_decode_scratch);
   if (e != cudaSuccess) return int(e);
-  if (dev < 0 || dev >= kMaxDevices) return int(cudaErrorInvalidDevice);
-  std::lock_guard<std::mutex> lock(g_scratch_mutex);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return int(e);
-    g_scratch_ptr[dev] = static_cast<uint8_t*>(p);
-  }
-  *out = g_scratch_ptr[dev];
+  *out = static_cast<uint8_t*>(p);
   return 0;
 }
 }  // namespace

@@ -173,6 +173,9 @@ struct oscar_cache {
   bool planned_with_reservation = false;  // the plan already counts the reserved tokens
   int dec_n_req = 0, dec_items = 0, dec_bf16_items = 0, dec_max_pages = 0;
   DecodeWorkspace ws{};
+  int device = 0;              // the device current at creation (the device of `base`)
+  uint32_t counter_polls = 0;  // oscar_set_wait_limit (0 = kDefaultCounterPolls)
+  uint32_t inject = 0;         // oscar_inject_fault: host-side faults armed for the next plan
 };
 
 namespace {
@@ -197,6 +200,7 @@ KernelParams kernel_params(const oscar_cache* c) {
   kp.max_requests = c->cfg.max_requests;
   kp.max_pages = c->cfg.max_pages;
   kp.max_pages_per_request = c->cfg.max_pages_per_request;
+  kp.counter_polls = c->counter_polls ? c->counter_polls : kDefaultCounterPolls;
   kp.lay = c->lay;
   return kp;
 }
@@ -292,6 +296,7 @@ oscar_status oscar_cache_create(const oscar_config* cfg, void* device_mem, size_
   c->base = static_cast<uint8_t*>(device_mem);
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
+  c->device = dev;
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&c->n_sm, cudaDevAttrMultiProcessorCount, dev);
   c->reqs.resize(cfg->max_requests);
   c->refcount.assign(cfg->max_pages, 0);
@@ -417,6 +422,17 @@ oscar_status oscar_request_free(oscar_cache* c, int slot) {
             c->h_page_table + size_t(slot + 1) * c->cfg.max_pages_per_request, -1);
   r = Request();
   c->planned = false;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_cache_stats(const oscar_cache* c, int* free_pages, int* free_slots) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (free_pages) *free_pages = int(c->free_pages.size());
+  if (free_slots) {
+    int n = 0;
+    for (const Request& r : c->reqs) n += !r.in_use;
+    *free_slots = n;
+  }
   return OSCAR_OK;
 }
 
@@ -696,6 +712,13 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   }
   const int nw = decode_warps(G, wide);
   for (int i = 0; i < n_req; ++i) app_expect[i] = 2 * append_task_split(nw) * app_items[i];  // per kv-head
+  if ((c->inject & OSCAR_FAULT_LOST_APPEND_SIGNAL) && c->reserved)
+    for (int i = 0; i < n_req; ++i)
+      if (app_expect[i] > 0) {  // one signal more than the append tasks send: it never arrives
+        ++app_expect[i];
+        c->inject &= ~OSCAR_FAULT_LOST_APPEND_SIGNAL;
+        break;
+      }
   auto split_count = [](int a, int b, int step) { return (a > 0 ? ceil_div(a, step) : 0) + (b > a ? ceil_div(b - a, step) : 0); };
   long long n_bf_items = 0;
   // BF16 items of one CTA chunk: 16 tokens per warp
@@ -920,6 +943,12 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int layer, const voi
   if (!c->planned) return fail(OSCAR_ERR_STATE, "no decode plan (plan after every append commit)");
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (!q || !out) return fail(OSCAR_ERR_INVALID_ARG, "NULL q or out");
+  int dev = -1;
+  cudaError_t de = cudaGetDevice(&dev);
+  if (de != cudaSuccess) return fail(OSCAR_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(de));
+  if (dev != c->device)
+    return fail(OSCAR_ERR_INVALID_ARG, "current device %d is not the cache's device %d (the library scratch is looked "
+                "up on the current device)", dev, c->device);
   bool too_big = false;
   int e = launch_decode_static_scratch(kernel_params(c), layer, q, out, out_f32, c->ws, c->dec_wide,
                                        c->n_sm, stream, &g_launches, &too_big);
@@ -932,6 +961,48 @@ oscar_status oscar_decode_attention_noalloc(oscar_cache* c, int layer, const voi
   return OSCAR_OK;
 }
 
+size_t oscar_calibration_workspace_bytes(int n_tokens, int n_q_heads, int n_kv_heads) {
+  if (n_tokens <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads) return 0;
+  return calib_workspace(n_tokens, n_q_heads, n_kv_heads).total;
+}
+
+oscar_status oscar_calibrate_layer(const void* q, const void* k, const void* v, int n_tokens, int n_q_heads,
+                                   int n_kv_heads, long long clip_rank, int rotation, float* R_K, float* R_V,
+                                   float* clip_K, float* clip_V, double* covariances, void* workspace,
+                                   size_t ws_bytes, void* stream) {
+  g_launches = 0;
+  if (!q || !k || !v || !R_K || !R_V || !clip_K || !clip_V || !workspace)
+    return fail(OSCAR_ERR_INVALID_ARG, "NULL input, output or workspace");
+  if (n_tokens <= 0 || n_q_heads <= 0 || n_kv_heads <= 0 || n_q_heads % n_kv_heads)
+    return fail(OSCAR_ERR_INVALID_ARG, "bad shape: %d tokens, %d query heads, %d kv-heads", n_tokens, n_q_heads,
+                n_kv_heads);
+  if (rotation != OSCAR_ROTATION_OSCAR && rotation != OSCAR_ROTATION_HADAMARD)
+    return fail(OSCAR_ERR_INVALID_ARG, "unknown rotation %d", rotation);
+  if (clip_rank < 1 || clip_rank > (long long)n_tokens * kHeadDim)
+    return fail(OSCAR_ERR_INVALID_ARG, "clip_rank %lld outside [1, %lld]", clip_rank, (long long)n_tokens * kHeadDim);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(OSCAR_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  const size_t need = calib_workspace(n_tokens, n_q_heads, n_kv_heads).total;
+  if (ws_bytes < need) return fail(OSCAR_ERR_INVALID_ARG, "calibration workspace of %zu bytes < %zu needed", ws_bytes, need);
+  const int e = launch_calibrate(q, k, v, n_tokens, n_q_heads, n_kv_heads, long(clip_rank),
+                                 rotation == OSCAR_ROTATION_HADAMARD, R_K, R_V, clip_K, clip_V, covariances,
+                                 static_cast<uint8_t*>(workspace), stream, &g_launches);
+  if (e) return fail(OSCAR_ERR_CUDA, "calibration launch: %s", cudaGetErrorString(cudaError_t(e)));
+  return OSCAR_OK;
+}
+
+oscar_status oscar_set_wait_limit(oscar_cache* c, uint32_t counter_polls) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  c->counter_polls = counter_polls;
+  return OSCAR_OK;
+}
+
+oscar_status oscar_inject_fault(oscar_cache* c, uint32_t faults) {
+  if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
+  if (faults & ~uint32_t(OSCAR_FAULT_LOST_APPEND_SIGNAL)) return fail(OSCAR_ERR_INVALID_ARG, "unknown faults %#x", faults);
+  c->inject |= faults;
+  return OSCAR_OK;
+}
+
 oscar_status oscar_get_status(oscar_cache* c, void* stream, uint32_t* flags) {
   if (!c) return fail(OSCAR_ERR_INVALID_ARG, "cache is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -941,6 +1012,14 @@ oscar_status oscar_get_status(oscar_cache* c, void* stream, uint32_t* flags) {
   if (flags) *flags = f;
   if (f) {
     CUDA_TRY(cudaMemsetAsync(c->base + c->lay.status, 0, 4, s));
+    if (f & OSCAR_FLAG_TIMEOUT) {
+      // a wait gave up: the append-dependency counters may be off by the signals that never
+      // came (or came late), so they restart from zero (no launch of this cache is in flight:
+      // the stream is synchronised and a cache has one launch at a time)
+      CUDA_TRY(cudaMemsetAsync(c->base + c->lay.app_done, 0,
+                               size_t(c->cfg.n_layers) * c->cfg.max_requests * c->cfg.n_kv_heads * 8, s));
+      CUDA_TRY(cudaMemsetAsync(c->base + c->lay.counters, 0, size_t(c->cfg.max_requests) * c->cfg.n_kv_heads * 4, s));
+    }
     CUDA_TRY(cudaStreamSynchronize(s));
     if (f & OSCAR_FLAG_TIMEOUT) return fail(OSCAR_ERR_TIMEOUT, "device flags 0x%x: a bounded wait gave up", f);
     return fail(OSCAR_ERR_BAD_PAGE, "device flags 0x%x: an out-of-range page or slot was skipped", f);

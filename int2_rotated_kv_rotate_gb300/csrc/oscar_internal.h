@@ -111,8 +111,12 @@ struct KernelParams {
   uint8_t* base;
   int n_q_heads, n_kv_heads, gqa, group, n_sink, window, n_layers;
   int max_requests, max_pages, max_pages_per_request;
+  uint32_t counter_polls;  // bounded waits on append-dependency counters give up after this many polls
   DeviceLayout lay;
 };
+// Polls of a dependency-counter wait (each about 0.1-0.3 us: a sleep and an acquire load)
+// unless oscar_set_wait_limit sets another count: roughly a second.
+constexpr uint32_t kDefaultCounterPolls = 1u << 22;
 
 // Decode workspace layout (per plan).
 struct DecodeWorkspace {
@@ -141,6 +145,18 @@ int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* o
 // the planner sizes work items so that one wave holds them all.
 int decode_resident_ctas(int gqa, int group, bool wide, int n_sm);
 int bf16_decode_resident_ctas(int gqa, int n_sm);
+
+// Offline calibration of one layer on the GPU (calib.cu): workspace layout (byte offsets)
+// and the launcher.  C_out (nullable): fp64 [2 H_kv][d][d], C_Q of every kv-head then C_S.
+struct CalibWorkspace {
+  size_t O, partials, C, U, lam, sweeps, keys;
+  int splits;
+  size_t total;
+};
+CalibWorkspace calib_workspace(int n_tokens, int n_q_heads, int n_kv_heads);
+int launch_calibrate(const void* q, const void* k, const void* v, int n_tokens, int n_q_heads, int n_kv_heads,
+                     long clip_rank, bool hadamard_only, float* R_K, float* R_V, float* clip_K, float* clip_V,
+                     double* C_out, uint8_t* ws, void* stream, int* launches);
 
 // Decode with the library's own fixed device scratch instead of a caller workspace
 // (decode.cu).  Returns a cudaError_t as int; `too_big` is set when the plan's workspace

@@ -5,8 +5,11 @@ every device allocation, a serving loop that may not allocate once running), so 
 cannot hand the decode a workspace.  This entry point uses a fixed scratch array inside
 the library instead.  Here it is called through the C ABI twice in a row, with different
 queries, and each output is checked against the ordinary entry point's output on the
-same plan, within the tolerance the parity tests use.  This file runs last so that a
-failure here cannot hide any other test.
+same plan: both run the same kernel on the same plan, so they must agree bit for bit.
+The scratch keeps whatever the previous call left in it, so a larger multi-wave plan of
+another cache (its items taken from the work-queue counters) runs through the same
+scratch first; a wrong scratch offset or a read of stale partials would show.  This file
+runs last so that a failure here cannot hide any other test.
 """
 import numpy as np
 import pytest
@@ -29,11 +32,9 @@ def close(a: torch.Tensor, b: torch.Tensor):
     return err <= MAX_ABS and rel <= REL_L2, (err, rel)
 
 
-def test_noalloc_decode_matches_workspace_decode_twice():
-    w = wl.scaled(wl.WORKLOADS["tiny"], name="noalloc", lognormal_sigma=0.5)
-    cache, _, _ = make_pair(w, SEED, 1, 2, 1500)
-    slots = [cache.alloc(), cache.alloc()]
-    lens = [1500, 700]
+def _filled(w, lens):
+    cache, _, _ = make_pair(w, SEED, 1, len(lens), max(lens))
+    slots = [cache.alloc() for _ in lens]
     ks, vs = [], []
     for r, n in enumerate(lens):
         k, v = wl.gen_kv(w, SEED, 0, r, 0, n, device="cuda")
@@ -42,21 +43,60 @@ def test_noalloc_decode_matches_workspace_decode_twice():
     cache.reserve(slots, lens)
     cache.quantize_append(0, torch.cat(ks).contiguous(), torch.cat(vs).contiguous())
     cache.commit()
+    return cache, slots
+
+
+def _both(cache, q):
+    """(workspace decode, no-allocation decode) fp32 outputs, and the no-alloc bf16 output."""
+    ref = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+    cache.decode(0, q, out_f32=ref)
+    out = torch.empty_like(q)
+    out32 = torch.full(q.shape, float("nan"), dtype=torch.float32, device="cuda")
+    N.oscar_decode_attention_noalloc(cache.handle, 0, q, out, out32)
+    torch.cuda.synchronize()
+    return ref, out32, out
+
+
+def test_noalloc_decode_matches_workspace_decode_twice():
+    w = wl.scaled(wl.WORKLOADS["tiny"], name="noalloc", lognormal_sigma=0.5)
+    cache, slots = _filled(w, [1500, 700])
     cache.plan(slots, max_split_pages=3)
     assert N.oscar_decode_workspace_bytes(cache.handle) <= 8 << 20
     for step in range(2):  # two calls in a row share (and leave behind) the library scratch
         q = wl.gen_q(w, SEED, 0, step, 2, device="cuda")
-        ref = torch.empty(q.shape, dtype=torch.float32, device="cuda")
-        cache.decode(0, q, out_f32=ref)
-        out = torch.empty_like(q)
-        out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
-        N.oscar_decode_attention_noalloc(cache.handle, 0, q, out, out32)
-        torch.cuda.synchronize()
+        ref, out32, out = _both(cache, q)
         ok, (err, rel) = close(out32, ref)
         assert ok, f"call {step}: max-abs {err:.3e}, rel-L2 {rel:.3e}"
+        assert torch.equal(out32, ref), f"call {step}: the two entry points differ"
         assert torch.equal(out.cpu(), out32.cpu().to(torch.bfloat16))
     st, flags = cache.status()
     assert st == 0 and flags == 0
+
+
+def test_noalloc_after_a_larger_multi_wave_plan_of_another_cache():
+    """A plan of single-page items, several times more than the resident CTAs (so the CTAs
+    take them from the work-queue counters), fills much of the scratch; then a smaller plan
+    of the first cache reuses it.  Both agree with the workspace path bit for bit."""
+    big_w = wl.scaled(wl.WORKLOADS["tiny"], name="noalloc_waves", n_q_heads=32, n_kv_heads=8, lognormal_sigma=0.5)
+    big, big_slots = _filled(big_w, [6000, 5000])
+    big.plan(big_slots, max_split_pages=1)
+    n_items, _, _ = big.plan_info()
+    assert n_items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
+    assert N.oscar_decode_workspace_bytes(big.handle) <= 8 << 20
+    w = wl.scaled(wl.WORKLOADS["tiny"], name="noalloc_small", lognormal_sigma=0.5)
+    small, small_slots = _filled(w, [1300, 400])
+    for step in range(2):
+        q = wl.gen_q(big_w, SEED, 0, step, 2, device="cuda")
+        ref, out32, _ = _both(big, q)
+        assert torch.equal(out32, ref), f"large plan, call {step}"
+        small.plan(small_slots, max_split_pages=2 + step)
+        q = wl.gen_q(w, SEED, 0, step, 2, device="cuda")
+        ref, out32, _ = _both(small, q)
+        assert torch.equal(out32, ref), f"small plan after the large one, call {step}"
+    for c in (big, small):
+        st, flags = c.status()
+        assert st == 0 and flags == 0
+        c.close()
 
 
 def test_noalloc_rejects_plans_beyond_the_fixed_scratch():
