@@ -39,13 +39,16 @@ def parse_args(argv=None):
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="qwen3_8b_layer")
+    ap.add_argument("--workload", default="all",
+                    help="one workload, or 'all': the headline workload (the 32B-shaped capacity run) and "
+                         "every other workload under per_workload")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=2026)
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling runs only)")
     ap.add_argument("--no-bf16", action="store_true", help="skip the BF16 comparison")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-serving", action="store_true", help="skip the throughput-mode serving comparison")
     ap.add_argument("--rotation", default="oscar", choices=["oscar", "hadamard"],
                     help="calibrated rotations: OSCAR's (default) or the Hadamard-only ablation")
     return ap.parse_args(argv)
@@ -328,7 +331,7 @@ def bf16_bytes_per_layer(w, L_list):
 
 
 # ---------------------------------------------------------------------------- our arm
-def run_ours(args, world, rank, local):
+def run_ours(args, w, world, rank, local):
     import torch
 
     from int2_rotated_kv_rotate_gb300 import KVCache, OSCAR_FORMAT_BF16, calibrate, workloads as wl
@@ -337,7 +340,6 @@ def run_ours(args, world, rank, local):
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
     dist_init(world, "nccl")
-    w = wl.WORKLOADS[args.workload]
     n_layers = args.layers or w.n_layers
     seed = args.seed + 1000 * rank  # each replica holds its own requests
     total_steps = args.warmup + args.steps
@@ -352,7 +354,7 @@ def run_ours(args, world, rank, local):
     t_cal = time.time()
     for layer in range(n_layers):
         qc, kc, vc = wl.gen_calibration(w, seed, layer, device=dev)
-        RK, RV, cK, cV = calibrate.calibrate_layer_device(qc, kc, vc, w.clip_percentile, rotation=args.rotation)
+        RK, RV, cK, cV = calibrate.calibrate_layer_gpu(qc, kc, vc, w.clip_percentile, rotation=args.rotation)
         cache.set_layer_params(layer, RK, RV, cK, cV)
     t_cal = time.time() - t_cal
     slots = [cache.alloc() for _ in range(B)]
@@ -674,10 +676,11 @@ def bf16_comparison(w, seed, n_layers, lengths, qin, dev, reps):
 
 
 # ---------------------------------------------------------------------------- CPU oracle
-def oracle_sample(w, seed, n_heads_sample: int, context: int):
-    """Build one (layer 0, request 0) oracle stream pair per sampled kv-head at `context`
-    tokens (untimed), returning closures that time one step: append of the step's tokens
-    and decode of one query, for the sampled heads."""
+def oracle_sample(w, seed, heads, context: int):
+    """One (layer 0, request 0) oracle stream pair per entry of `heads` (a kv-head index;
+    entries may repeat, each gets its own streams) at `context` tokens (built untimed), and
+    a function that times one step of entry i: append of the step's tokens and decode of
+    one query."""
     import numpy as np
 
     import oracle
@@ -687,58 +690,107 @@ def oracle_sample(w, seed, n_heads_sample: int, context: int):
 
     qc, kc, vc = wl.gen_calibration(w, seed, 0)
     G = w.gqa
-    streams = []
     K, V = wl.gen_kv(w, seed, 0, 0, 0, context)
     kb, vb = as_bits(K), as_bits(V)
-    for h in range(n_heads_sample):
-        RK, RV, cK, cV = ocal.calibrate_head(qc[:, h * G:(h + 1) * G].float().numpy(), kc[:, h].float().numpy(),
-                                             vc[:, h].float().numpy(), w.clip_percentile)
+    q = as_bits(wl.gen_q(w, seed, 0, 0, 1))[0]
+    n_app = w.append_per_step or 1
+    newK, newV = wl.gen_kv(w, seed, 0, 0, context, n_app)
+    nkb, nvb = as_bits(newK), as_bits(newV)
+    params = {}
+    streams = []
+    for h in heads:
+        if h not in params:
+            params[h] = ocal.calibrate_head(qc[:, h * G:(h + 1) * G].float().numpy(), kc[:, h].float().numpy(),
+                                            vc[:, h].float().numpy(), w.clip_percentile)
+        RK, RV, cK, cV = params[h]
         cap = context + 4096
         sk = oracle.Stream(w.head_dim, w.group, w.n_sink, w.window, cap, RK, cK)
         sv = oracle.Stream(w.head_dim, w.group, w.n_sink, w.window, cap, RV, cV)
         sk.append(np.ascontiguousarray(kb[:, h]))
         sv.append(np.ascontiguousarray(vb[:, h]))
-        streams.append((sk, sv, RK, RV))
-    q = as_bits(wl.gen_q(w, seed, 0, 0, 1))[0]
-    n_app = w.append_per_step or 1
-    newK, newV = wl.gen_kv(w, seed, 0, 0, context, n_app)
-    nkb, nvb = as_bits(newK), as_bits(newV)
+        streams.append((h, sk, sv, RK, RV))
 
-    def one_step(step):
+    def one_head_step(i):
+        h, sk, sv, RK, RV = streams[i]
         t = time.perf_counter()
-        for h, (sk, sv, RK, RV) in enumerate(streams):
-            if sk.length + n_app <= sk.capacity:
-                sk.append(np.ascontiguousarray(nkb[:, h]))
-                sv.append(np.ascontiguousarray(nvb[:, h]))
-            oracle.decode(np.ascontiguousarray(q[h * G:(h + 1) * G]), sk, sv, RK, RV)
+        if sk.length + n_app <= sk.capacity:
+            sk.append(np.ascontiguousarray(nkb[:, h]))
+            sv.append(np.ascontiguousarray(nvb[:, h]))
+        oracle.decode(np.ascontiguousarray(q[h * G:(h + 1) * G]), sk, sv, RK, RV)
         return time.perf_counter() - t
 
-    return one_step
+    return one_head_step
 
 
-def cpu_baseline(w, seed, budget_s=20.0):
-    """Oracle (as it stands) on one host core: µs per layer-step, scaled from a sample of
-    kv-heads of layer 0 of request 0.  The oracle's decode is serial (only its rotation
-    runs on several threads), so the sample runs on one thread and says so."""
+def host_cpu():
+    """(logical cores, CPU model) of the host."""
+    model = ""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu model")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    if not model:
+        try:
+            out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+            for line in out.splitlines():
+                if line.startswith("Model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except (OSError, subprocess.SubprocessError):
+            pass
+    import platform
+
+    return os.cpu_count() or 1, (model or "unknown") + f" ({platform.machine()})"
+
+
+def cpu_baseline(w, seed, budget_s=12.0):
+    """The oracle, as it stands, on the host cores, scaled from a bounded sample of one
+    layer-step of the workload: its decode of one (request, kv-head) is serial C, so the
+    single-thread row runs one head at a time on one thread, and the all-cores row runs one
+    head per host core at once (threads: the oracle's C calls release the interpreter lock).
+    Both rows: layer 0 of request 0 at up to 32768 tokens of context, append of the
+    step's tokens + decode of one query per head, scaled to the workload's batch, kv-heads
+    and context."""
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
 
     oracle.set_threads(1)
+    nproc, model = host_cpu()
     context = min(w.context, 32768)
-    n_heads = 2
-    step = oracle_sample(w, seed, n_heads, context)
+    heads = [i % w.n_kv_heads for i in range(min(nproc, w.n_kv_heads * w.batch))]
+    step = oracle_sample(w, seed, heads, context)  # one stream pair per thread of the all-cores row
+    scale = w.n_kv_heads * w.batch * (w.context / context)  # head-steps of one layer-step
+    # one thread
     times = []
-    t_end = time.time() + budget_s
-    s = 0
-    while time.time() < t_end and s < 50:
-        times.append(step(s))
-        s += 1
-    per_head = statistics.median(times) / n_heads
-    scale_layer = w.n_kv_heads * w.batch * (w.context / context)
-    us = per_head * scale_layer * 1e6
-    return {"value": round(us, 1), "unit": "us/layer/step", "cores": 1, "kind": "oracle",
-            "sample": f"one thread; {n_heads} of {w.n_kv_heads} kv-heads of one request, layer 0, context {context}: append "
-                      f"{w.append_per_step or 1} token(s) + decode 1 per step, {len(times)} steps, median, scaled "
-                      f"x{scale_layer:.1f} to one layer-step of the workload"}
+    t_end = time.time() + budget_s / 2
+    while time.time() < t_end and len(times) < 30:
+        times.append(step(len(times) % len(heads)))
+    per_head = statistics.median(times)
+    one = per_head * scale * 1e6
+    # all cores: one head per thread, nproc heads at once (heads beyond the workload's
+    # kv-heads reuse their streams: the same work)
+    rounds = []
+    t_end = time.time() + budget_s / 2
+    with ThreadPoolExecutor(max_workers=len(heads)) as ex:
+        while time.time() < t_end and len(rounds) < 10:
+            t = time.perf_counter()
+            list(ex.map(step, range(len(heads))))
+            rounds.append(time.perf_counter() - t)
+    per_round = statistics.median(rounds)
+    allc = per_round * (scale / len(heads)) * 1e6
+    return {"value": round(one, 1), "unit": "us/layer/step", "cores": 1, "kind": "oracle", "nproc": nproc,
+            "cpu_model": model,
+            "sample": f"layer 0 of request 0, context {context}: append {w.append_per_step or 1} token(s) + decode "
+                      f"1 query per kv-head; one thread: median of {len(times)} head-steps, scaled x{scale:.0f} "
+                      f"(kv-heads x batch x context ratio) to one layer-step",
+            "all_cores": {"value": round(allc, 1), "unit": "us/layer/step", "cores": len(heads),
+                          "sample": f"{len(heads)} head-steps at once on {len(heads)} threads, median of "
+                                    f"{len(rounds)} rounds, scaled x{scale / len(heads):.1f}"}}
 
 
 # ---------------------------------------------------------------------------- output
@@ -747,20 +799,57 @@ def config_of(w, n_layers, rotation="oscar"):
             "rotation": rotation,
             "context": w.context, "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
             "group": w.group, "page": w.page, "sink": w.n_sink, "window": w.window,
-            "l2": "inputs larger than L2: every layer's cache is distinct and the step cycles through all layers"}
+            "l2": "inputs larger than L2: every layer's cache is distinct and the step cycles through all layers"
+                  if n_layers > 1 or w.batch > 1 else
+                  "one layer of one request (about 1 MB) fits in L2: the step is launch-bound and reported in us only"}
 
 
-def main(argv=None):
-    args = parse_args(argv)
-    world, rank, local = dist_info()
+def serving_comparison(seed: int, dev, budget_gib: float = 2.0):
+    """Throughput mode: the serving loop (continuous batching, prefix-cache hits) over the
+    INT2 cache and over the BF16 cache, each sized to the same HBM budget, serving the same
+    requests to completion.  Shape: the 8B-shaped layer (32q/8kv, g128) with 8 layers."""
+    import torch
+
+    from int2_rotated_kv_rotate_gb300 import OSCAR_FORMAT_BF16, OSCAR_FORMAT_INT2, calibrate, serving
     from int2_rotated_kv_rotate_gb300 import workloads as wl
 
-    w = wl.WORKLOADS[args.workload]
-    if args.impl == "reference":
-        return main_reference(args, world, rank, w)
-    r = run_ours(args, world, rank, local)
-    if rank != 0:
-        return 0
+    w = wl.scaled(wl.WORKLOADS["qwen3_8b_layer"], name="serving_8b_8layers", n_layers=8)
+    budget = int(budget_gib * (1 << 30))
+    spec = dict(n=48, prompt=(4096, 12288), gen=(64, 192), groups=12, prefix=2048)
+    tokens = serving.TokenSource(w, seed, pool_tokens=16384, device=dev)
+    params = [[], [], [], []]
+    for layer in range(w.n_layers):
+        qc, kc, vc = wl.gen_calibration(w, seed, layer, device=dev)
+        for i, a in enumerate(calibrate.calibrate_layer_gpu(qc, kc, vc, w.clip_percentile)):
+            params[i].append(a)
+    out = {"shape": w.description.split(",")[0] + ", 8 layers", "hbm_budget_bytes": budget,
+           "requests": spec["n"], "prompt_tokens": list(spec["prompt"]), "generated_tokens": list(spec["gen"]),
+           "prefix": f"{spec['groups']} groups of {spec['n'] // spec['groups']} requests share a "
+                     f"{spec['prefix']}-token prefix (prefix holder + shared pages)"}
+    for name, fmt in (("int2", OSCAR_FORMAT_INT2), ("bf16", OSCAR_FORMAT_BF16)):
+        reqs = serving.make_requests(spec["n"], spec["prompt"], spec["gen"], spec["groups"], seed)
+        loop = serving.ServingLoop(w, fmt, budget, tokens, layer_params=params if fmt == OSCAR_FORMAT_INT2 else None,
+                                   max_requests=spec["n"] + spec["groups"] + 1, max_len=spec["prompt"][1] + spec["gen"][1] + 64,
+                                   prefix_tokens=spec["prefix"], device=dev)
+        st = loop.run(reqs)
+        status, flags = loop.cache.status()
+        assert status == 0, f"serving {name}: device flags {flags:#x}"
+        loop.close()
+        out[name] = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in st.items() if k != "batch_sum"}
+        del loop
+        torch.cuda.empty_cache()
+    out["throughput_ratio_int2_over_bf16"] = round(out["int2"]["tokens_per_s"] / out["bf16"]["tokens_per_s"], 3)
+    out["decode_throughput_ratio_int2_over_bf16"] = round(
+        out["int2"]["decode_tokens_per_s"] / out["bf16"]["decode_tokens_per_s"], 3)
+    return out
+
+
+HEADLINE = "qwen3_32b_capacity"
+OTHERS = ["tiny", "qwen3_8b_layer", "long_batch", "ragged_prefix"]
+
+
+def result_line(args, w, r, world):
+    """The JSON object of one workload's measurement."""
     n_layers = r["n_layers"]
     us_layer_step = r["step_ms"] * 1000.0 / n_layers
     peak, peak_kind = measured_peaks()
@@ -800,35 +889,85 @@ def main(argv=None):
         # per request-layer: the BF16 cache may hold fewer requests of the batch (HBM capacity)
         line["speedup_vs_bf16_decode"] = round((r["bf16"]["us_per_layer"] / r["bf16"]["requests"]) /
                                                (r["decode_us"] / r["B"]), 3)
-    if world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, args.seed)
+    return line
+
+
+def release_gpu_memory():
+    import gc
+
+    import torch
+
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    world, rank, local = dist_info()
+    from int2_rotated_kv_rotate_gb300 import workloads as wl
+
+    names = [HEADLINE] + OTHERS if args.workload == "all" else [args.workload]
+    if args.impl == "reference":
+        return main_reference(args, world, rank, wl.WORKLOADS[names[0]])
+    if args.layers and len(names) > 1:
+        raise SystemExit("--layers applies to one workload (--workload NAME)")
+    lines = {}
+    for name in names:
+        w = wl.WORKLOADS[name]
+        r = run_ours(args, w, world, rank, local)
+        lines[name] = result_line(args, w, r, world)
+        if rank == 0 and world == 1 and not args.no_cpu_baseline and name == names[0]:
+            lines[name]["cpu_baseline"] = cpu_baseline(w, args.seed)
+        del r
+        release_gpu_memory()
+    serving_line = None
+    if len(names) > 1 and not args.no_serving:
+        import torch
+
+        serving_line = serving_comparison(args.seed + 1000 * rank, torch.device("cuda", local))
+        release_gpu_memory()
+    if rank != 0:
+        return 0
+    line = lines[names[0]]
+    if serving_line:
+        line["serving"] = serving_line
+    if len(names) > 1:
+        line["per_workload"] = {n: {k: v for k, v in lines[n].items() if k not in ("metric", "n_gpus", "steps", "warmup",
+                                                                                  "higher_is_better", "scaling",
+                                                                                  "vs_baseline", "data")}
+                                for n in names[1:]}
     print(json.dumps(line), flush=True)
     return 0
 
 
 def main_reference(args, world, rank, w):
-    """The CPU oracle on the host cores, same metric and workload, bounded samples."""
+    """The CPU oracle on the host cores, same metric and workload: each step is a bounded
+    sample (one kv-head of one request at up to 32768 tokens: append + decode), timed as
+    it runs; the line's value scales the sample to one layer-step of the workload, and
+    ms_per_step is the sample's own measured time, so ms_per_step x steps is time spent."""
     if rank != 0:
         return 0
     import oracle
 
     oracle.set_threads(1)  # the oracle's decode is serial; its rotation alone would use more
+    nproc, model = host_cpu()
     context = min(w.context, 32768)
-    n_heads = 1
-    step = oracle_sample(w, args.seed, n_heads, context)
+    step = oracle_sample(w, args.seed, [0], context)
     for s in range(args.warmup):
-        step(s)
-    times = [step(args.warmup + s) for s in range(args.steps)]
-    scale = w.n_kv_heads * w.batch * (w.context / context) / n_heads
+        step(0)
+    times = [step(0) for s in range(args.steps)]
+    scale = w.n_kv_heads * w.batch * (w.context / context)
     us = statistics.mean(times) * scale * 1e6
+    sample = (f"one thread; per step one kv-head of request 0, layer 0, context {context}: append "
+              f"{w.append_per_step or 1} token(s) + decode 1 query, measured {statistics.mean(times) * 1e3:.1f} ms; "
+              f"value = that x{scale:.0f} (kv-heads x batch x context ratio) = one layer-step of the workload")
     line = {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": "us/layer/step", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us * w.n_layers / 1000.0, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(statistics.mean(times) * 1e3, 3),
+            "sample_scale": round(scale, 3),
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64 attention, f32 quantizer",
             "data": "synthetic", "config": config_of(w, w.n_layers),
-            "cpu_baseline": {"value": round(us, 1), "unit": "us/layer/step", "cores": 1,
-                             "kind": "oracle",
-                             "sample": f"one thread; {n_heads} kv-head of one request, layer 0, context {context}, append "
-                                       f"{w.append_per_step or 1} + decode 1 per step, scaled x{scale:.1f}"},
+            "cpu_baseline": {"value": round(us, 1), "unit": "us/layer/step", "cores": 1, "kind": "oracle",
+                             "nproc": nproc, "cpu_model": model, "sample": sample},
             "e2e": {"value": round(us, 1), "unit": "us/layer/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "liboscar.so")
-SOURCES = ["oscar_host.cpp", "append.cu", "decode.cu", "bf16.cu"]
+SOURCES = ["oscar_host.cpp", "append.cu", "decode.cu", "bf16.cu", "calib.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -148,28 +148,25 @@ class KVCache:
 
     def int2_rows(self, layer: int, slot: int, kvh: int, kv: int, positions):
         """Device-stored 32-byte code rows and scale/zero words of INT2 positions (host)."""
-        pages = self.pages(slot)
         H = self.cfg.n_kv_heads
         ng = 128 // self.cfg.group
+        pos = torch.as_tensor(list(positions) if not torch.is_tensor(positions) else positions, dtype=torch.long)
+        if pos.numel() == 0:
+            return torch.empty((0, 32), dtype=torch.uint8), torch.empty((0, ng * 2), dtype=torch.int16)
+        pages = torch.tensor(self.pages(slot), dtype=torch.long)
+        phys = pages[pos // 64]
+        t = pos % 64
         code_head = self.layout.codes_page_bytes
         sz_head = self.layout.sz_page_bytes
         code_layer = self.cfg.max_pages * H * code_head
         sz_layer = self.cfg.max_pages * H * sz_head
-        mem = self.mem
-        idx_c, idx_s = [], []
-        for p in positions:
-            phys = pages[p // 64]
-            t = p % 64
-            c0 = self.layout.codes + layer * code_layer + (phys * H + kvh) * code_head + kv * 64 * 32 + t * 32
-            s0 = self.layout.sz + layer * sz_layer + (phys * H + kvh) * sz_head + kv * 64 * ng * 4 + t * ng * 4
-            idx_c.append(torch.arange(c0, c0 + 32))
-            idx_s.append(torch.arange(s0, s0 + ng * 4))
-        if not idx_c:
-            return torch.empty((0, 32), dtype=torch.uint8), torch.empty((0, ng * 2), dtype=torch.int16)
-        ic = torch.stack(idx_c).to(mem.device)
-        is_ = torch.stack(idx_s).to(mem.device)
-        rows = mem[ic].cpu()
-        sz = mem[is_].cpu().contiguous().view(torch.int16)
+        c0 = self.layout.codes + layer * code_layer + (phys * H + kvh) * code_head + kv * 64 * 32 + t * 32
+        s0 = self.layout.sz + layer * sz_layer + (phys * H + kvh) * sz_head + kv * 64 * ng * 4 + t * ng * 4
+        dev = self.mem.device
+        ic = (c0[:, None] + torch.arange(32)[None, :]).to(dev)
+        is_ = (s0[:, None] + torch.arange(ng * 4)[None, :]).to(dev)
+        rows = self.mem[ic].cpu()
+        sz = self.mem[is_].cpu().contiguous().view(torch.int16)
         return rows, sz
 
     def _head_block(self, pool_off: int, per_head: int, slot: int, layer: int, kvh: int):

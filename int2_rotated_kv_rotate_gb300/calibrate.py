@@ -144,40 +144,37 @@ def calibrate_layer(q, k, v, percentile: float = 99.9, rotation: str = "oscar"):
     return RK, RV, cK, cV
 
 
-def calibrate_layer_device(q, k, v, percentile: float = 99.9, rotation: str = "oscar"):
-    """Same calibration with the heavy products on the tensors' device (torch): the causal
-    attention in fp32, covariances and rotated activations in fp64, eigendecomposition
-    on the host in fp64.  q [N, H_q, d], k and v [N, H_kv, d] torch tensors.
-    Returns fp32 numpy R_K, R_V [H_kv, d, d] and clip_K, clip_V [H_kv]."""
+def clip_rank(n_values: int, percentile: float) -> int:
+    """1-based nearest rank of a percentile among n values: ceil(p / 100 * n), evaluated on
+    the decimal percentile (99.9 is 999/10 exactly)."""
+    num, den = _decimal_ratio(percentile)
+    return max(1, -(-(num * n_values) // (den * 100)))
+
+
+def calibrate_layer_gpu(q, k, v, percentile: float = 99.9, rotation: str = "oscar", covariances: bool = False):
+    """The same calibration on the GPU, in fp64, by the library's CUDA kernels
+    (oscar_calibrate_layer: covariances, causal attention, Jacobi eigenbases, R = U H P,
+    radix-selected clip).  q [N, H_q, d], k and v [N, H_kv, d] bf16 torch tensors on the
+    device.  Returns fp32 numpy R_K, R_V [H_kv, d, d] and clip_K, clip_V [H_kv] (and, with
+    covariances=True, the fp64 covariances [2 H_kv, d, d] as a torch tensor: C_Q of every
+    kv-head, then C_S)."""
     import torch
 
+    from . import _native as N
+
     _check_rotation(rotation)
-    n, Hq, d = q.shape
-    Hkv = k.shape[1]
-    G = Hq // Hkv
-    qf, kf, vf = q.float(), k.float(), v.float()
-    future = torch.ones(n, n, dtype=torch.bool, device=q.device).triu(1)
-    RK = np.empty((Hkv, d, d), np.float32)
-    RV = np.empty((Hkv, d, d), np.float32)
-    cK = np.empty(Hkv, np.float32)
-    cV = np.empty(Hkv, np.float32)
-    num, den = _decimal_ratio(percentile)
-    for h in range(Hkv):
-        Qh = qf[:, h * G:(h + 1) * G, :]
-        flat = Qh.reshape(-1, d).double()
-        C_Q = (flat.T @ flat) / (n * G)
-        logits = torch.einsum("ngd,md->gnm", Qh, kf[:, h]) / math.sqrt(d)
-        logits.masked_fill_(future, float("-inf"))
-        O = torch.softmax(logits, dim=-1) @ vf[:, h]
-        Of = O.reshape(-1, d).double()
-        C_S = (Of.T @ Of) / (n * G)
-        if rotation == "hadamard":
-            RK[h] = RV[h] = rotation_from_eigenbasis(np.eye(d)).astype(np.float32)
-        else:
-            RK[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_Q.cpu().numpy())).astype(np.float32)
-            RV[h] = rotation_from_eigenbasis(sorted_eigenbasis(C_S.cpu().numpy())).astype(np.float32)
-        for R, X, out in ((RK[h], kf[:, h], cK), (RV[h], vf[:, h], cV)):
-            rot = (X.double() @ torch.from_numpy(R).to(X.device).double()).abs().flatten()
-            rank = max(1, -(-(num * rot.numel()) // (den * 100)))
-            out[h] = np.float32(torch.kthvalue(rot, rank).values.item())
-    return RK, RV, cK, cV
+    q, k, v = (t.to(torch.bfloat16).contiguous() for t in (q, k, v))
+    n, hq, d = q.shape
+    hkv = k.shape[1]
+    dev = q.device
+    ws = torch.empty(N.oscar_calibration_workspace_bytes(n, hq, hkv), dtype=torch.uint8, device=dev)
+    RK = torch.empty((hkv, d, d), dtype=torch.float32, device=dev)
+    RV = torch.empty_like(RK)
+    cK = torch.empty(hkv, dtype=torch.float32, device=dev)
+    cV = torch.empty_like(cK)
+    C = torch.zeros((2 * hkv, d, d), dtype=torch.float64, device=dev) if covariances else None
+    N.oscar_calibrate_layer(q, k, v, clip_rank(n * d, percentile),
+                            N.OSCAR_ROTATION_HADAMARD if rotation == "hadamard" else N.OSCAR_ROTATION_OSCAR,
+                            RK, RV, cK, cV, ws, covariances=C)
+    out = (RK.cpu().numpy(), RV.cpu().numpy(), cK.cpu().numpy(), cV.cpu().numpy())
+    return out + (C,) if covariances else out

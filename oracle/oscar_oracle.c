@@ -93,11 +93,16 @@ void oo_unpack_row(const uint8_t* row, int d, uint8_t* codes) {
  * i = 0..d-1 ascending; r_j = bf16_rne(acc_j).   ([OSCAR summary] §2.2-A.3, §2.2-B)
  * ---------------------------------------------------------------------------------- */
 static void rotate_one(const float* R, const uint16_t* x, int d, uint16_t* r) {
-  for (int j = 0; j < d; ++j) {
-    float acc = 0.0f;
-    for (int i = 0; i < d; ++i) acc = fmaf(R[(size_t)i * d + j], bf16_to_f32(x[i]), acc);
-    r[j] = f32_to_bf16_rne(acc);
+  /* acc[j] takes its fmaf steps in the order i = 0..d-1; the outputs are independent, so
+   * they advance together (j inner), which changes no output's sequence of operations */
+  float acc[512];
+  for (int j = 0; j < d; ++j) acc[j] = 0.0f;
+  for (int i = 0; i < d; ++i) {
+    const float xi = bf16_to_f32(x[i]);
+    const float* Ri = R + (size_t)i * d;
+    for (int j = 0; j < d; ++j) acc[j] = fmaf(Ri[j], xi, acc[j]);
   }
+  for (int j = 0; j < d; ++j) r[j] = f32_to_bf16_rne(acc[j]);
 }
 
 void oo_rotate(const float* R, const uint16_t* x, long n_tok, int d, uint16_t* r) {
