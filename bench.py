@@ -368,7 +368,8 @@ def run_ours(args, w, world, rank, local):
     # ---- per-step inputs (device) and fixed buffers the captured step reads
     Hkv, Hq, d = w.n_kv_heads, w.n_q_heads, w.head_dim
     steps_in = []
-    for s in range(total_steps + 1):
+    n_inputs = total_steps + 1 + (0 if args.no_e2e else E2E_STEPS)  # timed, roofline, end-to-end steps
+    for s in range(n_inputs):
         cur, n_new = plan.steps[s]
         rows = sum(n_new)
         K = torch.empty((n_layers, rows, Hkv, d), dtype=torch.bfloat16, device=dev)
@@ -514,9 +515,12 @@ def run_ours(args, w, world, rank, local):
     # step i computes (both inside the timed region)
     e2e = None
     if not args.no_e2e:
-        hK = [steps_in[s][0].cpu().pin_memory() for s in range(total_steps + 1)]
-        hV = [steps_in[s][1].cpu().pin_memory() for s in range(total_steps + 1)]
-        hQ = [steps_in[s][2].cpu().pin_memory() for s in range(total_steps + 1)]
+        # the end-to-end steps continue the sequence after the roofline's step (their own
+        # appends, as the plan sized the page pool for)
+        e2e_first = total_steps + 1
+        hK = {s: steps_in[s][0].cpu().pin_memory() for s in range(e2e_first, n_inputs)}
+        hV = {s: steps_in[s][1].cpu().pin_memory() for s in range(e2e_first, n_inputs)}
+        hQ = {s: steps_in[s][2].cpu().pin_memory() for s in range(e2e_first, n_inputs)}
         hout = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
         bufs = [(kin, vin, qin, out), tuple(torch.empty_like(t) for t in (kin, vin, qin, out))]
         views = [tuple([t[layer] for layer in range(n_layers)] for t in bset) for bset in bufs]
@@ -530,7 +534,7 @@ def run_ours(args, w, world, rank, local):
         used = [False, False]
 
         def upload(i, b):
-            s = total_steps - n_e2e + i  # reuse shapes; values are inputs only
+            s = e2e_first + i
             with torch.cuda.stream(cs):
                 if used[b]:
                     cs.wait_event(in_free[b])
@@ -547,7 +551,7 @@ def run_ours(args, w, world, rank, local):
             b = i % 2
             if i + 1 < n_e2e:
                 upload(i + 1, 1 - b)
-            cache.reserve(slots, steps_in[total_steps - n_e2e + i][3])
+            cache.reserve(slots, steps_in[e2e_first + i][3])
             cache.plan(slots)
             comp.wait_event(in_ready[b])
             if used[b]:

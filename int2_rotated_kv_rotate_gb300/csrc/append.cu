@@ -1,9 +1,8 @@
 // Quantize-on-append into the mixed-precision paged cache, and the plain BF16 page append.
 //
-// One CTA = one work item x one kv-head x {K, V} (grid y, z); 512 threads: thread (g, j)
-// owns rotated channel j of the item's tokens 4g..4g+3 (four token groups keep four warps
-// per scheduler busy; one warp each left the kernel latency-bound).  The item logic is in
-// append_dev.cuh.
+// Standalone append: one CTA takes passes of four work items x one kv-head x {K, V}
+// (grid y, z), loading R once; see append_kernel.  The item logic of the fused append tasks
+// (inside the decode launch) is in append_dev.cuh; both follow the same format.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -22,52 +21,210 @@ constexpr int kThreads = 512;
 // before the wait on the preceding kernel (R is written long before, by
 // oscar_set_layer_params).
 constexpr int kRBytes = kHeadDim * kHeadDim * 4;
-constexpr int kAppendSmem = kRBytes + 16;
+constexpr int kGroupItems = 4;                 // items (16 tokens or ring slots each) per CTA pass
+constexpr int kGroupTok = kGroupItems * kTok;  // 64: warp w owns tokens 4w .. 4w + 3 of them
+constexpr int kXsBytes = kHeadDim * kGroupTok * 4;  // new tokens' values, transposed: xs[i][token]
+constexpr int kAppendSmem = kRBytes + kXsBytes + 16;
 
+// INT2 row of one token from the clipped values of the calling lane's four channels
+// (lane l holds channels 4l .. 4l + 3); all 32 lanes of the warp call it together.
+// Format: per group s = bf16((max - min) / 3), z = bf16(min), code = s == 0 ? 0 :
+// clamp(rint((x - z) / s), 0, 3); channel c = 16f + 2w + h at bit 32w + 16h + 2f of the row,
+// so lane l's channels land in words 2(l & 3) and 2(l & 3) + 1, field l >> 2.
+template <int GROUP>
+__device__ __forceinline__ void quantize_row(const float (&x)[4], const RowPtr& dst) {
+  const int lane = threadIdx.x & 31;
+  float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
+  float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+  // group of 128 channels: the whole warp; of 32: lanes 8G .. 8G + 7
+#pragma unroll
+  for (int off = GROUP == 128 ? 16 : 4; off > 0; off >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, off));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  }
+  const uint16_t sb = bf16_rne(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
+  const uint16_t zb = bf16_rne(mn);
+  const float sc = bf16_f32(sb), z = bf16_f32(zb);
+  uint32_t code[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    code[c] = sc != 0.0f ? static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[c], z), sc)), 0.0f), 3.0f))
+                         : 0u;
+  const int f = lane >> 2;
+  uint32_t wa = (code[0] << (2 * f)) | (code[1] << (16 + 2 * f));
+  uint32_t wb = (code[2] << (2 * f)) | (code[3] << (16 + 2 * f));
+#pragma unroll
+  for (int off = 4; off < 32; off <<= 1) {  // the eight lanes sharing (l & 3) hold the eight fields
+    wa |= __shfl_xor_sync(0xffffffffu, wa, off);
+    wb |= __shfl_xor_sync(0xffffffffu, wb, off);
+  }
+  if (!dst.code) return;
+  if (lane < 4) reinterpret_cast<uint2*>(dst.code)[lane] = make_uint2(wa, wb);
+  if ((lane & (GROUP / 4 - 1)) == 0)
+    reinterpret_cast<uint32_t*>(dst.sz)[lane / (GROUP / 4)] = uint32_t(sb) | (uint32_t(zb) << 16);
+}
+
+// Column of warp w's four tokens in row i of xs: the token groups are swizzled by row, so
+// that the transposing stores of a warp (lane l writes rows 4l .. 4l + 3) spread over the
+// banks; a row's four tokens stay one aligned 16-byte load.
+__device__ __forceinline__ int xs_col(int i, int w) { return 4 * (w ^ ((i >> 2) & 7)); }
+
+// Four bf16 values (8 bytes) as floats.
+__device__ __forceinline__ void load4(const uint16_t* p, float (&v)[4]) {
+  const uint2 w = *reinterpret_cast<const uint2*>(p);
+  v[0] = bf16_lo(w.x);
+  v[1] = bf16_hi(w.x);
+  v[2] = bf16_lo(w.y);
+  v[3] = bf16_hi(w.y);
+}
+
+// Quantize-on-append, standalone launch: grid (CTA passes, kv-heads, K|V), 512 threads.
+// Each pass takes kGroupItems consecutive work items of the reservation (any requests) for
+// this CTA's (kv-head, K|V), whose R is loaded once: warp w takes item w / 4, tokens (or
+// ring slots) 4(w % 4) .. + 3 of it; lane l owns rotated channels 4l .. 4l + 3, so a thread
+// computes 16 outputs, each one fixed-order fp32 fma chain over i = 0..127 (bit-exact with
+// the format), from two 16-byte shared-memory loads per four steps of four chains.
+// Per item (format, OSCAR technical summary §2.2-B): ring slots first quantise their old
+// occupants that leave the window into INT2 (from the stored bf16 value; before the wait
+// on the preceding kernel, as nothing still running reads those rows), then the new
+// tokens are rotated and routed to their sink, ring slot or INT2 row.  A lane reads an
+// evicted token's channels before it writes the same channels of the slot's new token.
 template <int GROUP>
 __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ k_new,
                                                      const uint16_t* __restrict__ v_new) {
-  __shared__ Smem sm;
   extern __shared__ __align__(128) uint8_t dsm[];
   float* Rs = reinterpret_cast<float*>(dsm);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + kRBytes);
-  const int kvh = blockIdx.y, kv = blockIdx.z;
+  float* xs = reinterpret_cast<float*>(dsm + kRBytes);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + kRBytes + kXsBytes);
+  const int kvh = blockIdx.y, kv = blockIdx.z, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const float* R = reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.R_V : kp.lay.R_K)) +
                    (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.append_counts)[0];
-  const bool work = int(blockIdx.x) < n_items;
+  const int n_pass = (n_items + kGroupItems - 1) / kGroupItems;
+  const bool work = int(blockIdx.x) < n_pass;
   if (threadIdx.x == 0 && work) {
     mbar_init(smem_u32(bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     mbar_expect_tx(smem_u32(bar), kRBytes);
     bulk_g2s(smem_u32(Rs), R, kRBytes, smem_u32(bar));
   }
-  ItemState st;
-  AppendItem it{};
-  if (work) {
-    it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[blockIdx.x];
-    prepare_item<GROUP, kThreads>(sm, kp, layer, it, kvh, kv, st);
-    __syncthreads();  // row pointers visible
-    evict_item<GROUP, kThreads>(sm, it, st);
-  }
-  pdl_wait();
-  pdl_trigger();
-  if (!work) return;
-  __syncthreads();  // barrier initialised
-  if (!mbar_wait(smem_u32(bar), 0)) {
-    if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
-    mbar_wait(smem_u32(bar), 0);  // drain (bounded) before exit
-    return;
-  }
-  for (int ix = blockIdx.x; ix < n_items; ix += gridDim.x) {
-    if (ix != int(blockIdx.x)) {
+  const int S = kp.n_sink, W = kp.window;
+  const uint16_t* X = kv ? v_new : k_new;
+  bool waited = false, have_r = false;
+  for (int pass = blockIdx.x; pass < n_pass; pass += gridDim.x) {
+    // ---- this warp's item and its four token (slot) positions
+    const int ix = pass * kGroupItems + warp / 4, t0 = 4 * (warp % 4);
+    AppendItem it{0, 1, 0, 0};
+    AppendReq a{-1, 0, 0, 0, 0, 0};
+    if (ix < n_items) {
       it = reinterpret_cast<const AppendItem*>(kp.base + kp.lay.append_items)[ix];
-      prepare_item<GROUP, kThreads>(sm, kp, layer, it, kvh, kv, st);
-      __syncthreads();
-      evict_item<GROUP, kThreads>(sm, it, st);
+      a = reinterpret_cast<const AppendReq*>(kp.base + kp.lay.append_reqs)[it.req];
     }
-    finish_item<GROUP, kThreads>(sm, Rs, kp, layer, it, kvh, kv, st, k_new, v_new, [] {});
-    __syncthreads();  // shared memory is reused by the next item
+    const bool ok = ix < n_items && a.slot >= 0 && a.slot < kp.max_requests;
+    if (ix < n_items && !ok && lane == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+    const float clip =
+        ok ? reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.clip_V : kp.lay.clip_K))[layer * kp.n_kv_heads + kvh]
+           : 0.f;
+    const int e0 = a.H0, e1 = min(a.L0, a.H1);  // evicted ring positions
+    const int n0 = max(a.L0, a.H1), n1 = a.L1;  // new ring positions
+    int ev[4], nw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int t = t0 + u;
+      ev[u] = nw[u] = -1;
+      if (!ok || t >= it.count) continue;
+      if (it.kind == 1) {
+        nw[u] = it.begin + t;
+      } else {
+        const int sl = it.begin + t;
+        if (e1 > e0) {
+          const int p = e0 + ((sl - e0 % W) % W + W) % W;
+          if (p < e1) ev[u] = p;
+        }
+        if (n1 > n0) {
+          const int p = n0 + ((sl - n0 % W) % W + W) % W;
+          if (p < n1) nw[u] = p;
+        }
+      }
+    }
+    // ---- eviction: old ring occupants leave the window into INT2
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      if (ev[u] < 0) continue;  // warp-uniform
+      float xe[4];
+      load4(ring_ptr(kp, a.slot, layer, kvh, kv, ev[u]) + 4 * lane, xe);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) xe[c] = fmaxf(fminf(xe[c], clip), -clip);
+      quantize_row<GROUP>(xe, int2_row(kp, a.slot, layer, kvh, kv, ev[u]));
+    }
+    if (!waited) {
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    // ---- new tokens' inputs (written by the caller) into xs, transposed
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float xv[4] = {0.f, 0.f, 0.f, 0.f};
+      if (nw[u] >= 0) load4(X + (size_t(a.x_offset + nw[u] - a.L0) * kp.n_kv_heads + kvh) * kHeadDim + 4 * lane, xv);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int i = 4 * lane + c;
+        xs[i * kGroupTok + xs_col(i, warp) + u] = xv[c];
+      }
+    }
+    __syncthreads();
+    if (!have_r) {
+      const bool r_ok = mbar_wait(smem_u32(bar), 0);
+      if (__syncthreads_or(!r_ok)) {  // the same decision in every thread
+        if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_TIMEOUT);
+        mbar_wait(smem_u32(bar), 0);  // drain (bounded) before exit
+        return;
+      }
+      have_r = true;
+    }
+    // ---- rotation: acc[u][c] = sum_i R[i][4l + c] x_u[i], i ascending
+    float acc[4][4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+#pragma unroll
+      for (int c = 0; c < 4; ++c) acc[u][c] = 0.0f;
+    const float* rrow = Rs + 4 * lane;
+#pragma unroll 8
+    for (int i = 0; i < kHeadDim; ++i) {
+      const float4 xv = *reinterpret_cast<const float4*>(xs + i * kGroupTok + xs_col(i, warp));
+      const float4 rv = *reinterpret_cast<const float4*>(rrow + i * kHeadDim);
+      const float xu[4] = {xv.x, xv.y, xv.z, xv.w}, rc[4] = {rv.x, rv.y, rv.z, rv.w};
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[u][c] = __fmaf_rn(rc[c], xu[u], acc[u][c]);
+    }
+    // ---- route: sink / ring (bf16 r) or INT2 (clip + quantise)
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int p = nw[u];
+      if (p < 0) continue;  // warp-uniform
+      uint16_t rb[4];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) rb[c] = bf16_rne(acc[u][c]);
+      if (p < S || p >= a.H1) {
+        uint16_t* row = p < S ? sink_ptr(kp, a.slot, layer, kvh, kv, p) : ring_ptr(kp, a.slot, layer, kvh, kv, p);
+        *reinterpret_cast<uint2*>(row + 4 * lane) =
+            make_uint2(uint32_t(rb[0]) | (uint32_t(rb[1]) << 16), uint32_t(rb[2]) | (uint32_t(rb[3]) << 16));
+      } else {
+        float xq[4];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) xq[c] = fmaxf(fminf(bf16_f32(rb[c]), clip), -clip);
+        quantize_row<GROUP>(xq, int2_row(kp, a.slot, layer, kvh, kv, p));
+      }
+    }
+    __syncthreads();  // xs is refilled by the next pass
+  }
+  if (work && !have_r) mbar_wait(smem_u32(bar), 0);  // (no pass ran) the copy lands before exit
+  if (!waited) {
+    pdl_wait();
+    pdl_trigger();
   }
 }
 
@@ -112,9 +269,12 @@ __global__ void __launch_bounds__(128) bf16_append_kernel(KernelParams kp, int l
 
 }  // namespace
 
-int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid_x, void* stream,
-                  int* launches) {
-  dim3 grid(grid_x, kp.n_kv_heads, 2);
+int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_items, int n_sm,
+                  void* stream, int* launches) {
+  // passes of kGroupItems items; at most one wave of resident CTAs, each looping over passes
+  const int passes = (n_items + kGroupItems - 1) / kGroupItems;
+  const int per_head = (2 * n_sm + 2 * kp.n_kv_heads - 1) / (2 * kp.n_kv_heads);  // two CTAs per SM
+  dim3 grid(passes < per_head ? passes : per_head, kp.n_kv_heads, 2);
   const uint16_t* k = static_cast<const uint16_t*>(k_new);
   const uint16_t* v = static_cast<const uint16_t*>(v_new);
   static bool attr = false;

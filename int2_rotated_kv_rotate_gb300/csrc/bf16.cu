@@ -17,18 +17,21 @@
 namespace oscar {
 namespace {
 
-// The merge stages partial slots over the row buffers.
-template <int G>
-constexpr int kBf16SlabSlots = Bf16Rows<4, 2>::kSmemBytes / PartialSlot<G>::kBytes;
+// Row buffers of a CTA: chunks of 64 tokens, NBUF - 1 of them in flight while one is
+// attended.  Plans of one wave (small steps, latency-bound) run the deeper pipeline
+// (NBUF 3, two CTAs per SM); larger plans NBUF 2 (three CTAs per SM, more CTAs to overlap
+// one another's prologues and merges).
+template <int G, int NBUF>
+constexpr int kBf16SlabSlots = Bf16Rows<4, NBUF>::kSmemBytes / PartialSlot<G>::kBytes;
 
-template <int G>
+template <int G, int NBUF>
 __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q,
                                                          uint8_t* __restrict__ partials, uint16_t* __restrict__ out,
                                                          float* __restrict__ out_f32) {
   extern __shared__ __align__(128) uint8_t smem[];
-  float* qs = reinterpret_cast<float*>(smem + Bf16Rows<4, 2>::kSmemBytes);
-  int* s_last_p = reinterpret_cast<int*>(smem + Bf16Rows<4, 2>::kSmemBytes + G * kQRow * 4);
-  uint64_t* slab_bar = reinterpret_cast<uint64_t*>(smem + Bf16Rows<4, 2>::kSmemBytes + G * kQRow * 4 + 16);
+  float* qs = reinterpret_cast<float*>(smem + Bf16Rows<4, NBUF>::kSmemBytes);
+  int* s_last_p = reinterpret_cast<int*>(smem + Bf16Rows<4, NBUF>::kSmemBytes + G * kQRow * 4);
+  uint64_t* slab_bar = reinterpret_cast<uint64_t*>(smem + Bf16Rows<4, NBUF>::kSmemBytes + G * kQRow * 4 + 16);
   if (threadIdx.x == 0) {
     mbar_init(smem_u32(slab_bar), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -69,10 +72,10 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     };
     auto rowK = [=](int u) { return page_of(u) + size_t(u % kPage) * kHeadDim; };
     auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
-    bf16_rows_mma<G, 4, 2>(rowK, rowV, t0, t1, qs, part, smem, 0, [] {});
+    bf16_rows_mma<G, 4, NBUF>(rowK, rowV, t0, t1, qs, part, smem, 0, [] {});
 
     MergeAcc<G, 128> acc;
-    if (merge_partial<G, 128>(kp, it, partials, acc, s_last_p, smem, kBf16SlabSlots<G>, smem_u32(slab_bar), slab_phase,
+    if (merge_partial<G, 128>(kp, it, partials, acc, s_last_p, smem, kBf16SlabSlots<G, NBUF>, smem_u32(slab_bar), slab_phase,
                               [] {})) {
       const int c = threadIdx.x;
 #pragma unroll
@@ -87,49 +90,55 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
   wq.leave();
 }
 
-constexpr int kBf16KernelSmem(int G) { return Bf16Rows<4, 2>::kSmemBytes + G * kQRow * 4 + 32; }  // + flags, barrier
+constexpr int kBf16KernelSmem(int G, int nbuf) {
+  return (nbuf == 3 ? Bf16Rows<4, 3>::kSmemBytes : Bf16Rows<4, 2>::kSmemBytes) + G * kQRow * 4 + 32;  // + flags, barrier
+}
 
-template <int G>
+template <int G, int NBUF>
 int resident_ctas(int n_sm) {
   static int resident = 0;
   if (resident == 0) {
-    int e = int(cudaFuncSetAttribute(bf16_split_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kBf16KernelSmem(G)));
+    int e = int(cudaFuncSetAttribute(bf16_split_kernel<G, NBUF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kBf16KernelSmem(G, NBUF)));
     int per_sm = 0;
-    if (!e) e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf16_split_kernel<G>, 128, kBf16KernelSmem(G)));
+    if (!e)
+      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, bf16_split_kernel<G, NBUF>, 128,
+                                                            kBf16KernelSmem(G, NBUF)));
     if (e) return -e;
     resident = (per_sm > 0 ? per_sm : 1) * n_sm;
   }
   return resident;
 }
 
-template <int G>
+template <int G, int NBUF>
 int launch_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-             const DecodeWorkspace& wl, int n_items, int n_sm, void* stream, int* launches) {
+             const DecodeWorkspace& wl, int n_sm, void* stream, int* launches) {
   uint8_t* partials = ws + wl.partials;
-  const int resident = resident_ctas<G>(n_sm);
+  const int resident = resident_ctas<G, NBUF>(n_sm);
   if (resident < 0) return -resident;
-  (void)n_items;
   const int grid = resident;  // persistent-style: CTAs loop over the plan's items
-  int e = launch_ex(bf16_split_kernel<G>, dim3(grid), dim3(128), size_t(kBf16KernelSmem(G)), stream, kp, layer,
-                    static_cast<const uint16_t*>(q), partials, static_cast<uint16_t*>(out), out_f32);
+  int e = launch_ex(bf16_split_kernel<G, NBUF>, dim3(grid), dim3(128), size_t(kBf16KernelSmem(G, NBUF)), stream, kp,
+                    layer, static_cast<const uint16_t*>(q), partials, static_cast<uint16_t*>(out), out_f32);
   if (!e) *launches += 1;
   return e;
 }
 
 }  // namespace
 
-int bf16_decode_resident_ctas(int gqa, int n_sm) {
-  if (gqa == 4) return resident_ctas<4>(n_sm);
-  if (gqa == 8) return resident_ctas<8>(n_sm);
+int bf16_decode_resident_ctas(int gqa, bool deep, int n_sm) {
+  if (gqa == 4) return deep ? resident_ctas<4, 3>(n_sm) : resident_ctas<4, 2>(n_sm);
+  if (gqa == 8) return deep ? resident_ctas<8, 3>(n_sm) : resident_ctas<8, 2>(n_sm);
   return n_sm;
 }
 
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                       const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches) {
-  (void)n_req;
-  if (kp.gqa == 4) return launch_t<4>(kp, layer, q, out, out_f32, ws, wl, n_items, n_sm, stream, launches);
-  if (kp.gqa == 8) return launch_t<8>(kp, layer, q, out, out_f32, ws, wl, n_items, n_sm, stream, launches);
+                       const DecodeWorkspace& wl, bool deep, int n_sm, void* stream, int* launches) {
+  if (kp.gqa == 4)
+    return deep ? launch_t<4, 3>(kp, layer, q, out, out_f32, ws, wl, n_sm, stream, launches)
+                : launch_t<4, 2>(kp, layer, q, out, out_f32, ws, wl, n_sm, stream, launches);
+  if (kp.gqa == 8)
+    return deep ? launch_t<8, 3>(kp, layer, q, out, out_f32, ws, wl, n_sm, stream, launches)
+                : launch_t<8, 2>(kp, layer, q, out, out_f32, ws, wl, n_sm, stream, launches);
   return int(cudaErrorInvalidValue);
 }
 

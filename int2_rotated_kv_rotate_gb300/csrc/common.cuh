@@ -80,6 +80,13 @@ template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
+// Wait until at most n (0..3) of this thread's committed cp.async groups are pending.
+__device__ __forceinline__ void cp_async_wait_upto(int n) {
+  if (n >= 3) cp_async_wait<3>();
+  else if (n == 2) cp_async_wait<2>();
+  else if (n == 1) cp_async_wait<1>();
+  else cp_async_wait<0>();
+}
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
@@ -245,14 +252,13 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
     cp_async_commit();
   };
   before_rest();
+  // NBUF buffers: chunks c + 1 .. c + NBUF - 1 are in flight while chunk c is computed
+  constexpr int kAhead = NBUF > 1 ? NBUF - 1 : 0;
   if (n_chunks > 0) stage(0);
+  for (int c = 1; c < kAhead && c < n_chunks; ++c) stage(c);
   for (int c = 0; c < n_chunks; ++c) {
-    if (NBUF > 1 && c + 1 < n_chunks) {
-      stage(c + 1);
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    if (NBUF > 1 && c + kAhead < n_chunks) stage(c + kAhead);  // into the buffer chunk c - 1 left
+    cp_async_wait_upto(min(kAhead, n_chunks - 1 - c));       // chunk c has landed
     __syncthreads();
     const uint32_t kb = sbase + (c % NBUF) * kBf16BufBytes;
     const uint32_t vb = kb + kChunkTok * kRowPad;

@@ -167,7 +167,7 @@ struct oscar_cache {
   std::vector<int> app_req_items;  // append items of each reservation request
   int app_items = 0, app_rows = 0;
   bool plan_covers_reservation = false;  // the plan lists every slot of the pending reservation
-  bool dec_wide = false;                  // the plan is for 16-warp split-kernel CTAs
+  bool dec_wide = false;                  // INT2: the plan is for 16-warp split-kernel CTAs; BF16: for the deep pipeline
   // decode plan
   bool planned = false;
   bool planned_with_reservation = false;  // the plan already counts the reserved tokens
@@ -613,7 +613,7 @@ oscar_status oscar_quantize_append(oscar_cache* c, int layer, const void* k_new,
   if (layer < 0 || layer >= c->cfg.n_layers) return fail(OSCAR_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (c->app_rows > 0 && (!k_new || !v_new)) return fail(OSCAR_ERR_INVALID_ARG, "NULL token arrays");
   if (c->app_items == 0) return OSCAR_OK;
-  int e = launch_append(kernel_params(c), layer, k_new, v_new, std::min(c->app_items, 4 * c->n_sm), stream, &g_launches);
+  int e = launch_append(kernel_params(c), layer, k_new, v_new, c->app_items, c->n_sm, stream, &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "append launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }
@@ -710,6 +710,10 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
     const int r_wide = decode_resident_ctas(G, c->cfg.group, true, c->n_sm);
     wide = r_wide > 0 && total_bytes <= kItemBytes * r_wide;
   }
+  if (!is_int2(c)) {  // BF16: the deeper row pipeline for steps that one wave holds
+    const int r_deep = bf16_decode_resident_ctas(G, true, c->n_sm);
+    wide = r_deep > 0 && total_bytes <= kItemBytes * r_deep;
+  }
   const int nw = decode_warps(G, wide);
   for (int i = 0; i < n_req; ++i) app_expect[i] = 2 * append_task_split(nw) * app_items[i];  // per kv-head
   if ((c->inject & OSCAR_FAULT_LOST_APPEND_SIGNAL) && c->reserved)
@@ -736,7 +740,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   int chunk = max_split_pages;
   if (chunk == 0) {
     int resident =
-        is_int2(c) ? decode_resident_ctas(G, c->cfg.group, wide, c->n_sm) : bf16_decode_resident_ctas(G, c->n_sm);
+        is_int2(c) ? decode_resident_ctas(G, c->cfg.group, wide, c->n_sm) : bf16_decode_resident_ctas(G, wide, c->n_sm);
     if (resident <= 0) resident = 2 * c->n_sm;
     if (total_bytes <= kItemBytes * resident) {
       // a fused append + decode launch runs the reservation's append tasks in the same wave
@@ -913,8 +917,7 @@ oscar_status oscar_append_decode_attention(oscar_cache* c, int layer, const void
       (long long)c->app_items * c->cfg.n_kv_heads * 2 * append_task_split(decode_warps(G, c->dec_wide));
   const bool fused = n_tasks <= (long long)resident;
   if (!fused && c->app_items > 0) {
-    int e = launch_append(kernel_params(c), layer, k_new, v_new, std::min(c->app_items, 4 * c->n_sm), stream,
-                          &g_launches);
+    int e = launch_append(kernel_params(c), layer, k_new, v_new, c->app_items, c->n_sm, stream, &g_launches);
     if (e) return fail(OSCAR_ERR_CUDA, "append launch: %s", cudaGetErrorString(cudaError_t(e)));
   }
   int e = launch_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws, c->dec_wide,
@@ -930,7 +933,7 @@ oscar_status oscar_bf16_decode_attention(oscar_cache* c, int layer, const void* 
   if (st) return st;
   if (is_int2(c)) return fail(OSCAR_ERR_STATE, "oscar_bf16_decode_attention needs the BF16 format");
   int e = launch_bf16_decode(kernel_params(c), layer, q, out, out_f32, static_cast<uint8_t*>(workspace), c->ws,
-                             c->dec_n_req, c->dec_items, c->n_sm, stream, &g_launches);
+                             c->dec_wide, c->n_sm, stream, &g_launches);
   if (e) return fail(OSCAR_ERR_CUDA, "bf16 decode launch: %s", cudaGetErrorString(cudaError_t(e)));
   return OSCAR_OK;
 }

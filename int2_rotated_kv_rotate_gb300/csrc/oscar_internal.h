@@ -128,8 +128,8 @@ struct DecodeWorkspace {
 // Work-item counts live in device memory (the plan blocks); `grid` is the number of CTAs the
 // host launches, each CTA loops over items blockIdx.x, + gridDim.x, ... so a captured
 // launch stays valid when a later plan has a different item count.
-int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid, void* stream,
-                  int* launches);
+int launch_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int n_items, int n_sm,
+                  void* stream, int* launches);
 int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, const void* v_new, int grid, void* stream,
                        int* launches);
 // Decode; with `fused`, the same launch first runs the pending reservation's append tasks
@@ -138,13 +138,15 @@ int launch_bf16_append(const KernelParams& kp, int layer, const void* k_new, con
 int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                   const DecodeWorkspace& wl, bool wide, int n_sm, void* stream, int* launches,
                   const void* k_new = nullptr, const void* v_new = nullptr, bool fused = false);
+// `deep`: the BF16 kernel with the deeper row pipeline (one-wave plans; the plan was made
+// for it).
 int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
-                       const DecodeWorkspace& wl, int n_req, int n_items, int n_sm, void* stream, int* launches);
+                       const DecodeWorkspace& wl, bool deep, int n_sm, void* stream, int* launches);
 
 // CTAs of the decode kernel of this shape that fit on the GPU at once (occupancy x SMs);
 // the planner sizes work items so that one wave holds them all.
 int decode_resident_ctas(int gqa, int group, bool wide, int n_sm);
-int bf16_decode_resident_ctas(int gqa, int n_sm);
+int bf16_decode_resident_ctas(int gqa, bool deep, int n_sm);
 
 // Offline calibration of one layer on the GPU (calib.cu): workspace layout (byte offsets)
 // and the launcher.  C_out (nullable): fp64 [2 H_kv][d][d], C_Q of every kv-head then C_S.
