@@ -307,9 +307,9 @@ def source_digest() -> str:
 
 
 def profiled_traffic(workload: str):
-    """DRAM bytes per launch of the step's kernel from the committed ncu summary of this
-    workload, if it was taken on the current kernel sources (else None)."""
-    path = os.path.join(ROOT, "profiles", f"split_kernel_fused_{workload}.md")
+    """DRAM bytes per layer-step of the step's kernel(s) from the committed ncu summary of
+    this workload, if it was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", f"step_kernels_{workload}.md")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -321,7 +321,7 @@ def profiled_traffic(workload: str):
     if fields.get("source_sha256") != source_digest():
         return None
     try:
-        return int(fields["dram_bytes_per_launch"])
+        return int(fields["dram_bytes_per_step_kernels"])
     except (KeyError, ValueError):
         return None
 

@@ -249,13 +249,18 @@ class ServingLoop:
         slots = [r.slot for r in reqs]
         c.reserve(slots, [1] * len(reqs))
         c.plan(slots)
+        # pool rows of every request's new token and query, all layers: row = (A * stream +
+        # B * layer + position) mod P, one device tensor per step
+        tk = self.tokens
+        base = torch.tensor([[TokenSource.A * TokenSource.stream(r, r.length, self.prefix) + r.length,
+                              TokenSource.A * (r.rid + 17) + r.length] for r in reqs], dtype=torch.long)
+        rows = ((base.to(tk.device)[None] + TokenSource.B * torch.arange(self.w.n_layers, device=tk.device)[:, None, None])
+                % tk.P)  # [layer, request, (token, query)]
         for layer in range(self.w.n_layers):
-            idx = self.tokens.index(layer, [p for r in reqs for p in self._pieces(r, r.length, 1)])
-            K = self.tokens.K.index_select(0, idx)
-            V = self.tokens.V.index_select(0, idx)
-            qi = torch.tensor([(TokenSource.A * (r.rid + 17) + TokenSource.B * layer + r.length) % self.tokens.P
-                               for r in reqs], device=self.tokens.device)
-            q = self.tokens.Q.index_select(0, qi)
+            idx, qi = rows[layer, :, 0], rows[layer, :, 1]
+            K = tk.K.index_select(0, idx)
+            V = tk.V.index_select(0, idx)
+            q = tk.Q.index_select(0, qi)
             o32 = torch.empty(q.shape, dtype=torch.float32, device=q.device) if on_output else None
             if self.fmt == N.OSCAR_FORMAT_INT2:
                 out = c.append_decode(layer, K, V, q, out_f32=o32)
