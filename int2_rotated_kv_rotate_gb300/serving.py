@@ -274,9 +274,23 @@ class ServingLoop:
             r.length += 1
             r.generated += 1
 
+    def _warm_gathers(self, n_max: int) -> None:
+        """Run the step's gathers once for every batch size (set-up, untimed): the first use
+        of a torch gather of a given size can stall for seconds while its device code loads."""
+        tk = self.tokens
+        idx = torch.zeros((self.w.n_layers, n_max, 2), dtype=torch.long, device=tk.device)
+        for n in range(1, n_max + 1):
+            for t in (tk.K, tk.V, tk.Q):
+                t.index_select(0, idx[0, :n, 0])
+        base = torch.zeros((n_max, 2), dtype=torch.long)
+        _ = ((base.to(tk.device)[None] + TokenSource.B * torch.arange(self.w.n_layers, device=tk.device)[:, None, None])
+             % tk.P)
+        torch.cuda.synchronize(tk.device)
+
     def run(self, requests, on_output: Optional[Callable] = None, on_step: Optional[Callable] = None):
         """Serve every request to completion; returns the statistics."""
         waiting = list(requests)
+        self._warm_gathers(min(len(requests), self.cache.cfg.max_requests))
         self.running = []
         st = self.stats
         free0 = self.cache.stats()[0]
