@@ -49,6 +49,8 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-serving", action="store_true", help="skip the throughput-mode serving comparison")
+    ap.add_argument("--format", default="int2", choices=["int2", "int2_cm"],
+                    help="INT2 page format: token-major (int2) or channel-major value pages (int2_cm)")
     ap.add_argument("--rotation", default="oscar", choices=["oscar", "hadamard"],
                     help="calibrated rotations: OSCAR's (default) or the Hadamard-only ablation")
     return ap.parse_args(argv)
@@ -349,8 +351,10 @@ def run_ours(args, w, world, rank, local):
     ppr = (plan.max_len() + 63) // 64 + 2
     # page pool: private pages of every request (shared prefixes counted once per group)
     pages = sum((L + 63) // 64 + 1 for L in plan.final) + 8
-    cache = KVCache(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, group=w.group, n_sink=w.n_sink, window=w.window,
-                    n_layers=n_layers, max_requests=B, max_pages=pages, max_pages_per_request=ppr, device=dev)
+    fmt = N.OSCAR_FORMAT_INT2_CM if args.format == "int2_cm" else N.OSCAR_FORMAT_INT2
+    cache = KVCache(fmt=fmt, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, group=w.group, n_sink=w.n_sink,
+                    window=w.window, n_layers=n_layers, max_requests=B, max_pages=pages, max_pages_per_request=ppr,
+                    device=dev)
     t_cal = time.time()
     for layer in range(n_layers):
         qc, kc, vc = wl.gen_calibration(w, seed, layer, device=dev)

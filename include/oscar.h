@@ -43,7 +43,11 @@
  *   c = 16 f + 2 w + h at bit 32 w + 16 h + 2 f (word w little-endian, half h, field f).
  *
  * Device pools (byte offsets are exposed through oscar_cache_layout for tests):
- *   codes : [layer][phys_page][kv_head][K|V][64 tokens][32 B]
+ *   codes : [layer][phys_page][kv_head][K|V][64 tokens][32 B]   (token-major rows)
+ *           format OSCAR_FORMAT_INT2_CM: the K block as above; the V block (2048 B) is
+ *           channel-major: 32-bit word 128 b + c holds channel c of the page's tokens
+ *           16 b .. 16 b + 15, token 16 b + 8 h + f at bit 16 h + 2 f (b 0..3, h 0..1,
+ *           f 0..7).  Codes, scale and zero are the same numbers as in OSCAR_FORMAT_INT2.
  *   sz    : [layer][phys_page][kv_head][K|V][64 tokens][d/group][scale, zero] bf16
  *   sink  : [request_slot][layer][kv_head][K|V][S][d] bf16
  *   ring  : [request_slot][layer][kv_head][K|V][W][d] bf16
@@ -78,7 +82,12 @@ typedef enum {
 #define OSCAR_FLAG_TIMEOUT 0x2u
 #define OSCAR_FLAG_BAD_SLOT 0x4u
 
-typedef enum { OSCAR_FORMAT_INT2 = 0, OSCAR_FORMAT_BF16 = 1 } oscar_format;
+/* OSCAR_FORMAT_INT2: INT2 history, token-major pages, decoded with warp-level MMAs; the
+ * step's append can run inside the decode launch.  OSCAR_FORMAT_INT2_CM: the same stored
+ * numbers with channel-major value pages, decoded on the tcgen05 tensor cores with the
+ * code operands in tensor memory (GQA 4 or 8 at group 128, GQA 4 at group 32); the append
+ * always runs as its own launch.  OSCAR_FORMAT_BF16: the uncompressed comparison cache. */
+typedef enum { OSCAR_FORMAT_INT2 = 0, OSCAR_FORMAT_BF16 = 1, OSCAR_FORMAT_INT2_CM = 2 } oscar_format;
 
 typedef struct {
   int format;                /* oscar_format */

@@ -5,7 +5,7 @@ this package is a ctypes binding (_native), a torch-facing cache handle (cache),
 offline calibration step (calibrate) and seeded synthetic workloads (workloads).
 """
 from . import _native
-from ._native import OSCAR_FORMAT_BF16, OSCAR_FORMAT_INT2, OscarError
+from ._native import OSCAR_FORMAT_BF16, OSCAR_FORMAT_INT2, OSCAR_FORMAT_INT2_CM, OscarError
 from .cache import KVCache
 
-__all__ = ["KVCache", "OscarError", "OSCAR_FORMAT_INT2", "OSCAR_FORMAT_BF16", "_native"]
+__all__ = ["KVCache", "OscarError", "OSCAR_FORMAT_INT2", "OSCAR_FORMAT_INT2_CM", "OSCAR_FORMAT_BF16", "_native"]

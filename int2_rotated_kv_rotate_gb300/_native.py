@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(HERE, "liboscar.so")
 
 OSCAR_FORMAT_INT2 = 0
 OSCAR_FORMAT_BF16 = 1
+OSCAR_FORMAT_INT2_CM = 2  # INT2, channel-major value pages (tcgen05 decode)
 OSCAR_FLAG_BAD_PAGE = 0x1
 OSCAR_FLAG_TIMEOUT = 0x2
 OSCAR_FLAG_BAD_SLOT = 0x4

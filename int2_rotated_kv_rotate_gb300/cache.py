@@ -11,7 +11,8 @@ from . import _native as N
 
 
 class KVCache:
-    """One cache: INT2 mixed-precision (fmt=N.OSCAR_FORMAT_INT2) or plain BF16 pages."""
+    """One cache: INT2 mixed-precision (fmt=N.OSCAR_FORMAT_INT2, or N.OSCAR_FORMAT_INT2_CM with
+    channel-major value pages) or plain BF16 pages (N.OSCAR_FORMAT_BF16)."""
 
     def __init__(self, *, fmt: int = N.OSCAR_FORMAT_INT2, n_q_heads: int, n_kv_heads: int, group: int = 128,
                  n_sink: int = 4, window: int = 128, n_layers: int = 1, max_requests: int = 1, max_pages: int,
@@ -25,6 +26,7 @@ class KVCache:
         self.layout = N.oscar_cache_layout(self.handle)
         self.workspace = None
         self.fmt = fmt
+        self.is_int2 = fmt in (N.OSCAR_FORMAT_INT2, N.OSCAR_FORMAT_INT2_CM)
         self._rows = None  # rows of k_new / v_new the pending reservation expects
         self._n_plan = None  # requests of the current decode plan
 
@@ -85,7 +87,7 @@ class KVCache:
         N.oscar_bf16_append(self.handle, layer, k_new, v_new, stream)
 
     def append(self, layer: int, k_new, v_new, stream=None) -> None:
-        if self.fmt == N.OSCAR_FORMAT_INT2:
+        if self.is_int2:
             self.quantize_append(layer, k_new, v_new, stream)
         else:
             self.bf16_append(layer, k_new, v_new, stream)
@@ -125,7 +127,7 @@ class KVCache:
 
     def decode(self, layer: int, q, out=None, out_f32=None, stream=None):
         out = self._check_decode(q, out, out_f32)
-        if self.fmt == N.OSCAR_FORMAT_INT2:
+        if self.is_int2:
             N.oscar_decode_attention(self.handle, layer, q, out, self.workspace, out_f32, stream)
         else:
             N.oscar_bf16_decode_attention(self.handle, layer, q, out, self.workspace, out_f32, stream)
@@ -163,11 +165,31 @@ class KVCache:
         c0 = self.layout.codes + layer * code_layer + (phys * H + kvh) * code_head + kv * 64 * 32 + t * 32
         s0 = self.layout.sz + layer * sz_layer + (phys * H + kvh) * sz_head + kv * 64 * ng * 4 + t * ng * 4
         dev = self.mem.device
-        ic = (c0[:, None] + torch.arange(32)[None, :]).to(dev)
         is_ = (s0[:, None] + torch.arange(ng * 4)[None, :]).to(dev)
-        rows = self.mem[ic].cpu()
         sz = self.mem[is_].cpu().contiguous().view(torch.int16)
+        if self.fmt == N.OSCAR_FORMAT_INT2_CM and kv == 1:
+            return self._cm_rows(c0 - t * 32, t), sz
+        ic = (c0[:, None] + torch.arange(32)[None, :]).to(dev)
+        rows = self.mem[ic].cpu()
         return rows, sz
+
+    def _cm_rows(self, vblock: torch.Tensor, t: torch.Tensor) -> torch.Tensor:
+        """Token-major 32-byte rows of positions t (in their pages) rebuilt from channel-major
+        value blocks at byte offsets vblock: word 128 b + c holds channel c of tokens
+        16 b .. 16 b + 15, token 16 b + 8 h + f at bit 16 h + 2 f."""
+        dev = self.mem.device
+        c = torch.arange(128)
+        word0 = vblock + 4 * (128 * (t // 16))
+        iw = (word0[:, None, None] + 4 * c[None, :, None] + torch.arange(4)[None, None, :]).to(dev)
+        words = self.mem[iw].cpu().to(torch.int64)
+        words = words[..., 0] | (words[..., 1] << 8) | (words[..., 2] << 16) | (words[..., 3] << 24)  # [n, 128]
+        sh = (16 * ((t // 8) % 2) + 2 * (t % 8))[:, None]
+        codes = (words >> sh) & 3  # [n, 128] code of channel c
+        f, w, h = c // 16, (c % 16) // 2, c % 2  # channel c = 16 f + 2 w + h: bit 32 w + 16 h + 2 f of the row
+        row_words = torch.zeros((t.numel(), 8), dtype=torch.int64)
+        row_words.scatter_add_(1, w[None, :].expand(t.numel(), 128), codes << (16 * h + 2 * f)[None, :])
+        row_words = torch.where(row_words >= 2**31, row_words - 2**32, row_words)  # two's complement words
+        return row_words.to(torch.int32).view(torch.uint8).reshape(t.numel(), 32)
 
     def _head_block(self, pool_off: int, per_head: int, slot: int, layer: int, kvh: int):
         H = self.cfg.n_kv_heads

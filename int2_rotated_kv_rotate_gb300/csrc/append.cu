@@ -26,14 +26,12 @@ constexpr int kGroupTok = kGroupItems * kTok;  // 64: warp w owns tokens 4w .. 4
 constexpr int kXsBytes = kHeadDim * kGroupTok * 4;  // new tokens' values, transposed: xs[i][token]
 constexpr int kAppendSmem = kRBytes + kXsBytes + 16;
 
-// INT2 row of one token from the clipped values of the calling lane's four channels
-// (lane l holds channels 4l .. 4l + 3); all 32 lanes of the warp call it together.
-// Format: per group s = bf16((max - min) / 3), z = bf16(min), code = s == 0 ? 0 :
-// clamp(rint((x - z) / s), 0, 3); channel c = 16f + 2w + h at bit 32w + 16h + 2f of the row,
-// so lane l's channels land in words 2(l & 3) and 2(l & 3) + 1, field l >> 2.
+// INT2 codes of one token from the clipped values of the calling lane's four channels
+// (lane l holds channels 4l .. 4l + 3; all 32 lanes of the warp call it together), and the
+// (scale, zero) word of the lane's group.  Format: per group s = bf16((max - min) / 3),
+// z = bf16(min), code = s == 0 ? 0 : clamp(rint((x - z) / s), 0, 3).
 template <int GROUP>
-__device__ __forceinline__ void quantize_row(const float (&x)[4], const RowPtr& dst) {
-  const int lane = threadIdx.x & 31;
+__device__ __forceinline__ uint32_t quantize4(const float (&x)[4], uint32_t (&code)[4]) {
   float mn = fminf(fminf(x[0], x[1]), fminf(x[2], x[3]));
   float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
   // group of 128 channels: the whole warp; of 32: lanes 8G .. 8G + 7
@@ -45,11 +43,27 @@ __device__ __forceinline__ void quantize_row(const float (&x)[4], const RowPtr& 
   const uint16_t sb = bf16_rne(__fdiv_rn(__fsub_rn(mx, mn), 3.0f));
   const uint16_t zb = bf16_rne(mn);
   const float sc = bf16_f32(sb), z = bf16_f32(zb);
-  uint32_t code[4];
 #pragma unroll
   for (int c = 0; c < 4; ++c)
     code[c] = sc != 0.0f ? static_cast<uint32_t>(fminf(fmaxf(rintf(__fdiv_rn(__fsub_rn(x[c], z), sc)), 0.0f), 3.0f))
                          : 0u;
+  return uint32_t(sb) | (uint32_t(zb) << 16);
+}
+
+// Store the (scale, zero) word of the lane's group at dst.sz.
+template <int GROUP>
+__device__ __forceinline__ void store_sz(uint32_t szw, const RowPtr& dst) {
+  const int lane = threadIdx.x & 31;
+  if (dst.sz && (lane & (GROUP / 4 - 1)) == 0) reinterpret_cast<uint32_t*>(dst.sz)[lane / (GROUP / 4)] = szw;
+}
+
+// Token-major 32-byte row: channel c = 16f + 2w + h at bit 32w + 16h + 2f, so lane l's
+// channels land in words 2(l & 3) and 2(l & 3) + 1, field l >> 2.
+template <int GROUP>
+__device__ __forceinline__ void quantize_row(const float (&x)[4], const RowPtr& dst) {
+  const int lane = threadIdx.x & 31;
+  uint32_t code[4];
+  const uint32_t szw = quantize4<GROUP>(x, code);
   const int f = lane >> 2;
   uint32_t wa = (code[0] << (2 * f)) | (code[1] << (16 + 2 * f));
   uint32_t wb = (code[2] << (2 * f)) | (code[3] << (16 + 2 * f));
@@ -60,8 +74,80 @@ __device__ __forceinline__ void quantize_row(const float (&x)[4], const RowPtr& 
   }
   if (!dst.code) return;
   if (lane < 4) reinterpret_cast<uint2*>(dst.code)[lane] = make_uint2(wa, wb);
-  if ((lane & (GROUP / 4 - 1)) == 0)
-    reinterpret_cast<uint32_t*>(dst.sz)[lane / (GROUP / 4)] = uint32_t(sb) | (uint32_t(zb) << 16);
+  store_sz<GROUP>(szw, dst);
+}
+
+// Channel-major value codes (format OSCAR_FORMAT_INT2_CM): a page's V block holds, per
+// 16-position block b and channel c, the 32-bit word 128 b + c with position 16 b + 8 h + f
+// at bit 16 h + 2 f.  A pass gathers the words of each item's blocks in shared memory
+// (an item's positions fall in at most two blocks: a ring item's slots wrap once, a
+// direct item never leaves its block) and writes them once the pass is quantised.
+struct CmAgg {
+  uint32_t bits[kGroupItems][2][kHeadDim];
+  uint32_t mask[kGroupItems][2];  // positions of the block this pass writes (2 bits each)
+  int base[kGroupItems][2];       // first position of the block
+  int slot[kGroupItems];
+};
+constexpr int kAppendSmemCm = kAppendSmem + int(sizeof(CmAgg));  // the CmAgg after the barrier
+static_assert(kAppendSmem % 16 == 0, "CmAgg alignment");
+
+// Add the lane's four codes of position p (item i of the pass) to the block words.
+__device__ __forceinline__ void cm_add(CmAgg& ag, int i, int p, int W, const uint32_t (&code)[4]) {
+  const int lane = threadIdx.x & 31;
+  const int sel = W > 0 ? (p / W) & 1 : 0;  // the two blocks of a wrapping ring item lie W apart
+  const int sh = 16 * ((p >> 3) & 1) + 2 * (p & 7);
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    if (code[c]) atomicOr(&ag.bits[i][sel][4 * lane + c], code[c] << sh);
+  if (lane == 0) {
+    atomicOr(&ag.mask[i][sel], 3u << sh);
+    ag.base[i][sel] = p & ~15;
+  }
+}
+
+// INT2 codes of position p: the token-major row, or (channel-major V) the pass's block words.
+template <int GROUP>
+__device__ __forceinline__ void store_int2(bool cm, CmAgg& ag, int item, int W, const float (&x)[4],
+                                           const KernelParams& kp, int slot, int layer, int kvh, int kv, int p) {
+  const RowPtr dst = int2_row(kp, slot, layer, kvh, kv, p);
+  if (!cm) {
+    quantize_row<GROUP>(x, dst);
+    return;
+  }
+  uint32_t code[4];
+  const uint32_t szw = quantize4<GROUP>(x, code);
+  if (!dst.code) return;  // page id out of range (flagged)
+  store_sz<GROUP>(szw, dst);
+  cm_add(ag, item, p, W, code);
+}
+
+// Write the pass's block words of the V pages (all threads, after a barrier): a block the
+// pass fills whole is stored, one it fills in part is merged with atomics (other positions
+// of it belong to earlier steps or to another item of this launch).
+__device__ void cm_write(CmAgg& ag, const KernelParams& kp, int layer, int kvh) {
+  for (int e = threadIdx.x; e < kGroupItems * 2 * kHeadDim; e += kThreads) {
+    const int c = e % kHeadDim, sel = (e / kHeadDim) & 1, i = e / (2 * kHeadDim);
+    const uint32_t mask = ag.mask[i][sel];
+    if (mask == 0u) continue;
+    const uint32_t bits = ag.bits[i][sel][c];
+    ag.bits[i][sel][c] = 0u;
+    const int slot = ag.slot[i], p0 = ag.base[i][sel];
+    if (slot < 0) continue;
+    const int lp = p0 / kPage;  // a page out of range gave no codes (store_int2 flags it)
+    if (lp >= kp.max_pages_per_request) continue;
+    const int phys = reinterpret_cast<const int*>(kp.base + kp.lay.page_table)[size_t(slot) * kp.max_pages_per_request + lp];
+    if (phys < 0 || phys >= kp.max_pages) continue;
+    uint32_t* w = reinterpret_cast<uint32_t*>(kp.base + kp.lay.codes + size_t(layer) * kp.lay.codes_layer_stride +
+                                              size_t(phys) * kp.lay.codes_page_stride +
+                                              size_t(kvh) * kp.lay.codes_head_stride + kPage * kRowBytes) +
+                  kHeadDim * ((p0 % kPage) / 16) + c;
+    if (mask == 0xffffffffu) {
+      *w = bits;
+    } else {
+      atomicAnd(w, ~mask);
+      atomicOr(w, bits);
+    }
+  }
 }
 
 // Column of warp w's four tokens in row i of xs: the token groups are swizzled by row, so
@@ -89,14 +175,21 @@ __device__ __forceinline__ void load4(const uint16_t* p, float (&v)[4]) {
 // on the preceding kernel, as nothing still running reads those rows), then the new
 // tokens are rotated and routed to their sink, ring slot or INT2 row.  A lane reads an
 // evicted token's channels before it writes the same channels of the slot's new token.
-template <int GROUP>
+// CM: channel-major value pages (the V CTAs gather code words in shared memory, CmAgg).
+template <int GROUP, bool CM>
 __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ k_new,
                                                      const uint16_t* __restrict__ v_new) {
   extern __shared__ __align__(128) uint8_t dsm[];
   float* Rs = reinterpret_cast<float*>(dsm);
   float* xs = reinterpret_cast<float*>(dsm + kRBytes);
   uint64_t* bar = reinterpret_cast<uint64_t*>(dsm + kRBytes + kXsBytes);
+  CmAgg& ag = *reinterpret_cast<CmAgg*>(dsm + kAppendSmem);
   const int kvh = blockIdx.y, kv = blockIdx.z, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const bool cm = CM && kv == 1;
+  if (cm) {
+    for (int e = threadIdx.x; e < int(sizeof(CmAgg) / 4); e += kThreads) reinterpret_cast<uint32_t*>(&ag)[e] = 0u;
+    __syncthreads();
+  }
   const float* R = reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.R_V : kp.lay.R_K)) +
                    (size_t(layer) * kp.n_kv_heads + kvh) * kHeadDim * kHeadDim;
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.append_counts)[0];
@@ -122,6 +215,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
     }
     const bool ok = ix < n_items && a.slot >= 0 && a.slot < kp.max_requests;
     if (ix < n_items && !ok && lane == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
+    if (cm && warp % 4 == 0 && lane == 0) ag.slot[warp / 4] = ok ? a.slot : -1;
     const float clip =
         ok ? reinterpret_cast<const float*>(kp.base + (kv ? kp.lay.clip_V : kp.lay.clip_K))[layer * kp.n_kv_heads + kvh]
            : 0.f;
@@ -155,7 +249,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
       load4(ring_ptr(kp, a.slot, layer, kvh, kv, ev[u]) + 4 * lane, xe);
 #pragma unroll
       for (int c = 0; c < 4; ++c) xe[c] = fmaxf(fminf(xe[c], clip), -clip);
-      quantize_row<GROUP>(xe, int2_row(kp, a.slot, layer, kvh, kv, ev[u]));
+      store_int2<GROUP>(cm, ag, warp / 4, W, xe, kp, a.slot, layer, kvh, kv, ev[u]);
     }
     if (!waited) {
       pdl_wait();
@@ -216,10 +310,16 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
         float xq[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) xq[c] = fmaxf(fminf(bf16_f32(rb[c]), clip), -clip);
-        quantize_row<GROUP>(xq, int2_row(kp, a.slot, layer, kvh, kv, p));
+        store_int2<GROUP>(cm, ag, warp / 4, W, xq, kp, a.slot, layer, kvh, kv, p);
       }
     }
     __syncthreads();  // xs is refilled by the next pass
+    if (cm) {
+      cm_write(ag, kp, layer, kvh);
+      __syncthreads();
+      if (threadIdx.x < kGroupItems * 2) (&ag.mask[0][0])[threadIdx.x] = 0u;
+      __syncthreads();
+    }
   }
   if (work && !have_r) mbar_wait(smem_u32(bar), 0);  // (no pass ran) the copy lands before exit
   if (!waited) {
@@ -279,14 +379,24 @@ int launch_append(const KernelParams& kp, int layer, const void* k_new, const vo
   const uint16_t* v = static_cast<const uint16_t*>(v_new);
   static bool attr = false;
   if (!attr) {
-    int e = int(cudaFuncSetAttribute(append_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem));
-    if (!e) e = int(cudaFuncSetAttribute(append_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem));
+    int e = int(cudaFuncSetAttribute(append_kernel<32, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem));
+    if (!e)
+      e = int(cudaFuncSetAttribute(append_kernel<128, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmem));
+    if (!e)
+      e = int(cudaFuncSetAttribute(append_kernel<32, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmemCm));
+    if (!e)
+      e = int(cudaFuncSetAttribute(append_kernel<128, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAppendSmemCm));
     if (e) return e;
     attr = true;
   }
-  int e = kp.group == 32
-              ? launch_ex(append_kernel<32>, grid, dim3(kThreads), size_t(kAppendSmem), stream, kp, layer, k, v)
-              : launch_ex(append_kernel<128>, grid, dim3(kThreads), size_t(kAppendSmem), stream, kp, layer, k, v);
+  const size_t smem = size_t(kp.v_cm ? kAppendSmemCm : kAppendSmem);
+  int e;
+  if (kp.v_cm)
+    e = kp.group == 32 ? launch_ex(append_kernel<32, true>, grid, dim3(kThreads), smem, stream, kp, layer, k, v)
+                       : launch_ex(append_kernel<128, true>, grid, dim3(kThreads), smem, stream, kp, layer, k, v);
+  else
+    e = kp.group == 32 ? launch_ex(append_kernel<32, false>, grid, dim3(kThreads), smem, stream, kp, layer, k, v)
+                       : launch_ex(append_kernel<128, false>, grid, dim3(kThreads), smem, stream, kp, layer, k, v);
   if (!e) *launches += 1;
   return e;
 }

@@ -10,7 +10,6 @@
 namespace oscar {
 
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint32_t kSpinLimit = 1u << 26;  // bounded mbarrier wait (~seconds of polling)
 
 __device__ __forceinline__ uint16_t bf16_rne(float f) {
   uint32_t u = __float_as_uint(f);
@@ -57,10 +56,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Bounded wait; false if the copy did not land within kSpinLimit polls.
+// The same, suspending the thread until the phase completes or `ns` nanoseconds pass (a
+// waiting warp takes no issue slots).
+__device__ __forceinline__ bool mbar_try_wait_for(uint32_t bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait: false if the phase did not complete within kWaitPolls suspensions of at
+// most 1 ms each (about a second or two).
+constexpr uint32_t kWaitPolls = 2048;
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (uint32_t i = 0; i < kSpinLimit; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
+  for (uint32_t i = 0; i < kWaitPolls; ++i)
+    if (mbar_try_wait_for(bar, parity, 1000000u)) return true;
   return false;
 }
 __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {

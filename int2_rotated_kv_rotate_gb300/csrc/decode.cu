@@ -32,6 +32,7 @@
 #include "append_dev.cuh"
 #include "common.cuh"
 #include "oscar_internal.h"
+#include "tmem.cuh"
 
 namespace oscar {
 namespace {
@@ -150,7 +151,24 @@ __device__ void rotate_q(const uint16_t* __restrict__ q_head0, const float (&rk)
 }
 
 // ---------------------------------------------------------------- split kernel
-template <int G, int GROUP, int NW_>
+// Tensor-memory INT2 path (format OSCAR_FORMAT_INT2_CM): a warpgroup takes tiles of two
+// pages (128 tokens).  B columns n = (group g, head h, hi|lo) = 2 G g + 2 h + hi|lo.
+template <int G, int GROUP>
+struct TcShape {
+  static constexpr int NG = kHeadDim / GROUP;
+  static constexpr int NCOL = NG * 2 * G;           // B columns in use
+  static constexpr int N = NCOL < 16 ? 16 : NCOL;   // MMA N (M = 128 takes multiples of 16)
+  static constexpr int NB = N / 8;                  // 8-column core blocks
+  static constexpr int TS = GROUP == 32 ? 3 : 4;    // tile stages per warpgroup
+  static constexpr int kCols = 128;                 // tensor-memory columns per warpgroup
+  static constexpr int kColD = 64;                  // A: columns [0, 64) (128 x 128 fp16); D after it
+  static constexpr int kColX = 96;                  // values of a tile's first page (written during the score MMA)
+  static constexpr int kBqBytes = kHeadDim * N * 2;  // q~ columns, K-major
+  static constexpr int kBpBytes = 128 * N * 2;       // P' of a tile, MN-major (per warpgroup)
+  static constexpr int kRedFloats = G + NG * G;       // per warp: sums of p and of p z_V
+};
+
+template <int G, int GROUP, int NW_, bool CM = false>
 struct Cfg {
   static constexpr int NW = NW_, NTH = Shape<NW>::NTH;
   static constexpr int kPerSM = NW == 8 ? 2 : 1;  // resident CTAs per SM (128 registers a thread)
@@ -159,10 +177,18 @@ struct Cfg {
   static constexpr int kCodeBytes = 2 * kPage * kRowBytes;  // K then V codes
   static constexpr int kSzBytes = 2 * kPage * NG * 4;       // K then V (scale, zero)
   static constexpr int kStageBytes = kCodeBytes + kSzBytes;
-  static constexpr int kPipeBytes = NW * kStages * kStageBytes;
+  // tensor-memory path: tile stages, then each warpgroup's P' block, warp maxima and sums
+  using T = TcShape<G, GROUP>;
+  static constexpr int NWG = NW / 4;
+  static constexpr int kTcBp = ((NWG * T::TS * 2 * kStageBytes + 127) / 128) * 128;
+  static constexpr int kTcWmax = kTcBp + NWG * T::kBpBytes;  // fp32 [NW][G]
+  static constexpr int kTcRed = kTcWmax + NW * G * 4;        // fp32 [NW][kRedFloats]
+  static constexpr int kTcPok = kTcRed + NW * T::kRedFloats * 4;  // uint8 [NWG][TS]: pages copied per tile stage
+  static constexpr int kTcEnd = kTcPok + 64;
+  static constexpr int kPipeBytes = CM ? kTcEnd : NW * kStages * kStageBytes;
   // fused append tasks: R (fp32 [d][d]) then the append scratch, in the same memory
   static constexpr int kAppendR = kHeadDim * kHeadDim * 4;
-  static constexpr int kAppendBytes = kAppendR + int(sizeof(append_dev::Smem));
+  static constexpr int kAppendBytes = CM ? 0 : kAppendR + int(sizeof(append_dev::Smem));
   // the merge: R_V^T (64 KB) then a slab of at least 32 partial slots (64 / G at two CTAs per SM)
   static constexpr int kSlabOff = kHeadDim * kHeadDim * 4;
   static constexpr int kMergeBytes = kSlabOff + (kPerSM == 2 ? 64 / G : 32) * PartialSlot<G>::kBytes;
@@ -171,21 +197,28 @@ struct Cfg {
   static constexpr int kSlabSlots = (kWorkBytes - kSlabOff) / PartialSlot<G>::kBytes;
   static constexpr int kCtl = kWorkBytes;           // control area
   // control: page barriers (NW x kStages), merge flag, next item, R_V^T and slab barriers,
-  // poison flag
-  static constexpr int kCtlBytes = ((NW * kStages * 8 + 32 + 127) / 128) * 128;
+  // poison flag, per-warpgroup MMA barriers (tensor-memory path), tensor-memory base
+  static constexpr int kCtlMma = kCtl + NW * kStages * 8 + 32;
+  static constexpr int kCtlTmem = kCtlMma + 32;
+  static constexpr int kCtlBytes = ((NW * kStages * 8 + 72 + 127) / 128) * 128;
   static constexpr int kQin = kCtl + kCtlBytes;     // fp32 [G][kQinRow] query staging
   static constexpr int kQts = kQin + G * Shape<NW>::kQinRow * 4;  // fp32 [G][kQRow] q~
   static constexpr int kQss = kQts + G * kQRow * 4;  // fp32 [NW][G] sums of q~ per warp's channels
-  // packed B fragments of q~ for the INT2 pages: [4 NT chunks][32 lanes][4 words]
+  // packed B fragments of q~ for the INT2 pages: [4 NT chunks][32 lanes][4 words]; the
+  // tensor-memory path keeps its K-major q~ columns there
   static constexpr int kQbWords = 16 * NT;  // per lane
-  static constexpr int kQb = ((kQss + NW * G * 4 + 15) / 16) * 16;
-  static constexpr int kSmemBytes = kQb + 32 * kQbWords * 4;
+  static constexpr int kQb = ((kQss + NW * G * 4 + 127) / 128) * 128;
+  static constexpr int kQbBytes = CM && T::kBqBytes > 32 * kQbWords * 4 ? T::kBqBytes : 32 * kQbWords * 4;
+  static constexpr int kSmemBytes = kQb + kQbBytes;
+  static constexpr int kTmemCols = NWG * T::kCols;  // tensor-memory columns of a CTA (a power of two)
   static_assert(kSmemBytes + 1024 <= 228 * 1024 / kPerSM, "resident CTAs per SM");
   static_assert(kWorkBytes >= Bf16Rows<NW, 1>::kSmemBytes, "BF16 items reuse the page pipeline memory");
   static_assert(kWorkBytes >= (NW * G * (kHeadDim + 4) + 4 * ((G + 3) / 4)) * 4,
                 "per-warp results reuse the page pipeline memory");
   static_assert(kSlabOff + (1 + NTH / kHeadDim) * G * kHeadDim * 4 <= kMergeBytes,
                 "o~ and the partial sums of the output rotation are staged over the slab");
+  static_assert(!CM || NWG * T::TS <= NW * kStages, "tile-stage barriers");
+  static_assert(!CM || kTmemCols * kPerSM <= 512, "tensor memory of the resident CTAs");
 };
 
 // Start the bulk copy of R_V^T (64 KB) of (layer, kv-head) into smem[0, 64 KB).
@@ -663,6 +696,487 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
   }
 }
 
+// ---------------------------------------------------------------- INT2 pages on tcgen05
+// Named barrier of warpgroup u (128 threads; id 0 is __syncthreads), with immediate ids so
+// that the kernel reserves only the barriers it uses; and the same with an OR of a
+// predicate over the warpgroup.
+#define OSCAR_BAR_WG(ID) asm volatile("bar.sync " #ID ", 128;" ::: "memory")
+template <int NWG>
+__device__ __forceinline__ void bar_wg(int u) {
+  if (u == 0) OSCAR_BAR_WG(1);
+  else if constexpr (NWG == 2) OSCAR_BAR_WG(2);
+  else if (u == 1) OSCAR_BAR_WG(2);
+  else if (u == 2) OSCAR_BAR_WG(3);
+  else OSCAR_BAR_WG(4);
+}
+#undef OSCAR_BAR_WG
+#define OSCAR_BAR_WG_OR(ID)                                                                                  \
+  asm volatile("{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, " #ID                       \
+               ", 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"                                                          \
+               : "=r"(r)                                                                                     \
+               : "r"(uint32_t(v))                                                                            \
+               : "memory")
+template <int NWG>
+__device__ __forceinline__ bool bar_wg_or(int u, bool v) {
+  uint32_t r;
+  if (u == 0) OSCAR_BAR_WG_OR(1);
+  else if constexpr (NWG == 2) OSCAR_BAR_WG_OR(2);
+  else if (u == 1) OSCAR_BAR_WG_OR(2);
+  else if (u == 2) OSCAR_BAR_WG_OR(3);
+  else OSCAR_BAR_WG_OR(4);
+  return r != 0;
+}
+#undef OSCAR_BAR_WG_OR
+// One lane of the (converged) warp: true there, false elsewhere.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t r;
+  asm volatile("{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n" : "=r"(r));
+  return r != 0;
+}
+__device__ __forceinline__ float warp_max(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+// fp16 hi and lo parts of x (x ~ hi + lo to about 22 bits), as the two halves of a word
+__device__ __forceinline__ uint32_t hi_lo(float x) {
+  const float hi = __half2float(__float2half_rn(x));
+  return pack_h2(hi, x - hi);
+}
+
+// INT2 history pages [it.begin, it.end) of one (request, kv-head) on the tcgen05 tensor
+// cores (format OSCAR_FORMAT_INT2_CM).  Warpgroup u (warps 4u .. 4u + 3) takes tiles of two
+// pages, tiles u, u + NWG, ...; per tile (128 tokens):
+//   1. thread t = token t: its 32-byte key row, one AND per two codes (fp16 subnormals
+//      code * 4^(f & 3) * 2^-24 of field f), into A (tensor memory, lane t);
+//   2. one thread: S = A x B_q (8 MMAs of K = 16), B_q = q~ * 4^-(f & 3) as fp16 hi and lo
+//      columns per (group, head), so q~ keeps about 22 bits.  Meanwhile thread c = channel
+//      c moves its channel-major value words of the first page into X (lane c), one AND per
+//      two codes (tokens 16 b + f and 16 b + 8 + f of word b share a column);
+//   3. thread t: scores s = (S_hi + S_lo) s_K 2^24 + z_K sum(q~) per group, masked outside
+//      [S, H); p = 2^(s - m) against the warpgroup's reference maximum m per head, which
+//      is raised (and the sums rescaled) only when a score exceeds it by more than 8, so
+//      p <= 2^8; P' = p s_V 4^-(f & 3) 2^kappa (fp16 hi and lo) into B_P, row k(t); the
+//      second page's values into A;
+//   4. one thread: D = [X | A] x B_P (8 MMAs, K = 16 tokens each); read back at the next
+//      tile by thread c: o += D 2^(24 - kappa).
+// The warpgroups of the SM overlap one another's MMA waits.
+template <int G, int GROUP, int NW>
+__device__ void int2_tc_item(const KernelParams& kp, int layer, const DecodeItem& it, const DecodeReq& dr,
+                             const float* qts, const float* qss, uint8_t* part, uint8_t* smem, uint32_t& phase_bits,
+                             uint32_t& mma_phase, uint32_t tmem_base, int* s_poison) {
+  using C = Cfg<G, GROUP, NW, true>;
+  using T = TcShape<G, GROUP>;
+  constexpr int NG = T::NG, NWG = C::NWG, TS = T::TS, N = T::N, NB = T::NB;
+  static_assert(T::kColD + N <= T::kColX && T::kColX + 32 <= T::kCols, "tensor-memory columns of a warpgroup");
+  static_assert(N == 16 || N == 32, "D loads of 16 or 32 columns");
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = warp >> 2, q = warp & 3, t = tid & 127;
+  const bool leader = t == 0;
+  const int S = kp.n_sink, H = dr.H;
+  const uint32_t tm = tmem_base + uint32_t(u * T::kCols);  // this warpgroup's columns
+  const uint32_t tl = tm + (uint32_t(32 * q) << 16);        // ... at this warp's lanes
+  uint8_t* stages = smem + size_t(u) * TS * 2 * C::kStageBytes;
+  uint64_t* sbars = reinterpret_cast<uint64_t*>(smem + C::kCtl) + u * TS;
+  uint8_t* pok = smem + C::kTcPok + u * TS;  // per tile stage: bit p = page p was copied
+  const uint32_t mbar = smem_u32(reinterpret_cast<uint64_t*>(smem + C::kCtlMma) + u);
+  uint8_t* bp = smem + C::kTcBp + size_t(u) * T::kBpBytes;
+  float* wmax = reinterpret_cast<float*>(smem + C::kTcWmax);
+  float* wred = reinterpret_cast<float*>(smem + C::kTcRed);
+  uint8_t* bq = smem + C::kQb;
+  const int* ptab = reinterpret_cast<const int*>(kp.base + kp.lay.page_table) + size_t(dr.slot) * kp.max_pages_per_request;
+
+  // ---- B_q (all threads): column n, channels 8 kb .. 8 kb + 7 per 16-byte core row
+  for (int e = tid; e < N * 16; e += C::NTH) {
+    const int n = e % N, kb = e / N;
+    const int g = n / (2 * G), h = (n % (2 * G)) >> 1, hl = n & 1;
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float v[2];
+#pragma unroll
+      for (int z = 0; z < 2; ++z) {
+        const int c = 8 * kb + 2 * i + z;
+        v[z] = 0.f;
+        if (n < T::NCOL && c / GROUP == g) {
+          const float x = qts[h * kQRow + c] * (1.0f / float(1 << (2 * ((c >> 4) & 3))));
+          const float hi = __half2float(__float2half_rn(x));
+          v[z] = hl ? x - hi : hi;
+        }
+      }
+      w[i] = pack_h2(v[0], v[1]);
+    }
+    *reinterpret_cast<uint4*>(bq + (kb * NB + n / 8) * 128 + (n % 8) * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  fence_proxy_async();  // generic writes of B_q before the tensor cores read them
+  __syncthreads();
+
+  const float scale = kLog2e * rsqrtf(float(kHeadDim));
+  const float scale24 = scale * 16777216.0f;
+  float qsc[NG][G];  // sum of q~ over group g, times scale
+#pragma unroll
+  for (int g = 0; g < NG; ++g)
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      constexpr int WPG = NW / NG;
+      float sq = 0.f;
+#pragma unroll
+      for (int w = 0; w < WPG; ++w) sq += qss[(WPG * g + w) * G + h];
+      qsc[g][h] = sq * scale;
+    }
+  // P' scale 2^kappa keeps p s_V (p <= 2^8, s_V < clip_V) below 2^14 in fp16
+  const float clipv = reinterpret_cast<const float*>(kp.base + kp.lay.clip_V)[layer * kp.n_kv_heads + it.kvh];
+  const int kappa = clipv > 0.f && clipv < 1e30f ? min(60, max(-60, 5 - ilogbf(clipv))) : 0;
+  const float pscale = ldexpf(1.0f, kappa - 2 * (t & 3));  // and 4^-(f & 3) of my token's field f = t & 7
+  const float oscale = ldexpf(1.0f, 24 - kappa);
+  const int kidx = (t & ~15) + 2 * (t & 7) + ((t >> 3) & 1);  // my token's row of B_P (K index)
+  const int gc = GROUP == 32 ? q : 0;                         // group of my channel t
+
+  const int n_tiles = (it.end - it.begin + 1) / 2;
+  const int n_my = n_tiles > u ? (n_tiles - u + NWG - 1) / NWG : 0;
+  auto tile_lp0 = [&](int k) { return it.begin + 2 * (u + NWG * k); };
+  auto load_ids = [&](int k, int (&ph)[2]) {  // page ids of my k-th tile (-1: none or out of range)
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      const int lp = tile_lp0(k) + p;
+      ph[p] = lp < it.end && lp < kp.max_pages_per_request ? ptab[lp] : -1;
+    }
+  };
+  auto issue = [&](int k, const int (&ph)[2]) {  // the leader: my k-th tile into stage k % TS
+    const int st = k % TS, lp0 = tile_lp0(k);
+    uint8_t* dst = stages + size_t(st) * 2 * C::kStageBytes;
+    const uint32_t bar = smem_u32(&sbars[st]);
+    uint32_t bytes = 0, ok = 0;
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      if (ph[p] >= 0 && ph[p] < kp.max_pages) {
+        bytes += C::kStageBytes;
+        ok |= 1u << p;
+      } else if (lp0 + p < it.end) {
+        flag(kp, OSCAR_FLAG_BAD_PAGE);
+      }
+    }
+    pok[st] = uint8_t(ok);  // read by the warpgroup after the stage's barrier completes
+    // (no proxy fence: the stage's earlier generic reads were all consumed before the
+    // warpgroup barrier that precedes this)
+    mbar_expect_tx(bar, bytes);  // the arrival; the phase completes once the bytes land
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      if (!((ok >> p) & 1u)) continue;
+      const uint8_t* code = kp.base + kp.lay.codes + size_t(layer) * kp.lay.codes_layer_stride +
+                            size_t(ph[p]) * kp.lay.codes_page_stride + size_t(it.kvh) * kp.lay.codes_head_stride;
+      const uint8_t* sz = kp.base + kp.lay.sz + size_t(layer) * kp.lay.sz_layer_stride +
+                          size_t(ph[p]) * kp.lay.sz_page_stride + size_t(it.kvh) * kp.lay.sz_head_stride;
+      bulk_g2s(smem_u32(dst + p * C::kStageBytes), code, C::kCodeBytes, bar);
+      bulk_g2s(smem_u32(dst + p * C::kStageBytes + C::kCodeBytes), sz, C::kSzBytes, bar);
+    }
+  };
+  // warp 0 of the warpgroup issues the MMAs, warp 3 the page copies (one elected lane
+  // each); the lanes of warp 3 all hold the page ids of the next tile to copy
+  int nph[2] = {-1, -1};
+  if (q == 3) {
+    fence_proxy_async();  // the item's generic writes of this memory (B_q, the last results)
+    for (int k = 0; k < min(TS, n_my); ++k) {
+      int ph[2];
+      load_ids(k, ph);
+      if (elect_one()) issue(k, ph);
+      __syncwarp();
+    }
+    if (TS < n_my) load_ids(TS, nph);
+  }
+  int n_issued = min(TS, n_my), next_wait = 0;  // tiles copied; first tile not yet waited for
+
+  float m_ref[G], l_acc[G], zv[NG][G], o_acc[G];
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    m_ref[h] = -INFINITY;
+    l_acc[h] = 0.f;
+    o_acc[h] = 0.f;
+#pragma unroll
+    for (int g = 0; g < NG; ++g) zv[g][h] = 0.f;
+  }
+  bool broken = false, mma_out = false;  // mma_out: a value MMA not yet read back
+  bool mma_lost = false;                   // an MMA wait gave up (its barrier phase is unknown)
+  // wait for this warpgroup's last commit (all threads of the warpgroup); false on timeout
+  auto wait_mma = [&]() -> bool {
+    const bool ok = mbar_wait(mbar, mma_phase & 1u);
+    mma_phase ^= 1u;
+    tmem::fence_after();
+    return !bar_wg_or<NWG>(u, !ok);
+  };
+  // o += D 2^(24 - kappa) for my channel t, after the value MMA of the last tile
+  auto read_values = [&]() -> bool {
+    if (!wait_mma()) return false;
+    uint32_t dv[2 * G];
+    if constexpr (G == 4) tmem::ld_x8(tl + T::kColD + 2 * G * gc, dv);
+    else tmem::ld_x16(tl + T::kColD + 2 * G * gc, dv);
+    tmem::wait_ld();
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+      o_acc[h] = fmaf(__uint_as_float(dv[2 * h]) + __uint_as_float(dv[2 * h + 1]), oscale, o_acc[h]);
+    return true;
+  };
+  // values of channel t in page pg of the stage into tensor-memory columns col .. col + 31
+  auto put_values = [&](const uint8_t* stg, int pg, uint32_t col) {
+    const uint32_t* vw = reinterpret_cast<const uint32_t*>(stg + pg * C::kStageBytes + kPage * kRowBytes) + t;
+    uint32_t r[32];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      const uint32_t W = vw[kHeadDim * b], Ws = W >> 8;
+#pragma unroll
+      for (int f = 0; f < 8; ++f) r[8 * b + f] = (f < 4 ? W : Ws) & (0x00030003u << (2 * (f & 3)));
+    }
+    tmem::st_x32(tl + col, r);
+  };
+
+  for (int k = 0; k < n_my; ++k) {
+    const int st = k % TS, lp0 = tile_lp0(k);
+    uint8_t* stg = stages + size_t(st) * 2 * C::kStageBytes;
+    const bool landed = mbar_wait(smem_u32(&sbars[st]), (phase_bits >> st) & 1u);
+    if (bar_wg_or<NWG>(u, !landed)) {
+      if (leader) flag(kp, OSCAR_FLAG_TIMEOUT);
+      broken = true;
+      break;
+    }
+    phase_bits ^= 1u << st;
+    ++next_wait;
+    const uint32_t okp = pok[st];
+    if (mma_out) {  // the last tile's values: frees A, X and D
+      if (!read_values()) {
+        if (leader) flag(kp, OSCAR_FLAG_TIMEOUT);
+        broken = mma_lost = true;
+        break;
+      }
+      mma_out = false;
+    }
+    // ---- 1. keys of token t into A
+    const int tp = t >> 6, tr = t & 63;
+    {
+      const uint8_t* kr = stg + tp * C::kStageBytes + tr * kRowBytes;
+      const uint4 a = *reinterpret_cast<const uint4*>(kr), b = *reinterpret_cast<const uint4*>(kr + 16);
+      const uint32_t wd[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+      uint32_t r[32];
+#pragma unroll
+      for (int f = 0; f < 4; ++f)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) r[8 * f + w] = wd[w] & (0x00030003u << (2 * f));
+      tmem::st_x32(tl, r);
+#pragma unroll
+      for (int f = 0; f < 4; ++f)
+#pragma unroll
+        for (int w = 0; w < 8; ++w) r[8 * f + w] = (wd[w] >> 8) & (0x00030003u << (2 * f));
+      tmem::st_x32(tl + 32, r);
+    }
+    tmem::wait_st();
+    tmem::fence_before();
+    bar_wg<NWG>(u);
+    // ---- 2. scores; meanwhile the first page's values into X
+    if (q == 0) {
+      if (elect_one()) {
+        tmem::fence_after();
+        const uint32_t b0 = smem_u32(bq);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          tmem::mma_ts(tm + T::kColD, tm + 8 * s, tmem::sdesc(b0 + s * 2 * NB * 128, NB * 128, 128),
+                       tmem::idesc_f16(128, N, false), s > 0);
+        tmem::commit(mbar);
+      }
+      __syncwarp();
+    }
+    put_values(stg, 0, T::kColX);
+    if (k > 0 && k + TS - 1 < n_my) {  // refill the last tile's stage while the MMA runs
+      if (q == 3) {
+        if (elect_one()) issue(k + TS - 1, nph);
+        __syncwarp();
+        if (k + TS < n_my) load_ids(k + TS, nph);
+      }
+      ++n_issued;
+    }
+    const int lp = lp0 + tp, pos = lp * kPage + tr;
+    const bool valid = ((okp >> tp) & 1u) && pos >= S && pos < H;
+    const uint32_t* ksz = reinterpret_cast<const uint32_t*>(stg + tp * C::kStageBytes + C::kCodeBytes) + tr * NG;
+    const uint32_t* vsz = ksz + kPage * NG;
+    uint32_t kszw[NG], vszw[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {
+      kszw[g] = ksz[g];
+      vszw[g] = vsz[g];
+    }
+    if (!wait_mma()) {
+      if (leader) flag(kp, OSCAR_FLAG_TIMEOUT);
+      broken = mma_lost = true;
+      break;
+    }
+    uint32_t dsv[N];
+    if constexpr (N == 16) tmem::ld_x16(tl + T::kColD, dsv);
+    else tmem::ld_x32(tl + T::kColD, dsv);
+    put_values(stg, 1, 0);  // the score MMA is done with A
+    tmem::wait_ld();
+    // ---- 3. softmax of token t against the reference maxima
+    float sc[G];
+    bool over = false;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      float v = 0.f;
+#pragma unroll
+      for (int g = 0; g < NG; ++g) {
+        const float T2 = __uint_as_float(dsv[2 * G * g + 2 * h]) + __uint_as_float(dsv[2 * G * g + 2 * h + 1]);
+        v += fmaf(T2, bf16_lo(kszw[g]) * scale24, bf16_hi(kszw[g]) * qsc[g][h]);
+      }
+      sc[h] = valid ? v : -INFINITY;
+      over |= sc[h] > m_ref[h] + 8.0f;
+    }
+    float sv[NG], zz[NG];
+#pragma unroll
+    for (int g = 0; g < NG; ++g) {  // masked tokens: s_V = z_V = 0 (their words may be stale)
+      sv[g] = valid ? bf16_lo(vszw[g]) * pscale : 0.f;
+      zz[g] = valid ? bf16_hi(vszw[g]) : 0.f;
+    }
+    // row kidx of B_P (MN-major): 8 columns = 4 heads x hi|lo per 16-byte core row
+    auto write_bp = [&](const float (&p)[G]) {
+#pragma unroll
+      for (int nb = 0; nb < NB; ++nb) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int n = 8 * nb + 2 * i, g = n / (2 * G), h = (n % (2 * G)) >> 1;
+          w[i] = n < T::NCOL ? hi_lo(p[h] * sv[g]) : 0u;
+        }
+        *reinterpret_cast<uint4*>(bp + ((kidx >> 3) * NB + nb) * 128 + (kidx & 7) * 16) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+    };
+    float p[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) p[h] = over || !valid ? 0.f : ex2(sc[h] - m_ref[h]);
+    write_bp(p);
+    tmem::wait_st();
+    fence_proxy_async();  // B_P rows before the tensor cores read them
+    tmem::fence_before();
+    if (bar_wg_or<NWG>(u, over)) {
+      // a score above the reference by more than 8 (or the first scores): the tile's maxima
+      // become the reference, the sums so far are rescaled, and p is taken again
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float mx = warp_max(sc[h]);
+        if (lane == 0) wmax[warp * G + h] = mx;
+      }
+      bar_wg<NWG>(u);
+#pragma unroll
+      for (int h = 0; h < G; ++h) {
+        const float* wm = wmax + 4 * u * G + h;
+        const float mnew = fmaxf(m_ref[h], fmaxf(fmaxf(wm[0], wm[G]), fmaxf(wm[2 * G], wm[3 * G])));
+        const float muse = mnew == -INFINITY ? 0.f : mnew;
+        const float alpha = ex2(m_ref[h] - muse);  // 0 while the reference was -inf
+        m_ref[h] = mnew;
+        l_acc[h] *= alpha;
+        o_acc[h] *= alpha;
+#pragma unroll
+        for (int g = 0; g < NG; ++g) zv[g][h] *= alpha;
+        p[h] = ex2(sc[h] - muse);
+      }
+      write_bp(p);
+      fence_proxy_async();
+      tmem::fence_before();
+      bar_wg<NWG>(u);
+    }
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      l_acc[h] += p[h];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) zv[g][h] = fmaf(p[h], zz[g], zv[g][h]);
+    }
+    // ---- 4. values; the stage is free again
+    if (q == 0) {
+      if (elect_one()) {
+        tmem::fence_after();
+        const uint32_t b0 = smem_u32(bp);
+#pragma unroll
+        for (int s = 0; s < 8; ++s)
+          tmem::mma_ts(tm + T::kColD, s < 4 ? tm + T::kColX + 8 * s : tm + 8 * (s - 4),
+                       tmem::sdesc(b0 + s * 2 * NB * 128, NB * 128, 128), tmem::idesc_f16(128, N, true), s > 0);
+        tmem::commit(mbar);
+      }
+      __syncwarp();
+    }
+    mma_out = true;
+  }
+  if (!broken && mma_out) {
+    if (read_values()) mma_out = false;
+    else {
+      if (leader) flag(kp, OSCAR_FLAG_TIMEOUT);
+      broken = mma_lost = true;
+    }
+  }
+  if (broken) {
+    // copies still in flight land (bounded) before the stages are reused or the CTA exits;
+    // if one does not, or an MMA did not complete, the barrier phases are unknown and the
+    // CTA takes no further work
+    bool drained = !mma_lost && (!mma_out || wait_mma());
+    for (int j = next_wait; j < n_issued; ++j) {
+      const int st = j % TS;
+      if (mbar_wait(smem_u32(&sbars[st]), (phase_bits >> st) & 1u)) phase_bits ^= 1u << st;
+      else drained = false;
+    }
+    if (!drained) *s_poison = 1;
+  }
+
+  // ---- sums over the warpgroup's tokens, then the warpgroups into the partial
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l_acc[h] += __shfl_xor_sync(0xffffffffu, l_acc[h], off);
+#pragma unroll
+    for (int g = 0; g < NG; ++g)
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) zv[g][h] += __shfl_xor_sync(0xffffffffu, zv[g][h], off);
+  }
+  if (lane == 0) {
+    float* r = wred + warp * T::kRedFloats;
+#pragma unroll
+    for (int h = 0; h < G; ++h) {
+      r[h] = l_acc[h];
+#pragma unroll
+      for (int g = 0; g < NG; ++g) r[G + g * G + h] = zv[g][h];
+    }
+  }
+  __syncthreads();  // every warpgroup is done with its stages and tensor memory
+  constexpr int kRow = kHeadDim + 4;
+  float* wm = reinterpret_cast<float*>(smem);  // [NWG][G] maxima
+  float* wl = wm + NWG * G;                     // [NWG][G] l
+  float* wo = wl + NWG * G;                     // [NWG][G][kRow] o
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float zsum = 0.f, lsum = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float* r = wred + (4 * u + w) * T::kRedFloats;
+      lsum += r[h];
+      zsum += r[G + gc * G + h];
+    }
+    wo[(u * G + h) * kRow + t] = broken ? 0.f : o_acc[h] + zsum;
+    if (t == 0) {
+      wm[u * G + h] = broken ? -INFINITY : m_ref[h];
+      wl[u * G + h] = broken ? 0.f : lsum;
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < G * kHeadDim; e += C::NTH) {
+    const int h = e / kHeadDim, c = e % kHeadDim;
+    float ms = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NWG; ++w) ms = fmaxf(ms, wm[w * G + h]);
+    float l = 0.f, o = 0.f;
+#pragma unroll
+    for (int w = 0; w < NWG; ++w) {
+      const float a = ms == -INFINITY ? 0.f : ex2(wm[w * G + h] - ms);
+      l = fmaf(wl[w * G + h], a, l);
+      o = fmaf(wo[(w * G + h) * kRow + c], a, o);
+    }
+    store_slot<G>(part, h, c, ms, l, o);
+  }
+}
+
 // One fused append task: part `half` (all 16 tokens or ring slots of the item at GQA 4, 8
 // of them at GQA 8) of append item `item` of the pending reservation, for (kv-head kvh,
 // K|V kv), as the append kernel does
@@ -720,14 +1234,16 @@ __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uin
   if (ait.kind != 0) signal(1);
 }
 
-template <int G, int GROUP, bool FUSED, int NW>
-__global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
+// CM: INT2 value pages channel-major, INT2 items on the tcgen05 tensor cores (never fused).
+template <int G, int GROUP, bool FUSED, int NW, bool CM>
+__global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW, CM>::kPerSM)
     split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q, uint8_t* __restrict__ partials,
                  uint16_t* __restrict__ out, float* __restrict__ out_f32, const uint16_t* __restrict__ k_new,
                  const uint16_t* __restrict__ v_new) {
+  static_assert(!(FUSED && CM), "the channel-major format appends in its own launch");
   constexpr bool fused = FUSED;
   extern __shared__ __align__(128) uint8_t smem[];
-  using C = Cfg<G, GROUP, NW>;
+  using C = Cfg<G, GROUP, NW, CM>;
   constexpr int kWarps = C::NW, kThreads = C::NTH;
   int* s_last = reinterpret_cast<int*>(smem + C::kCtl + kWarps * kStages * 8);
   int* s_next = s_last + 1;
@@ -743,9 +1259,20 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
     mbar_init(smem_u32(merge_bar), 1);
     mbar_init(smem_u32(slab_bar), 1);
     *s_poison = 0;
+    if constexpr (CM)
+      for (int i = 0; i < C::NWG; ++i) mbar_init(smem_u32(reinterpret_cast<uint64_t*>(smem + C::kCtlMma) + i), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
+  if constexpr (CM) {  // each warpgroup's tensor-memory columns, held until the CTA exits
+    if (threadIdx.x < 32) tmem::alloc(smem_u32(smem + C::kCtlTmem), C::kTmemCols);
+    tmem::fence_before();
+  }
   __syncthreads();
+  uint32_t tmem_base = 0, mma_phase = 0;
+  if constexpr (CM) {
+    tmem::fence_after();
+    tmem_base = *reinterpret_cast<const uint32_t*>(smem + C::kCtlTmem);
+  }
   // The plan, the page table and R_K were uploaded before the preceding kernels; of the
   // pages, only those wholly below H_pre are final before the wait (a preceding append may
   // still be writing the rest), so the first item copies those early.  Fused launches put
@@ -784,7 +1311,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
       bf16_item_prestage<NW>(kp, layer, it, dr, smem);
       prestaged = true;
     }
-    if (it.kind == 0 && slot_ok) {
+    if (!CM && it.kind == 0 && slot_ok) {
       const int warp = threadIdx.x >> 5;
       const int n_my = it.end - it.begin > warp ? (it.end - it.begin - warp + kWarps - 1) / kWarps : 0;
       for (int k = 0; k < min(kStages, n_my); ++k) {
@@ -821,8 +1348,11 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
       if (threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
       for (int e = threadIdx.x; e < G * kHeadDim; e += kThreads) store_slot<G>(part, e / kHeadDim, e % kHeadDim, -INFINITY, 0.f, 0.f);
     } else if (it.kind == 0) {
-      int2_pages_item<G, GROUP, NW>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask,
-                                    pending && it.dep == kDepNone ? ctrs + 1 : nullptr, s_poison);
+      if constexpr (CM)
+        int2_tc_item<G, GROUP, NW>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, mma_phase, tmem_base, s_poison);
+      else
+        int2_pages_item<G, GROUP, NW>(kp, layer, it, dr, qts, qss, part, smem, phase_bits, pre_mask,
+                                      pending && it.dep == kDepNone ? ctrs + 1 : nullptr, s_poison);
     } else {
       bf16_tokens_item<G, NW>(kp, layer, it, dr, qts, part, smem, prestaged, wait_dep);
     }
@@ -845,19 +1375,39 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW>::kPerSM)
     fence_proxy_async();
   }
   wq.leave();
+  if constexpr (CM) {  // every MMA of this CTA was waited for
+    tmem::fence_before();
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      tmem::fence_after();
+      tmem::dealloc(tmem_base, C::kTmemCols);
+    }
+  }
 }
 
-template <int G, int GROUP, bool FUSED, int NW>
+template <int G, int GROUP, bool FUSED, int NW, bool CM>
 int resident_ctas_t(int n_sm) {
-  using C = Cfg<G, GROUP, NW>;
+  using C = Cfg<G, GROUP, NW, CM>;
   static int resident = 0;  // CTAs of split_kernel that fit on the GPU at once
   if (resident == 0) {
-    int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP, FUSED, NW>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     C::kSmemBytes));
+    int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP, FUSED, NW, CM>,
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     int per_sm = 0;
     if (!e)
-      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED, NW>, C::NTH,
+      e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED, NW, CM>, C::NTH,
                                                             C::kSmemBytes));
+    if (CM && !e) {
+      // The runtime's occupancy for a kernel that allocates tensor memory assumes one CTA
+      // per SM; registers (128 a thread), shared memory and the 512 tensor-memory columns
+      // of an SM decide here.  (A CTA that did not fit would start when another exits:
+      // no CTA of this kernel waits for another.)
+      int dev = 0, smem_sm = 0;
+      e = int(cudaGetDevice(&dev));
+      if (!e) e = int(cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev));
+      const int by_regs = 65536 / (C::NTH * 128), by_smem = smem_sm / (C::kSmemBytes + 1024);
+      per_sm = by_regs < by_smem ? by_regs : by_smem;
+      if (per_sm * C::kTmemCols > 512) per_sm = 512 / C::kTmemCols;
+    }
     if (e) return -e;
     resident = (per_sm > 0 ? per_sm : 1) * n_sm;
     // One CTA per SM (16-warp shape): leave a few SMs to the preceding launch's last CTAs
@@ -869,21 +1419,22 @@ int resident_ctas_t(int n_sm) {
 
 // The decode and the fused append + decode kernels of a shape get one plan: the smaller
 // resident count of the two.
-template <int G, int GROUP, int NW>
+template <int G, int GROUP, int NW, bool CM>
 int resident_ctas(int n_sm) {
-  const int a = resident_ctas_t<G, GROUP, false, NW>(n_sm), b = resident_ctas_t<G, GROUP, true, NW>(n_sm);
+  if constexpr (CM) return resident_ctas_t<G, GROUP, false, NW, true>(n_sm);
+  const int a = resident_ctas_t<G, GROUP, false, NW, false>(n_sm), b = resident_ctas_t<G, GROUP, true, NW, false>(n_sm);
   if (a < 0) return a;
   if (b < 0) return b;
   return a < b ? a : b;
 }
 
-template <int G, int GROUP, int NW>
+template <int G, int GROUP, int NW, bool CM>
 int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out, float* out_f32, uint8_t* ws,
                     const DecodeWorkspace& wl, int n_sm, void* stream, int* launches, const void* k_new,
                     const void* v_new, bool fused) {
-  using C = Cfg<G, GROUP, NW>;
+  using C = Cfg<G, GROUP, NW, CM>;
   uint8_t* partials = ws + wl.partials;
-  const int resident = resident_ctas<G, GROUP, NW>(n_sm);
+  const int resident = resident_ctas<G, GROUP, NW, CM>(n_sm);
   if (resident < 0) return -resident;
   // persistent-style grid: every resident CTA slot, each looping over work items, so a
   // captured launch serves later plans with other item counts
@@ -891,22 +1442,33 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
   uint16_t* ob = static_cast<uint16_t*>(out);
   const uint16_t* kb = static_cast<const uint16_t*>(k_new);
   const uint16_t* vb = static_cast<const uint16_t*>(v_new);
-  int e = fused ? launch_ex(split_kernel<G, GROUP, true, NW>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
-                            stream, kp, layer, qb, partials, ob, out_f32, kb, vb)
-                : launch_ex(split_kernel<G, GROUP, false, NW>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
-                            stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
+  int e;
+  if constexpr (CM)
+    e = launch_ex(split_kernel<G, GROUP, false, NW, true>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
+                  stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
+  else
+    e = fused ? launch_ex(split_kernel<G, GROUP, true, NW, false>, dim3(resident), dim3(C::NTH),
+                          size_t(C::kSmemBytes), stream, kp, layer, qb, partials, ob, out_f32, kb, vb)
+              : launch_ex(split_kernel<G, GROUP, false, NW, false>, dim3(resident), dim3(C::NTH),
+                          size_t(C::kSmemBytes), stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
   if (!e) *launches += 1;
   return e;
 }
 
 }  // namespace
 
-int decode_resident_ctas(int gqa, int group, bool wide, int n_sm) {
+int decode_resident_ctas(int gqa, int group, bool wide, bool cm, int n_sm) {
   const bool w = wide && gqa == 4;
-  if (gqa == 4 && group == 128) return w ? resident_ctas<4, 128, 16>(n_sm) : resident_ctas<4, 128, 8>(n_sm);
-  if (gqa == 4 && group == 32) return w ? resident_ctas<4, 32, 16>(n_sm) : resident_ctas<4, 32, 8>(n_sm);
-  if (gqa == 8 && group == 128) return resident_ctas<8, 128, 8>(n_sm);
-  if (gqa == 8 && group == 32) return resident_ctas<8, 32, 8>(n_sm);
+  if (cm) {
+    if (gqa == 4 && group == 128) return w ? resident_ctas<4, 128, 16, true>(n_sm) : resident_ctas<4, 128, 8, true>(n_sm);
+    if (gqa == 4 && group == 32) return w ? resident_ctas<4, 32, 16, true>(n_sm) : resident_ctas<4, 32, 8, true>(n_sm);
+    if (gqa == 8 && group == 128) return resident_ctas<8, 128, 8, true>(n_sm);
+    return n_sm;
+  }
+  if (gqa == 4 && group == 128) return w ? resident_ctas<4, 128, 16, false>(n_sm) : resident_ctas<4, 128, 8, false>(n_sm);
+  if (gqa == 4 && group == 32) return w ? resident_ctas<4, 32, 16, false>(n_sm) : resident_ctas<4, 32, 8, false>(n_sm);
+  if (gqa == 8 && group == 128) return resident_ctas<8, 128, 8, false>(n_sm);
+  if (gqa == 8 && group == 32) return resident_ctas<8, 32, 8, false>(n_sm);
   return n_sm;
 }
 
@@ -914,16 +1476,21 @@ int launch_decode(const KernelParams& kp, int layer, const void* q, void* out, f
                   const DecodeWorkspace& wl, bool wide, int n_sm, void* stream, int* launches, const void* k_new,
                   const void* v_new, bool fused) {
   const bool w = wide && kp.gqa == 4;
-#define OSCAR_DECODE_CASE(G_, GROUP_, NW_)                                                                       \
-  if (kp.gqa == G_ && kp.group == GROUP_ && (NW_ == 16) == w)                                                   \
-    return launch_decode_t<G_, GROUP_, NW_>(kp, layer, q, out, out_f32, ws, wl, n_sm, stream, launches, k_new, \
-                                            v_new, fused);
-  OSCAR_DECODE_CASE(4, 128, 16)
-  OSCAR_DECODE_CASE(4, 128, 8)
-  OSCAR_DECODE_CASE(4, 32, 16)
-  OSCAR_DECODE_CASE(4, 32, 8)
-  OSCAR_DECODE_CASE(8, 128, 8)
-  OSCAR_DECODE_CASE(8, 32, 8)
+#define OSCAR_DECODE_CASE(G_, GROUP_, NW_, CM_)                                                            \
+  if (kp.gqa == G_ && kp.group == GROUP_ && (NW_ == 16) == w && bool(kp.v_cm) == CM_)                     \
+    return launch_decode_t<G_, GROUP_, NW_, CM_>(kp, layer, q, out, out_f32, ws, wl, n_sm, stream, launches, \
+                                                 k_new, v_new, fused);
+  OSCAR_DECODE_CASE(4, 128, 16, false)
+  OSCAR_DECODE_CASE(4, 128, 8, false)
+  OSCAR_DECODE_CASE(4, 32, 16, false)
+  OSCAR_DECODE_CASE(4, 32, 8, false)
+  OSCAR_DECODE_CASE(8, 128, 8, false)
+  OSCAR_DECODE_CASE(8, 32, 8, false)
+  OSCAR_DECODE_CASE(4, 128, 16, true)
+  OSCAR_DECODE_CASE(4, 128, 8, true)
+  OSCAR_DECODE_CASE(4, 32, 16, true)
+  OSCAR_DECODE_CASE(4, 32, 8, true)
+  OSCAR_DECODE_CASE(8, 128, 8, true)
 #undef OSCAR_DECODE_CASE
   return int(cudaErrorInvalidValue);
 }

@@ -59,7 +59,8 @@ bool config_ok(const oscar_config* c, std::string* why) {
     return false;
   };
   if (!c) return bad("config is NULL");
-  if (c->format != OSCAR_FORMAT_INT2 && c->format != OSCAR_FORMAT_BF16) return bad("format must be INT2 or BF16");
+  if (c->format != OSCAR_FORMAT_INT2 && c->format != OSCAR_FORMAT_BF16 && c->format != OSCAR_FORMAT_INT2_CM)
+    return bad("format must be INT2, INT2_CM or BF16");
   if (c->head_dim != kHeadDim) return bad("head_dim must be 128");
   if (c->page != kPage) return bad("page must be 64");
   if (c->n_kv_heads <= 0 || c->n_q_heads <= 0 || c->n_q_heads % c->n_kv_heads) return bad("bad head counts");
@@ -68,8 +69,10 @@ bool config_ok(const oscar_config* c, std::string* why) {
   if (c->n_layers <= 0 || c->max_requests <= 0 || c->max_pages <= 0 || c->max_pages_per_request <= 0)
     return bad("layers, requests and pages must be positive");
   if (c->max_pages_per_request > (1 << 20)) return bad("max_pages_per_request too large");
-  if (c->format == OSCAR_FORMAT_INT2) {
+  if (c->format == OSCAR_FORMAT_INT2 || c->format == OSCAR_FORMAT_INT2_CM) {
     if (c->group != 32 && c->group != 128) return bad("group must be 32 or 128");
+    if (c->format == OSCAR_FORMAT_INT2_CM && c->group == 32 && g != 4)
+      return bad("the INT2_CM format supports group 32 at GQA 4 only");
     if (c->n_sink < 0 || c->n_sink > kPage) return bad("n_sink must be in [0, 64]");
     if (c->window < 0 || c->window > kMaxWindow || c->window % 16) return bad("window must be a multiple of 16 in [0, 1024]");
   }
@@ -87,7 +90,7 @@ DeviceLayout compute_layout(const oscar_config& c) {
   };
   const size_t d = kHeadDim, Hkv = c.n_kv_heads, layers = c.n_layers, pages = c.max_pages;
   const size_t reqs = c.max_requests;
-  if (c.format == OSCAR_FORMAT_INT2) {
+  if (c.format == OSCAR_FORMAT_INT2 || c.format == OSCAR_FORMAT_INT2_CM) {
     const size_t ng = d / c.group;
     L.codes_head_stride = 2 * kPage * kRowBytes;
     L.codes_page_stride = Hkv * L.codes_head_stride;
@@ -119,7 +122,7 @@ DeviceLayout compute_layout(const oscar_config& c) {
   L.page_table = take(reqs * size_t(c.max_pages_per_request) * 4);
   L.status = take(256);
   L.counters = take(reqs * Hkv * 4);
-  L.max_append_items = kMaxAppendTokenItems + reqs * (kMaxWindow / kAppendChunk);
+  L.max_append_items = kMaxAppendTokenItems + reqs * (kMaxWindow / kAppendChunk + 1);  // + 1: a block-aligned split
   L.max_decode_items = reqs * Hkv * (2 + kMaxWindow / kBf16ItemTokens) + 16384;
   L.append_plan = take(append_items_offset(reqs) + L.max_append_items * sizeof(AppendItem));
   L.append_counts = L.append_plan;
@@ -201,6 +204,7 @@ KernelParams kernel_params(const oscar_cache* c) {
   kp.max_pages = c->cfg.max_pages;
   kp.max_pages_per_request = c->cfg.max_pages_per_request;
   kp.counter_polls = c->counter_polls ? c->counter_polls : kDefaultCounterPolls;
+  kp.v_cm = c->cfg.format == OSCAR_FORMAT_INT2_CM;
   kp.lay = c->lay;
   return kp;
 }
@@ -248,7 +252,11 @@ oscar_status upload_rows(oscar_cache* c, const Upload& u, const std::vector<int>
   return OSCAR_OK;
 }
 
-bool is_int2(const oscar_cache* c) { return c->cfg.format == OSCAR_FORMAT_INT2; }
+bool is_int2(const oscar_cache* c) {
+  return c->cfg.format == OSCAR_FORMAT_INT2 || c->cfg.format == OSCAR_FORMAT_INT2_CM;
+}
+// Channel-major value pages, decoded on the tcgen05 tensor cores; never a fused launch.
+bool is_cm(const oscar_cache* c) { return c->cfg.format == OSCAR_FORMAT_INT2_CM; }
 
 // Pages a request needs to hold its stored tokens: the INT2 format pages positions < H
 // (sinks and recent tokens live elsewhere), the BF16 format pages all L positions.
@@ -542,7 +550,13 @@ oscar_status oscar_reserve(oscar_cache* c, const int* slots, const int* n_new, i
       }
     }
     const int d0 = a.L0, d1 = is_int2(c) ? std::min(a.L1, a.H1) : a.L1;
-    for (int p = d0; p < d1; p += kAppendChunk) items.push_back({i, 1, p, std::min(kAppendChunk, d1 - p)});
+    // channel-major value pages: an item's positions stay inside one 16-position block,
+    // whose code words (one per channel) the append kernel writes whole
+    for (int p = d0; p < d1;) {
+      const int e = is_cm(c) ? std::min(d1, (p / kAppendChunk + 1) * kAppendChunk) : std::min(d1, p + kAppendChunk);
+      items.push_back({i, 1, p, e - p});
+      p = e;
+    }
   }
   if (items.size() > c->lay.max_append_items)
     return fail(OSCAR_ERR_INVALID_ARG, "append of %lld tokens is too large for one reservation; split it", rows);
@@ -707,7 +721,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   const int G = c->cfg.n_q_heads / Hkv;
   bool wide = false;
   if (is_int2(c) && G == 4 && !(flags & OSCAR_PLAN_NARROW)) {
-    const int r_wide = decode_resident_ctas(G, c->cfg.group, true, c->n_sm);
+    const int r_wide = decode_resident_ctas(G, c->cfg.group, true, is_cm(c), c->n_sm);
     wide = r_wide > 0 && total_bytes <= kItemBytes * r_wide;
   }
   if (!is_int2(c)) {  // BF16: the deeper row pipeline for steps that one wave holds
@@ -740,11 +754,12 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   int chunk = max_split_pages;
   if (chunk == 0) {
     int resident =
-        is_int2(c) ? decode_resident_ctas(G, c->cfg.group, wide, c->n_sm) : bf16_decode_resident_ctas(G, wide, c->n_sm);
+        is_int2(c) ? decode_resident_ctas(G, c->cfg.group, wide, is_cm(c), c->n_sm) : bf16_decode_resident_ctas(G, wide, c->n_sm);
     if (resident <= 0) resident = 2 * c->n_sm;
     if (total_bytes <= kItemBytes * resident) {
       // a fused append + decode launch runs the reservation's append tasks in the same wave
-      const long long n_app_tasks = c->reserved ? (long long)c->app_items * Hkv * 2 * append_task_split(nw) : 0;
+      const long long n_app_tasks =
+          c->reserved && !is_cm(c) ? (long long)c->app_items * Hkv * 2 * append_task_split(nw) : 0;
       const long long slots = std::max<long long>(1, resident - n_bf_items - n_app_tasks);
       chunk = int(std::max<long long>(4, (total_pages + slots - 1) / slots));
       while (chunk < max_np && count_items(chunk) + n_app_tasks > resident) ++chunk;
@@ -912,10 +927,10 @@ oscar_status oscar_append_decode_attention(oscar_cache* c, int layer, const void
   // (long chunks, many requests) would hold back the decode, so those go to the append
   // kernel, which is launched first.
   const int G = c->cfg.n_q_heads / c->cfg.n_kv_heads;
-  const int resident = decode_resident_ctas(G, c->cfg.group, c->dec_wide, c->n_sm);
+  const int resident = decode_resident_ctas(G, c->cfg.group, c->dec_wide, is_cm(c), c->n_sm);
   const long long n_tasks =
       (long long)c->app_items * c->cfg.n_kv_heads * 2 * append_task_split(decode_warps(G, c->dec_wide));
-  const bool fused = n_tasks <= (long long)resident;
+  const bool fused = !is_cm(c) && n_tasks <= (long long)resident;
   if (!fused && c->app_items > 0) {
     int e = launch_append(kernel_params(c), layer, k_new, v_new, c->app_items, c->n_sm, stream, &g_launches);
     if (e) return fail(OSCAR_ERR_CUDA, "append launch: %s", cudaGetErrorString(cudaError_t(e)));

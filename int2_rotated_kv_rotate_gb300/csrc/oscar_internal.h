@@ -112,6 +112,7 @@ struct KernelParams {
   int n_q_heads, n_kv_heads, gqa, group, n_sink, window, n_layers;
   int max_requests, max_pages, max_pages_per_request;
   uint32_t counter_polls;  // bounded waits on append-dependency counters give up after this many polls
+  int v_cm;                // INT2 value pages channel-major (OSCAR_FORMAT_INT2_CM)
   DeviceLayout lay;
 };
 // Polls of a dependency-counter wait (each about 0.1-0.3 us: a sleep and an acquire load)
@@ -145,7 +146,7 @@ int launch_bf16_decode(const KernelParams& kp, int layer, const void* q, void* o
 
 // CTAs of the decode kernel of this shape that fit on the GPU at once (occupancy x SMs);
 // the planner sizes work items so that one wave holds them all.
-int decode_resident_ctas(int gqa, int group, bool wide, int n_sm);
+int decode_resident_ctas(int gqa, int group, bool wide, bool cm, int n_sm);
 int bf16_decode_resident_ctas(int gqa, bool deep, int n_sm);
 
 // Offline calibration of one layer on the GPU (calib.cu): workspace layout (byte offsets)

@@ -35,10 +35,11 @@ def make_pair(w: wl.Workload, seed: int, n_layers: int, n_requests: int, max_len
     cache = KVCache(fmt=fmt, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, group=w.group, n_sink=w.n_sink,
                     window=w.window, n_layers=n_layers, max_requests=n_requests,
                     max_pages=n_requests * ppr + extra_pages, max_pages_per_request=ppr)
-    if params is None and fmt == N.OSCAR_FORMAT_INT2:
+    int2 = fmt in (N.OSCAR_FORMAT_INT2, N.OSCAR_FORMAT_INT2_CM)
+    if params is None and int2:
         params = oracle_params(w, seed, n_layers)
     oc = None
-    if fmt == N.OSCAR_FORMAT_INT2:
+    if int2:
         RK, RV, cK, cV = params
         for layer in range(n_layers):
             cache.set_layer_params(layer, RK[layer], RV[layer], cK[layer], cV[layer])
