@@ -30,6 +30,7 @@ import torch
 
 import oracle
 from int2_rotated_kv_rotate_gb300 import KVCache, workloads as wl
+from int2_rotated_kv_rotate_gb300 import _native as N
 from oracle import calibration as ocal
 from oracle.model import as_bits
 
@@ -146,8 +147,11 @@ def _check_page_sample(w, cache, slots, plan, layer, params, H_now, rng, frac=0.
     return checked
 
 
+@pytest.mark.parametrize("fmt", [pytest.param(N.OSCAR_FORMAT_INT2, id="tm"), pytest.param(N.OSCAR_FORMAT_INT2_CM, id="cm")])
 @pytest.mark.parametrize("name", ["qwen3_8b_layer", "long_batch", "ragged_prefix", "qwen3_32b_capacity"])
-def test_full_size_every_head(name):
+def test_full_size_every_head(name, fmt):
+    """Both INT2 formats: the token-major one (the bench's headline) and the channel-major
+    one with the tcgen05 decode (the bench's int2_cm_format line)."""
     w = wl.WORKLOADS[name]
     dev = torch.device("cuda")
     n_layers = w.n_layers if name == "qwen3_32b_capacity" else 1
@@ -158,8 +162,9 @@ def test_full_size_every_head(name):
     pages = sum((L + 63) // 64 + 1 for L in plan.final) + 8
     rng = random.Random(SEED)
     full_layers = [0] if n_layers == 1 else [0, rng.randrange(1, n_layers)]
-    cache = KVCache(n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, group=w.group, n_sink=w.n_sink, window=w.window,
-                    n_layers=n_layers, max_requests=B, max_pages=pages, max_pages_per_request=ppr, device=dev)
+    cache = KVCache(fmt=fmt, n_q_heads=w.n_q_heads, n_kv_heads=w.n_kv_heads, group=w.group, n_sink=w.n_sink,
+                    window=w.window, n_layers=n_layers, max_requests=B, max_pages=pages, max_pages_per_request=ppr,
+                    device=dev)
     try:
         params = {}
         for layer in range(n_layers):
