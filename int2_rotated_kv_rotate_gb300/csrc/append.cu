@@ -105,11 +105,12 @@ __device__ __forceinline__ void cm_add(CmAgg& ag, int i, int p, int W, const uin
   }
 }
 
-// INT2 codes of position p: the token-major row, or (channel-major V) the pass's block words.
+// INT2 codes of position p (in physical page phys, looked up beforehand): the token-major
+// row, or (channel-major V) the pass's block words.
 template <int GROUP>
 __device__ __forceinline__ void store_int2(bool cm, CmAgg& ag, int item, int W, const float (&x)[4],
-                                           const KernelParams& kp, int slot, int layer, int kvh, int kv, int p) {
-  const RowPtr dst = int2_row(kp, slot, layer, kvh, kv, p);
+                                           const KernelParams& kp, int phys, int layer, int kvh, int kv, int p) {
+  const RowPtr dst = int2_row_at(kp, phys, layer, kvh, kv, p);
   if (!cm) {
     quantize_row<GROUP>(x, dst);
     return;
@@ -241,15 +242,24 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
         }
       }
     }
+    // the tokens' INT2 pages and the evicted values, all loads issued before any is used
+    // (a token's stores would otherwise wait for the next token's loads)
+    int phys_ev[4], phys_nw[4];
+    uint2 evw[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      phys_ev[u] = ev[u] >= 0 ? int2_page(kp, a.slot, ev[u]) : -1;
+      phys_nw[u] = nw[u] >= S && nw[u] < a.H1 ? int2_page(kp, a.slot, nw[u]) : -1;
+      evw[u] = ev[u] >= 0 ? *reinterpret_cast<const uint2*>(ring_ptr(kp, a.slot, layer, kvh, kv, ev[u]) + 4 * lane)
+                          : make_uint2(0u, 0u);
+    }
     // ---- eviction: old ring occupants leave the window into INT2
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       if (ev[u] < 0) continue;  // warp-uniform
-      float xe[4];
-      load4(ring_ptr(kp, a.slot, layer, kvh, kv, ev[u]) + 4 * lane, xe);
-#pragma unroll
-      for (int c = 0; c < 4; ++c) xe[c] = fmaxf(fminf(xe[c], clip), -clip);
-      store_int2<GROUP>(cm, ag, warp / 4, W, xe, kp, a.slot, layer, kvh, kv, ev[u]);
+      const float xe[4] = {fmaxf(fminf(bf16_lo(evw[u].x), clip), -clip), fmaxf(fminf(bf16_hi(evw[u].x), clip), -clip),
+                           fmaxf(fminf(bf16_lo(evw[u].y), clip), -clip), fmaxf(fminf(bf16_hi(evw[u].y), clip), -clip)};
+      store_int2<GROUP>(cm, ag, warp / 4, W, xe, kp, phys_ev[u], layer, kvh, kv, ev[u]);
     }
     if (!waited) {
       pdl_wait();
@@ -310,7 +320,7 @@ __global__ void __launch_bounds__(kThreads) append_kernel(KernelParams kp, int l
         float xq[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) xq[c] = fmaxf(fminf(bf16_f32(rb[c]), clip), -clip);
-        store_int2<GROUP>(cm, ag, warp / 4, W, xq, kp, a.slot, layer, kvh, kv, p);
+        store_int2<GROUP>(cm, ag, warp / 4, W, xq, kp, phys_nw[u], layer, kvh, kv, p);
       }
     }
     __syncthreads();  // xs is refilled by the next pass

@@ -55,18 +55,25 @@ struct RowPtr {
   uint8_t* sz;
 };
 
-__device__ inline RowPtr int2_row(const KernelParams& kp, int slot, int layer, int kvh, int kv, int p) {
+// Physical page of position p of the request in `slot` (-1, flagged, if out of range).
+__device__ inline int int2_page(const KernelParams& kp, int slot, int p) {
   const int lp = p / kPage;
-  RowPtr r{nullptr, nullptr};
   if (lp >= kp.max_pages_per_request) {
     flag(kp, OSCAR_FLAG_BAD_PAGE);
-    return r;
+    return -1;
   }
   const int phys = reinterpret_cast<const int*>(kp.base + kp.lay.page_table)[size_t(slot) * kp.max_pages_per_request + lp];
   if (phys < 0 || phys >= kp.max_pages) {
     flag(kp, OSCAR_FLAG_BAD_PAGE);
-    return r;
+    return -1;
   }
+  return phys;
+}
+
+// INT2 row and sz entry of position p in physical page phys (nullptr if phys < 0).
+__device__ inline RowPtr int2_row_at(const KernelParams& kp, int phys, int layer, int kvh, int kv, int p) {
+  RowPtr r{nullptr, nullptr};
+  if (phys < 0) return r;
   const int ng = kHeadDim / kp.group;
   const int t = p % kPage;
   r.code = kp.base + kp.lay.codes + size_t(layer) * kp.lay.codes_layer_stride + size_t(phys) * kp.lay.codes_page_stride +
@@ -74,6 +81,10 @@ __device__ inline RowPtr int2_row(const KernelParams& kp, int slot, int layer, i
   r.sz = kp.base + kp.lay.sz + size_t(layer) * kp.lay.sz_layer_stride + size_t(phys) * kp.lay.sz_page_stride +
          size_t(kvh) * kp.lay.sz_head_stride + size_t(kv) * (kPage * ng * 4) + size_t(t) * ng * 4;
   return r;
+}
+
+__device__ inline RowPtr int2_row(const KernelParams& kp, int slot, int layer, int kvh, int kv, int p) {
+  return int2_row_at(kp, int2_page(kp, slot, p), layer, kvh, kv, p);
 }
 
 __device__ __forceinline__ uint16_t* ring_ptr(const KernelParams& kp, int slot, int layer, int kvh, int kv, int p) {
