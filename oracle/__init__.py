@@ -61,6 +61,7 @@ def lib():
             L.oo_append.argtypes = [i32, i32, i32, i32, f32, P, P, P, P, P, P, P, i64, P, i64]
             L.oo_append.restype = i32
             L.oo_decode.argtypes = [i32, i32, i32, i32, i32, i32, i32] + [P] * 12
+            L.oo_decode_folded.argtypes = [i32, i32, i32, i32, i32, i32, i32] + [P] * 10
             L.oo_bf16_decode.argtypes = [i32, i32, i64, P, P, P, P]
             L.oo_max_threads.restype = i32
             L.oo_set_threads.argtypes = [i32]
@@ -209,6 +210,19 @@ def decode(q, K: Stream, V: Stream, R_K: np.ndarray, R_V: np.ndarray) -> np.ndar
     assert K.length == V.length and K.history_end == V.history_end
     lib().oo_decode(d, G, K.g, K.S, K.W, K.length, K.history_end, _p(K.sink), _p(V.sink), _p(K.ring),
                     _p(V.ring), _p(K.rows), _p(K.sz), _p(V.rows), _p(V.sz), _p(q), _p(R_K), _p(R_V), _p(out))
+    return out
+
+
+def decode_folded(qt, K: Stream, V: Stream) -> np.ndarray:
+    """decode() with the rotations folded into the model's projections: qt are the rotated
+    queries (bf16 bits [G, d]); the result is the output in the rotated basis (fp64 [G, d]),
+    before the inverse value rotation."""
+    qt = _u16(qt)
+    G, d = qt.shape
+    out = np.zeros((G, d), np.float64)
+    assert K.length == V.length and K.history_end == V.history_end
+    lib().oo_decode_folded(d, G, K.g, K.S, K.W, K.length, K.history_end, _p(K.sink), _p(V.sink), _p(K.ring),
+                           _p(V.ring), _p(K.rows), _p(K.sz), _p(V.rows), _p(V.sz), _p(qt), _p(out))
     return out
 
 

@@ -8,7 +8,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from . import Stream, bf16_decode, decode
+from . import Stream, bf16_decode, decode, decode_folded
 
 
 def as_bits(t) -> np.ndarray:
@@ -56,6 +56,17 @@ class OracleCache:
             K, V = self.streams[layer][request][h]
             out[h * G:(h + 1) * G] = decode(np.ascontiguousarray(q_bits[h * G:(h + 1) * G]), K, V, self.R_K[layer, h],
                                             self.R_V[layer, h])
+        return out
+
+    def decode_folded(self, layer: int, request: int, qt_bits: np.ndarray) -> np.ndarray:
+        """decode() with the rotations folded into the model's projections: qt_bits are the
+        rotated queries (uint16 [H_q, d]); fp64 [H_q, d] in the rotated basis."""
+        Hq = qt_bits.shape[0]
+        G = Hq // self.Hkv
+        out = np.zeros((Hq, self.d))
+        for h in range(self.Hkv):
+            K, V = self.streams[layer][request][h]
+            out[h * G:(h + 1) * G] = decode_folded(np.ascontiguousarray(qt_bits[h * G:(h + 1) * G]), K, V)
         return out
 
     def length(self, request: int) -> int:

@@ -220,22 +220,15 @@ static void stream_token_values(int d, int g, int S, int W, int H, long p, const
   }
 }
 
-void oo_decode(int d, int G, int g, int S, int W, int L, int H, const uint16_t* sinkK, const uint16_t* sinkV,
-               const uint16_t* ringK, const uint16_t* ringV, const uint8_t* rowsK, const uint16_t* szK,
-               const uint8_t* rowsV, const uint16_t* szV, const uint16_t* q, const float* R_K, const float* R_V,
-               double* out) {
-  memset(out, 0, sizeof(double) * (size_t)G * d);
-  if (L <= 0) return;
-  double* qt = (double*)calloc((size_t)G * d, sizeof(double));
+/* Attention of G query heads over one (K, V) stream in the rotated basis: qt [G][d] (the
+ * rotated queries), ot [G][d] (the rotated output, before the inverse value rotation).
+ * Scores against the stored rotated keys, fp64 softmax, weighted stored rotated values. */
+static void attend_rotated(int d, int G, int g, int S, int W, int L, int H, const uint16_t* sinkK,
+                           const uint16_t* sinkV, const uint16_t* ringK, const uint16_t* ringV, const uint8_t* rowsK,
+                           const uint16_t* szK, const uint8_t* rowsV, const uint16_t* szV, const double* qt,
+                           double* ot) {
   double* logit = (double*)malloc(sizeof(double) * (size_t)G * L);
-  double* ot = (double*)calloc((size_t)G * d, sizeof(double));
   double kv[512];
-  for (int h = 0; h < G; ++h)
-    for (int c = 0; c < d; ++c) {
-      double s = 0.0;
-      for (int i = 0; i < d; ++i) s += (double)R_K[(size_t)i * d + c] * (double)bf16_to_f32(q[(size_t)h * d + i]);
-      qt[(size_t)h * d + c] = s;
-    }
   double inv_sqrt_d = 1.0 / sqrt((double)d);
   for (long p = 0; p < L; ++p) {
     stream_token_values(d, g, S, W, H, p, sinkK, ringK, rowsK, szK, kv);
@@ -263,6 +256,24 @@ void oo_decode(int d, int G, int g, int S, int W, int L, int H, const uint16_t* 
       for (int c = 0; c < d; ++c) ot[(size_t)h * d + c] += w * kv[c];
     }
   }
+  free(logit);
+}
+
+void oo_decode(int d, int G, int g, int S, int W, int L, int H, const uint16_t* sinkK, const uint16_t* sinkV,
+               const uint16_t* ringK, const uint16_t* ringV, const uint8_t* rowsK, const uint16_t* szK,
+               const uint8_t* rowsV, const uint16_t* szV, const uint16_t* q, const float* R_K, const float* R_V,
+               double* out) {
+  memset(out, 0, sizeof(double) * (size_t)G * d);
+  if (L <= 0) return;
+  double* qt = (double*)calloc((size_t)G * d, sizeof(double));
+  double* ot = (double*)calloc((size_t)G * d, sizeof(double));
+  for (int h = 0; h < G; ++h)
+    for (int c = 0; c < d; ++c) {
+      double s = 0.0;
+      for (int i = 0; i < d; ++i) s += (double)R_K[(size_t)i * d + c] * (double)bf16_to_f32(q[(size_t)h * d + i]);
+      qt[(size_t)h * d + c] = s;
+    }
+  attend_rotated(d, G, g, S, W, L, H, sinkK, sinkV, ringK, ringV, rowsK, szK, rowsV, szV, qt, ot);
   for (int h = 0; h < G; ++h)
     for (int c = 0; c < d; ++c) {
       double s = 0.0;
@@ -270,8 +281,21 @@ void oo_decode(int d, int G, int g, int S, int W, int L, int H, const uint16_t* 
       out[(size_t)h * d + c] = s;
     }
   free(qt);
-  free(logit);
   free(ot);
+}
+
+/* The same with the rotations folded into the model's projections: qt are the rotated
+ * queries themselves (bf16, q~ = R_K^T q computed outside), and the output is left in the
+ * rotated basis (o~; the inverse value rotation R_V is applied outside). */
+void oo_decode_folded(int d, int G, int g, int S, int W, int L, int H, const uint16_t* sinkK, const uint16_t* sinkV,
+                      const uint16_t* ringK, const uint16_t* ringV, const uint8_t* rowsK, const uint16_t* szK,
+                      const uint8_t* rowsV, const uint16_t* szV, const uint16_t* qt_bf16, double* out) {
+  memset(out, 0, sizeof(double) * (size_t)G * d);
+  if (L <= 0) return;
+  double* qt = (double*)calloc((size_t)G * d, sizeof(double));
+  for (size_t e = 0; e < (size_t)G * d; ++e) qt[e] = (double)bf16_to_f32(qt_bf16[e]);
+  attend_rotated(d, G, g, S, W, L, H, sinkK, sinkV, ringK, ringV, rowsK, szK, rowsV, szV, qt, out);
+  free(qt);
 }
 
 /* Uncompressed comparison: plain softmax(q K^T / sqrt(d)) V over bf16 K, V [L][d]. */

@@ -425,6 +425,43 @@ def test_decode_change_of_basis_invariance(exact):
         assert np.allclose(got, brute_attention(f64(q), f64(xk), f64(xv)), atol=1e-12, rtol=0)
 
 
+@pytest.mark.parametrize("exact", [True, False])
+def test_folded_decode_is_attention_in_the_rotated_basis(exact):
+    """With the rotations folded into the model's projections the oracle takes q~ (bf16)
+    and returns o~: plain attention of q~ over the stored rotated keys and values (INT2
+    history dequantised by hand here); with a signed permutation (exact rotations) o~ is
+    R_V^T of the unfolded decode of q."""
+    rng = np.random.default_rng(31)
+    RK = signed_permutation(128, 32) if exact else random_orthogonal(128, 32)
+    RV = signed_permutation(128, 33) if exact else random_orthogonal(128, 33)
+    K = oracle.Stream(128, 32, 4, 64, 320, RK, 4.0)
+    V = oracle.Stream(128, 32, 4, 64, 320, RV, 4.0)
+    xk, xv = bits(rng.standard_normal((300, 128)) * 2), bits(rng.standard_normal((300, 128)))
+    K.append(xk)
+    V.append(xv)
+    q = bits(rng.standard_normal((4, 128)))
+    qt = bits((f64(q) @ RK.astype(np.float64)))  # q~ = R_K^T q (rows), rounded to bf16
+
+    def stored(st, p):
+        route = st.route(p)
+        if route == "sink":
+            return f64(st.sink[p])
+        if route == "ring":
+            return f64(st.ring[p % 64])
+        return oracle.dequant_token(st.rows[p], st.sz[p], 32).astype(np.float64)
+
+    sk = np.array([stored(K, p) for p in range(300)])
+    sv = np.array([stored(V, p) for p in range(300)])
+    assert K.route(100) == "int2"
+    got = oracle.decode_folded(qt, K, V)
+    assert np.allclose(got, brute_attention(f64(qt), sk, sv), atol=1e-12, rtol=0)
+    if exact:  # q~ is exact, so the folded output is R_V^T times the unfolded one
+        full = oracle.decode(q, K, V, RK, RV)
+        assert np.allclose(got, full @ RV.astype(np.float64), atol=1e-12, rtol=0)
+    assert not np.any(oracle.decode_folded(np.zeros((2, 128), np.uint16), oracle.Stream(128, 32, 4, 64, 8, RK, 1.0),
+                                           oracle.Stream(128, 32, 4, 64, 8, RV, 1.0)))
+
+
 def test_decode_single_token_and_equal_logits():
     rng = np.random.default_rng(21)
     RK, RV = signed_permutation(128, 22), signed_permutation(128, 23)
