@@ -51,6 +51,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-serving", action="store_true", help="skip the throughput-mode serving comparison")
     ap.add_argument("--format", default="int2", choices=["int2", "int2_cm"],
                     help="INT2 page format: token-major (int2) or channel-major value pages (int2_cm)")
+    ap.add_argument("--folded", action="store_true",
+                    help="plan with OSCAR_PLAN_FOLDED_ROTATIONS (q arrives rotated, the output stays rotated)")
+    ap.add_argument("--no-folded", action="store_true",
+                    help="skip the 8B-shaped step's second run with OSCAR_PLAN_FOLDED_ROTATIONS")
     ap.add_argument("--no-cm", action="store_true",
                     help="skip the headline workload's second run in the channel-major format (tcgen05 decode)")
     ap.add_argument("--rotation", default="oscar", choices=["oscar", "hadamard"],
@@ -397,9 +401,11 @@ def run_ours(args, w, world, rank, local):
     out = torch.empty_like(qin)
     stream = torch.cuda.current_stream()
 
+    plan_flags = N.OSCAR_PLAN_FOLDED_ROTATIONS if args.folded else 0
+
     def host_plan(s):
         cache.reserve(slots, steps_in[s][3])
-        cache.plan(slots)
+        cache.plan(slots, flags=plan_flags)
 
     # per-layer views, made once (the calls below are the step's whole host work per layer)
     kin_l, vin_l = [kin[layer] for layer in range(n_layers)], [vin[layer] for layer in range(n_layers)]
@@ -473,7 +479,7 @@ def run_ours(args, w, world, rank, local):
     L_pre = [cache.info(sl)[0] for sl in slots]
     H_pre = [cache.info(sl)[1] for sl in slots]
     cache.reserve(slots, n_new_k)
-    cache.plan(slots)
+    cache.plan(slots, flags=plan_flags)
     fgraph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(fgraph):
         device_step()
@@ -497,7 +503,7 @@ def run_ours(args, w, world, rank, local):
 
     # ---- decode-only timing (n_layers back-to-back decode calls, captured)
     dgraph = torch.cuda.CUDAGraph()
-    cache.plan(slots)
+    cache.plan(slots, flags=plan_flags)
     with torch.cuda.graph(dgraph):
         for layer in range(n_layers):
             cache.decode(layer, qin[layer], out=out[layer])
@@ -558,7 +564,7 @@ def run_ours(args, w, world, rank, local):
             if i + 1 < n_e2e:
                 upload(i + 1, 1 - b)
             cache.reserve(slots, steps_in[e2e_first + i][3])
-            cache.plan(slots)
+            cache.plan(slots, flags=plan_flags)
             comp.wait_event(in_ready[b])
             if used[b]:
                 comp.wait_event(out_free[b])
@@ -950,6 +956,24 @@ def main(argv=None):
         cm_line["format"] = "OSCAR_FORMAT_INT2_CM"
         del r
         release_gpu_memory()
+    folded_line = None
+    if len(names) > 1 and not args.no_folded and not args.folded and "qwen3_8b_layer" in names:
+        # the latency-bound 8B-shaped step again with the rotations folded into the model's
+        # projections (q~ in, o~ out): the q and output rotations leave the launch
+        import copy
+
+        a2 = copy.copy(args)
+        a2.folded, a2.no_bf16 = True, True
+        w = wl.WORKLOADS["qwen3_8b_layer"]
+        r = run_ours(a2, w, world, rank, local)
+        full = result_line(a2, w, r, world)
+        folded_line = {k: full[k] for k in ("value", "unit", "ms_per_step", "decode_us_per_layer", "roofline",
+                                            "step_us_per_layer_p10_p50_p90", "gpu_launches", "clocks")}
+        if "e2e" in full:
+            folded_line["e2e"] = full["e2e"]
+        folded_line["plan_flags"] = "OSCAR_PLAN_FOLDED_ROTATIONS"
+        del r
+        release_gpu_memory()
     serving_line = None
     if len(names) > 1 and not args.no_serving:
         import torch
@@ -968,6 +992,8 @@ def main(argv=None):
                                                                                   "higher_is_better", "scaling",
                                                                                   "vs_baseline", "data")}
                                 for n in names[1:]}
+        if folded_line and "qwen3_8b_layer" in line["per_workload"]:
+            line["per_workload"]["qwen3_8b_layer"]["folded_rotations"] = folded_line
     print(json.dumps(line), flush=True)
     return 0
 

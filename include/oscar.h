@@ -177,6 +177,13 @@ oscar_status oscar_plan_decode(oscar_cache* cache, const int* slots, int n_req, 
  * the 8-warp CTA shape (two CTAs per SM at GQA 4), which the automatic choice takes only
  * for steps larger than one wave of 16-warp CTAs; results are the same either way. */
 #define OSCAR_PLAN_NARROW 0x1u
+/* OSCAR_PLAN_FOLDED_ROTATIONS (INT2 formats): the model folds the rotations into its
+ * projections ([OSCAR] §2.2-A.3 and B: R_K into the query projection, R_V into the output
+ * projection), so the decode calls of this plan take q already rotated, q~ = R_K^T q (bf16,
+ * same layout as q), and write o~, the output in the rotated basis (o = R_V o~ is left to
+ * the model).  The stored cache is the same; only the two matrix-vector products at the
+ * ends of the decode are skipped. */
+#define OSCAR_PLAN_FOLDED_ROTATIONS 0x2u
 oscar_status oscar_plan_decode_ex(oscar_cache* cache, const int* slots, int n_req, int max_split_pages, uint32_t flags,
                                   void* stream);
 

@@ -227,6 +227,7 @@ def oscar_plan_decode(handle: int, slots, max_split_pages: int = 0, stream=None)
 
 
 OSCAR_PLAN_NARROW = 0x1
+OSCAR_PLAN_FOLDED_ROTATIONS = 0x2  # q arrives rotated (R_K folded into W_q), the output stays rotated
 
 
 def oscar_plan_decode_ex(handle: int, slots, max_split_pages: int = 0, flags: int = 0, stream=None) -> None:

@@ -282,6 +282,43 @@ __device__ void finish_output(const KernelParams& kp, const DecodeItem& it, cons
   }
 }
 
+// Final merge with the rotations folded into the model's projections: o~ = O / L, bf16
+// and optional fp32 store, no inverse rotation.
+template <int G, int NW>
+__device__ void finish_output_folded(const KernelParams& kp, const DecodeItem& it,
+                                     const MergeAcc<G, Shape<NW>::NTH>& acc, uint16_t* out, float* out_f32) {
+  using A = MergeAcc<G, Shape<NW>::NTH>;
+  constexpr int HPT = A::HPT, KS = A::kStride;
+  const int t = threadIdx.x, c = t & (kHeadDim - 1), hb = t >> 7;
+  const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
+#pragma unroll
+  for (int q = 0; q < HPT; ++q) {
+    const int h = hb + KS * q;
+    const float v = acc.L[q] > 0.f ? acc.O[q] / acc.L[q] : 0.f;
+    out[(head0 + h) * kHeadDim + c] = bf16_rne(v);
+    if (out_f32) out_f32[(head0 + h) * kHeadDim + c] = v;
+  }
+}
+
+// The rotated queries given (R_K folded into the model's query projection): q~ (bf16) into
+// qts[G][kQRow] (fp32, shared), and per warp w the sum of q~ over the channels rotate_q gives
+// warp w (kHeadDim / NW of them) into qpart[w][G].  All threads; one barrier.
+template <int G, int NW>
+__device__ void load_q_folded(const uint16_t* __restrict__ qt_head0, float* qts, float* qpart) {
+  using Sh = Shape<NW>;
+  constexpr int CPW = kHeadDim / NW;  // channels of warp w: [CPW w, CPW (w + 1))
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  for (int e = tid; e < G * kHeadDim; e += Sh::NTH) qts[(e / kHeadDim) * kQRow + e % kHeadDim] = bf16_f32(qt_head0[e]);
+#pragma unroll
+  for (int h = 0; h < G; ++h) {
+    float v = lane < CPW ? bf16_f32(qt_head0[h * kHeadDim + CPW * warp + lane]) : 0.f;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    if (lane == 0) qpart[warp * G + h] = v;
+  }
+  __syncthreads();
+}
+
 // BF16 rows of the sink + ring list of (request, kv-head): list index u < min(L, S) is
 // sink u, otherwise position H + u - min(L, S) in ring slot p % W.
 struct SinkRingRows {
@@ -1320,19 +1357,21 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW, CM>::kPerSM)
           pre_mask |= 1u << k;
       }
     }
-    if (threadIdx.x == 0 && it.slot == it.head_first)  // R_V^T for the merge of this (request, kv-head)
+    const bool folded = kp.folded;  // q arrives rotated and the output stays rotated
+    if (!folded && threadIdx.x == 0 && it.slot == it.head_first)  // R_V^T for the merge of this (request, kv-head)
       bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                            (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim,
                        kHeadDim * kHeadDim * 4);
     float rk[Shape<NW>::kRows];
-    load_rk_cols<NW>(kp, layer, it.kvh, rk);
+    if (!folded) load_rk_cols<NW>(kp, layer, it.kvh, rk);
     if (!waited) {
       pdl_wait();
       pdl_trigger();
       waited = true;
     }
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
-    rotate_q<G, NW>(q + head0 * kHeadDim, rk, qin, qts, qss);
+    if (folded) load_q_folded<G, NW>(q + head0 * kHeadDim, qts, qss);
+    else rotate_q<G, NW>(q + head0 * kHeadDim, rk, qin, qts, qss);
     // rows this launch's append tasks write: wait for their signal (all threads)
     auto wait_dep = [&] {
       if (!dep) return;
@@ -1361,7 +1400,9 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW, CM>::kPerSM)
     MergeAcc<G, kThreads> acc;
     if (merge_partial<G, kThreads>(kp, it, partials, acc, s_last, smem + C::kSlabOff, C::kSlabSlots,
                                    smem_u32(slab_bar), slab_phase,
-                                   [&] { fetch_rvt(kp, layer, it.kvh, smem, smem_u32(merge_bar)); })) {
+                                   [&] {
+                                     if (!folded) fetch_rvt(kp, layer, it.kvh, smem, smem_u32(merge_bar));
+                                   })) {
       // every item of (request, kv-head) is done, so are its waits: ready for the next launch
       // (subtracting the launch's count: a task's last increment may still be on its way)
       if (fused && slot_ok && dr.app_expect > 0 && threadIdx.x == 0) {
@@ -1369,7 +1410,8 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW, CM>::kPerSM)
         atomicSub(ctr, unsigned(dr.app_expect));
         atomicSub(ctr + 1, unsigned(dr.app_expect));
       }
-      finish_output<G, NW>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
+      if (folded) finish_output_folded<G, NW>(kp, it, acc, out, out_f32);
+      else finish_output<G, NW>(kp, it, acc, out, out_f32, smem, smem_u32(merge_bar), merge_phase);
     }
     // generic-proxy use of the stage memory is over before the next item's bulk copies
     fence_proxy_async();

@@ -171,6 +171,7 @@ struct oscar_cache {
   int app_items = 0, app_rows = 0;
   bool plan_covers_reservation = false;  // the plan lists every slot of the pending reservation
   bool dec_wide = false;                  // INT2: the plan is for 16-warp split-kernel CTAs; BF16: for the deep pipeline
+  bool dec_folded = false;                // OSCAR_PLAN_FOLDED_ROTATIONS: q~ in, o~ out
   // decode plan
   bool planned = false;
   bool planned_with_reservation = false;  // the plan already counts the reserved tokens
@@ -205,6 +206,7 @@ KernelParams kernel_params(const oscar_cache* c) {
   kp.max_pages_per_request = c->cfg.max_pages_per_request;
   kp.counter_polls = c->counter_polls ? c->counter_polls : kDefaultCounterPolls;
   kp.v_cm = c->cfg.format == OSCAR_FORMAT_INT2_CM;
+  kp.folded = c->dec_folded;
   kp.lay = c->lay;
   return kp;
 }
@@ -654,7 +656,10 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
                                   void* stream) {
   if (!c || !slots || n_req <= 0 || n_req > c->cfg.max_requests)
     return fail(OSCAR_ERR_INVALID_ARG, "bad plan arguments");
-  if (flags & ~OSCAR_PLAN_NARROW) return fail(OSCAR_ERR_INVALID_ARG, "unknown plan flags %#x", flags);
+  if (flags & ~(OSCAR_PLAN_NARROW | OSCAR_PLAN_FOLDED_ROTATIONS))
+    return fail(OSCAR_ERR_INVALID_ARG, "unknown plan flags %#x", flags);
+  if ((flags & OSCAR_PLAN_FOLDED_ROTATIONS) && !is_int2(c))
+    return fail(OSCAR_ERR_INVALID_ARG, "OSCAR_PLAN_FOLDED_ROTATIONS applies to the INT2 formats");
   if (max_split_pages < 0) return fail(OSCAR_ERR_INVALID_ARG, "max_split_pages < 0");
   std::vector<char> seen(c->cfg.max_requests, 0);
   const int Hkv = c->cfg.n_kv_heads, S = is_int2(c) ? c->cfg.n_sink : 0;
@@ -869,6 +874,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
   c->planned = true;
   c->planned_with_reservation = c->reserved;
   c->dec_wide = wide;
+  c->dec_folded = (flags & OSCAR_PLAN_FOLDED_ROTATIONS) != 0;
   c->plan_covers_reservation = c->reserved && n_reserved_planned == int(c->app_reqs.size());
   return OSCAR_OK;
 }

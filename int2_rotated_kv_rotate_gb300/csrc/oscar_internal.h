@@ -113,6 +113,7 @@ struct KernelParams {
   int max_requests, max_pages, max_pages_per_request;
   uint32_t counter_polls;  // bounded waits on append-dependency counters give up after this many polls
   int v_cm;                // INT2 value pages channel-major (OSCAR_FORMAT_INT2_CM)
+  int folded;              // decode: q arrives rotated, the output stays rotated (OSCAR_PLAN_FOLDED_ROTATIONS)
   DeviceLayout lay;
 };
 // Polls of a dependency-counter wait (each about 0.1-0.3 us: a sleep and an acquire load)

@@ -416,3 +416,61 @@ def test_bad_page_entry_is_flagged_not_faulting(fmt):
     st, flags = cache.status()
     assert flags & N.OSCAR_FLAG_BAD_PAGE and st == 4
     assert torch.isfinite(out.float()).all()
+
+
+@pytest.mark.parametrize("fmt,gqa,group", [(N.OSCAR_FORMAT_INT2, 4, 128), (N.OSCAR_FORMAT_INT2, 8, 32),
+                                           (N.OSCAR_FORMAT_INT2_CM, 4, 128), (N.OSCAR_FORMAT_INT2_CM, 8, 128),
+                                           (N.OSCAR_FORMAT_INT2_CM, 4, 32)])
+def test_folded_rotations(fmt, gqa, group):
+    """OSCAR_PLAN_FOLDED_ROTATIONS: the decode takes q~ = R_K^T q (bf16) and writes o~, the
+    output in the rotated basis; against the oracle's folded decode, both the plain decode
+    and the one-call append + decode (steps of 1 and 16 tokens), one-wave and multi-wave
+    plans."""
+    w = wl.scaled(wl.WORKLOADS["tiny"], name=f"folded_{gqa}_{group}", n_q_heads=4 * gqa, n_kv_heads=4, group=group,
+                  window=64, lognormal_sigma=0.5)
+    lens = [3000, 700, 20]
+    cache, oc, params = make_pair(w, SEED, 1, 3, 3200, fmt=fmt)
+    RK = params[0][0]  # [H_kv][d][d]
+    slots = [cache.alloc() for _ in lens]
+    cache.reserve(slots, lens)
+    append_both(cache, oc, w, 0, slots, [0, 1, 2], [0, 0, 0], lens)
+    cache.commit()
+
+    def rotated(q):  # q~ = R_K^T q per kv-head, rounded to bf16 (what a folded W_q would give)
+        qf = q.float().cpu().numpy().reshape(len(lens), 4, gqa, 128)
+        qt = np.einsum("rhgi,hij->rhgj", qf.astype(np.float64), RK.astype(np.float64)).reshape(len(lens), 4 * gqa, 128)
+        return torch.from_numpy(qt.astype(np.float32)).to(torch.bfloat16).cuda().contiguous()
+
+    flags = N.OSCAR_PLAN_FOLDED_ROTATIONS
+    for step, msp in enumerate((0, 1)):
+        cache.plan(slots, max_split_pages=msp, flags=flags)
+        qt = rotated(wl.gen_q(w, SEED, 0, step, 3, device="cuda"))
+        o32 = torch.empty(qt.shape, dtype=torch.float32, device="cuda")
+        out = cache.decode(0, qt, out_f32=o32)
+        torch.cuda.synchronize()
+        st, fl = cache.status()
+        assert st == 0 and fl == 0, f"device flags {fl:#x}"
+        qb = bits(qt)
+        for i in range(3):
+            compare_decode(o32[i], out[i], oc.decode_folded(0, i, qb[i]), f"folded msp {msp} req {i}")
+    pos = list(lens)
+    for step, counts in enumerate(([1, 16, 1], [16, 1, 16])):
+        cache.reserve(slots, counts)
+        cache.plan(slots, flags=flags)
+        K, V = kv_rows(w, 0, [0, 1, 2], pos, counts)
+        qt = rotated(wl.gen_q(w, SEED, 0, 10 + step, 3, device="cuda"))
+        o32 = torch.empty(qt.shape, dtype=torch.float32, device="cuda")
+        out = cache.append_decode(0, K, V, qt, out_f32=o32)
+        torch.cuda.synchronize()
+        cache.commit()
+        kb, vb = bits(K), bits(V)
+        off = 0
+        for r, n in enumerate(counts):
+            oc.append(0, r, kb[off:off + n], vb[off:off + n])
+            off += n
+        qb = bits(qt)
+        for i in range(3):
+            compare_decode(o32[i], out[i], oc.decode_folded(0, i, qb[i]), f"folded fused step {step} req {i}")
+        pos = [p + n for p, n in zip(pos, counts)]
+    assert cache.status() == (0, 0)
+    cache.close()
