@@ -30,6 +30,8 @@ from typing import Callable, Optional
 import torch
 
 from . import _native as N
+
+_INT2 = (N.OSCAR_FORMAT_INT2, N.OSCAR_FORMAT_INT2_CM)  # both INT2 page formats
 from . import workloads as wl
 from .cache import KVCache
 
@@ -88,7 +90,7 @@ class TokenSource:
 
 def pages_needed(fmt: int, L: int, S: int, W: int) -> int:
     """Pages of a request of length L (the library's rule: INT2 pages hold history rows only)."""
-    if fmt == N.OSCAR_FORMAT_INT2:
+    if fmt in _INT2:
         H = max(S, L - W)
         return -(-H // 64) if H > S else 0
     return -(-L // 64)
@@ -123,12 +125,12 @@ class ServingLoop:
                  max_requests: int = 128, max_len: int = 1 << 16, prefix_tokens: int = 0,
                  prefill_chunk: int = 16384, device="cuda"):
         self.w, self.fmt, self.tokens = w, fmt, tokens
-        self.S = w.n_sink if fmt == N.OSCAR_FORMAT_INT2 else 0
-        self.W = w.window if fmt == N.OSCAR_FORMAT_INT2 else 0
+        self.S = w.n_sink if fmt in _INT2 else 0
+        self.W = w.window if fmt in _INT2 else 0
         self.prefix = prefix_tokens
         self.prefill_chunk = prefill_chunk
         self.cache = cache_for_budget(w, fmt, budget_bytes, max_requests, max_len, device)
-        if fmt == N.OSCAR_FORMAT_INT2:
+        if fmt in _INT2:
             RK, RV, cK, cV = layer_params
             for layer in range(w.n_layers):
                 self.cache.set_layer_params(layer, RK[layer], RV[layer], cK[layer], cV[layer])
@@ -145,7 +147,7 @@ class ServingLoop:
         never rewrite)."""
         if not self.prefix:
             return 0
-        held = self.prefix if self.fmt != N.OSCAR_FORMAT_INT2 else max(self.S, self.prefix - self.W)
+        held = self.prefix if self.fmt not in _INT2 else max(self.S, self.prefix - self.W)
         return held // 64 * 64
 
     # ------------------------------------------------------------------ appends
@@ -262,7 +264,7 @@ class ServingLoop:
             V = tk.V.index_select(0, idx)
             q = tk.Q.index_select(0, qi)
             o32 = torch.empty(q.shape, dtype=torch.float32, device=q.device) if on_output else None
-            if self.fmt == N.OSCAR_FORMAT_INT2:
+            if self.fmt in _INT2:
                 out = c.append_decode(layer, K, V, q, out_f32=o32)
             else:
                 c.bf16_append(layer, K, V)

@@ -74,15 +74,16 @@ class Mirror:
         return out
 
 
-@pytest.mark.parametrize("fmt", [N.OSCAR_FORMAT_INT2, N.OSCAR_FORMAT_BF16])
+@pytest.mark.parametrize("fmt", [N.OSCAR_FORMAT_INT2, N.OSCAR_FORMAT_INT2_CM, N.OSCAR_FORMAT_BF16])
 def test_serving_loop_against_the_oracle(fmt):
     w = _shape()
     prefix = 384
     tokens = serving.TokenSource(w, SEED, pool_tokens=4096)
-    params = _params(w) if fmt == N.OSCAR_FORMAT_INT2 else None
+    int2 = fmt in (N.OSCAR_FORMAT_INT2, N.OSCAR_FORMAT_INT2_CM)
+    params = _params(w) if int2 else None
     reqs = serving.make_requests(9, (450, 1400), (3, 14), n_groups=2, seed=SEED)
     # about three or four requests at once at this budget
-    per_token = w.n_layers * w.n_kv_heads * 2 * (36 if fmt == N.OSCAR_FORMAT_INT2 else 256)
+    per_token = w.n_layers * w.n_kv_heads * 2 * (36 if int2 else 256)
     budget = N.oscar_cache_device_bytes(N.oscar_config(fmt, 128, w.n_q_heads, w.n_kv_heads, w.group, 64, w.n_sink,
                                                        w.window, w.n_layers, 16, 1, 40)) + 3500 * per_token
     loop = serving.ServingLoop(w, fmt, budget, tokens, layer_params=params, max_requests=16, max_len=2560,
@@ -97,7 +98,7 @@ def test_serving_loop_against_the_oracle(fmt):
         qb = as_bits(q)
         for i, r in enumerate(reqs_):
             L = r.length + 1  # the step appends the request's next token first
-            if fmt == N.OSCAR_FORMAT_INT2:
+            if int2:
                 ref = np.zeros((w.n_q_heads, 128))
                 for h, (sk, sv) in enumerate(mirror.int2_streams(r, layer, L)):
                     ref[h * G:(h + 1) * G] = oracle.decode(np.ascontiguousarray(qb[i, h * G:(h + 1) * G]), sk, sv,
@@ -109,7 +110,7 @@ def test_serving_loop_against_the_oracle(fmt):
             checked[0] += 1
 
     def on_step(step, done):
-        if fmt != N.OSCAR_FORMAT_INT2 or step % 4:
+        if not int2 or step % 4:
             return
         for r in loop.running:
             for layer in range(w.n_layers):
