@@ -1272,7 +1272,8 @@ __device__ void fused_append_task(const KernelParams& kp, int layer, int id, uin
 }
 
 // CM: INT2 value pages channel-major, INT2 items on the tcgen05 tensor cores (never fused).
-template <int G, int GROUP, bool FUSED, int NW, bool CM>
+// FOLD: the plan's rotations are folded into the model (q~ in, o~ out).
+template <int G, int GROUP, bool FUSED, int NW, bool CM, bool FOLD = false>
 __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW, CM>::kPerSM)
     split_kernel(KernelParams kp, int layer, const uint16_t* __restrict__ q, uint8_t* __restrict__ partials,
                  uint16_t* __restrict__ out, float* __restrict__ out_f32, const uint16_t* __restrict__ k_new,
@@ -1357,7 +1358,7 @@ __global__ void __launch_bounds__(Shape<NW>::NTH, Cfg<G, GROUP, NW, CM>::kPerSM)
           pre_mask |= 1u << k;
       }
     }
-    const bool folded = kp.folded;  // q arrives rotated and the output stays rotated
+    constexpr bool folded = FOLD;  // q arrives rotated and the output stays rotated
     if (!folded && threadIdx.x == 0 && it.slot == it.head_first)  // R_V^T for the merge of this (request, kv-head)
       bulk_prefetch_l2(reinterpret_cast<const float*>(kp.base + kp.lay.R_Vt) +
                            (size_t(layer) * kp.n_kv_heads + it.kvh) * kHeadDim * kHeadDim,
@@ -1434,6 +1435,9 @@ int resident_ctas_t(int n_sm) {
   if (resident == 0) {
     int e = int(cudaFuncSetAttribute(split_kernel<G, GROUP, FUSED, NW, CM>,
                                      cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
+    if (!e)
+      e = int(cudaFuncSetAttribute(split_kernel<G, GROUP, FUSED, NW, CM, true>,
+                                   cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes));
     int per_sm = 0;
     if (!e)
       e = int(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, split_kernel<G, GROUP, FUSED, NW, CM>, C::NTH,
@@ -1484,15 +1488,18 @@ int launch_decode_t(const KernelParams& kp, int layer, const void* q, void* out,
   uint16_t* ob = static_cast<uint16_t*>(out);
   const uint16_t* kb = static_cast<const uint16_t*>(k_new);
   const uint16_t* vb = static_cast<const uint16_t*>(v_new);
+  auto go = [&](auto kernel) {
+    return launch_ex(kernel, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes), stream, kp, layer, qb, partials, ob,
+                     out_f32, kb, vb);
+  };
   int e;
   if constexpr (CM)
-    e = launch_ex(split_kernel<G, GROUP, false, NW, true>, dim3(resident), dim3(C::NTH), size_t(C::kSmemBytes),
-                  stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
+    e = kp.folded ? go(split_kernel<G, GROUP, false, NW, true, true>) : go(split_kernel<G, GROUP, false, NW, true, false>);
+  else if (fused)
+    e = kp.folded ? go(split_kernel<G, GROUP, true, NW, false, true>) : go(split_kernel<G, GROUP, true, NW, false, false>);
   else
-    e = fused ? launch_ex(split_kernel<G, GROUP, true, NW, false>, dim3(resident), dim3(C::NTH),
-                          size_t(C::kSmemBytes), stream, kp, layer, qb, partials, ob, out_f32, kb, vb)
-              : launch_ex(split_kernel<G, GROUP, false, NW, false>, dim3(resident), dim3(C::NTH),
-                          size_t(C::kSmemBytes), stream, kp, layer, qb, partials, ob, out_f32, kb, vb);
+    e = kp.folded ? go(split_kernel<G, GROUP, false, NW, false, true>)
+                  : go(split_kernel<G, GROUP, false, NW, false, false>);
   if (!e) *launches += 1;
   return e;
 }
