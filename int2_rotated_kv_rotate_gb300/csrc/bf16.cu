@@ -38,18 +38,18 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
   }
   __syncthreads();
   uint32_t slab_phase = 0;
-  pdl_wait();
-  pdl_trigger();
+  // The plan and the page table were uploaded before the preceding kernels, and no kernel
+  // of the step writes the rows below H_pre (the length before the step's append), so the
+  // first item copies those of its first chunks before the wait on the preceding kernel.
   const int n_items = reinterpret_cast<const int*>(kp.base + kp.lay.decode_counts)[0];
   const WorkQueue wq{reinterpret_cast<unsigned*>(kp.base + kp.lay.sched), n_items, 0, n_items};
   int* s_next = s_last_p + 1;
+  bool waited = false;
   for (int ix = wq.first(); ix >= 0; ix = wq.next(s_next)) {
     const DecodeItem it = reinterpret_cast<const DecodeItem*>(kp.base + kp.lay.decode_items)[ix];
     const DecodeReq dr = reinterpret_cast<const DecodeReq*>(kp.base + kp.lay.decode_reqs)[it.req];
     const size_t head0 = size_t(it.req) * kp.n_q_heads + size_t(it.kvh) * G;
     uint8_t* part = partials + size_t(it.slot) * PartialSlot<G>::kBytes;
-    for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[(e / kHeadDim) * kQRow + e % kHeadDim] = bf16_f32(q[head0 * kHeadDim + e]);
-    __syncthreads();
     const bool slot_ok = dr.slot >= 0 && dr.slot < kp.max_requests;
     if (!slot_ok && threadIdx.x == 0) flag(kp, OSCAR_FLAG_BAD_SLOT);
     int t0 = 0, t1 = 0;
@@ -72,7 +72,21 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     };
     auto rowK = [=](int u) { return page_of(u) + size_t(u % kPage) * kHeadDim; };
     auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
-    bf16_rows_mma<G, 4, NBUF>(rowK, rowV, t0, t1, qs, part, smem, 0, [] {});
+    int staged = 0;
+    if (!waited) {
+      constexpr int kAheadTok = (NBUF > 1 ? NBUF - 1 : 1) * Bf16Rows<4, NBUF>::kChunk;
+      const int upto = min(min(t1, dr.H_pre), t0 + kAheadTok);
+      if (upto > t0) {
+        bf16_prestage<4, NBUF>(rowK, rowV, t0, upto, smem);
+        staged = upto - t0;
+      }
+      pdl_wait();
+      pdl_trigger();
+      waited = true;
+    }
+    for (int e = threadIdx.x; e < G * kHeadDim; e += 128) qs[(e / kHeadDim) * kQRow + e % kHeadDim] = bf16_f32(q[head0 * kHeadDim + e]);
+    __syncthreads();
+    bf16_rows_mma<G, 4, NBUF>(rowK, rowV, t0, t1, qs, part, smem, staged, [] {});
 
     MergeAcc<G, 128> acc;
     if (merge_partial<G, 128>(kp, it, partials, acc, s_last_p, smem, kBf16SlabSlots<G, NBUF>, smem_u32(slab_bar), slab_phase,
@@ -86,6 +100,10 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
       }
     }
     fence_proxy_async();  // generic use of the buffers is over before later bulk copies
+  }
+  if (!waited) {  // no item: the launch still orders itself after the preceding kernel
+    pdl_wait();
+    pdl_trigger();
   }
   wq.leave();
 }

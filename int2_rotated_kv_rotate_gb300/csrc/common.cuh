@@ -177,24 +177,29 @@ constexpr int kQRow = kHeadDim + 4;
 // (zero-filled past `end`) into NBUF buffers (2 = double buffered); warp w takes tokens
 // 16w..16w+15 of each chunk.  Scores and values use mma.sync bf16 with q split into bf16 hi + lo columns
 // (4 heads per n-tile) and p split the same way, so both products keep ~16 significant
-// bits.  The first `staged` tokens of chunk 0 may have been copied already (bf16_prestage);
-// before_rest() runs (all threads) before the rest of chunk 0 is copied.  Writes the
+// bits.  The first `staged` tokens may have been copied already (bf16_prestage; at most the
+// chunks in flight before the first is attended, max(NBUF - 1, 1) of them); before_rest()
+// runs (all threads) before the rest of them is copied.  Writes the
 // partial slot (PartialSlot<G>) at part.  smem must hold
 // Bf16Rows<NW, NBUF>::kSmemBytes and NW * G * (d + 2) floats (the two may alias).
-// Issue the cp.async copies of the rows of tokens [begin, upto) of chunk 0 (upto <= the
-// chunk's end) in bf16_rows_mma's layout, as one commit group: rows that may be copied
-// early (before the wait on the preceding kernel).
-template <int NW, typename RowK, typename RowV>
+// Issue the cp.async copies of the rows of tokens [begin, upto) in bf16_rows_mma<.., NBUF>'s
+// layout (upto <= begin + max(NBUF - 1, 1) chunks: those that the first chunk's attention
+// finds in flight), as one commit group: rows that may be copied early (before the wait on
+// the preceding kernel).
+template <int NW, int NBUF = 1, typename RowK, typename RowV>
 __device__ void bf16_prestage(RowK rowK, RowV rowV, int begin, int upto, uint8_t* smem) {
-  constexpr int kChunkTok = Bf16Rows<NW, 1>::kChunk;
+  constexpr int kChunkTok = Bf16Rows<NW, NBUF>::kChunk;
+  constexpr int kAhead = NBUF > 1 ? NBUF - 1 : 1;
   const int t = threadIdx.x, seg = t & 15;
-  const uint32_t buf = smem_u32(smem);
-  for (int k = 0; k < 16; ++k) {
-    const int row = (t >> 4) + 2 * NW * k;  // K rows then V rows
-    const int u = begin + (row & (kChunkTok - 1));
-    if (u < upto) {
-      const uint16_t* src = row < kChunkTok ? rowK(u) : rowV(u);
-      cp_async16(buf + row * kRowPad + seg * 16, src + seg * 8, 16u);
+  for (int c = 0; c < kAhead && begin + c * kChunkTok < upto; ++c) {
+    const uint32_t buf = smem_u32(smem) + (c % NBUF) * Bf16Rows<NW, NBUF>::kBufBytes;
+    for (int k = 0; k < 16; ++k) {
+      const int row = (t >> 4) + 2 * NW * k;  // K rows then V rows
+      const int u = begin + c * kChunkTok + (row & (kChunkTok - 1));
+      if (u < upto) {
+        const uint16_t* src = row < kChunkTok ? rowK(u) : rowV(u);
+        cp_async16(buf + row * kRowPad + seg * 16, src + seg * 8, 16u);
+      }
     }
   }
   cp_async_commit();
@@ -257,7 +262,7 @@ __device__ void bf16_rows_mma(RowK rowK, RowV rowV, int begin, int end, const fl
 #pragma unroll 4
     for (int k = 0; k < 16; ++k) {
       const int row = (t >> 4) + 2 * NW * k;  // K rows then V rows
-      if (c == 0 && (row & (kChunkTok - 1)) < staged) continue;  // copied already
+      if (c * kChunkTok + (row & (kChunkTok - 1)) < staged) continue;  // copied already
       const uint16_t* src = rp[row];
       cp_async16(buf + row * kRowPad + seg * 16, (src ? src : any) + seg * 8, src ? 16u : 0u);
     }

@@ -784,7 +784,7 @@ oscar_status oscar_plan_decode_ex(oscar_cache* c, const int* slots, int n_req, i
     q.slot = slots[i];
     q.L = Ls[i];
     q.H = is_int2(c) ? Hs[i] : Ls[i];
-    q.H_pre = is_int2(c) ? Hpre[i] : 0;
+    q.H_pre = is_int2(c) ? Hpre[i] : Lpre[i];
     q.app_expect = is_int2(c) ? app_expect[i] : 0;
     const int np = np_of[i], n_bf = nbf_of[i], bf_new = bfnew_of[i], pg_new = pgnew_of[i];
     // BF16 list index of this step's first new row (index < min(L, S): sink, else ring

@@ -36,9 +36,10 @@ struct AppendItem {
 struct DecodeReq {
   int slot;
   int L, H;          // length, history end (INT2 format); H = L for BF16 format
-  int H_pre;         // history end before this step's append: no kernel of the step writes
-                     // the INT2 pages wholly below it, so they may be copied before the wait
-                     // on the preceding kernel
+  int H_pre;         // history end (BF16 format: length) before this step's append: no
+                     // kernel of the step writes the INT2 pages wholly below it (the BF16
+                     // rows below it), so they may be copied before the wait on the
+                     // preceding kernel
   int app_expect;    // fused append + decode: append tasks of this request per kv-head (K and
                      // V, times append_task_split, per append item); 0 = nothing to wait for
   int first_item;    // items of this request, kv-head-major: first_item + kvh*items_per_head ..

@@ -373,7 +373,7 @@ def test_bf16_comparison_path(gqa):
     """Uncompressed BF16 pages: decode equals plain softmax attention on the bf16 tokens."""
     w = wl.scaled(wl.WORKLOADS["tiny"], name=f"bf16_{gqa}", n_q_heads=2 * gqa, lognormal_sigma=0.5)
     lens = [1000, 77, 1]
-    cache, _, _ = make_pair(w, SEED, 1, 3, 1000, fmt=N.OSCAR_FORMAT_BF16)
+    cache, _, _ = make_pair(w, SEED, 1, 3, 1200, fmt=N.OSCAR_FORMAT_BF16)
     slots = [cache.alloc() for _ in lens]
     Ks, Vs = [], []
     for r, n in enumerate(lens):
@@ -394,6 +394,32 @@ def test_bf16_comparison_path(gqa):
         for r in range(3):
             ref = bf16_reference(qb[r], bits(Ks[r]), bits(Vs[r]))
             compare_decode(out32[r], out[r], ref, f"bf16 msp {msp} req {r}")
+    # steps planned while their new rows are reserved: the decode launch may start while the
+    # append launch before it still writes those rows, so it copies early only the rows below
+    # the pre-append length (here inside the first chunks of the first items)
+    for step, (msp, n_new) in enumerate(((4, 3), (1, 70))):
+        news = [n_new, 1, 2 * n_new]
+        cache.reserve(slots, news)
+        cache.plan(slots, max_split_pages=msp)
+        kn, vn = [], []
+        for r, n in enumerate(news):
+            k, v = wl.gen_kv(w, SEED, 0, r, Ks[r].shape[0], n, device="cuda")
+            kn.append(k)
+            vn.append(v)
+        q = wl.gen_q(w, SEED, 0, 10 + step, 3, device="cuda")
+        cache.bf16_append(0, torch.cat(kn).contiguous(), torch.cat(vn).contiguous())
+        out32 = torch.empty(q.shape, dtype=torch.float32, device="cuda")
+        out = cache.decode(0, q, out_f32=out32)
+        cache.commit()
+        torch.cuda.synchronize()
+        qb = bits(q)
+        for r in range(3):
+            Ks[r] = torch.cat([Ks[r], kn[r]])
+            Vs[r] = torch.cat([Vs[r], vn[r]])
+            ref = bf16_reference(qb[r], bits(Ks[r]), bits(Vs[r]))
+            compare_decode(out32[r], out[r], ref, f"bf16 reserved step {step} req {r}")
+    st, flags = cache.status()
+    assert st == 0 and flags == 0
 
 
 @pytest.mark.parametrize("fmt", INT2_FORMATS)

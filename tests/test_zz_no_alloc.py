@@ -8,8 +8,9 @@ queries, and each output is checked against the ordinary entry point's output on
 same plan: both run the same kernel on the same plan, so they must agree bit for bit.
 The scratch keeps whatever the previous call left in it, so a larger multi-wave plan of
 another cache (its items taken from the work-queue counters) runs through the same
-scratch first; a wrong scratch offset or a read of stale partials would show.  This file
-runs last so that a failure here cannot hide any other test.
+scratch first; a wrong scratch offset or a read of stale partials would show.  Both INT2
+layouts (token-major values, and channel-major values on the tensor-core decode) run
+through it.  This file runs last so that a failure here cannot hide any other test.
 """
 import numpy as np
 import pytest
@@ -32,8 +33,11 @@ def close(a: torch.Tensor, b: torch.Tensor):
     return err <= MAX_ABS and rel <= REL_L2, (err, rel)
 
 
-def _filled(w, lens):
-    cache, _, _ = make_pair(w, SEED, 1, len(lens), max(lens))
+FORMATS = pytest.mark.parametrize("fmt", [N.OSCAR_FORMAT_INT2, N.OSCAR_FORMAT_INT2_CM], ids=["tm", "cm"])
+
+
+def _filled(w, lens, fmt=N.OSCAR_FORMAT_INT2):
+    cache, _, _ = make_pair(w, SEED, 1, len(lens), max(lens), fmt=fmt)
     slots = [cache.alloc() for _ in lens]
     ks, vs = [], []
     for r, n in enumerate(lens):
@@ -57,9 +61,10 @@ def _both(cache, q):
     return ref, out32, out
 
 
-def test_noalloc_decode_matches_workspace_decode_twice():
+@FORMATS
+def test_noalloc_decode_matches_workspace_decode_twice(fmt):
     w = wl.scaled(wl.WORKLOADS["tiny"], name="noalloc", lognormal_sigma=0.5)
-    cache, slots = _filled(w, [1500, 700])
+    cache, slots = _filled(w, [1500, 700], fmt)
     cache.plan(slots, max_split_pages=3)
     assert N.oscar_decode_workspace_bytes(cache.handle) <= 8 << 20
     for step in range(2):  # two calls in a row share (and leave behind) the library scratch
@@ -73,18 +78,19 @@ def test_noalloc_decode_matches_workspace_decode_twice():
     assert st == 0 and flags == 0
 
 
-def test_noalloc_after_a_larger_multi_wave_plan_of_another_cache():
+@FORMATS
+def test_noalloc_after_a_larger_multi_wave_plan_of_another_cache(fmt):
     """A plan of single-page items, several times more than the resident CTAs (so the CTAs
     take them from the work-queue counters), fills much of the scratch; then a smaller plan
     of the first cache reuses it.  Both agree with the workspace path bit for bit."""
     big_w = wl.scaled(wl.WORKLOADS["tiny"], name="noalloc_waves", n_q_heads=32, n_kv_heads=8, lognormal_sigma=0.5)
-    big, big_slots = _filled(big_w, [6000, 5000])
+    big, big_slots = _filled(big_w, [6000, 5000], fmt)
     big.plan(big_slots, max_split_pages=1)
     n_items, _, _ = big.plan_info()
     assert n_items > 2 * torch.cuda.get_device_properties(0).multi_processor_count
     assert N.oscar_decode_workspace_bytes(big.handle) <= 8 << 20
     w = wl.scaled(wl.WORKLOADS["tiny"], name="noalloc_small", lognormal_sigma=0.5)
-    small, small_slots = _filled(w, [1300, 400])
+    small, small_slots = _filled(w, [1300, 400], fmt)
     for step in range(2):
         q = wl.gen_q(big_w, SEED, 0, step, 2, device="cuda")
         ref, out32, _ = _both(big, q)
