@@ -74,6 +74,7 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(KernelParams kp, int la
     auto rowV = [=](int u) { return page_of(u) + size_t(kPage + u % kPage) * kHeadDim; };
     int staged = 0;
     if (!waited) {
+      if (threadIdx.x < 2 * G) prefetch_l2(q + head0 * kHeadDim + 64 * threadIdx.x);  // q's lines, loaded after the wait
       constexpr int kAheadTok = (NBUF > 1 ? NBUF - 1 : 1) * Bf16Rows<4, NBUF>::kChunk;
       const int upto = min(min(t1, dr.H_pre), t0 + kAheadTok);
       if (upto > t0) {

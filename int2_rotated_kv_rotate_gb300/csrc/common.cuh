@@ -102,6 +102,10 @@ __device__ __forceinline__ void cp_async_wait_upto(int n) {
 __device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
 }
+// Pull the 128-byte line holding p into L2.  A prefetch only warms the cache, which stays
+// coherent with every later write, so it may be issued for data that the preceding kernel
+// is still writing, before the wait on it; the data is loaded after the wait.
+__device__ __forceinline__ void prefetch_l2(const void* p) { asm volatile("prefetch.global.L2 [%0];" ::"l"(p)); }
 
 // bf16 x bf16 -> fp32 tensor-core MMA, m16n8k16, A row-major, B column-major.
 __device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
