@@ -78,6 +78,12 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
+// max(a, b, c) in one instruction (a NaN operand is ignored, as by fmaxf).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 // 2-bit field f (0..7) of each 16-bit half of w, as fp16 code * 4^(f&3) * 2^-24.
 __device__ __forceinline__ uint32_t field(uint32_t w, uint32_t w_shr8, int f) {
   const uint32_t m = 0x00030003u << (2 * (f & 3));
@@ -545,7 +551,6 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
         for (int j = 0; j < NT; ++j)
           mma16816(acc[NG == 1 ? (kc & 1) : (kc >> 1)][j], a0, a1, a2, a3, bq[kc][j][0], bq[kc][j][1]);
       }
-      const bool v0 = unsigned(t0 - vlo) < unsigned(vn), v1 = unsigned(t1 - vlo) < unsigned(vn);
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         float s0 = 0.f, s1 = 0.f;
@@ -563,8 +568,20 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
           s0 += fmaf(T0, bf16_lo(sz0) * scale24, bf16_hi(sz0) * qs_scaled[j][g]);
           s1 += fmaf(T1, bf16_lo(sz1) * scale24, bf16_hi(sz1) * qs_scaled[j][g]);
         }
-        lg[b][j][0] = v0 ? s0 : -INFINITY;
-        lg[b][j][1] = v1 ? s1 : -INFINITY;
+        lg[b][j][0] = s0;
+        lg[b][j][1] = s1;
+      }
+    }
+    if (vlo != 0 || vn != kPage) {  // (warp-uniform) the page holds positions outside [S, H)
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        const int t0 = 16 * b + tok_a, t1 = t0 + 8;
+        const bool v0 = unsigned(t0 - vlo) < unsigned(vn), v1 = unsigned(t1 - vlo) < unsigned(vn);
+#pragma unroll
+        for (int j = 0; j < NT; ++j) {
+          if (!v0) lg[b][j][0] = -INFINITY;
+          if (!v1) lg[b][j][1] = -INFINITY;
+        }
       }
     }
     // ---- online softmax over the page (per head: 8 scores per thread, 8 lanes per head)
@@ -573,9 +590,8 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
     float alpha[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      float mx = -INFINITY;
-#pragma unroll
-      for (int b = 0; b < 4; ++b) mx = fmaxf(mx, fmaxf(lg[b][j][0], lg[b][j][1]));
+      float mx = fmax3(fmax3(lg[0][j][0], lg[0][j][1], lg[1][j][0]), fmax3(lg[1][j][1], lg[2][j][0], lg[2][j][1]),
+                       fmaxf(lg[3][j][0], lg[3][j][1]));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
       mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
