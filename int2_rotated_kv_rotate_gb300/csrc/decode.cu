@@ -78,11 +78,6 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
   return r;
 }
-// Lazy softmax reference of the token-major page loop: the running maximum is raised only
-// when a score exceeds it by more than this (log2 units), so p = 2^(score - reference)
-// stays at most 16 and P' = p s_V stays far inside the fp16 range.
-constexpr float kLazyMax = 4.0f;
-
 // max(a, b, c) in one instruction (a NaN operand is ignored, as by fmaxf).
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -485,14 +480,11 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       qs_scaled[j][g] = sq * scale;
     }
 
-  // m_run: the warp's reference maximum per head (lazy: raised only when a page's score
-  // exceeds it by more than kLazyMax, so p <= 2^kLazyMax); muse: the same, 0 while -inf
-  float m_run[NT], muse[NT], l_part[NT], zv[NT][NG];
+  float m_run[NT], l_part[NT], zv[NT][NG];
   float oacc[8][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     m_run[j] = -INFINITY;
-    muse[j] = 0.f;
     l_part[j] = 0.f;
 #pragma unroll
     for (int g = 0; g < NG; ++g) zv[j][g] = 0.f;
@@ -593,30 +585,23 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       }
     }
     // ---- online softmax over the page (per head: 8 scores per thread, 8 lanes per head)
-    // with a lazy reference: the page's maxima are reduced over the head's lanes, and the
-    // sums rescaled, only when some score exceeds the reference by more than kLazyMax (the
-    // first valid scores always do: the reference starts at -inf)
-    float mloc[NT];
-    bool over = false;
+    float muse[NT];
+    bool rescale = false;
+    float alpha[NT];
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      mloc[j] = fmax3(fmax3(lg[0][j][0], lg[0][j][1], lg[1][j][0]), fmax3(lg[1][j][1], lg[2][j][0], lg[2][j][1]),
-                      fmaxf(lg[3][j][0], lg[3][j][1]));
-      over |= mloc[j] > m_run[j] + kLazyMax;
+      float mx = fmax3(fmax3(lg[0][j][0], lg[0][j][1], lg[1][j][0]), fmax3(lg[1][j][1], lg[2][j][0], lg[2][j][1]),
+                       fmaxf(lg[3][j][0], lg[3][j][1]));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+      const float mnew = fmaxf(m_run[j], mx);
+      muse[j] = mnew == -INFINITY ? 0.f : mnew;
+      alpha[j] = ex2(m_run[j] - muse[j]);
+      rescale |= mnew > m_run[j];
+      m_run[j] = mnew;
     }
-    if (__any_sync(0xffffffffu, over)) {
-      float alpha[NT];
-#pragma unroll
-      for (int j = 0; j < NT; ++j) {
-        float mx = mloc[j];
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-        const float mnew = fmaxf(m_run[j], mx);
-        muse[j] = mnew == -INFINITY ? 0.f : mnew;
-        alpha[j] = ex2(m_run[j] - muse[j]);  // 0 while the reference was -inf
-        m_run[j] = mnew;
-      }
+    if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         l_part[j] *= alpha[j];
@@ -640,8 +625,7 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       float p[NT][2];
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
-        // masked tokens carry lg = -inf and muse is finite: ex2 gives exactly 0; the
-        // others give at most 2^kLazyMax
+        // masked tokens carry lg = -inf and muse is finite: ex2 gives exactly 0
         p[j][0] = ex2(lg[b][j][0] - muse[j]);
         p[j][1] = ex2(lg[b][j][1] - muse[j]);
         l_part[j] += p[j][0] + p[j][1];
