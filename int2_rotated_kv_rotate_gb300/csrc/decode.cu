@@ -480,11 +480,13 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
       qs_scaled[j][g] = sq * scale;
     }
 
-  float m_run[NT], l_part[NT], zv[NT][NG];
+  // m_run: the warp's running maximum per head; muse: the same, 0 while -inf
+  float m_run[NT], muse[NT], l_part[NT], zv[NT][NG];
   float oacc[8][4];
 #pragma unroll
   for (int j = 0; j < NT; ++j) {
     m_run[j] = -INFINITY;
+    muse[j] = 0.f;
     l_part[j] = 0.f;
 #pragma unroll
     for (int g = 0; g < NG; ++g) zv[j][g] = 0.f;
@@ -584,24 +586,32 @@ __device__ void int2_pages_item(const KernelParams& kp, int layer, const DecodeI
         }
       }
     }
-    // ---- online softmax over the page (per head: 8 scores per thread, 8 lanes per head)
-    float muse[NT];
-    bool rescale = false;
-    float alpha[NT];
+    // ---- online softmax over the page (per head: 8 scores per thread, 8 lanes per head):
+    // the page's maxima are reduced over the head's lanes, and the sums rescaled, only
+    // when some score exceeds the running maximum.  The maximum stays exact (not a lazy
+    // reference), so the token that holds it gets p = 1 and an exact P' = s_V: with one
+    // dominant token, the fp16 rounding of its P' would be the output's error.
+    float mloc[NT];
+    bool over = false;
 #pragma unroll
     for (int j = 0; j < NT; ++j) {
-      float mx = fmax3(fmax3(lg[0][j][0], lg[0][j][1], lg[1][j][0]), fmax3(lg[1][j][1], lg[2][j][0], lg[2][j][1]),
-                       fmaxf(lg[3][j][0], lg[3][j][1]));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-      mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-      const float mnew = fmaxf(m_run[j], mx);
-      muse[j] = mnew == -INFINITY ? 0.f : mnew;
-      alpha[j] = ex2(m_run[j] - muse[j]);
-      rescale |= mnew > m_run[j];
-      m_run[j] = mnew;
+      mloc[j] = fmax3(fmax3(lg[0][j][0], lg[0][j][1], lg[1][j][0]), fmax3(lg[1][j][1], lg[2][j][0], lg[2][j][1]),
+                      fmaxf(lg[3][j][0], lg[3][j][1]));
+      over |= mloc[j] > m_run[j];
     }
-    if (__any_sync(0xffffffffu, rescale)) {
+    if (__any_sync(0xffffffffu, over)) {
+      float alpha[NT];
+#pragma unroll
+      for (int j = 0; j < NT; ++j) {
+        float mx = mloc[j];
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const float mnew = fmaxf(m_run[j], mx);
+        muse[j] = mnew == -INFINITY ? 0.f : mnew;
+        alpha[j] = ex2(m_run[j] - muse[j]);  // 0 while the reference was -inf
+        m_run[j] = mnew;
+      }
 #pragma unroll
       for (int j = 0; j < NT; ++j) {
         l_part[j] *= alpha[j];
